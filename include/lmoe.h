@@ -1,0 +1,188 @@
+/*
+ * lmoe.h -- C ABI of the GB300 (sm_103a) latent-MoE layer forward.
+ *
+ * The operations follow three pages:
+ *   [vLLM-50088]   vLLM PR #50088, "[MoE] Latent-MoE runner, fused MoE tail,
+ *                  SituGLU activation and single-group top-k routing";
+ *   [TRTLLM-20541] TensorRT-LLM PR #20541, "Kimi K3 MoE decode: router GEMM and
+ *                  routing kernel on a router stream";
+ *   [vLLM-runner]  vLLM API page vllm.models.kimi_k3.amd.latent_moe_runner
+ *                  (ROCmLatentMoERunner).
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; it must
+ *     stay valid until the work enqueued on `stream` has finished.  Tensors are
+ *     dense and row-major (last index fastest).  Every pointer must be 16-byte
+ *     aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     The calls are asynchronous: the return code covers argument validation
+ *     and launch errors only.  No call synchronises the host with the device
+ *     and no call allocates device memory; scratch memory is the caller's
+ *     workspace.  The enqueued work can be captured in a CUDA graph.
+ *   - On a validation error nothing is launched and a negative lmoe_status is
+ *     returned.  A zero-sized problem (T == 0, N == 0, E == 0) returns LMOE_OK
+ *     and launches nothing.
+ *   - bf16 values are carried as raw 16-bit patterns (lmoe_bf16).
+ *   - Internal waits in the tensor-core kernels are bounded; if one ever gives
+ *     up, the kernel records a code in a device error word and returns early
+ *     (its outputs are then undefined).  lmoe_device_error() reads that word.
+ */
+#ifndef LMOE_H
+#define LMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LMOE_OK = 0,
+  LMOE_ERR_NULL = -1,        /* a required pointer is NULL                     */
+  LMOE_ERR_DIM = -2,         /* a size is out of range or not a supported multiple */
+  LMOE_ERR_UNSUPPORTED = -3, /* n_group/topk_group other than 1                 */
+  LMOE_ERR_BETA = -4,        /* beta <= 0 or not finite                         */
+  LMOE_ERR_WORKSPACE = -5,   /* workspace NULL or smaller than required         */
+  LMOE_ERR_CUDA = -6,        /* a CUDA runtime/driver call failed               */
+  LMOE_ERR_ALIGN = -7        /* a pointer is not 16-byte aligned                */
+} lmoe_status;
+
+typedef uint16_t lmoe_bf16;
+
+/* ------------------------------------------------------------------------ */
+/* Routing: [vLLM-50088] commit 1 (single-group fast path of grouped top-k:   */
+/* with n_group == 1 and topk_group == 1 it is plain top-k over all experts) */
+/* and commit 4 (DeepSeekV3 routing on FP32 logits).                          */
+/*                                                                            */
+/*   s[t,e]   = sigmoid(router_logits[t,e])  (fp32, a fixed IEEE operation     */
+/*              sequence so that the selection is reproducible to the bit)    */
+/*   key[t,e] = s[t,e] + e_score_correction_bias[e]    (selection only)       */
+/*   topk_ids[t,:]     = the topk experts of largest key, in descending key    */
+/*                       order; equal keys go to the lower expert index        */
+/*   topk_weights[t,j] = s[t,ids_j] / sum_j s[t,ids_j] * routed_scaling_factor */
+/*                       (without the division when renormalize == 0)          */
+/*                                                                            */
+/* router_logits [T,E] fp32; e_score_correction_bias [E] fp32 or NULL (zero); */
+/* topk_ids [T,topk] int32 and topk_weights [T,topk] fp32 are outputs.         */
+/* Limits: 1 <= E <= 1024, 1 <= topk <= min(E, 32), n_group == topk_group == 1 */
+/* (else LMOE_ERR_UNSUPPORTED).  NaN logits are not supported.                */
+/* ------------------------------------------------------------------------ */
+int moe_route(const float* router_logits, const float* e_score_correction_bias,
+              int T, int E, int topk, int n_group, int topk_group,
+              int renormalize, float routed_scaling_factor,
+              int32_t* topk_ids, float* topk_weights, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* SituGLU: [vLLM-50088] commit 2 (formula, dense and masked kernels, fp32   */
+/* arithmetic, written straight to the output) and commit 3 (beta required;  */
+/* linear_beta <= 0 means unset and up passes through).                       */
+/*                                                                            */
+/*   gate_out = beta * tanh(gate / beta) * sigmoid(gate)                      */
+/*   up_out   = linear_beta * tanh(up / linear_beta)   if linear_beta > 0     */
+/*            = up                                      otherwise             */
+/*   out      = gate_out * up_out                                             */
+/*                                                                            */
+/* situ_and_mul: in [N, 2d] bf16 with gate = in[:, :d], up = in[:, d:];      */
+/* out [N, d] bf16.  Requires d % 8 == 0.  beta <= 0 -> LMOE_ERR_BETA.        */
+/* ------------------------------------------------------------------------ */
+int situ_and_mul(const lmoe_bf16* in, lmoe_bf16* out, int64_t N, int d,
+                 float beta, float linear_beta, void* stream);
+
+/* masked_situ_and_mul: batched MoE layout.  in [E, T_max, 2d] bf16, out      */
+/* [E, T_max, d] bf16, expert_num_tokens [E] int32 on the device.  Row t of   */
+/* expert e is computed iff t < expert_num_tokens[e]; every other output row  */
+/* is left untouched (its bytes are never written).  Counts outside           */
+/* [0, T_max] are clamped to that range on the device.  Requires d % 8 == 0.  */
+int masked_situ_and_mul(const lmoe_bf16* in, lmoe_bf16* out,
+                        const int32_t* expert_num_tokens, int E, int T_max,
+                        int d, float beta, float linear_beta, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* The latent-MoE layer forward on one GPU: [vLLM-runner] _fused_forward and */
+/* _shard_up_proj_tail, [vLLM-50088] commits 1-3 and 7, [TRTLLM-20541]       */
+/* Commit 2 (decode order).                                                   */
+/*                                                                            */
+/*   ids, w = moe_route(router_logits)                                        */
+/*   Z      = bf16(hidden W_down^T)                          [T, latent]       */
+/*   rows   = (token, slot) pairs grouped by expert, tokens ascending         */
+/*   per expert e:  G = bf16(Z W13_e^T)                      [n_e, 2*inter]     */
+/*                  A = bf16(SituGLU(G))                     [n_e, inter]       */
+/*                  Y = bf16(A W2_e^T)                       [n_e, latent]      */
+/*   C[t]   = sum_j w[t,j] * Y[row(t,j)]      (fp32, the complete routed sum)  */
+/*   N      = bf16(C / sqrt(mean(C^2) + rms_eps) * norm_w)                     */
+/*   Sh     = bf16(bf16(SituGLU(bf16(hidden Ws13^T))) Ws2^T)  shared expert    */
+/*   out    = bf16(N W_up^T + Sh)                (Sh added in the GEMM epilogue) */
+/*                                                                            */
+/* Limits: hidden % 128 == 0, latent % 128 == 0, inter % 64 == 0,             */
+/* shared_inter % 64 == 0 (when the shared expert is present), the routing    */
+/* limits above, T >= 0.                                                      */
+/* ------------------------------------------------------------------------ */
+typedef struct lmoe_dims {
+  int T;                 /* tokens                                           */
+  int hidden;            /* H                                                */
+  int latent;            /* L                                                */
+  int num_experts;       /* E                                                */
+  int topk;              /* k                                                */
+  int inter;             /* d: per-expert intermediate size                  */
+  int shared_inter;      /* ds: shared-expert intermediate size              */
+  int n_group;           /* must be 1                                        */
+  int topk_group;        /* must be 1                                        */
+  int renormalize;       /* 1: w = s / sum(s) * rsf;  0: w = s * rsf          */
+  float routed_scaling_factor;
+  float beta;            /* SituGLU beta (> 0)                               */
+  float linear_beta;     /* SituGLU linear_beta (<= 0: unset)                */
+  float rms_eps;         /* RMSNorm epsilon (inside the square root)         */
+} lmoe_dims;
+
+typedef struct lmoe_weights {
+  const lmoe_bf16* w_down;  /* [L, H]                                        */
+  const lmoe_bf16* w13;     /* [E, 2d, L]: rows 0..d-1 gate, d..2d-1 up       */
+  const lmoe_bf16* w2;      /* [E, L, d]                                     */
+  const lmoe_bf16* ws13;    /* [2ds, H] or NULL (no shared expert)           */
+  const lmoe_bf16* ws2;     /* [H, ds] (NULL iff ws13 is NULL)                */
+  const lmoe_bf16* norm_w;  /* [L] RMSNorm gamma, or NULL (= ones)           */
+  const lmoe_bf16* w_up;    /* [H, L]                                        */
+  const float* e_score_correction_bias; /* [E] or NULL (= zeros)             */
+} lmoe_weights;
+
+/* Optional copies of the layer's routing and permutation (any may be NULL). */
+typedef struct lmoe_debug {
+  int32_t* topk_ids;          /* [T, k]                                      */
+  float* topk_weights;        /* [T, k]                                      */
+  int32_t* expert_num_tokens; /* [E]                                         */
+  int32_t* expert_offsets;    /* [E+1]: expert e owns rows off[e]..off[e+1]-1 */
+  int32_t* row_of;            /* [T, k]: permuted row of (token, slot)       */
+} lmoe_debug;
+
+/* Bytes of device workspace latent_moe_forward needs for these dims (0 on   */
+/* invalid dims).  Depends on the dims only.                                  */
+size_t latent_moe_workspace_bytes(const lmoe_dims* dims);
+
+/* hidden [T, H] bf16, router_logits [T, E] fp32, out [T, H] bf16; workspace  */
+/* at least latent_moe_workspace_bytes(dims) bytes, 256-byte aligned, not     */
+/* shared with a concurrent call.  dbg may be NULL.                           */
+int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* weights,
+                       const lmoe_bf16* hidden, const float* router_logits,
+                       lmoe_bf16* out, void* workspace, size_t workspace_bytes,
+                       const lmoe_debug* dbg, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Utilities                                                                  */
+/* ------------------------------------------------------------------------ */
+/* Static description of a status code (never NULL).                         */
+const char* lmoe_status_string(int status);
+
+/* Reads (and with clear != 0 resets) the device error word of the current    */
+/* device.  0 = no bounded wait has given up.  Synchronises the device.      */
+/* Returns the word, or LMOE_ERR_CUDA if it cannot be read.                   */
+int lmoe_device_error(int clear);
+
+/* ABI version of this header (major * 100 + minor).                          */
+int lmoe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LMOE_H */

@@ -1,0 +1,74 @@
+"""Planted mistakes: each plausible bug, put into the oracle on the CPU, must be
+caught by one of the pins.  This shows the pins bite."""
+import numpy as np
+import pytest
+
+from oracle import lmoe_oracle as O
+import tests.test_oracle_numerics as N
+import tests.test_oracle_route as R
+import tests.test_oracle_layer as L
+
+_route = O.route
+_situ = O.situ
+_permute = O.permute
+
+
+def _situ_no_sigmoid(g, u, beta, lb):
+    up = lb * np.tanh(u / lb) if lb > 0 else u
+    return beta * np.tanh(g / beta) * up
+
+
+def _situ_and_mul_swapped(x_bits, beta, lb):
+    x = O.bf16_to_f64(x_bits)
+    d = x.shape[-1] // 2
+    return O.f64_to_bf16_bits(_situ(x[..., d:], x[..., :d], beta, lb))
+
+
+def _route_no_bias(logits, bias, *a, **k):
+    return _route(logits, None, *a, **k)
+
+
+def _route_weights_from_keys(logits, bias, topk, rsf, *a, **k):
+    ids, _ = _route(logits, bias, topk, rsf, *a, **k)
+    key = (O.sigmoid_f32(logits) + (0 if bias is None else bias)).astype(np.float64)
+    w = np.take_along_axis(key, ids.astype(np.int64), 1)
+    return ids, w / w.sum(1, keepdims=True) * rsf
+
+
+def _route_not_renormalised(logits, bias, topk, rsf, renormalize=1, *a, **k):
+    return _route(logits, bias, topk, rsf, 0, *a, **k)
+
+
+def _route_weights_reversed(*a, **k):
+    ids, w = _route(*a, **k)
+    return ids, w[:, ::-1].copy()
+
+
+def _rms_norm_over_tokens(x, gamma, eps):
+    return x / np.sqrt(np.mean(x * x, axis=0, keepdims=True) + eps) * gamma
+
+
+def _permute_descending(ids, E):
+    counts, offsets, row_of, tok_of_row = _permute(ids[::-1].copy(), E)
+    return counts, offsets, row_of[::-1].copy(), (ids.shape[0] - 1 - tok_of_row).astype(np.int32)
+
+
+MUTATIONS = [
+    ("situ", _situ_no_sigmoid, N.test_situ_large_beta_is_silu_gated_and_up_passes_through),
+    ("situ_and_mul", _situ_and_mul_swapped, N.test_situ_and_mul_gate_is_first_half),
+    ("route", _route_no_bias, R.check_equal_logits_bias_decides),
+    ("route", _route_weights_from_keys, R.check_equal_logits_bias_decides),
+    ("route", _route_not_renormalised, L.check_identical_experts_reduce_to_dense_mlp),
+    ("route", _route_weights_reversed, L.check_power_of_two_scaled_experts),
+    ("rms_norm", _rms_norm_over_tokens, L.check_token_independence),
+    ("permute", _permute_descending, lambda: R.check_permute(
+        np.stack([np.random.default_rng(t).permutation(16)[:3] for t in range(20)]).astype(np.int32), 16)),
+]
+
+
+@pytest.mark.parametrize("name,bad,check", MUTATIONS,
+                         ids=[f"{m[0]}:{m[1].__name__}" for m in MUTATIONS])
+def test_planted_mistake_is_caught(monkeypatch, name, bad, check):
+    monkeypatch.setattr(O, name, bad)
+    with pytest.raises(AssertionError):
+        check()
