@@ -168,6 +168,18 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* weights,
                        const lmoe_debug* dbg, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Dense linear layer on the same tensor-core GEMM engine (the up-projection */
+/* with its shared-output add, [vLLM-runner] _shard_up_proj_tail:             */
+/* hidden_shard.addmm_(latent, up_proj_shard.t())):                           */
+/*   out[t, n] = bf16( sum_c x[t, c] * w[n, c]  (+ add[t, n]) )                */
+/* x [T, K] bf16, w [N, K] bf16 (PyTorch Linear layout), add [T, N] bf16 or  */
+/* NULL, out [T, N] bf16.  fp32 accumulation, one rounding.  Requires          */
+/* K % 64 == 0, N % 128 == 0, T >= 0.  No workspace (no split K).             */
+/* ------------------------------------------------------------------------ */
+int lmoe_linear(const lmoe_bf16* x, const lmoe_bf16* w, const lmoe_bf16* add, lmoe_bf16* out,
+                int T, int N, int K, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Utilities                                                                  */
 /* ------------------------------------------------------------------------ */
 /* Static description of a status code (never NULL).                         */

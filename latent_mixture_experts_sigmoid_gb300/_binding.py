@@ -1,0 +1,213 @@
+"""Thin ctypes binding of liblmoe.so (include/lmoe.h).
+
+Argument marshalling only: torch tensors supply device pointers and the
+current CUDA stream; every step of the computation runs in the library's CUDA
+kernels.  There is no CPU fallback: if the library is missing or a call fails,
+an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "liblmoe.so")
+
+LMOE_OK = 0
+LMOE_ERR_NULL = -1
+LMOE_ERR_DIM = -2
+LMOE_ERR_UNSUPPORTED = -3
+LMOE_ERR_BETA = -4
+LMOE_ERR_WORKSPACE = -5
+LMOE_ERR_CUDA = -6
+LMOE_ERR_ALIGN = -7
+
+ABI_FUNCTIONS = ("moe_route", "situ_and_mul", "masked_situ_and_mul", "latent_moe_forward",
+                 "latent_moe_workspace_bytes", "lmoe_linear", "lmoe_status_string",
+                 "lmoe_device_error", "lmoe_abi_version")
+
+
+class LmoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class LmoeDims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("hidden", ctypes.c_int), ("latent", ctypes.c_int),
+                ("num_experts", ctypes.c_int), ("topk", ctypes.c_int), ("inter", ctypes.c_int),
+                ("shared_inter", ctypes.c_int), ("n_group", ctypes.c_int),
+                ("topk_group", ctypes.c_int), ("renormalize", ctypes.c_int),
+                ("routed_scaling_factor", ctypes.c_float), ("beta", ctypes.c_float),
+                ("linear_beta", ctypes.c_float), ("rms_eps", ctypes.c_float)]
+
+
+class LmoeWeights(ctypes.Structure):
+    _fields_ = [("w_down", ctypes.c_void_p), ("w13", ctypes.c_void_p), ("w2", ctypes.c_void_p),
+                ("ws13", ctypes.c_void_p), ("ws2", ctypes.c_void_p), ("norm_w", ctypes.c_void_p),
+                ("w_up", ctypes.c_void_p), ("e_score_correction_bias", ctypes.c_void_p)]
+
+
+class LmoeDebug(ctypes.Structure):
+    _fields_ = [("topk_ids", ctypes.c_void_p), ("topk_weights", ctypes.c_void_p),
+                ("expert_num_tokens", ctypes.c_void_p), ("expert_offsets", ctypes.c_void_p),
+                ("row_of", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load liblmoe.so once; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(f"liblmoe.so not built at {p}; run __graft_entry__.build() "
+                          "or python -m latent_mixture_experts_sigmoid_gb300.build")
+    lib = ctypes.CDLL(p)
+    vp, i32, f32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int64
+    lib.moe_route.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, vp, vp]
+    lib.moe_route.restype = i32
+    lib.situ_and_mul.argtypes = [vp, vp, i64, i32, f32, f32, vp]
+    lib.situ_and_mul.restype = i32
+    lib.masked_situ_and_mul.argtypes = [vp, vp, vp, i32, i32, i32, f32, f32, vp]
+    lib.masked_situ_and_mul.restype = i32
+    lib.latent_moe_workspace_bytes.argtypes = [ctypes.POINTER(LmoeDims)]
+    lib.latent_moe_workspace_bytes.restype = ctypes.c_size_t
+    lib.latent_moe_forward.argtypes = [ctypes.POINTER(LmoeDims), ctypes.POINTER(LmoeWeights), vp,
+                                       vp, vp, vp, ctypes.c_size_t, ctypes.POINTER(LmoeDebug), vp]
+    lib.latent_moe_forward.restype = i32
+    lib.lmoe_linear.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
+    lib.lmoe_linear.restype = i32
+    lib.lmoe_status_string.argtypes = [i32]
+    lib.lmoe_status_string.restype = ctypes.c_char_p
+    lib.lmoe_device_error.argtypes = [i32]
+    lib.lmoe_device_error.restype = i32
+    lib.lmoe_abi_version.argtypes = []
+    lib.lmoe_abi_version.restype = i32
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().lmoe_status_string(int(status)).decode()
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        if torch.cuda.is_available():
+            return torch.cuda.current_stream().cuda_stream
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, what: str) -> None:
+    if status != LMOE_OK:
+        raise LmoeError(status, what)
+
+
+def moe_route(router_logits, e_score_correction_bias, topk: int, routed_scaling_factor: float,
+              topk_ids, topk_weights, renormalize: int = 1, n_group: int = 1,
+              topk_group: int = 1, stream=None, T: int | None = None, E: int | None = None):
+    """Single-group sigmoid top-k routing; writes topk_ids [T,k] and topk_weights [T,k]."""
+    if T is None:
+        T, E = router_logits.shape
+    st = load_library().moe_route(_ptr(router_logits), _ptr(e_score_correction_bias), int(T),
+                                  int(E), int(topk), int(n_group), int(topk_group),
+                                  int(renormalize), float(routed_scaling_factor), _ptr(topk_ids),
+                                  _ptr(topk_weights), _stream(stream))
+    _check(st, "moe_route")
+
+
+def situ_and_mul(inp, out, beta: float, linear_beta: float, stream=None,
+                 N: int | None = None, d: int | None = None):
+    """SituGLU over a dense [N, 2d] bf16 tensor into out [N, d]."""
+    if N is None:
+        d = inp.shape[-1] // 2
+        N = inp.numel() // (2 * d)
+    st = load_library().situ_and_mul(_ptr(inp), _ptr(out), int(N), int(d), float(beta),
+                                      float(linear_beta), _stream(stream))
+    _check(st, "situ_and_mul")
+
+
+def masked_situ_and_mul(inp, out, expert_num_tokens, beta: float, linear_beta: float,
+                        stream=None, shape: tuple | None = None):
+    """SituGLU over the batched [E, T_max, 2d] layout; padded rows untouched."""
+    E, T_max, two_d = shape if shape is not None else tuple(inp.shape)
+    st = load_library().masked_situ_and_mul(_ptr(inp), _ptr(out), _ptr(expert_num_tokens),
+                                            int(E), int(T_max), int(two_d // 2), float(beta),
+                                            float(linear_beta), _stream(stream))
+    _check(st, "masked_situ_and_mul")
+
+
+def make_dims(d) -> LmoeDims:
+    """LmoeDims from any object with the lmoe_dims field names."""
+    return LmoeDims(int(d.T), int(d.hidden), int(d.latent), int(d.num_experts), int(d.topk),
+                    int(d.inter), int(d.shared_inter), int(d.n_group), int(d.topk_group),
+                    int(d.renormalize), float(d.routed_scaling_factor), float(d.beta),
+                    float(d.linear_beta), float(d.rms_eps))
+
+
+def make_weights(w: dict) -> LmoeWeights:
+    g = lambda k: _ptr(w.get(k))  # noqa: E731
+    return LmoeWeights(g("w_down"), g("w13"), g("w2"), g("ws13"), g("ws2"), g("norm_w"),
+                       g("w_up"), g("bias"))
+
+
+def latent_moe_workspace_bytes(dims) -> int:
+    dd = dims if isinstance(dims, LmoeDims) else make_dims(dims)
+    return int(load_library().latent_moe_workspace_bytes(ctypes.byref(dd)))
+
+
+def latent_moe_forward(dims, weights, hidden, router_logits, out, workspace,
+                       workspace_bytes: int | None = None, debug: dict | None = None,
+                       stream=None):
+    """The latent-MoE layer forward; writes out [T, hidden] bf16."""
+    dd = dims if isinstance(dims, LmoeDims) else make_dims(dims)
+    ww = weights if isinstance(weights, LmoeWeights) else make_weights(weights)
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    dbg = None
+    if debug:
+        dbg = LmoeDebug(_ptr(debug.get("topk_ids")), _ptr(debug.get("topk_weights")),
+                        _ptr(debug.get("expert_num_tokens")), _ptr(debug.get("expert_offsets")),
+                        _ptr(debug.get("row_of")))
+    st = load_library().latent_moe_forward(ctypes.byref(dd), ctypes.byref(ww), _ptr(hidden),
+                                           _ptr(router_logits), _ptr(out), _ptr(workspace),
+                                           int(workspace_bytes),
+                                           ctypes.byref(dbg) if dbg is not None else None,
+                                           _stream(stream))
+    _check(st, "latent_moe_forward")
+
+
+def lmoe_linear(x, w, out, add=None, stream=None, T: int | None = None, N: int | None = None,
+                K: int | None = None):
+    """out [T,N] = bf16(x [T,K] @ w [N,K]^T (+ add)) on the tensor-core GEMM."""
+    if T is None:
+        T, K = x.shape
+        N = w.shape[0]
+    st = load_library().lmoe_linear(_ptr(x), _ptr(w), _ptr(add), _ptr(out), int(T), int(N),
+                                    int(K), _stream(stream))
+    _check(st, "lmoe_linear")
+
+
+def lmoe_device_error(clear: bool = False) -> int:
+    return int(load_library().lmoe_device_error(1 if clear else 0))
+
+
+def lmoe_abi_version() -> int:
+    return int(load_library().lmoe_abi_version())

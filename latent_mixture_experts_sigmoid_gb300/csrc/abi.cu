@@ -1,0 +1,428 @@
+// The C ABI of liblmoe.so (declared in include/lmoe.h): argument validation,
+// the workspace layout and the schedule of kernels of one layer forward.
+//
+// Layer schedule (one stream, no host synchronisation), following the data
+// flow of the vLLM latent_moe_runner page (ROCmLatentMoERunner._fused_forward
+// and _shard_up_proj_tail) on one device, with the decode order of
+// TensorRT-LLM PR #20541, Commit 2:
+//   1 route             ids, w                        (routing kernel)
+//   2 down-projection   Z = X W_down^T                (tcgen05 GEMM)
+//   3 permute           counts, offsets, row_of       (bitmap counting sort)
+//   4 scatter           A[row_of[t,j]] = bf16(Z[t])
+//   5 GEMM1 (grouped)   G = A W13_e^T                 (tcgen05 GEMM)
+//   6 SituGLU           act = SituGLU(G)
+//   7 GEMM2 (grouped)   Y = act W2_e^T                (tcgen05 GEMM)
+//   8 combine + norm    N = RMSNorm(sum_j w Y) * gamma
+//   9 shared GEMM1      Gs = X Ws13^T                 (tcgen05 GEMM)
+//  10 SituGLU           As = SituGLU(Gs)
+//  11 shared GEMM2      Sh = As Ws2^T                 (tcgen05 GEMM)
+//  12 up-projection     out = N W_up^T + Sh           (tcgen05 GEMM, Sh added
+//                                                      in the epilogue)
+// Two regimes.  Small T (<= 128 tokens, decode): every GEMM puts the weight
+// rows on the MMA's M side and the tokens on N (16..128), dense GEMMs split K
+// so that all SMs stream weights, and the split partials are summed in a fixed
+// order by the consumer (the scatter of step 4, the SituGLU of step 10, and
+// the final reduction that also adds Sh).  Large T (prefill): tokens on M,
+// 128 x (128|256) tiles, no split, bf16 stored straight from the epilogue.
+#include <math.h>
+#include <string.h>
+
+#include "gemm_tc.cuh"
+#include "lmoe_internal.cuh"
+#include "moe_data.cuh"
+
+namespace lmoe {
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kNumSmsDefault;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = kNumSmsDefault;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+namespace {
+
+constexpr int kDecodeMaxT = 128;
+constexpr int kMaxSplits = 32;
+
+bool finite_pos(float x) { return isfinite(x) && x > 0.0f; }
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+struct DenseCfg {
+  int tok_on_m, bn, splits;
+};
+
+// Split count minimising the modelled makespan in K blocks (one unit of
+// per-tile overhead), for `tiles` output tiles of `nkb` K blocks each.
+int choose_splits(int tiles, int nkb, int nsm) {
+  int best = 1;
+  long long best_cost = -1;
+  for (int s = 1; s <= kMaxSplits && s <= nkb; ++s) {
+    const long long waves = ((long long)tiles * s + nsm - 1) / nsm;
+    const long long cost = waves * ((nkb + s - 1) / s + 1);
+    if (best_cost < 0 || cost < best_cost) { best = s; best_cost = cost; }
+  }
+  return best;
+}
+
+DenseCfg dense_cfg(int T, int M_feat, int K, int nsm) {
+  DenseCfg c;
+  if (T <= kDecodeMaxT) {
+    c.tok_on_m = 0;
+    c.bn = round_up(T, 16);
+    const int tiles = M_feat / 128;
+    c.splits = choose_splits(tiles, K / 64, nsm);
+  } else {
+    c.tok_on_m = 1;
+    c.bn = (M_feat % 256 == 0) ? 256 : 128;
+    c.splits = 1;
+  }
+  return c;
+}
+
+// Workspace carving (256-byte aligned pieces).
+struct Carver {
+  size_t off = 0;
+  char* base = nullptr;
+  template <typename T>
+  T* take(size_t count) {
+    off = (off + 255) & ~size_t(255);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+struct Ws {
+  int32_t* ids; float* w;
+  int32_t* counts; int32_t* offsets; int32_t* tile_prefix; int32_t* row_of; int32_t* tok_of_row;
+  void* perm_scratch;
+  uint16_t *Z, *A, *G, *act, *Y, *N, *Gs, *As, *Sh;
+  float *Pa, *Pb;
+};
+
+size_t carve(const lmoe_dims& d, char* base, Ws* ws) {
+  Carver c;
+  c.base = base;
+  const size_t T = d.T, k = d.topk, E = d.num_experts, L = d.latent, H = d.hidden;
+  const size_t dI = d.inter, ds = d.shared_inter > 0 ? d.shared_inter : 0;
+  Ws w{};
+  w.ids = c.take<int32_t>(T * k);
+  w.w = c.take<float>(T * k);
+  w.counts = c.take<int32_t>(E);
+  w.offsets = c.take<int32_t>(E + 1);
+  w.tile_prefix = c.take<int32_t>(E + 1);
+  w.row_of = c.take<int32_t>(T * k);
+  w.tok_of_row = c.take<int32_t>(T * k);
+  w.perm_scratch = c.take<char>(permute_scratch_bytes(d.T, d.num_experts));
+  w.Z = c.take<uint16_t>(T * L);
+  w.A = c.take<uint16_t>(T * k * L);
+  w.G = c.take<uint16_t>(T * k * 2 * dI);
+  w.act = c.take<uint16_t>(T * k * dI);
+  w.Y = c.take<uint16_t>(T * k * L);
+  w.N = c.take<uint16_t>(T * L);
+  w.Gs = c.take<uint16_t>(T * 2 * ds);
+  w.As = c.take<uint16_t>(T * ds);
+  w.Sh = c.take<uint16_t>(T * H);
+  if (d.T <= kDecodeMaxT) {
+    const size_t ma = L > H ? L : H;
+    const size_t mb = (2 * ds > H) ? 2 * ds : H;
+    w.Pa = c.take<float>((size_t)kMaxSplits * T * ma);
+    w.Pb = c.take<float>((size_t)kMaxSplits * T * mb);
+  } else {
+    w.Pa = w.Pb = nullptr;
+  }
+  if (ws) *ws = w;
+  return (c.off + 255) & ~size_t(255);
+}
+
+int validate_dims(const lmoe_dims* d) {
+  if (!d) return LMOE_ERR_NULL;
+  if (d->T < 0) return LMOE_ERR_DIM;
+  if (d->n_group != 1 || d->topk_group != 1) return LMOE_ERR_UNSUPPORTED;
+  if (d->num_experts < 1 || d->num_experts > 1024) return LMOE_ERR_DIM;
+  if (d->topk < 1 || d->topk > d->num_experts || d->topk > 32) return LMOE_ERR_DIM;
+  if (d->hidden <= 0 || d->hidden % 128 || d->latent <= 0 || d->latent % 128 ||
+      d->latent > 8192 || d->inter <= 0 || d->inter % 64)
+    return LMOE_ERR_DIM;
+  if (d->shared_inter < 0 || d->shared_inter % 64) return LMOE_ERR_DIM;
+  if (!finite_pos(d->beta)) return LMOE_ERR_BETA;
+  if (!isfinite(d->linear_beta) || !isfinite(d->routed_scaling_factor) || !isfinite(d->rms_eps) ||
+      d->rms_eps < 0.0f)
+    return LMOE_ERR_DIM;
+  if ((long long)d->T * d->topk * (long long)(2 * d->inter > d->latent ? 2 * d->inter : d->latent) >
+      (1ll << 40))
+    return LMOE_ERR_DIM;
+  return LMOE_OK;
+}
+
+cudaError_t gemm_dense(const uint16_t* W, int M_feat, const uint16_t* X, int T, int K,
+                       const DenseCfg& c, void* out, int out_fp32, long long split_stride,
+                       const uint16_t* add, cudaStream_t s) {
+  GemmDesc g{};
+  g.W = W;
+  g.X = X;
+  g.x_rows = T;
+  g.K = K;
+  g.M_feat = M_feat;
+  g.G = 1;
+  g.T_dense = T;
+  g.tok_on_m = c.tok_on_m;
+  g.bn = c.bn;
+  g.splits = c.splits;
+  g.out = out;
+  g.ldo = M_feat;
+  g.out_fp32 = out_fp32;
+  g.split_stride = split_stride;
+  g.add = add;
+  const int tok_tile = c.tok_on_m ? 128 : c.bn;
+  const int feat_tile = c.tok_on_m ? c.bn : 128;
+  g.max_units = ((T + tok_tile - 1) / tok_tile) * (M_feat / feat_tile) * c.splits;
+  return launch_gemm(g, s);
+}
+
+cudaError_t gemm_grouped(const uint16_t* W, int E, int M_feat, const uint16_t* X, long long rows,
+                         int K, int tok_on_m, int bn, const Ws& ws, int tile, void* out,
+                         cudaStream_t s) {
+  GemmDesc g{};
+  g.W = W;
+  g.X = X;
+  g.x_rows = rows;
+  g.K = K;
+  g.M_feat = M_feat;
+  g.G = E;
+  g.grp_count = ws.counts;
+  g.grp_offset = ws.offsets;
+  g.tile_prefix = ws.tile_prefix;
+  g.tok_on_m = tok_on_m;
+  g.bn = bn;
+  g.splits = 1;
+  g.out = out;
+  g.ldo = M_feat;
+  const int feat_tile = tok_on_m ? bn : 128;
+  const long long nonempty = rows < E ? rows : E;
+  g.max_units = (int)(((rows + tile - 1) / tile + nonempty) * (M_feat / feat_tile));
+  return launch_gemm(g, s);
+}
+
+#define LMOE_TRY(x)                                  \
+  do {                                               \
+    if ((x) != cudaSuccess) return LMOE_ERR_CUDA;    \
+  } while (0)
+
+}  // namespace
+}  // namespace lmoe
+
+using namespace lmoe;
+
+extern "C" {
+
+int lmoe_abi_version(void) { return 100; }
+
+const char* lmoe_status_string(int status) {
+  switch (status) {
+    case LMOE_OK: return "ok";
+    case LMOE_ERR_NULL: return "a required pointer is NULL";
+    case LMOE_ERR_DIM: return "a size is out of range or not a supported multiple";
+    case LMOE_ERR_UNSUPPORTED: return "unsupported routing mode (n_group/topk_group must be 1)";
+    case LMOE_ERR_BETA: return "SituGLU beta must be finite and > 0";
+    case LMOE_ERR_WORKSPACE: return "workspace is NULL, misaligned or too small";
+    case LMOE_ERR_CUDA: return "a CUDA call failed";
+    case LMOE_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    default: return "unknown status";
+  }
+}
+
+int lmoe_device_error(int clear) { return read_device_error(clear); }
+
+int moe_route(const float* router_logits, const float* bias, int T, int E, int topk, int n_group,
+              int topk_group, int renormalize, float rsf, int32_t* topk_ids, float* topk_weights,
+              void* stream) {
+  if (n_group != 1 || topk_group != 1) return LMOE_ERR_UNSUPPORTED;
+  if (T < 0 || E < 1 || E > 1024 || topk < 1 || topk > E || topk > 32) return LMOE_ERR_DIM;
+  if (!isfinite(rsf)) return LMOE_ERR_DIM;
+  if (T == 0) return LMOE_OK;
+  if (!router_logits || !topk_ids || !topk_weights) return LMOE_ERR_NULL;
+  if (!aligned16(router_logits) || !aligned16(topk_ids) || !aligned16(topk_weights) ||
+      (bias && !aligned16(bias)))
+    return LMOE_ERR_ALIGN;
+  if (launch_route(router_logits, bias, T, E, topk, renormalize, rsf, topk_ids, topk_weights,
+                   (cudaStream_t)stream) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  return LMOE_OK;
+}
+
+int situ_and_mul(const lmoe_bf16* in, lmoe_bf16* out, int64_t N, int d, float beta,
+                 float linear_beta, void* stream) {
+  if (!finite_pos(beta)) return LMOE_ERR_BETA;
+  if (N < 0 || d <= 0 || d % 8 || !isfinite(linear_beta)) return LMOE_ERR_DIM;
+  if (N == 0) return LMOE_OK;
+  if (!in || !out) return LMOE_ERR_NULL;
+  if (!aligned16(in) || !aligned16(out)) return LMOE_ERR_ALIGN;
+  if (launch_situ(in, out, N, d, beta, linear_beta, (cudaStream_t)stream) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  return LMOE_OK;
+}
+
+int masked_situ_and_mul(const lmoe_bf16* in, lmoe_bf16* out, const int32_t* expert_num_tokens,
+                        int E, int T_max, int d, float beta, float linear_beta, void* stream) {
+  if (!finite_pos(beta)) return LMOE_ERR_BETA;
+  if (E < 0 || E > 65535 || T_max < 0 || d <= 0 || d % 8 || !isfinite(linear_beta))
+    return LMOE_ERR_DIM;
+  if (E == 0 || T_max == 0) return LMOE_OK;
+  if (!in || !out || !expert_num_tokens) return LMOE_ERR_NULL;
+  if (!aligned16(in) || !aligned16(out) || !aligned16(expert_num_tokens)) return LMOE_ERR_ALIGN;
+  if (launch_masked_situ(in, out, expert_num_tokens, E, T_max, d, beta, linear_beta,
+                         (cudaStream_t)stream) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  return LMOE_OK;
+}
+
+int lmoe_linear(const lmoe_bf16* x, const lmoe_bf16* w, const lmoe_bf16* add, lmoe_bf16* out,
+                int T, int N, int K, void* stream) {
+  if (T < 0 || N <= 0 || N % 128 || K <= 0 || K % 64) return LMOE_ERR_DIM;
+  if (T == 0) return LMOE_OK;
+  if (!x || !w || !out) return LMOE_ERR_NULL;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(out) || (add && !aligned16(add)))
+    return LMOE_ERR_ALIGN;
+  DenseCfg c = dense_cfg(T, N, K, num_sms());
+  c.splits = 1;
+  if (gemm_dense(w, N, x, T, K, c, out, 0, 0, add, (cudaStream_t)stream) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  return LMOE_OK;
+}
+
+size_t latent_moe_workspace_bytes(const lmoe_dims* dims) {
+  if (validate_dims(dims) != LMOE_OK) return 0;
+  return carve(*dims, nullptr, nullptr);
+}
+
+int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe_bf16* hidden,
+                       const float* router_logits, lmoe_bf16* out, void* workspace,
+                       size_t workspace_bytes, const lmoe_debug* dbg, void* stream) {
+  const int v = validate_dims(dims);
+  if (v != LMOE_OK) return v;
+  if (!wt) return LMOE_ERR_NULL;
+  const lmoe_dims d = *dims;
+  if (d.T == 0) return LMOE_OK;
+  if (!hidden || !router_logits || !out || !wt->w_down || !wt->w13 || !wt->w2 || !wt->w_up)
+    return LMOE_ERR_NULL;
+  const bool shared = wt->ws13 != nullptr;
+  if (shared != (wt->ws2 != nullptr)) return LMOE_ERR_NULL;
+  if (shared && d.shared_inter <= 0) return LMOE_ERR_DIM;
+  const void* ptrs[] = {hidden, router_logits, out, wt->w_down, wt->w13, wt->w2, wt->w_up,
+                        wt->ws13, wt->ws2, wt->norm_w, wt->e_score_correction_bias};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return LMOE_ERR_ALIGN;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return LMOE_ERR_WORKSPACE;
+  Ws ws;
+  const size_t need = carve(d, static_cast<char*>(workspace), &ws);
+  if (workspace_bytes < need) return LMOE_ERR_WORKSPACE;
+  if (dbg) {
+    const void* dp[] = {dbg->topk_ids, dbg->topk_weights, dbg->expert_num_tokens,
+                        dbg->expert_offsets, dbg->row_of};
+    for (const void* p : dp)
+      if (p && !aligned16(p)) return LMOE_ERR_ALIGN;
+  }
+
+  cudaStream_t s = (cudaStream_t)stream;
+  const int T = d.T, k = d.topk, E = d.num_experts, H = d.hidden, L = d.latent;
+  const int dI = d.inter, ds = d.shared_inter;
+  const long long rows = (long long)T * k;
+  const int nsm = num_sms();
+  const bool decode = T <= kDecodeMaxT;
+  const int tile = decode ? round_up(T, 16) : 128;   // token tile of the grouped GEMMs
+  const uint16_t* X = hidden;
+
+  // 1. routing
+  LMOE_TRY(launch_route(router_logits, wt->e_score_correction_bias, T, E, k, d.renormalize,
+                        d.routed_scaling_factor, ws.ids, ws.w, s));
+  // 2. latent down-projection
+  const DenseCfg cdown = dense_cfg(T, L, H, nsm);
+  const bool down_split = cdown.splits > 1;
+  const long long down_stride = (long long)T * L;
+  LMOE_TRY(gemm_dense(wt->w_down, L, X, T, H, cdown, down_split ? (void*)ws.Pa : (void*)ws.Z,
+                      down_split, down_stride, nullptr, s));
+  // 3. permutation
+  LMOE_TRY(launch_permute(ws.ids, T, k, E, tile, ws.perm_scratch, ws.counts, ws.offsets,
+                          ws.tile_prefix, ws.row_of, ws.tok_of_row, s));
+  // 4. routed input into the expert-major rows
+  LMOE_TRY(launch_scatter_rows(down_split ? nullptr : ws.Z, down_split ? ws.Pa : nullptr,
+                               cdown.splits, down_stride, T, L, k, ws.row_of, ws.A, s));
+  // 5-7. experts
+  const int g1_bn = decode ? tile : ((2 * dI) % 256 == 0 ? 256 : 128);
+  const int g2_bn = decode ? tile : (L % 256 == 0 ? 256 : 128);
+  LMOE_TRY(gemm_grouped(wt->w13, E, 2 * dI, ws.A, rows, L, !decode, g1_bn, ws, tile, ws.G, s));
+  LMOE_TRY(launch_situ(ws.G, ws.act, rows, dI, d.beta, d.linear_beta, s));
+  LMOE_TRY(gemm_grouped(wt->w2, E, L, ws.act, rows, dI, !decode, g2_bn, ws, tile, ws.Y, s));
+  // 8. combine + RMSNorm
+  LMOE_TRY(launch_combine_norm(ws.Y, ws.w, ws.row_of, T, k, L, wt->norm_w, d.rms_eps, ws.N, s));
+  // 9-11. shared expert on the original hidden states
+  const float* sh_part = nullptr;
+  int sh_splits = 0;
+  long long sh_stride = 0;
+  const uint16_t* sh_bf16 = nullptr;
+  if (shared) {
+    const DenseCfg c1 = dense_cfg(T, 2 * ds, H, nsm);
+    const long long s1_stride = (long long)T * 2 * ds;
+    if (c1.splits > 1) {
+      LMOE_TRY(gemm_dense(wt->ws13, 2 * ds, X, T, H, c1, ws.Pb, 1, s1_stride, nullptr, s));
+      LMOE_TRY(launch_reduce_situ(ws.Pb, c1.splits, s1_stride, T, ds, d.beta, d.linear_beta,
+                                  ws.As, s));
+    } else {
+      LMOE_TRY(gemm_dense(wt->ws13, 2 * ds, X, T, H, c1, ws.Gs, 0, 0, nullptr, s));
+      LMOE_TRY(launch_situ(ws.Gs, ws.As, T, ds, d.beta, d.linear_beta, s));
+    }
+    const DenseCfg c2 = dense_cfg(T, H, ds, nsm);
+    sh_stride = (long long)T * H;
+    if (c2.splits > 1) {
+      LMOE_TRY(gemm_dense(wt->ws2, H, ws.As, T, ds, c2, ws.Pb, 1, sh_stride, nullptr, s));
+      sh_part = ws.Pb;
+      sh_splits = c2.splits;
+    } else {
+      LMOE_TRY(gemm_dense(wt->ws2, H, ws.As, T, ds, c2, ws.Sh, 0, 0, nullptr, s));
+      sh_bf16 = ws.Sh;
+    }
+  }
+  // 12. up-projection with the shared output added in the epilogue
+  const DenseCfg cup = dense_cfg(T, H, L, nsm);
+  if (cup.splits > 1) {
+    const long long up_stride = (long long)T * H;
+    LMOE_TRY(gemm_dense(wt->w_up, H, ws.N, T, L, cup, ws.Pa, 1, up_stride, nullptr, s));
+    LMOE_TRY(launch_reduce_splits(ws.Pa, cup.splits, up_stride, sh_part, sh_splits, sh_stride,
+                                  sh_bf16, (long long)T * H, out, s));
+  } else {
+    if (sh_part) {
+      // shared output still in partials: materialise it in bf16 first
+      LMOE_TRY(launch_reduce_splits(sh_part, sh_splits, sh_stride, nullptr, 0, 0, nullptr,
+                                    (long long)T * H, ws.Sh, s));
+      sh_bf16 = ws.Sh;
+    }
+    LMOE_TRY(gemm_dense(wt->w_up, H, ws.N, T, L, cup, out, 0, 0, sh_bf16, s));
+  }
+  // optional copies of the routing and permutation
+  if (dbg) {
+    if (dbg->topk_ids)
+      LMOE_TRY(cudaMemcpyAsync(dbg->topk_ids, ws.ids, rows * 4, cudaMemcpyDeviceToDevice, s));
+    if (dbg->topk_weights)
+      LMOE_TRY(cudaMemcpyAsync(dbg->topk_weights, ws.w, rows * 4, cudaMemcpyDeviceToDevice, s));
+    if (dbg->expert_num_tokens)
+      LMOE_TRY(cudaMemcpyAsync(dbg->expert_num_tokens, ws.counts, (size_t)E * 4,
+                               cudaMemcpyDeviceToDevice, s));
+    if (dbg->expert_offsets)
+      LMOE_TRY(cudaMemcpyAsync(dbg->expert_offsets, ws.offsets, (size_t)(E + 1) * 4,
+                               cudaMemcpyDeviceToDevice, s));
+    if (dbg->row_of)
+      LMOE_TRY(cudaMemcpyAsync(dbg->row_of, ws.row_of, rows * 4, cudaMemcpyDeviceToDevice, s));
+  }
+  return LMOE_OK;
+}
+
+}  // extern "C"

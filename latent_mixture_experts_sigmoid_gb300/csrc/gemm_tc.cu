@@ -1,0 +1,514 @@
+// bf16 GEMMs of the latent-MoE layer on the 5th-generation tensor cores.
+//
+//   out[tok, f] = sum_c X[tok, c] * W[g*M_feat + f, c]   (+ add[tok, f])
+//
+// X holds token rows (K-major), W weight rows (K-major, PyTorch Linear
+// layout).  One kernel serves every contraction of the layer:
+//   * the latent down-projection and up-projection (dense; the up-projection
+//     adds the shared-expert output in its epilogue, the beta-add of the
+//     ``addmm_`` in the vLLM latent_moe_runner page, _shard_up_proj_tail);
+//   * the grouped expert GEMM1 / GEMM2 over the expert-major row blocks
+//     (group g owns token rows grp_offset[g] .. +grp_count[g]);
+//   * the shared expert's two GEMMs.
+//
+// Design (sm_103a): a persistent, warp-specialised kernel.
+//   warp 0      TMA producer: 64-wide K blocks of both operands, 128-byte
+//               swizzle, into a ring of shared-memory stages (mbarrier
+//               full/empty pairs);
+//   warp 1      allocates TMEM and one elected thread issues tcgen05.mma
+//               (kind::f16, bf16 in, fp32 accumulate, M = 128) into one of
+//               two TMEM accumulators, committing stage releases and
+//               accumulator-ready signals through tcgen05.commit;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, optional bf16 add,
+//               bf16 or fp32 stores straight to global memory.
+// The MMA's M side (128 rows) is either the tokens (large token counts) or
+// the weight rows ("swap AB", small token counts where N = 16..64 tokens); the
+// N side is the other operand.  Small dense problems split K across CTAs and
+// write fp32 partials that a reduction kernel sums in a fixed order.
+//
+// Every wait on an mbarrier is bounded (clock64 deadline).  A wait that gives
+// up records a code in the device error word, raises a CTA-wide abort flag,
+// and the CTA drains its own in-flight copies and MMAs (again bounded),
+// frees its TMEM and returns.
+#include <cuda.h>
+
+#include "lmoe_internal.cuh"
+#include "gemm_tc.cuh"
+
+namespace lmoe {
+
+__device__ int g_device_error = 0;
+
+namespace {
+
+constexpr int BK = 64;                 // K elements per stage (128 bytes of bf16)
+constexpr int BM = 128;                // MMA M
+constexpr int kThreads = 192;          // 6 warps
+constexpr long long kWaitCycles = 1ll << 32;   // ~2 s at 2 GHz
+
+// error codes written to g_device_error
+enum : int { kErrProducer = 1, kErrMmaFull = 2, kErrMmaTmem = 3, kErrEpilogue = 4,
+             kErrDrain = 5, kErrDone = 6 };
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: true when the phase completed; false on deadline or abort.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      atomicCAS(&g_device_error, 0, code);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint32_t dst, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), version 1.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                 // leading byte offset (unused with this swizzle)
+  d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
+  d |= (uint64_t)1 << 46;                 // descriptor version
+  d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct Unit {
+  int feat_tile;
+  int kb0, kb1;
+  int split;
+  int tok_row0;   // first token row of the tile (in X / out rows)
+  int nvalid;     // valid token rows in the tile
+  int w_row0;     // first weight row of the tile
+};
+
+__device__ __forceinline__ int total_units(const GemmParams& p, int tok_tile, int nfeat) {
+  const int tiles = p.tile_prefix ? __ldg(p.tile_prefix + p.num_groups)
+                                  : (p.T_dense + tok_tile - 1) / tok_tile;
+  return tiles * nfeat * p.splits;
+}
+
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int tok_tile,
+                                            int feat_tile, int nfeat, int nkb) {
+  Unit x;
+  x.split = u % p.splits;
+  const int v = u / p.splits;
+  x.feat_tile = v % nfeat;
+  const int gt = v / nfeat;
+  int g = 0, t_in_g = gt, count = p.T_dense, first = 0;
+  if (p.tile_prefix) {
+    int lo = 0, hi = p.num_groups - 1;   // last g with tile_prefix[g] <= gt
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(p.tile_prefix + mid) <= gt) lo = mid; else hi = mid - 1;
+    }
+    g = lo;
+    t_in_g = gt - __ldg(p.tile_prefix + g);
+    count = __ldg(p.grp_count + g);
+    first = __ldg(p.grp_offset + g);
+  }
+  x.tok_row0 = first + t_in_g * tok_tile;
+  x.nvalid = min(tok_tile, count - t_in_g * tok_tile);
+  x.w_row0 = g * p.M_feat + x.feat_tile * feat_tile;
+  x.kb0 = (int)((long long)x.split * nkb / p.splits);
+  x.kb1 = (int)((long long)(x.split + 1) * nkb / p.splits);
+  return x;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int S = p.stages;
+  const int bn = p.bn;
+  const uint32_t a_bytes = BM * BK * 2;
+  const uint32_t stage_bytes = a_bytes + (uint32_t)bn * BK * 2;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * stage_bytes);
+  // bars: full[S], empty[S], tfull[2], tempty[2], done
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
+  const uint32_t done_bar = bar0 + 8u * (2 * S + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4 * 32);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_holder)),
+                 "r"(p.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  const int tok_tile = p.tok_on_m ? BM : bn;
+  const int feat_tile = p.tok_on_m ? bn : BM;
+  const int nfeat = p.M_feat / feat_tile;
+  const int nkb = p.K / BK;
+  const int U = total_units(p, tok_tile, nfeat);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+        const Unit x = decode_unit(p, u, tok_tile, feat_tile, nfeat, nkb);
+        const int rowA = p.tok_on_m ? x.tok_row0 : x.w_row0;
+        const int rowB = p.tok_on_m ? x.w_row0 : x.tok_row0;
+        for (int kb = x.kb0; kb < x.kb1; ++kb, ++it) {
+          const int s = (int)(it % (uint32_t)S);
+          const uint32_t ph = (it / (uint32_t)S) & 1u;
+          if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kErrProducer)) { ok = false; break; }
+          const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
+          mbar_arrive_expect_tx(full_bar(s), stage_bytes);
+          tma_load_2d(&tmA, sa, full_bar(s), kb * BK, rowA);
+          tma_load_2d(&tmB, sa + a_bytes, full_bar(s), kb * BK, rowB);
+        }
+      }
+      // drain: every copy this thread issued has landed before the CTA exits
+      const uint32_t first = it > (uint32_t)S ? it - (uint32_t)S : 0u;
+      for (uint32_t j = first; j < it; ++j) {
+        volatile int never = 0;
+        const uint32_t bar = full_bar((int)(j % (uint32_t)S));
+        const uint32_t par = (j / (uint32_t)S) & 1u;
+        if (!wait_bounded(bar, par, &never, kErrDrain)) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      const uint32_t idesc = idesc_bf16(BM, bn);
+      uint32_t it = 0, uit = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++uit) {
+        const Unit x = decode_unit(p, u, tok_tile, feat_tile, nfeat, nkb);
+        const int acc = (int)(uit & 1u);
+        if (!wait_bounded(tempty_bar(acc), ((uit >> 1) & 1u) ^ 1u, abort_flag, kErrMmaTmem)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * bn);
+        for (int kb = x.kb0; kb < x.kb1; ++kb, ++it) {
+          const int s = (int)(it % (uint32_t)S);
+          const uint32_t ph = (it / (uint32_t)S) & 1u;
+          if (!wait_bounded(full_bar(s), ph, abort_flag, kErrMmaFull)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
+          const uint32_t sb = sa + a_bytes;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            mma_bf16(d_tmem, sdesc(sa + kk * 32), sdesc(sb + kk * 32), idesc,
+                     (kb > x.kb0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(empty_bar(s));
+        }
+        if (ok) mma_commit(tfull_bar(acc));
+      }
+      // every MMA this thread issued has completed before TMEM is freed
+      mma_commit(done_bar);
+      volatile int never = 0;
+      wait_bounded(done_bar, 0u, &never, kErrDone);
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q = warp & 3;                  // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;             // accumulator row of this thread
+    uint32_t uit = 0;
+    for (int u = blockIdx.x; u < U; u += gridDim.x, ++uit) {
+      const Unit x = decode_unit(p, u, tok_tile, feat_tile, nfeat, nkb);
+      const int acc = (int)(uit & 1u);
+      if (!wait_bounded(tfull_bar(acc), (uit >> 1) & 1u, abort_flag, kErrEpilogue)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * bn);
+      if (p.tok_on_m) {
+        // row r = token, columns = features
+        const bool valid = r < x.nvalid;
+        const long long orow = (long long)(x.tok_row0 + r);
+        const int fcol0 = x.feat_tile * bn;
+        for (int c0 = 0; c0 < bn; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tbase + (uint32_t)c0, v);
+          tmem_wait_ld();
+          if (!valid) continue;
+          if (p.out_fp32) {
+            float* o = reinterpret_cast<float*>(p.out) + (long long)x.split * p.split_stride +
+                       orow * p.ldo + fcol0 + c0;
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+              *reinterpret_cast<uint4*>(o + j) = make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          } else {
+            float f[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
+            if (p.add) {
+              const uint16_t* a = p.add + orow * p.ldo + fcol0 + c0;
+              const uint4 a0 = *reinterpret_cast<const uint4*>(a);
+              const uint4 a1 = *reinterpret_cast<const uint4*>(a + 8);
+              const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                f[2 * j] += bf16_lo(aw[j]);
+                f[2 * j + 1] += bf16_hi(aw[j]);
+              }
+            }
+            uint32_t pk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) pk[j] = pack_bf16x2(f[2 * j], f[2 * j + 1]);
+            uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + orow * p.ldo + fcol0 + c0;
+            *reinterpret_cast<uint4*>(o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(o + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          }
+        }
+      } else {
+        // row r = feature, columns = tokens
+        const int fcol = x.feat_tile * BM + r;
+        for (int c0 = 0; c0 < bn; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(tbase + (uint32_t)c0, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = c0 + j;
+            if (t < x.nvalid) {
+              const long long orow = (long long)(x.tok_row0 + t);
+              float f = __uint_as_float(v[j]);
+              if (p.out_fp32) {
+                reinterpret_cast<float*>(p.out)[(long long)x.split * p.split_stride +
+                                                 orow * p.ldo + fcol] = f;
+              } else {
+                if (p.add) f += __uint_as_float((uint32_t)p.add[orow * p.ldo + fcol] << 16);
+                reinterpret_cast<uint16_t*>(p.out)[orow * p.ldo + fcol] = to_bf16(f);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(p.tmem_cols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, long long rows, int K, int box_rows) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int stages_for(int bn) {
+  const int stage = BM * BK * 2 + bn * BK * 2;
+  const int budget = 200 * 1024;
+  int s = budget / stage;
+  return s > 12 ? 12 : (s < 2 ? 2 : s);
+}
+
+size_t smem_for(int bn, int stages) {
+  const size_t stage = (size_t)BM * BK * 2 + (size_t)bn * BK * 2;
+  return 1024 + stages * stage + (2 * stages + 5) * 8 + 16;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
+  GemmParams p{};
+  p.tok_on_m = g.tok_on_m;
+  p.M_feat = g.M_feat;
+  p.K = g.K;
+  p.bn = g.bn;
+  p.num_groups = g.G;
+  p.grp_count = g.grp_count;
+  p.grp_offset = g.grp_offset;
+  p.tile_prefix = g.tile_prefix;
+  p.T_dense = g.T_dense;
+  p.splits = g.splits;
+  p.out = g.out;
+  p.ldo = g.ldo;
+  p.split_stride = g.split_stride;
+  p.out_fp32 = g.out_fp32;
+  p.add = g.add;
+  p.stages = stages_for(g.bn);
+  uint32_t cols = 32;
+  while (cols < (uint32_t)(2 * g.bn)) cols <<= 1;
+  p.tmem_cols = cols;
+
+  CUtensorMap mw, mx;
+  const int w_box = g.tok_on_m ? g.bn : BM;
+  const int x_box = g.tok_on_m ? BM : g.bn;
+  if (!make_map(&mw, g.W, (long long)g.G * g.M_feat, g.K, w_box)) return cudaErrorInvalidValue;
+  if (!make_map(&mx, g.X, g.x_rows, g.K, x_box)) return cudaErrorInvalidValue;
+
+  const size_t smem = smem_for(g.bn, p.stages);
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  int grid = num_sms();
+  if (g.max_units > 0 && g.max_units < grid) grid = g.max_units;
+  if (grid < 1) grid = 1;
+  if (g.tok_on_m)
+    gemm_tc_kernel<<<grid, kThreads, smem, stream>>>(mx, mw, p);
+  else
+    gemm_tc_kernel<<<grid, kThreads, smem, stream>>>(mw, mx, p);
+  return cudaGetLastError();
+}
+
+int read_device_error(int clear) {
+  int v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return LMOE_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (clear) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return LMOE_ERR_CUDA;
+  }
+  return v;
+}
+
+}  // namespace lmoe

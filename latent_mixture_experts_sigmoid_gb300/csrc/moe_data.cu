@@ -1,0 +1,380 @@
+// Data movement of the latent-MoE layer: token permutation into the
+// expert-major layout, the scatter of the routed input into it, the top-k
+// weighted combine fused with the latent RMSNorm, and the fixed-order
+// reductions of split-K partials (with the fused SituGLU and epilogue add).
+//
+// Permutation (vLLM PR #50088, commits 2-3: the batched MoE layout with
+// expert_num_tokens).  The layer stores it compactly: expert e owns rows
+// offsets[e] .. offsets[e+1]-1, its (token, slot) pairs in ascending token
+// order.  The order is fixed by the data, not by atomics: per 256-token block
+// a shared-memory bitmap marks which tokens chose each expert; a token's rank
+// inside an expert is the population count of the bits below it plus the
+// counts of the earlier blocks.
+//
+// Combine + RMSNorm (vLLM PR #50088, commit 7: the routed output is summed
+// before the output transform; vLLM latent_moe_runner page,
+// _shard_up_proj_tail: transform.norm on the reduced latent):
+//   C[t] = sum_j w[t,j] * Y[row_of[t,j]]   (fp32, j ascending)
+//   N[t] = bf16(C[t] * rsqrt(mean(C[t]^2) + eps) * gamma)
+#include "lmoe_internal.cuh"
+#include "moe_data.cuh"
+
+namespace lmoe {
+namespace {
+
+constexpr int kBlkTok = 256;     // tokens per permutation block
+constexpr int kWords = kBlkTok / 32;
+
+// ---- permutation, pass 1: bitmaps and per-block counts -----------------------
+__global__ void __launch_bounds__(kBlkTok)
+perm_count_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
+                  uint32_t* __restrict__ bitmaps, int32_t* __restrict__ blk_cnt) {
+  extern __shared__ uint32_t bm[];   // [E][kWords]
+  const int b = blockIdx.x;
+  for (int i = threadIdx.x; i < E * kWords; i += blockDim.x) bm[i] = 0u;
+  __syncthreads();
+  const int t = b * kBlkTok + threadIdx.x;
+  if (t < T) {
+    for (int j = 0; j < k; ++j) {
+      const int e = __ldg(ids + (long long)t * k + j);
+      atomicOr(&bm[e * kWords + (threadIdx.x >> 5)], 1u << (threadIdx.x & 31));
+    }
+  }
+  __syncthreads();
+  uint32_t* gbm = bitmaps + (long long)b * E * kWords;
+  for (int i = threadIdx.x; i < E * kWords; i += blockDim.x) gbm[i] = bm[i];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < kWords; ++w) c += __popc(bm[e * kWords + w]);
+    blk_cnt[(long long)b * E + e] = c;
+  }
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x == 1024).
+__device__ int block_exclusive_scan(int v, int* sh /* [32] */, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) sh[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int s = sh[lane];
+    int si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xFFFFFFFFu, si, o);
+      if (lane >= o) si += n;
+    }
+    sh[lane] = si - s;                   // exclusive prefix of warp totals
+    if (lane == 31) sh[32] = si;
+  }
+  __syncthreads();
+  const int r = sh[warp] + incl - v;
+  *total = sh[32];
+  __syncthreads();
+  return r;
+}
+
+// ---- permutation, pass 2: counts, offsets, tile prefix, block bases ----------
+// One block of 1024 threads; expert e is handled by thread e (E <= 1024).
+__global__ void __launch_bounds__(1024)
+perm_scan_kernel(const int32_t* __restrict__ blk_cnt, int nblk, int E, int tile,
+                 int32_t* __restrict__ blk_base, int32_t* __restrict__ counts,
+                 int32_t* __restrict__ offsets, int32_t* __restrict__ tile_prefix) {
+  __shared__ int sh[33];
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < E) {
+    for (int b = 0; b < nblk; ++b) {
+      const int c = blk_cnt[(long long)b * E + e];
+      blk_base[(long long)b * E + e] = total;
+      total += c;
+    }
+  }
+  int all = 0, all_tiles = 0;
+  const int off = block_exclusive_scan(e < E ? total : 0, sh, &all);
+  const int ntile = (e < E) ? (total + tile - 1) / tile : 0;
+  const int toff = block_exclusive_scan(ntile, sh, &all_tiles);
+  if (e < E) {
+    counts[e] = total;
+    offsets[e] = off;
+    tile_prefix[e] = toff;
+    for (int b = 0; b < nblk; ++b) blk_base[(long long)b * E + e] += off;
+  }
+  if (e == 0) {
+    offsets[E] = all;
+    tile_prefix[E] = all_tiles;
+  }
+}
+
+// ---- permutation, pass 3: row of every (token, slot) -------------------------
+__global__ void __launch_bounds__(kBlkTok)
+perm_rows_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
+                 const uint32_t* __restrict__ bitmaps, const int32_t* __restrict__ blk_base,
+                 int32_t* __restrict__ row_of, int32_t* __restrict__ tok_of_row) {
+  const int b = blockIdx.x;
+  const int tl = threadIdx.x;
+  const int t = b * kBlkTok + tl;
+  if (t >= T) return;
+  const uint32_t* gbm = bitmaps + (long long)b * E * kWords;
+  const int w = tl >> 5;
+  const uint32_t below = (1u << (tl & 31)) - 1u;
+  for (int j = 0; j < k; ++j) {
+    const int e = __ldg(ids + (long long)t * k + j);
+    const uint32_t* m = gbm + e * kWords;
+    int rank = __popc(__ldg(m + w) & below);
+    for (int i = 0; i < w; ++i) rank += __popc(__ldg(m + i));
+    const int row = __ldg(blk_base + (long long)b * E + e) + rank;
+    row_of[(long long)t * k + j] = row;
+    tok_of_row[row] = t;
+  }
+}
+
+// ---- scatter of the routed input into the expert-major rows ------------------
+// A[row_of[t, j], :] = Z[t, :] for every slot j, where Z[t] is either a bf16
+// row or the bf16 rounding of the fixed-order sum of S fp32 split partials.
+__global__ void __launch_bounds__(256)
+scatter_rows_kernel(const uint16_t* __restrict__ Zb, const float* __restrict__ Zp, int S,
+                    long long split_stride, int L, int k, const int32_t* __restrict__ row_of,
+                    uint16_t* __restrict__ A) {
+  const int t = blockIdx.x;
+  const int nv = L / 8;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    uint4 o;
+    if (Zp) {
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int s = 0; s < S; ++s) {
+        const float4* p = reinterpret_cast<const float4*>(Zp + s * split_stride +
+                                                          (long long)t * L + v * 8);
+        const float4 a = __ldg(p), c = __ldg(p + 1);
+        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+        acc[4] += c.x; acc[5] += c.y; acc[6] += c.z; acc[7] += c.w;
+      }
+      o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                     pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    } else {
+      o = __ldg(reinterpret_cast<const uint4*>(Zb + (long long)t * L) + v);
+    }
+    for (int j = 0; j < k; ++j) {
+      const long long row = __ldg(row_of + (long long)t * k + j);
+      reinterpret_cast<uint4*>(A + row * L)[v] = o;
+    }
+  }
+}
+
+// ---- combine + RMSNorm -------------------------------------------------------
+__global__ void __launch_bounds__(256)
+combine_norm_kernel(const uint16_t* __restrict__ Y, const float* __restrict__ w,
+                    const int32_t* __restrict__ row_of, int k, int L,
+                    const uint16_t* __restrict__ gamma, float eps, uint16_t* __restrict__ N) {
+  __shared__ float red[32];
+  const int t = blockIdx.x;
+  const int nv = L / 8;
+  constexpr int kMaxV = 4;   // vectors per thread (L <= 8 * 256 * 4)
+  float acc[kMaxV][8];
+  float ss = 0.0f;
+#pragma unroll
+  for (int q = 0; q < kMaxV; ++q) {
+    const int v = threadIdx.x + q * blockDim.x;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[q][i] = 0.0f;
+    if (v < nv) {
+      for (int j = 0; j < k; ++j) {
+        const float wj = __ldg(w + (long long)t * k + j);
+        const long long row = __ldg(row_of + (long long)t * k + j);
+        const uint4 y = __ldg(reinterpret_cast<const uint4*>(Y + row * L) + v);
+        const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[q][2 * i] += wj * bf16_lo(yw[i]);
+          acc[q][2 * i + 1] += wj * bf16_hi(yw[i]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss += acc[q][i] * acc[q][i];
+    }
+  }
+  // block reduction of the sum of squares
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = (blockDim.x + 31) >> 5;
+    float s = lane < nw ? red[lane] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    if (lane == 0) red[0] = s;
+  }
+  __syncthreads();
+  const float r = rsqrtf(red[0] / (float)L + eps);
+#pragma unroll
+  for (int q = 0; q < kMaxV; ++q) {
+    const int v = threadIdx.x + q * blockDim.x;
+    if (v < nv) {
+      float g[8];
+      if (gamma) {
+        const uint4 gv = __ldg(reinterpret_cast<const uint4*>(gamma) + v);
+        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { g[2 * i] = bf16_lo(gw[i]); g[2 * i + 1] = bf16_hi(gw[i]); }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) g[i] = 1.0f;
+      }
+      uint32_t pk[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        pk[i] = pack_bf16x2(acc[q][2 * i] * r * g[2 * i], acc[q][2 * i + 1] * r * g[2 * i + 1]);
+      reinterpret_cast<uint4*>(N + (long long)t * L)[v] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+  }
+}
+
+// ---- fixed-order reduction of split-K partials -------------------------------
+// out[r, c] = bf16( sum_s P[s, r, c] + a ), where a = bf16(sum_s2 Q[s2, r, c]) if
+// Q is given, a = add[r, c] if add is given, else 0.
+__global__ void __launch_bounds__(256)
+reduce_splits_kernel(const float* __restrict__ P, int S, long long sstride,
+                     const float* __restrict__ Q, int S2, long long qstride,
+                     const uint16_t* __restrict__ add, long long n8, uint16_t* __restrict__ out) {
+  for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < n8;
+       v += (long long)gridDim.x * blockDim.x) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int s = 0; s < S; ++s) {
+      const float4* p = reinterpret_cast<const float4*>(P + s * sstride) + 2 * v;
+      const float4 a = __ldg(p), c = __ldg(p + 1);
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += c.x; acc[5] += c.y; acc[6] += c.z; acc[7] += c.w;
+    }
+    if (Q) {
+      float qa[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int s = 0; s < S2; ++s) {
+        const float4* p = reinterpret_cast<const float4*>(Q + s * qstride) + 2 * v;
+        const float4 a = __ldg(p), c = __ldg(p + 1);
+        qa[0] += a.x; qa[1] += a.y; qa[2] += a.z; qa[3] += a.w;
+        qa[4] += c.x; qa[5] += c.y; qa[6] += c.z; qa[7] += c.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        const uint32_t b2 = pack_bf16x2(qa[i], qa[i + 1]);   // the bf16 shared output
+        acc[i] += bf16_lo(b2);
+        acc[i + 1] += bf16_hi(b2);
+      }
+    } else if (add) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(add) + v);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { acc[2 * i] += bf16_lo(aw[i]); acc[2 * i + 1] += bf16_hi(aw[i]); }
+    }
+    reinterpret_cast<uint4*>(out)[v] =
+        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                   pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+  }
+}
+
+// SituGLU of split-K partials of a [T, 2d] GEMM output: G = bf16(sum_s P)
+// (gate = columns 0..d-1, up = d..2d-1), out[T, d] = bf16(SituGLU(G)).
+__global__ void __launch_bounds__(256)
+reduce_situ_kernel(const float* __restrict__ P, int S, long long sstride, int T, int d,
+                   SituParams sp, uint16_t* __restrict__ out) {
+  const long long n8 = (long long)T * (d / 8);
+  for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < n8;
+       v += (long long)gridDim.x * blockDim.x) {
+    const long long t = v / (d / 8);
+    const int c = (int)(v - t * (d / 8)) * 8;
+    float g[8] = {0, 0, 0, 0, 0, 0, 0, 0}, u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int s = 0; s < S; ++s) {
+      const float* base = P + s * sstride + t * (2LL * d) + c;
+      const float4 g0 = __ldg(reinterpret_cast<const float4*>(base));
+      const float4 g1 = __ldg(reinterpret_cast<const float4*>(base) + 1);
+      const float4 u0 = __ldg(reinterpret_cast<const float4*>(base + d));
+      const float4 u1 = __ldg(reinterpret_cast<const float4*>(base + d) + 1);
+      g[0] += g0.x; g[1] += g0.y; g[2] += g0.z; g[3] += g0.w;
+      g[4] += g1.x; g[5] += g1.y; g[6] += g1.z; g[7] += g1.w;
+      u[0] += u0.x; u[1] += u0.y; u[2] += u0.z; u[3] += u0.w;
+      u[4] += u1.x; u[5] += u1.y; u[6] += u1.z; u[7] += u1.w;
+    }
+    uint32_t pk[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t gb = pack_bf16x2(g[2 * i], g[2 * i + 1]);
+      const uint32_t ub = pack_bf16x2(u[2 * i], u[2 * i + 1]);
+      pk[i] = situ2(gb, ub, sp);
+    }
+    reinterpret_cast<uint4*>(out + t * d + c)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+}
+
+int grid_for(long long n, int threads) {
+  const long long b = (n + threads - 1) / threads;
+  const long long cap = (long long)num_sms() * 16;
+  return (int)(b < cap ? (b < 1 ? 1 : b) : cap);
+}
+
+}  // namespace
+
+size_t permute_scratch_bytes(int T, int E) {
+  const long long nblk = (T + kBlkTok - 1) / kBlkTok;
+  return (size_t)(nblk * E * kWords * 4 + 2 * nblk * E * 4);
+}
+
+cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int tile, void* scratch,
+                           int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
+                           int32_t* row_of, int32_t* tok_of_row, cudaStream_t s) {
+  const int nblk = (T + kBlkTok - 1) / kBlkTok;
+  uint32_t* bitmaps = reinterpret_cast<uint32_t*>(scratch);
+  int32_t* blk_cnt = reinterpret_cast<int32_t*>(bitmaps + (size_t)nblk * E * kWords);
+  int32_t* blk_base = blk_cnt + (size_t)nblk * E;
+  const size_t sm = (size_t)E * kWords * 4;
+  cudaError_t e = cudaFuncSetAttribute(perm_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sm);
+  if (e != cudaSuccess) return e;
+  perm_count_kernel<<<nblk, kBlkTok, sm, s>>>(ids, T, k, E, bitmaps, blk_cnt);
+  perm_scan_kernel<<<1, 1024, 0, s>>>(blk_cnt, nblk, E, tile, blk_base, counts, offsets,
+                                      tile_prefix);
+  perm_rows_kernel<<<nblk, kBlkTok, 0, s>>>(ids, T, k, E, bitmaps, blk_base, row_of, tok_of_row);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_rows(const uint16_t* Zb, const float* Zp, int S, long long split_stride,
+                                int T, int L, int k, const int32_t* row_of, uint16_t* A,
+                                cudaStream_t s) {
+  const int threads = L / 8 < 256 ? ((L / 8 + 31) / 32) * 32 : 256;
+  scatter_rows_kernel<<<T, threads, 0, s>>>(Zb, Zp, S, split_stride, L, k, row_of, A);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_norm(const uint16_t* Y, const float* w, const int32_t* row_of, int T,
+                                int k, int L, const uint16_t* gamma, float eps, uint16_t* N,
+                                cudaStream_t s) {
+  const int nv = L / 8;
+  int threads = nv < 256 ? ((nv + 31) / 32) * 32 : 256;
+  combine_norm_kernel<<<T, threads, 0, s>>>(Y, w, row_of, k, L, gamma, eps, N);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_splits(const float* P, int S, long long sstride, const float* Q, int S2,
+                                 long long qstride, const uint16_t* add, long long n,
+                                 uint16_t* out, cudaStream_t s) {
+  const long long n8 = n / 8;
+  reduce_splits_kernel<<<grid_for(n8, 256), 256, 0, s>>>(P, S, sstride, Q, S2, qstride, add, n8,
+                                                         out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_situ(const float* P, int S, long long sstride, int T, int d, float beta,
+                               float lbeta, uint16_t* out, cudaStream_t s) {
+  const long long n8 = (long long)T * (d / 8);
+  reduce_situ_kernel<<<grid_for(n8, 256), 256, 0, s>>>(P, S, sstride, T, d,
+                                                       make_situ_params(beta, lbeta), out);
+  return cudaGetLastError();
+}
+
+}  // namespace lmoe

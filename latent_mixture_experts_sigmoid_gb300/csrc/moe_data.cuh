@@ -1,0 +1,39 @@
+// Host interface of the permutation / scatter / combine / reduction kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lmoe {
+
+// Scratch bytes launch_permute needs for T tokens and E experts.
+size_t permute_scratch_bytes(int T, int E);
+
+// ids [T,k] -> counts [E], offsets [E+1], tile_prefix [E+1] (prefix of
+// ceil(count/tile)), row_of [T,k], tok_of_row [T*k].  E <= 1024.
+cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int tile, void* scratch,
+                           int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
+                           int32_t* row_of, int32_t* tok_of_row, cudaStream_t s);
+
+// A[row_of[t,j]] = Z[t] for j < k; Z from bf16 rows Zb or from the sum of S
+// fp32 partials Zp (split_stride elements apart).  L % 8 == 0.
+cudaError_t launch_scatter_rows(const uint16_t* Zb, const float* Zp, int S, long long split_stride,
+                                int T, int L, int k, const int32_t* row_of, uint16_t* A,
+                                cudaStream_t s);
+
+// N[t] = bf16(RMSNorm(sum_j w[t,j] Y[row_of[t,j]]) * gamma).  L % 8 == 0, L <= 8192.
+cudaError_t launch_combine_norm(const uint16_t* Y, const float* w, const int32_t* row_of, int T,
+                                int k, int L, const uint16_t* gamma, float eps, uint16_t* N,
+                                cudaStream_t s);
+
+// out[i] = bf16(sum_s P[s][i] + a[i]) over n elements (n % 8 == 0); a is
+// bf16(sum_s2 Q[s2][i]) when Q is given, add[i] when add is given, else 0.
+cudaError_t launch_reduce_splits(const float* P, int S, long long sstride, const float* Q, int S2,
+                                 long long qstride, const uint16_t* add, long long n,
+                                 uint16_t* out, cudaStream_t s);
+
+// out[T,d] = bf16(SituGLU(bf16(sum_s P[s]))) for a [T, 2d] partial GEMM output.
+cudaError_t launch_reduce_situ(const float* P, int S, long long sstride, int T, int d, float beta,
+                               float lbeta, uint16_t* out, cudaStream_t s);
+
+}  // namespace lmoe

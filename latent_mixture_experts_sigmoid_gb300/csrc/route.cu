@@ -1,0 +1,280 @@
+// Single-group sigmoid top-k routing (DeepSeekV3 style).
+//
+// vLLM PR #50088, commit 1: with n_group == 1 and topk_group == 1, grouped
+// top-k is plain top-k over all experts; commit 4: sigmoid scores of FP32
+// logits, e_score_correction_bias added for the selection only, weights from
+// the unbiased scores, renormalised, times routed_scaling_factor.
+//
+// One warp per token.  The selection key must be reproducible to the bit (the
+// expert ids are compared exactly), so the sigmoid that decides it is a fixed
+// sequence of IEEE fp32 operations (exact_sigmoid below).  Evaluating that
+// sequence for all E experts would make the kernel issue-bound, so the kernel
+// selects in two passes:
+//   A. a cheap key ka = fast_sigmoid(x) + b for every expert, packed with the
+//      expert index into one u32 (key truncated to 22 bits, index below), and
+//      the top-k of those by per-lane sorted lists merged with warp max
+//      (redux.sync.max.u32);
+//   B. every expert whose cheap key lies within a proven error bound of the
+//      k-th cheap key is a candidate; candidates (normally k or k+1 of them)
+//      get the exact key and are ordered by a 32-lane bitonic network on
+//      (exact key, lower index first).  More than 32 candidates (a row of tied
+//      logits) fall back to an exact selection over all experts.
+// Why the candidate set always holds the exact top-k: let |ka - key| <= D for
+// every expert and let A be the (truncated) cheap key of the k-th pick.  At
+// least k experts have ka >= A, so at least k have key >= A - D; hence the
+// k-th largest exact key K satisfies K >= A - D, and every member of the exact
+// top-k has ka >= key - D >= K - D >= A - 2D.  D is bounded from the documented
+// error of __expf (2 + floor(1.173|x|) ulp, |x| <= 87) and __fdividef (2 ulp):
+// |s_fast - s| <= s(1-s) * 1.24e-5 + 3 ulp <= 3.5e-6, plus the exact
+// sigmoid's own error (<= 3 ulp) and the rounding of the two bias additions
+// (<= 2^-23 |key|).  The kernel uses 2D = 1e-5 + 2^-20 * max(|A|, 1), about
+// 2.5x that bound.
+#include "lmoe_internal.cuh"
+
+namespace lmoe {
+namespace {
+
+// ---- the exact fp32 sigmoid ------------------------------------------------
+// y = clamp(-x, -87, 88); n = rint(y*log2e); r = (y - n*ln2_hi) - n*ln2_lo;
+// p = degree-7 Taylor polynomial of e^r (Horner, separate multiply and add);
+// e^y = p * 2^n; s = 1 / (1 + e^y).  Every operation is an explicitly rounded
+// intrinsic, so the compiler cannot contract or reorder it.
+constexpr float kLog2e = 0x1.715476p+0f;
+constexpr float kLn2Hi = 0x1.63p-1f;          // 355/512
+constexpr float kLn2Lo = -0x1.bd0106p-13f;    // ln2 - 355/512, rounded
+constexpr float kInvFact2 = 0x1p-1f;
+constexpr float kInvFact3 = 0x1.555556p-3f;
+constexpr float kInvFact4 = 0x1.555556p-5f;
+constexpr float kInvFact5 = 0x1.111112p-7f;
+constexpr float kInvFact6 = 0x1.6c16c2p-10f;
+constexpr float kInvFact7 = 0x1.a01a02p-13f;
+
+__device__ __forceinline__ float horner_step(float p, float r, float c) {
+  return __fadd_rn(__fmul_rn(p, r), c);
+}
+
+__device__ __forceinline__ float exact_sigmoid(float x) {
+  const float y = fminf(fmaxf(-x, -87.0f), 88.0f);
+  const float n = rintf(__fmul_rn(y, kLog2e));
+  float r = __fsub_rn(y, __fmul_rn(n, kLn2Hi));
+  r = __fsub_rn(r, __fmul_rn(n, kLn2Lo));
+  float p = kInvFact7;
+  p = horner_step(p, r, kInvFact6);
+  p = horner_step(p, r, kInvFact5);
+  p = horner_step(p, r, kInvFact4);
+  p = horner_step(p, r, kInvFact3);
+  p = horner_step(p, r, kInvFact2);
+  p = horner_step(p, r, 1.0f);   // 1/1!
+  p = horner_step(p, r, 1.0f);   // 1/0!
+  const float two_n = __int_as_float(((int)n + 127) << 23);
+  const float e = __fmul_rn(p, two_n);
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
+}
+
+__device__ __forceinline__ float fast_sigmoid(float x) {
+  const float xc = fminf(fmaxf(x, -87.0f), 87.0f);
+  return __fdividef(1.0f, 1.0f + __expf(-xc));
+}
+
+// Monotone map float -> u32 (larger float -> larger integer; -0 < +0).
+__device__ __forceinline__ uint32_t orderable(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float from_orderable(uint32_t o) {
+  const uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+  return __uint_as_float(u);
+}
+
+constexpr uint32_t kIdxBits = 10;  // E <= 1024
+constexpr uint32_t kIdxMask = (1u << kIdxBits) - 1u;
+
+__device__ __forceinline__ uint32_t pack_cheap(float ka, int e) {
+  return (orderable(ka) & ~kIdxMask) | (kIdxMask - (uint32_t)e);
+}
+
+// Exact key packed with the index: larger key first, then lower index first.
+__device__ __forceinline__ unsigned long long pack_exact(float key, int e) {
+  key = __fadd_rn(key, 0.0f);  // -0 -> +0
+  return ((unsigned long long)orderable(key) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
+}
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+  const uint32_t hi = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(v >> 32));
+  const uint32_t lo = __reduce_max_sync(0xFFFFFFFFu, ((uint32_t)(v >> 32) == hi) ? (uint32_t)v : 0u);
+  return ((unsigned long long)hi << 32) | lo;
+}
+
+__device__ __forceinline__ void insert4(uint32_t v, uint32_t& l0, uint32_t& l1, uint32_t& l2,
+                                        uint32_t& l3) {
+  uint32_t t = max(l0, v); v = min(l0, v); l0 = t;
+  t = max(l1, v); v = min(l1, v); l1 = t;
+  t = max(l2, v); v = min(l2, v); l2 = t;
+  l3 = max(l3, v);
+}
+
+constexpr int kWarpsPerBlock = 8;
+
+// EPL = experts per lane; expert e = lane + 32*i lives in lane e%32, slot e/32.
+template <int EPL>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
+                  int k, int renorm, float rsf, int32_t* __restrict__ ids,
+                  float* __restrict__ weights) {
+  __shared__ float sbias[EPL * 32];
+  __shared__ int scand[kWarpsPerBlock][32];
+  for (int i = threadIdx.x; i < EPL * 32; i += blockDim.x)
+    sbias[i] = (i < E && bias != nullptr) ? bias[i] : 0.0f;
+  __syncthreads();
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const unsigned FULL = 0xFFFFFFFFu;
+
+  for (long long t = (long long)blockIdx.x * kWarpsPerBlock + warp; t < T;
+       t += (long long)gridDim.x * kWarpsPerBlock) {
+    const float* row = logits + t * (long long)E;
+
+    // ---- pass A: cheap keys and per-lane top-4 lists -----------------------
+    float ka[EPL];
+    uint32_t l0 = 0, l1 = 0, l2 = 0, l3 = 0;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      ka[i] = -INFINITY;
+      if (e < E) {
+        ka[i] = fast_sigmoid(__ldg(row + e)) + sbias[e];
+        ka[i] = fmaxf(ka[i], -3.0e38f);
+        insert4(pack_cheap(ka[i], e), l0, l1, l2, l3);
+      }
+    }
+
+    // ---- merge: k rounds of warp max over the list heads -------------------
+    uint32_t mysel = 0, last = 0;
+    int popped = 0;
+    for (int r = 0; r < k; ++r) {
+      const uint32_t m = __reduce_max_sync(FULL, l0);
+      if (lane == r) mysel = m;
+      if (l0 == m) {
+        l0 = l1; l1 = l2; l2 = l3; l3 = 0; ++popped; last = m;
+      }
+      if (EPL > 4) {
+        // a lane that handed out its whole list may hold further large keys
+        const bool refill = (popped == 4);
+        if (__any_sync(FULL, refill) && refill) {
+          popped = 0;
+#pragma unroll
+          for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) {
+              const uint32_t p = pack_cheap(ka[i], e);
+              if (p < last) insert4(p, l0, l1, l2, l3);
+            }
+          }
+        }
+      }
+    }
+    const uint32_t a_k = __shfl_sync(FULL, mysel, k - 1);
+    const float trunc_k = from_orderable(a_k & ~kIdxMask);
+    const float thr = trunc_k - (1.0e-5f + 0x1p-20f * fmaxf(fabsf(trunc_k), 1.0f));
+
+    // ---- pass B: candidates within the bound --------------------------------
+    uint32_t cmask = 0;
+    int ccount = 0;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      if (ka[i] >= thr) { cmask |= 1u << i; ++ccount; }
+    }
+    const int total = (int)__reduce_add_sync(FULL, (uint32_t)ccount);
+
+    unsigned long long P = 0ull;
+    float s = 0.0f;
+    if (total <= 32) {
+      int incl = ccount;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int pos = incl - ccount;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (cmask & (1u << i)) scand[warp][pos++] = lane + 32 * i;
+      __syncwarp();
+      if (lane < total) {
+        const int e = scand[warp][lane];
+        s = exact_sigmoid(__ldg(row + e));
+        P = pack_exact(__fadd_rn(s, sbias[e]), e);
+      }
+      // bitonic sort of 32 (P, s) pairs, descending
+#pragma unroll
+      for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          const unsigned long long Po = __shfl_xor_sync(FULL, P, stride);
+          const float so = __shfl_xor_sync(FULL, s, stride);
+          const bool up = ((lane & size) == 0);        // this pair sorts descending
+          const bool lower = ((lane & stride) == 0);   // this lane keeps the larger
+          const bool take = (lower == up) ? (Po > P) : (Po < P);
+          if (take) { P = Po; s = so; }
+        }
+      }
+      __syncwarp();
+    } else {
+      // ---- fallback: exact selection over all experts ----------------------
+      unsigned long long lastP = ~0ull;
+      for (int r = 0; r < k; ++r) {
+        unsigned long long best = 0ull;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          const int e = lane + 32 * i;
+          if (e < E) {
+            const unsigned long long p =
+                pack_exact(__fadd_rn(exact_sigmoid(__ldg(row + e)), sbias[e]), e);
+            if (p < lastP && p > best) best = p;
+          }
+        }
+        const unsigned long long m = warp_max_u64(best);
+        if (lane == r) P = m;
+        lastP = m;
+      }
+      if (lane < k) s = exact_sigmoid(__ldg(row + (int)(0xFFFFFFFFu - (uint32_t)P)));
+    }
+
+    // ---- weights and outputs -------------------------------------------------
+    const int e = (int)(0xFFFFFFFFu - (uint32_t)P);
+    float sum = (lane < k) ? s : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
+    if (lane < k) {
+      const float wv = renorm ? __fmul_rn(__fdiv_rn(s, sum), rsf) : __fmul_rn(s, rsf);
+      ids[t * k + lane] = e;
+      weights[t * k + lane] = wv;
+    }
+  }
+}
+
+template <int EPL>
+cudaError_t launch_tier(const float* logits, const float* bias, int T, int E, int k, int renorm,
+                        float rsf, int32_t* ids, float* w, cudaStream_t s) {
+  const int blocks = ceil_div(T, kWarpsPerBlock);
+  route_warp_kernel<EPL><<<blocks, kWarpsPerBlock * 32, 0, s>>>(logits, bias, T, E, k, renorm,
+                                                                rsf, ids, w);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Compile-time tier list of experts-per-lane; E <= 32 * EPL.
+cudaError_t launch_route(const float* logits, const float* bias, int T, int E, int k, int renorm,
+                         float rsf, int32_t* ids, float* w, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (E <= 64) return launch_tier<2>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 128) return launch_tier<4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 256) return launch_tier<8>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 512) return launch_tier<16>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 896) return launch_tier<28>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  return launch_tier<32>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+}
+
+}  // namespace lmoe

@@ -1,0 +1,126 @@
+"""The C ABI library on the CPU: it loads, exports every declared function, and
+its host-side validation rejects bad arguments before touching any device."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from latent_mixture_experts_sigmoid_gb300 import build
+    build.build()
+    import latent_mixture_experts_sigmoid_gb300 as lm
+    return lm.load_library()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s+(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_function_is_exported(lib):
+    from latent_mixture_experts_sigmoid_gb300 import build, ABI_FUNCTIONS
+    decl = declared_functions()
+    assert set(ABI_FUNCTIONS) <= set(decl)
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (\w+)$", out, flags=re.M))
+    missing = [n for n in decl if n not in exported]
+    assert not missing, missing
+    for n in decl:
+        getattr(lib, n)
+
+
+def test_status_strings(lib):
+    for st in range(-7, 1):
+        assert lib.lmoe_status_string(st)
+    assert lib.lmoe_status_string(-99) == b"unknown status"
+    assert lib.lmoe_abi_version() == 100
+
+
+def test_route_validation(lib):
+    p = ctypes.c_void_p(16)       # never dereferenced: validation fails first
+    assert lib.moe_route(p, None, 4, 8, 2, 2, 1, 1, 1.0, p, p, None) == -3
+    assert lib.moe_route(p, None, 4, 8, 2, 1, 3, 1, 1.0, p, p, None) == -3
+    assert lib.moe_route(p, None, 4, 8, 9, 1, 1, 1, 1.0, p, p, None) == -2    # topk > E
+    assert lib.moe_route(p, None, 4, 2000, 8, 1, 1, 1, 1.0, p, p, None) == -2  # E > 1024
+    assert lib.moe_route(p, None, 4, 64, 33, 1, 1, 1, 1.0, p, p, None) == -2   # topk > 32
+    assert lib.moe_route(None, None, 4, 8, 2, 1, 1, 1, 1.0, p, p, None) == -1
+    assert lib.moe_route(ctypes.c_void_p(20), None, 4, 8, 2, 1, 1, 1, 1.0, p, p, None) == -7
+    assert lib.moe_route(None, None, 0, 8, 2, 1, 1, 1, 1.0, None, None, None) == 0  # empty
+
+
+def test_situ_validation(lib):
+    p = ctypes.c_void_p(16)
+    assert lib.situ_and_mul(p, p, 4, 8, 0.0, 8.0, None) == -4
+    assert lib.situ_and_mul(p, p, 4, 8, float("nan"), 8.0, None) == -4
+    assert lib.situ_and_mul(p, p, 4, 12, 4.0, 8.0, None) == -2
+    assert lib.situ_and_mul(p, p, 0, 8, 4.0, 8.0, None) == 0
+    assert lib.masked_situ_and_mul(p, p, p, 4, 8, 8, -1.0, 8.0, None) == -4
+    assert lib.masked_situ_and_mul(p, p, None, 4, 8, 8, 4.0, 8.0, None) == -1
+    assert lib.masked_situ_and_mul(p, p, p, 0, 8, 8, 4.0, 8.0, None) == 0
+
+
+def test_layer_validation_and_workspace(lib):
+    import workloads as W
+    import latent_mixture_experts_sigmoid_gb300 as lm
+    d = lm.make_dims(W.TINY)
+    n = lib.latent_moe_workspace_bytes(ctypes.byref(d))
+    assert n > 0 and n % 256 == 0
+    big = lm.make_dims(W.PREFILL)
+    assert lib.latent_moe_workspace_bytes(ctypes.byref(big)) > 800 * 2 ** 20
+    bad = lm.make_dims(W.TINY)
+    bad.beta = 0.0
+    assert lib.latent_moe_workspace_bytes(ctypes.byref(bad)) == 0
+    w = lm.LmoeWeights()
+    p = ctypes.c_void_p(256)
+    assert lib.latent_moe_forward(ctypes.byref(bad), ctypes.byref(w), p, p, p, p, n, None, None) == -4
+    bad = lm.make_dims(W.TINY)
+    bad.n_group = 8
+    assert lib.latent_moe_forward(ctypes.byref(bad), ctypes.byref(w), p, p, p, p, n, None, None) == -3
+    bad = lm.make_dims(W.TINY)
+    bad.latent = 100
+    assert lib.latent_moe_forward(ctypes.byref(bad), ctypes.byref(w), p, p, p, p, n, None, None) == -2
+    # missing weights
+    assert lib.latent_moe_forward(ctypes.byref(d), ctypes.byref(w), p, p, p, p, n, None, None) == -1
+    w2 = lm.LmoeWeights(256, 256, 256, None, None, None, 256, None)
+    # workspace misaligned / too small
+    assert lib.latent_moe_forward(ctypes.byref(d), ctypes.byref(w2), p, p, p,
+                                  ctypes.c_void_p(272), n, None, None) == -5
+    assert lib.latent_moe_forward(ctypes.byref(d), ctypes.byref(w2), p, p, p, p, n - 256, None,
+                                  None) == -5
+    # shared expert half given
+    w3 = lm.LmoeWeights(256, 256, 256, 256, None, None, 256, None)
+    assert lib.latent_moe_forward(ctypes.byref(d), ctypes.byref(w3), p, p, p, p, n, None, None) == -1
+    z = lm.make_dims(W.TINY)
+    z.T = 0
+    assert lib.latent_moe_forward(ctypes.byref(z), ctypes.byref(w), None, None, None, None, 0,
+                                  None, None) == 0
+
+
+def test_linear_validation(lib):
+    p = ctypes.c_void_p(16)
+    assert lib.lmoe_linear(p, p, None, p, 4, 100, 64, None) == -2
+    assert lib.lmoe_linear(p, p, None, p, 4, 128, 60, None) == -2
+    assert lib.lmoe_linear(None, p, None, p, 4, 128, 64, None) == -1
+    assert lib.lmoe_linear(p, p, None, p, 0, 128, 64, None) == 0
+
+
+def test_package_fails_loudly_without_library(tmp_path):
+    import latent_mixture_experts_sigmoid_gb300._binding as b
+    saved = b._lib
+    try:
+        b._lib = None
+        with pytest.raises(ImportError):
+            b.load_library(str(tmp_path / "missing.so"))
+    finally:
+        b._lib = saved

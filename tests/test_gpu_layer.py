@@ -1,0 +1,162 @@
+"""GPU parity of latent_moe_forward against the oracle.
+
+Layer outputs: max |gpu - oracle| / rms(oracle) <= 2e-2.  Expert ids,
+expert_num_tokens, offsets and the permuted row of every (token, slot): bit-exact.
+Routing weights: 1e-6 relative.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import lmoe_oracle as O
+
+pytestmark = pytest.mark.gpu
+lm = pytest.importorskip("latent_mixture_experts_sigmoid_gb300")
+
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_ok):
+    lm.load_library()
+
+
+def check_routing_and_permutation(d, dbg, logits, bias):
+    ids, w = O.route(logits, bias, d.topk, d.routed_scaling_factor, d.renormalize)
+    assert np.array_equal(dbg["topk_ids"], ids)
+    assert np.all(np.abs(dbg["topk_weights"] - w) <= 1e-6 * np.abs(w))
+    counts, offsets, row_of, _ = O.permute(ids, d.num_experts)
+    assert np.array_equal(dbg["expert_num_tokens"], counts)
+    assert np.array_equal(dbg["expert_offsets"], offsets)
+    assert np.array_equal(dbg["row_of"], row_of)
+
+
+def tiny_case(d, seed=0, gamma_noise=False, shared=True, zipf=False):
+    from tests.gpu_util import weights_to_device, run_layer, host_bits, rms_rel_err
+    wts = W.layer_weights(d, seed, gamma_noise)
+    if not shared:
+        wts["ws13"] = wts["ws2"] = None
+    x = W.hidden_states(d, seed)
+    lg = W.router_logits(d.T, d.num_experts, seed, zipf=zipf)
+    out, dbg = run_layer(lm, d, weights_to_device(wts), x, lg)
+    ref = O.bf16_to_f64(O.latent_moe_forward(d, wts, x, lg))
+    got = O.bf16_to_f64(host_bits(out))
+    assert rms_rel_err(got, ref) <= TOL, rms_rel_err(got, ref)
+    check_routing_and_permutation(d, dbg, lg, wts["bias"])
+    assert lm.lmoe_device_error() == 0
+
+
+def test_tiny_layer():
+    tiny_case(W.TINY)
+
+
+@pytest.mark.parametrize("T", [1, 3, 17, 100, 128, 129, 300, 1000])
+def test_tiny_layer_token_counts(T):
+    # decode regime up to 128 tokens, prefill regime above; ragged tails
+    tiny_case(dataclasses.replace(W.TINY, T=T), seed=T)
+
+
+@pytest.mark.parametrize("variant", ["no_shared", "linear_beta_unset", "gamma_noise", "top1",
+                                     "no_renorm", "zipf_prefill", "wide"])
+def test_tiny_layer_variants(variant):
+    d = W.TINY
+    kw = {}
+    if variant == "no_shared":
+        kw["shared"] = False
+    elif variant == "linear_beta_unset":
+        d = dataclasses.replace(d, linear_beta=0.0)
+    elif variant == "gamma_noise":
+        kw["gamma_noise"] = True
+    elif variant == "top1":
+        d = dataclasses.replace(d, topk=1)
+    elif variant == "no_renorm":
+        d = dataclasses.replace(d, renormalize=0, routed_scaling_factor=1.0)
+    elif variant == "zipf_prefill":
+        d = dataclasses.replace(d, T=700)
+        kw["zipf"] = True
+    elif variant == "wide":
+        d = dataclasses.replace(d, T=200, hidden=384, latent=256, inter=192, shared_inter=320,
+                                num_experts=40, topk=8)
+    tiny_case(d, seed=11, **kw)
+
+
+@pytest.fixture(scope="module")
+def big_weights():
+    from tests.gpu_util import device_layer_weights, oracle_layer_weights
+    d = W.DECODE
+    return device_layer_weights(d, 0), oracle_layer_weights(d, 0)
+
+
+def test_decode_layer_full(big_weights):
+    from tests.gpu_util import run_layer, host_bits, rms_rel_err
+    d = W.DECODE
+    wdev, wor = big_weights
+    x = W.hidden_states(d, 0)
+    lg = W.router_logits(d.T, d.num_experts, 0)
+    out, dbg = run_layer(lm, d, wdev, x, lg)
+    check_routing_and_permutation(d, dbg, lg, wor["bias"])
+    ref = O.bf16_to_f64(O.latent_moe_forward(d, wor, x, lg))
+    got = O.bf16_to_f64(host_bits(out))
+    assert rms_rel_err(got, ref) <= TOL, rms_rel_err(got, ref)
+    assert lm.lmoe_device_error() == 0
+
+
+def test_prefill_layer_zipf_sampled(big_weights):
+    from tests.gpu_util import run_layer, host_bits, rms_rel_err
+    d = W.PREFILL
+    wdev, wor = big_weights
+    x = W.hidden_states(d, 0)
+    lg = W.router_logits(d.T, d.num_experts, 0, zipf=True)
+    out, dbg = run_layer(lm, d, wdev, x, lg)
+    check_routing_and_permutation(d, dbg, lg, wor["bias"])
+    counts = dbg["expert_num_tokens"]
+    assert counts.max() > 500 and (counts == 0).sum() > 100     # the skew is real
+    toks = np.concatenate([[0, d.T - 1], np.random.default_rng(3).choice(d.T, 10, replace=False)])
+    ref = O.bf16_to_f64(O.latent_moe_forward(d, wor, x[toks], lg[toks]))
+    got = O.bf16_to_f64(host_bits(out))[toks]
+    assert rms_rel_err(got, ref) <= TOL, rms_rel_err(got, ref)
+    # every output finite
+    assert torch.isfinite(out.float()).all()
+    assert lm.lmoe_device_error() == 0
+
+
+def test_graph_replay_and_determinism():
+    from tests.gpu_util import weights_to_device, dev_bf16, dev_f32, DEV
+    d = dataclasses.replace(W.TINY, T=64)
+    wts = weights_to_device(W.layer_weights(d, 2))
+    x = dev_bf16(W.hidden_states(d, 2))
+    lg = dev_f32(W.router_logits(d.T, d.num_experts, 2))
+    ws = torch.empty(lm.latent_moe_workspace_bytes(d), dtype=torch.uint8, device=DEV)
+    a = torch.empty((d.T, d.hidden), dtype=torch.bfloat16, device=DEV)
+    b = torch.empty_like(a)
+    c = torch.zeros_like(a)
+    lm.latent_moe_forward(d, wts, x, lg, a, ws)
+    lm.latent_moe_forward(d, wts, x, lg, b, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        lm.latent_moe_forward(d, wts, x, lg, c, ws, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+
+
+def test_invalid_arguments_are_rejected():
+    from tests.gpu_util import DEV
+    d = W.TINY
+    ws = torch.empty(16, dtype=torch.uint8, device=DEV)
+    x = torch.zeros((d.T, d.hidden), dtype=torch.bfloat16, device=DEV)
+    lg = torch.zeros((d.T, d.num_experts), device=DEV)
+    with pytest.raises(lm.LmoeError) as e:
+        lm.latent_moe_forward(d, {"w_down": x, "w13": x, "w2": x, "w_up": x}, x, lg, x, ws)
+    assert e.value.status == -5   # workspace too small
+    for bad, st in [(dict(beta=0.0), -4), (dict(n_group=4), -3), (dict(hidden=200), -2),
+                    (dict(topk=65), -2)]:
+        with pytest.raises(lm.LmoeError) as e:
+            lm.latent_moe_forward(dataclasses.replace(d, **bad), {}, x, lg, x, ws)
+        assert e.value.status == st

@@ -1,0 +1,101 @@
+"""GPU parity of moe_route against the oracle: ids bit-exact, weights to 1e-6."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import lmoe_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+lm = pytest.importorskip("latent_mixture_experts_sigmoid_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_ok):
+    lm.load_library()
+    from tests.gpu_util import DEV  # noqa: F401
+
+
+def run_route(logits, bias, k, rsf, renorm=1):
+    from tests.gpu_util import dev_f32, DEV
+    T, E = logits.shape
+    ids = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    lm.moe_route(dev_f32(logits), None if bias is None else dev_f32(bias), k, rsf, ids, w,
+                 renormalize=renorm)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), w.cpu().numpy().astype(np.float64)
+
+
+def check(logits, bias, k, rsf, renorm=1):
+    ids, w = run_route(logits, bias, k, rsf, renorm)
+    rids, rw = O.route(logits, bias, k, rsf, renorm)
+    bad = np.nonzero((ids != rids).any(1))[0]
+    assert bad.size == 0, f"{bad.size} rows differ, first token {bad[0]}: {ids[bad[0]]} vs {rids[bad[0]]}"
+    rel = np.abs(w - rw) / np.abs(rw)
+    assert rel.max() <= 1e-6, rel.max()
+    assert lm.lmoe_device_error() == 0
+
+
+@pytest.mark.parametrize("T", W.ROUTE_TOKENS)
+def test_route_workload_896_top16(T):
+    logits = W.router_logits(T, W.ROUTE_E, seed=0, tie_every=64)
+    check(logits, W.score_bias(W.ROUTE_E, 0), W.ROUTE_K, W.ROUTE_RSF)
+
+
+def test_route_tie_run_zero_bias():
+    # bias = 0 makes every 64th row a full tie: ids 0..15, weights rsf/16
+    T = 1024
+    logits = W.router_logits(T, W.ROUTE_E, seed=1, tie_every=64)
+    check(logits, None, 16, 2.5)
+    ids, w = run_route(logits, None, 16, 2.5)
+    for t in range(0, T, 64):
+        assert ids[t].tolist() == list(range(16))
+        assert np.allclose(w[t], 2.5 / 16, rtol=1e-6)
+
+
+@pytest.mark.parametrize("E,k", [(1, 1), (8, 3), (33, 5), (64, 4), (100, 32), (256, 8),
+                                 (512, 16), (1000, 16), (1024, 1)])
+def test_route_shapes(E, k):
+    T = 97
+    g = np.random.default_rng(E * 100 + k)
+    logits = g.standard_normal((T, E)).astype(np.float32)
+    bias = (g.standard_normal(E) * 0.1).astype(np.float32)
+    check(logits, bias, k, 1.5)
+    check(logits, bias, k, 1.5, renorm=0)
+
+
+def test_route_sigmoid_bit_exact():
+    # E = 1, k = 1, no renormalisation, rsf = 1: the weight IS the fp32 sigmoid
+    x = np.concatenate([np.linspace(-120, 120, 200001, dtype=np.float32),
+                        np.float32([0.0, -0.0, 87.0, -87.0, 88.0, -88.0, 1e-30, -1e-30, 3.4e38,
+                                    -3.4e38])])
+    ids, w = run_route(x[:, None], None, 1, 1.0, renorm=0)
+    got = w[:, 0].astype(np.float32)
+    ref = O.sigmoid_f32(x)
+    diff = np.nonzero(got.view(np.uint32) != ref.view(np.uint32))[0]
+    assert diff.size == 0, f"{diff.size} differ, first x={x[diff[0]]}: {got[diff[0]]} vs {ref[diff[0]]}"
+
+
+def test_route_many_near_ties():
+    # logits on a coarse grid with a coarse bias give many equal and nearly
+    # equal keys, exercising the candidate bound and the fallback
+    T, E = 512, 896
+    g = np.random.default_rng(7)
+    logits = (g.integers(-8, 8, (T, E)) * 0.25).astype(np.float32)
+    bias = (g.integers(-2, 3, E) * 1e-6).astype(np.float32)
+    check(logits, bias, 16, 2.5)
+
+
+def test_route_invalid_arguments_launch_nothing():
+    from tests.gpu_util import DEV
+    x = torch.zeros((4, 8), device=DEV)
+    ids = torch.zeros((4, 2), dtype=torch.int32, device=DEV)
+    w = torch.zeros((4, 2), device=DEV)
+    for kw, st in [(dict(n_group=2), -3), (dict(topk_group=4), -3)]:
+        with pytest.raises(lm.LmoeError) as e:
+            lm.moe_route(x, None, 2, 1.0, ids, w, **kw)
+        assert e.value.status == st
+    with pytest.raises(lm.LmoeError):
+        lm.moe_route(x, None, 9, 1.0, ids, w)

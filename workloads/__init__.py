@@ -280,3 +280,18 @@ def masked_situ_input(E: int, T_max: int, two_d: int, seed: int = 0):
 
 def sentinel_like(shape) -> np.ndarray:
     return np.full(shape, SENTINEL, dtype=np.uint16)
+
+
+def expert_chunks(d: LayerDims, name: str, seed: int = 0, chunk: int = 64):
+    """Yield (e0, e1, bits[e1-e0, ...]) blocks of the stacked expert weights.
+
+    ``name`` is "w13" ([2*inter, latent] per expert) or "w2" ([latent, inter]).
+    Lets a caller fill a device tensor block by block without holding every
+    expert on the host.
+    """
+    fn = {"w13": w13_expert, "w2": w2_expert}[name]
+    for e0 in range(0, d.num_experts, chunk):
+        e1 = min(d.num_experts, e0 + chunk)
+        with ThreadPoolExecutor(_threads()) as ex:
+            parts = list(ex.map(lambda e: fn(d, e, seed), range(e0, e1)))
+        yield e0, e1, np.stack(parts)
