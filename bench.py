@@ -1,0 +1,402 @@
+"""Benchmark of the latent-MoE layer forward on GB300.
+
+Prints ONE JSON line (rank 0).  The headline workload is the prefill layer:
+T=4096 tokens, hidden 7168, latent 2048, 896 experts, top-16, expert
+intermediate 512, shared intermediate 4096, router logits skewed by a Zipf(1.1)
+per-expert offset; the T=8 decode layer of the same model is measured in the
+same run and reported under "decode".  A step is one latent_moe_forward call
+(routing, down-projection, permutation, grouped expert GEMMs with SituGLU,
+combine + RMSNorm, shared expert, up-projection with the shared add).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Inputs are seeded synthetic tensors (workloads/), resident in HBM before the
+timed region; L2 is flushed (a 512 MiB write) between timed steps.  --impl
+reference times the CPU oracle (oracle/) on a bounded sample of tokens of the
+same workload on the host cores.  With N > 1 (torchrun) every rank runs an
+independent replica (no collective on the data path) and rank 0 reports the
+whole-job rate over the slowest rank.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "latent-MoE layer tokens/s at T=8 and T=4096; % of HBM / bf16 TC roofline"
+UNIT = "tokens/s"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return dict(hbm=float(j["hbm_gbs"]), bf16=float(j["bf16_tflops"]),
+                    bf16_sus=float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+# --------------------------------------------------------------------------
+# algorithmic work per forward (counts only real rows: tokens actually routed)
+# --------------------------------------------------------------------------
+def gemm_flops(d, counts_nonzero):
+    T, H, L, dI, ds, k = d.T, d.hidden, d.latent, d.inter, d.shared_inter, d.topk
+    down = 2.0 * T * H * L
+    experts = 2.0 * T * k * (2 * dI * L + L * dI)
+    shared = 2.0 * T * (2 * ds * H + H * ds)
+    up = 2.0 * T * L * H
+    return dict(down=down, gemm1=2.0 * T * k * 2 * dI * L, gemm2=2.0 * T * k * L * dI,
+                shared1=2.0 * T * 2 * ds * H, shared2=2.0 * T * H * ds, up=up,
+                total=down + experts + shared + up)
+
+
+def gemm_bytes(d, n_used):
+    """Bytes a GEMM stage must move at least once (weights touched + activations)."""
+    T, H, L, dI, ds, k = d.T, d.hidden, d.latent, d.inter, d.shared_inter, d.topk
+    R = T * k
+    return dict(
+        down=2 * (L * H + T * H + T * L),
+        gemm1=2 * (n_used * 2 * dI * L + R * L + R * 2 * dI),
+        gemm2=2 * (n_used * L * dI + R * dI + R * L),
+        shared1=2 * (2 * ds * H + T * H + T * 2 * ds),
+        shared2=2 * (H * ds + T * ds + T * H),
+        up=2 * (H * L + T * L + 2 * T * H))
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = tempfile.mktemp(suffix=".csv")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    smax.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+def run_ours(args, rank, world):
+    import torch
+    import latent_mixture_experts_sigmoid_gb300 as lm
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    lm.load_library()
+    pk = peaks()
+
+    def dev_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    # weights shared by both workloads (same model)
+    dD = W.DECODE
+    w = {"w13": torch.empty((dD.num_experts, 2 * dD.inter, dD.latent), dtype=torch.bfloat16, device=dev),
+         "w2": torch.empty((dD.num_experts, dD.latent, dD.inter), dtype=torch.bfloat16, device=dev)}
+    for name in ("w13", "w2"):
+        for e0, e1, bits in W.expert_chunks(dD, name, 0):
+            w[name][e0:e1].copy_(dev_bf16(bits))
+    w.update(w_down=dev_bf16(W.w_down(dD)), w_up=dev_bf16(W.w_up(dD)), ws13=dev_bf16(W.ws13(dD)),
+             ws2=dev_bf16(W.ws2(dD)), norm_w=dev_bf16(W.norm_weight(dD)),
+             bias=torch.from_numpy(W.score_bias(dD.num_experts)).to(dev))
+    flush = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def measure(d, zipf, steps, warmup):
+        T = d.T
+        x_bits = W.hidden_states(d, 0)
+        lg = W.router_logits(T, d.num_experts, 0, zipf=zipf)
+        x = dev_bf16(x_bits)
+        lgd = torch.from_numpy(lg).to(dev)
+        out = torch.empty((T, d.hidden), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(lm.latent_moe_workspace_bytes(d), dtype=torch.uint8, device=dev)
+        counts = torch.empty(d.num_experts, dtype=torch.int32, device=dev)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(lm.NUM_STAGES + 1)]
+        dbg = {"expert_num_tokens": counts, "stage_events": evs}
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                lm.latent_moe_forward(d, w, x, lgd, out, ws, debug=dbg, stream=stream)
+        torch.cuda.synchronize()
+        n_used = int((counts.cpu().numpy() > 0).sum())
+        # device-timed region: K steps, stage events around every stage
+        barrier()
+        torch.cuda.synchronize()
+        per_step, per_stage = [], np.zeros(lm.NUM_STAGES)
+        for _ in range(steps):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                lm.latent_moe_forward(d, w, x, lgd, out, ws, debug=dbg, stream=stream)
+            stream.synchronize()
+            t = [evs[i].elapsed_time(evs[i + 1]) for i in range(lm.NUM_STAGES)]
+            per_stage += np.array(t)
+            per_step.append(evs[0].elapsed_time(evs[-1]))
+        torch.cuda.synchronize()
+        barrier()
+        ms = float(sum(per_step))
+        # end to end through the public API with host buffers
+        xh = torch.from_numpy(x_bits.view(np.int16)).pin_memory()
+        lh = torch.from_numpy(lg).pin_memory()
+        oh = torch.empty((T, d.hidden), dtype=torch.int16).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2e_ms = 0.0
+        for _ in range(steps):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                e0.record(stream)
+                x.view(torch.int16).copy_(xh, non_blocking=True)
+                lgd.copy_(lh, non_blocking=True)
+                lm.latent_moe_forward(d, w, x, lgd, out, ws, stream=stream)
+                oh.copy_(out.view(torch.int16), non_blocking=True)
+                e1.record(stream)
+            stream.synchronize()
+            e2e_ms += e0.elapsed_time(e1)
+        return dict(ms=ms, per_step=per_step, per_stage=per_stage / steps, n_used=n_used,
+                    e2e_ms=e2e_ms, h2d=T * d.hidden * 2 + T * d.num_experts * 4,
+                    d2h=T * d.hidden * 2)
+
+    clocks = Clocks(dev.index)
+    t_wall0 = time.time()
+    pre = measure(W.PREFILL, True, args.steps, args.warmup)
+    dec = measure(W.DECODE, False, args.steps, args.warmup)
+    clk = clocks.stop()
+    wall = time.time() - t_wall0
+
+    # max over ranks
+    def allmax(v):
+        if world == 1:
+            return v
+        import torch.distributed as dist
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    pre_ms = allmax(pre["ms"])
+    dec_ms = allmax(dec["ms"])
+    pre_e2e = allmax(pre["e2e_ms"])
+    dec_e2e = allmax(dec["e2e_ms"])
+    if rank != 0:
+        return
+    K = args.steps
+    dP, dDc = W.PREFILL, W.DECODE
+    value = world * dP.T * K / (pre_ms / 1e3)
+
+    # roofline of the dominant kernel (the tcgen05 GEMM, all its launches of a step)
+    names = lm.STAGE_NAMES
+    st = dict(zip(names, pre["per_stage"]))
+    fl = gemm_flops(dP, pre["n_used"])
+    gemm_stages = ["down", "gemm1", "gemm2", "shared1", "shared2", "up"]
+    gemm_ms = sum(st[s] for s in gemm_stages)
+    ach_tf = fl["total"] / (gemm_ms / 1e3) / 1e12
+    roof = {"kernel": "gemm_tc_kernel (all GEMM launches of one prefill forward)",
+            "bound": "tensor", "achieved": round(ach_tf, 1), "peak": pk["bf16_sus"],
+            "unit": "TFLOP/s", "frac": round(ach_tf / pk["bf16_sus"], 4),
+            "peak_source": f"{pk['source']} bf16 sustained", "traffic": None,
+            "flops_per_launch_set": fl["total"], "ms_per_launch_set": round(gemm_ms, 4)}
+    per_stage_pre = {n: round(v, 4) for n, v in st.items()}
+    per_stage_dec = {n: round(v, 4) for n, v in zip(names, dec["per_stage"])}
+    # decode roofline: weight streaming of the whole layer
+    by = gemm_bytes(dDc, dec["n_used"])
+    dec_bytes = sum(by.values())
+    dec_us = dec_ms / K * 1e3
+    dec_gbs = dec_bytes / (dec_us / 1e6) / 1e9
+    decode = {"workload": "decode T=8", "tokens_per_s": round(world * dDc.T * K / (dec_ms / 1e3), 1),
+              "us_per_step": round(dec_us, 2), "experts_used": dec["n_used"],
+              "algorithmic_bytes": dec_bytes,
+              "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": pk["hbm"],
+                           "unit": "GB/s", "frac": round(dec_gbs / pk["hbm"], 4)},
+              "per_stage_ms": per_stage_dec,
+              "e2e_tokens_per_s": round(world * dDc.T * K / (dec_e2e / 1e3), 1)}
+    launches = lm.latent_moe_launch_count(dP) + lm.latent_moe_launch_count(dDc)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(pre_ms / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) bf16 weights)",
+        "config": {"workload": "latent-MoE layer prefill T=4096, Zipf(1.1)-skewed routing",
+                   "T": dP.T, "hidden": dP.hidden, "latent": dP.latent,
+                   "num_experts": dP.num_experts, "topk": dP.topk, "inter": dP.inter,
+                   "shared_inter": dP.shared_inter, "experts_used": pre["n_used"],
+                   "l2": "flushed between timed steps (512 MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": round(world * dP.T * K / (pre_e2e / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": pre["h2d"], "d2h_bytes_per_step": pre["d2h"]},
+        "gpu_launches": launches * K,
+        "roofline": roof,
+        "per_stage_ms": per_stage_pre,
+        "layer_gflop": round(fl["total"] / 1e9, 1),
+        "layer_tflops": round(fl["total"] / (pre_ms / K / 1e3) / 1e12, 1),
+        "decode": decode,
+        "clocks": clk,
+        "wall_s": round(wall, 1),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(W.PREFILL, budget_s=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# the oracle on the host cores
+# --------------------------------------------------------------------------
+def _cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("internal_api") in
+             ("openblas", "mkl", "blis")]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def _oracle_sample(d, tokens, zipf):
+    """Inputs of a token sample plus the weights it touches (generated up front)."""
+    from oracle import lmoe_oracle as O
+    x = W.hidden_rows(d, tokens, 0)
+    lg = W.logits_rows(d.num_experts, tokens, 0, zipf=zipf)
+    ids, _ = O.route(lg, W.score_bias(d.num_experts, 0), d.topk, d.routed_scaling_factor)
+    used = sorted(set(ids.ravel().tolist()))
+    w13 = {e: W.w13_expert(d, e, 0) for e in used}
+    w2 = {e: W.w2_expert(d, e, 0) for e in used}
+    wts = dict(w_down=W.w_down(d), w_up=W.w_up(d), ws13=W.ws13(d), ws2=W.ws2(d),
+               norm_w=W.norm_weight(d), bias=W.score_bias(d.num_experts, 0),
+               w13=w13.__getitem__, w2=w2.__getitem__)
+    return x, lg, wts
+
+
+def cpu_baseline(d, budget_s=20.0, sample=16):
+    from oracle import lmoe_oracle as O
+    toks = list(range(0, d.T, max(1, d.T // sample)))[:sample]
+    x, lg, wts = _oracle_sample(d, toks, zipf=True)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        O.latent_moe_forward(d, wts, x, lg)
+        n += 1
+        if time.perf_counter() - t0 > min(budget_s, 5.0) or n >= 3:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": round(len(toks) / dt, 2), "unit": UNIT, "cores": _cores(), "kind": "oracle",
+            "sample": f"{len(toks)} of the {d.T} tokens of the prefill workload per call "
+                      f"(float64 NumPy oracle, weights pre-generated), {n} call(s)"}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step is a bounded token sample."""
+    if rank != 0:
+        return
+    from oracle import lmoe_oracle as O
+    d = W.PREFILL
+    sample = 8
+    toks = list(range(0, d.T, d.T // sample))[:sample]
+    x, lg, wts = _oracle_sample(d, toks, zipf=True)
+    for _ in range(args.warmup):
+        O.latent_moe_forward(d, wts, x, lg)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.latent_moe_forward(d, wts, x, lg)
+    dt = time.perf_counter() - t0
+    value = len(toks) * args.steps / dt
+    cores = _cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "latent-MoE layer prefill T=4096, Zipf(1.1)-skewed routing",
+                   "sample_tokens_per_step": len(toks)},
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{len(toks)} tokens of the T=4096 prefill workload per step"},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        dist.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -146,18 +146,43 @@ typedef struct lmoe_weights {
   const float* e_score_correction_bias; /* [E] or NULL (= zeros)             */
 } lmoe_weights;
 
-/* Optional copies of the layer's routing and permutation (any may be NULL). */
+/* Stages of one forward, in launch order (for per-stage timing).            */
+enum {
+  LMOE_STAGE_ROUTE = 0,        /* routing                                    */
+  LMOE_STAGE_DOWN = 1,         /* latent down-projection GEMM                */
+  LMOE_STAGE_PERMUTE = 2,      /* counts, offsets, rows                      */
+  LMOE_STAGE_SCATTER = 3,      /* routed input into expert-major rows        */
+  LMOE_STAGE_GEMM1 = 4,        /* grouped expert GEMM1                       */
+  LMOE_STAGE_SITU = 5,         /* SituGLU of the experts                     */
+  LMOE_STAGE_GEMM2 = 6,        /* grouped expert GEMM2                       */
+  LMOE_STAGE_COMBINE = 7,      /* top-k combine + RMSNorm                    */
+  LMOE_STAGE_SHARED1 = 8,      /* shared expert GEMM1 + SituGLU              */
+  LMOE_STAGE_SHARED2 = 9,      /* shared expert GEMM2                        */
+  LMOE_STAGE_UP = 10,          /* up-projection + shared add                 */
+  LMOE_NUM_STAGES = 11
+};
+
+/* Optional outputs for inspection (any member may be NULL / 0).              */
 typedef struct lmoe_debug {
   int32_t* topk_ids;          /* [T, k]                                      */
   float* topk_weights;        /* [T, k]                                      */
   int32_t* expert_num_tokens; /* [E]                                         */
   int32_t* expert_offsets;    /* [E+1]: expert e owns rows off[e]..off[e+1]-1 */
   int32_t* row_of;            /* [T, k]: permuted row of (token, slot)       */
+  void** stage_events;        /* LMOE_NUM_STAGES + 1 cudaEvent_t (host array, */
+                              /* created by the caller): event 0 is recorded */
+                              /* before the first stage, event i+1 after      */
+                              /* stage i, all on `stream`.                    */
 } lmoe_debug;
 
 /* Bytes of device workspace latent_moe_forward needs for these dims (0 on   */
 /* invalid dims).  Depends on the dims only.                                  */
 size_t latent_moe_workspace_bytes(const lmoe_dims* dims);
+
+/* Number of kernel launches latent_moe_forward makes for these dims (0 on   */
+/* invalid dims), without the optional debug copies.  Uses the current       */
+/* device's SM count.                                                         */
+int latent_moe_launch_count(const lmoe_dims* dims, int has_shared_expert);
 
 /* hidden [T, H] bf16, router_logits [T, E] fp32, out [T, H] bf16; workspace  */
 /* at least latent_moe_workspace_bytes(dims) bytes, 256-byte aligned, not     */

@@ -25,7 +25,7 @@ LMOE_ERR_CUDA = -6
 LMOE_ERR_ALIGN = -7
 
 ABI_FUNCTIONS = ("moe_route", "situ_and_mul", "masked_situ_and_mul", "latent_moe_forward",
-                 "latent_moe_workspace_bytes", "lmoe_linear", "lmoe_status_string",
+                 "latent_moe_workspace_bytes", "latent_moe_launch_count", "lmoe_linear", "lmoe_status_string",
                  "lmoe_device_error", "lmoe_abi_version")
 
 
@@ -53,7 +53,12 @@ class LmoeWeights(ctypes.Structure):
 class LmoeDebug(ctypes.Structure):
     _fields_ = [("topk_ids", ctypes.c_void_p), ("topk_weights", ctypes.c_void_p),
                 ("expert_num_tokens", ctypes.c_void_p), ("expert_offsets", ctypes.c_void_p),
-                ("row_of", ctypes.c_void_p)]
+                ("row_of", ctypes.c_void_p), ("stage_events", ctypes.c_void_p)]
+
+
+NUM_STAGES = 11
+STAGE_NAMES = ("route", "down", "permute", "scatter", "gemm1", "situ", "gemm2", "combine_norm",
+               "shared1", "shared2", "up")
 
 
 _lib = None
@@ -78,6 +83,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.masked_situ_and_mul.restype = i32
     lib.latent_moe_workspace_bytes.argtypes = [ctypes.POINTER(LmoeDims)]
     lib.latent_moe_workspace_bytes.restype = ctypes.c_size_t
+    lib.latent_moe_launch_count.argtypes = [ctypes.POINTER(LmoeDims), i32]
+    lib.latent_moe_launch_count.restype = i32
     lib.latent_moe_forward.argtypes = [ctypes.POINTER(LmoeDims), ctypes.POINTER(LmoeWeights), vp,
                                        vp, vp, vp, ctypes.c_size_t, ctypes.POINTER(LmoeDebug), vp]
     lib.latent_moe_forward.restype = i32
@@ -183,9 +190,17 @@ def latent_moe_forward(dims, weights, hidden, router_logits, out, workspace,
         workspace_bytes = workspace.numel() * workspace.element_size()
     dbg = None
     if debug:
+        ev = debug.get("stage_events")
+        ev_arr = None
+        if ev is not None:
+            for e in ev:                  # torch creates the CUDA event on first record
+                if not e.cuda_event:
+                    e.record()
+            ev_arr = (ctypes.c_void_p * len(ev))(*[e.cuda_event for e in ev])
         dbg = LmoeDebug(_ptr(debug.get("topk_ids")), _ptr(debug.get("topk_weights")),
                         _ptr(debug.get("expert_num_tokens")), _ptr(debug.get("expert_offsets")),
-                        _ptr(debug.get("row_of")))
+                        _ptr(debug.get("row_of")),
+                        ctypes.cast(ev_arr, ctypes.c_void_p) if ev_arr is not None else None)
     st = load_library().latent_moe_forward(ctypes.byref(dd), ctypes.byref(ww), _ptr(hidden),
                                            _ptr(router_logits), _ptr(out), _ptr(workspace),
                                            int(workspace_bytes),
@@ -203,6 +218,11 @@ def lmoe_linear(x, w, out, add=None, stream=None, T: int | None = None, N: int |
     st = load_library().lmoe_linear(_ptr(x), _ptr(w), _ptr(add), _ptr(out), int(T), int(N),
                                     int(K), _stream(stream))
     _check(st, "lmoe_linear")
+
+
+def latent_moe_launch_count(dims, has_shared_expert: bool = True) -> int:
+    dd = dims if isinstance(dims, LmoeDims) else make_dims(dims)
+    return int(load_library().latent_moe_launch_count(ctypes.byref(dd), 1 if has_shared_expert else 0))
 
 
 def lmoe_device_error(clear: bool = False) -> int:

@@ -212,6 +212,35 @@ cudaError_t gemm_grouped(const uint16_t* W, int E, int M_feat, const uint16_t* X
   return launch_gemm(g, s);
 }
 
+struct Plan {
+  bool decode;
+  int tile;          // token tile of the grouped GEMMs
+  int g1_bn, g2_bn;  // MMA N of the grouped GEMMs
+  DenseCfg down, s1, s2, up;
+};
+
+Plan make_plan(const lmoe_dims& d, int nsm) {
+  Plan p;
+  p.decode = d.T <= kDecodeMaxT;
+  p.tile = p.decode ? round_up(d.T, 16) : 128;
+  p.g1_bn = p.decode ? p.tile : ((2 * d.inter) % 256 == 0 ? 256 : 128);
+  p.g2_bn = p.decode ? p.tile : (d.latent % 256 == 0 ? 256 : 128);
+  p.down = dense_cfg(d.T, d.latent, d.hidden, nsm);
+  p.s1 = dense_cfg(d.T, 2 * d.shared_inter, d.hidden, nsm);
+  p.s2 = dense_cfg(d.T, d.hidden, d.shared_inter, nsm);
+  p.up = dense_cfg(d.T, d.hidden, d.latent, nsm);
+  return p;
+}
+
+int plan_launches(const Plan& p, bool shared) {
+  int n = 1 + 1 + 3 + 1 + 3 + 1;        // route, down, permute, scatter, experts, combine
+  if (shared) n += 3;                   // shared GEMM1 + SituGLU, shared GEMM2
+  n += 1;                               // up-projection GEMM
+  const bool sh_part = shared && p.s2.splits > 1;
+  if (p.up.splits > 1 || sh_part) n += 1;   // fixed-order reduction
+  return n;
+}
+
 #define LMOE_TRY(x)                                  \
   do {                                               \
     if ((x) != cudaSuccess) return LMOE_ERR_CUDA;    \
@@ -299,6 +328,12 @@ int lmoe_linear(const lmoe_bf16* x, const lmoe_bf16* w, const lmoe_bf16* add, lm
   return LMOE_OK;
 }
 
+int latent_moe_launch_count(const lmoe_dims* dims, int has_shared_expert) {
+  if (validate_dims(dims) != LMOE_OK) return 0;
+  if (dims->T == 0) return 0;
+  return plan_launches(make_plan(*dims, num_sms()), has_shared_expert != 0);
+}
+
 size_t latent_moe_workspace_bytes(const lmoe_dims* dims) {
   if (validate_dims(dims) != LMOE_OK) return 0;
   return carve(*dims, nullptr, nullptr);
@@ -336,41 +371,52 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
   const int T = d.T, k = d.topk, E = d.num_experts, H = d.hidden, L = d.latent;
   const int dI = d.inter, ds = d.shared_inter;
   const long long rows = (long long)T * k;
-  const int nsm = num_sms();
-  const bool decode = T <= kDecodeMaxT;
-  const int tile = decode ? round_up(T, 16) : 128;   // token tile of the grouped GEMMs
+  const Plan pl = make_plan(d, num_sms());
+  const bool decode = pl.decode;
+  const int tile = pl.tile;
   const uint16_t* X = hidden;
+  void** ev = dbg ? dbg->stage_events : nullptr;
+  auto mark = [&](int i) -> bool {
+    return ev == nullptr || cudaEventRecord((cudaEvent_t)ev[i], s) == cudaSuccess;
+  };
+  if (!mark(0)) return LMOE_ERR_CUDA;
 
   // 1. routing
   LMOE_TRY(launch_route(router_logits, wt->e_score_correction_bias, T, E, k, d.renormalize,
                         d.routed_scaling_factor, ws.ids, ws.w, s));
+  if (!mark(LMOE_STAGE_ROUTE + 1)) return LMOE_ERR_CUDA;
   // 2. latent down-projection
-  const DenseCfg cdown = dense_cfg(T, L, H, nsm);
+  const DenseCfg cdown = pl.down;
   const bool down_split = cdown.splits > 1;
   const long long down_stride = (long long)T * L;
   LMOE_TRY(gemm_dense(wt->w_down, L, X, T, H, cdown, down_split ? (void*)ws.Pa : (void*)ws.Z,
                       down_split, down_stride, nullptr, s));
+  if (!mark(LMOE_STAGE_DOWN + 1)) return LMOE_ERR_CUDA;
   // 3. permutation
   LMOE_TRY(launch_permute(ws.ids, T, k, E, tile, ws.perm_scratch, ws.counts, ws.offsets,
                           ws.tile_prefix, ws.row_of, ws.tok_of_row, s));
+  if (!mark(LMOE_STAGE_PERMUTE + 1)) return LMOE_ERR_CUDA;
   // 4. routed input into the expert-major rows
   LMOE_TRY(launch_scatter_rows(down_split ? nullptr : ws.Z, down_split ? ws.Pa : nullptr,
                                cdown.splits, down_stride, T, L, k, ws.row_of, ws.A, s));
+  if (!mark(LMOE_STAGE_SCATTER + 1)) return LMOE_ERR_CUDA;
   // 5-7. experts
-  const int g1_bn = decode ? tile : ((2 * dI) % 256 == 0 ? 256 : 128);
-  const int g2_bn = decode ? tile : (L % 256 == 0 ? 256 : 128);
-  LMOE_TRY(gemm_grouped(wt->w13, E, 2 * dI, ws.A, rows, L, !decode, g1_bn, ws, tile, ws.G, s));
+  LMOE_TRY(gemm_grouped(wt->w13, E, 2 * dI, ws.A, rows, L, !decode, pl.g1_bn, ws, tile, ws.G, s));
+  if (!mark(LMOE_STAGE_GEMM1 + 1)) return LMOE_ERR_CUDA;
   LMOE_TRY(launch_situ(ws.G, ws.act, rows, dI, d.beta, d.linear_beta, s));
-  LMOE_TRY(gemm_grouped(wt->w2, E, L, ws.act, rows, dI, !decode, g2_bn, ws, tile, ws.Y, s));
+  if (!mark(LMOE_STAGE_SITU + 1)) return LMOE_ERR_CUDA;
+  LMOE_TRY(gemm_grouped(wt->w2, E, L, ws.act, rows, dI, !decode, pl.g2_bn, ws, tile, ws.Y, s));
+  if (!mark(LMOE_STAGE_GEMM2 + 1)) return LMOE_ERR_CUDA;
   // 8. combine + RMSNorm
   LMOE_TRY(launch_combine_norm(ws.Y, ws.w, ws.row_of, T, k, L, wt->norm_w, d.rms_eps, ws.N, s));
+  if (!mark(LMOE_STAGE_COMBINE + 1)) return LMOE_ERR_CUDA;
   // 9-11. shared expert on the original hidden states
   const float* sh_part = nullptr;
   int sh_splits = 0;
   long long sh_stride = 0;
   const uint16_t* sh_bf16 = nullptr;
   if (shared) {
-    const DenseCfg c1 = dense_cfg(T, 2 * ds, H, nsm);
+    const DenseCfg c1 = pl.s1;
     const long long s1_stride = (long long)T * 2 * ds;
     if (c1.splits > 1) {
       LMOE_TRY(gemm_dense(wt->ws13, 2 * ds, X, T, H, c1, ws.Pb, 1, s1_stride, nullptr, s));
@@ -380,7 +426,10 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
       LMOE_TRY(gemm_dense(wt->ws13, 2 * ds, X, T, H, c1, ws.Gs, 0, 0, nullptr, s));
       LMOE_TRY(launch_situ(ws.Gs, ws.As, T, ds, d.beta, d.linear_beta, s));
     }
-    const DenseCfg c2 = dense_cfg(T, H, ds, nsm);
+  }
+  if (!mark(LMOE_STAGE_SHARED1 + 1)) return LMOE_ERR_CUDA;
+  if (shared) {
+    const DenseCfg c2 = pl.s2;
     sh_stride = (long long)T * H;
     if (c2.splits > 1) {
       LMOE_TRY(gemm_dense(wt->ws2, H, ws.As, T, ds, c2, ws.Pb, 1, sh_stride, nullptr, s));
@@ -391,8 +440,9 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
       sh_bf16 = ws.Sh;
     }
   }
+  if (!mark(LMOE_STAGE_SHARED2 + 1)) return LMOE_ERR_CUDA;
   // 12. up-projection with the shared output added in the epilogue
-  const DenseCfg cup = dense_cfg(T, H, L, nsm);
+  const DenseCfg cup = pl.up;
   if (cup.splits > 1) {
     const long long up_stride = (long long)T * H;
     LMOE_TRY(gemm_dense(wt->w_up, H, ws.N, T, L, cup, ws.Pa, 1, up_stride, nullptr, s));
@@ -407,6 +457,7 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
     }
     LMOE_TRY(gemm_dense(wt->w_up, H, ws.N, T, L, cup, out, 0, 0, sh_bf16, s));
   }
+  if (!mark(LMOE_STAGE_UP + 1)) return LMOE_ERR_CUDA;
   // optional copies of the routing and permutation
   if (dbg) {
     if (dbg->topk_ids)

@@ -32,10 +32,33 @@ __device__ __forceinline__ uint16_t to_bf16(float x) {
 // ---------------------------------------------------------------------------
 // SituGLU scalar math (vLLM PR #50088, commit 2), fp32
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float tanh_fast(float x) {
+// Written from the identities
+//   tanh(a)    = -m / (2 + m),   m = e^{-2|a|} - 1   (sign restored separately)
+//   sigmoid(g) = 1 / (1 + e^{-g})
+// so that one reciprocal serves the whole product:
+//   out = [beta*sgn(g)*(-m1)] * [linear_beta*sgn(u)*(-m2)  or  u]
+//         / [(2 + m1) * (1 + e^{-g}) * (2 + m2  or  1)]
+// m = e^z - 1 (z <= 0) comes from the hardware 2^x for |z| >= 0.2 and from
+// its Taylor series to z^5 below that (no cancellation); relative error of
+// every factor is about 1e-6, so the bf16 result is almost always the
+// correctly rounded one.  A denominator beyond 2^126 (gate below about -87)
+// gives 0, the value to bf16 precision.
+__device__ __forceinline__ float ex2_fast(float x) {
   float y;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ float expm1_neg(float z) {   // e^z - 1 for z <= 0
+  if (z > -0.2f) {
+    float p = 1.0f / 120.0f;
+    p = fmaf(p, z, 1.0f / 24.0f);
+    p = fmaf(p, z, 1.0f / 6.0f);
+    p = fmaf(p, z, 0.5f);
+    p = fmaf(p, z, 1.0f);
+    return p * z;
+  }
+  return ex2_fast(z * 1.4426950408889634f) - 1.0f;
 }
 
 struct SituParams {
@@ -44,10 +67,18 @@ struct SituParams {
 };
 
 __device__ __forceinline__ float situ1(float g, float u, const SituParams& p) {
-  const float sig = __fdividef(1.0f, 1.0f + __expf(-g));
-  const float gate_out = p.beta * tanh_fast(g * p.inv_beta) * sig;
-  const float up_out = p.has_lbeta ? p.lbeta * tanh_fast(u * p.inv_lbeta) : u;
-  return gate_out * up_out;
+  const float m1 = expm1_neg(-2.0f * fabsf(g * p.inv_beta));
+  const float e = ex2_fast(-g * 1.4426950408889634f);
+  float num = copysignf(p.beta, g) * (-m1);
+  float den = (2.0f + m1) * (1.0f + e);
+  if (p.has_lbeta) {
+    const float m2 = expm1_neg(-2.0f * fabsf(u * p.inv_lbeta));
+    num *= copysignf(p.lbeta, u) * (-m2);
+    den *= (2.0f + m2);
+  } else {
+    num *= u;
+  }
+  return __fdividef(num, den);
 }
 
 __device__ __forceinline__ uint32_t situ2(uint32_t g2, uint32_t u2, const SituParams& p) {

@@ -8,11 +8,9 @@
 // fp32 and results go straight to the output buffer.  The masked kernel reads
 // expert_num_tokens and never touches padded rows.
 //
-// Bandwidth-bound: every thread moves 16-byte vectors (8 bf16).  tanh uses the
-// hardware tanh.approx.f32 (relative error about 2^-11), sigmoid uses
-// __expf/__fdividef (relative error ~1e-5, also for large negative gates); the
-// product is rounded once to bf16, so the result is within one bf16 step of
-// the exactly rounded value.
+// Bandwidth-bound: every thread moves 16-byte vectors (8 bf16); the scalar
+// math (one hardware 2^x per exponential, one reciprocal per element, relative
+// error about 1e-6) lives with the other SituGLU users in lmoe_internal.cuh.
 #include "lmoe_internal.cuh"
 
 namespace lmoe {

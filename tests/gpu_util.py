@@ -96,3 +96,25 @@ def run_layer(lm, d, wdev: dict, hidden_bits, logits, debug=True, stream=None):
                           stream=stream)
     torch.cuda.synchronize()
     return out, ({k2: v.cpu().numpy() for k2, v in dbg.items()} if dbg else None)
+
+
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of the bf16 grid at |v| (2^(floor(log2|v|) - 7), at least 2^-133)."""
+    _, e = np.frexp(np.abs(v))
+    return np.ldexp(1.0, np.maximum(e - 1, -126) - 7)
+
+
+def assert_layer_close(got: np.ndarray, ref: np.ndarray, tol: float = 2e-2) -> dict:
+    """Layer parity: every element within tol * rms(ref), or within one bf16
+    step of ref (the output's own quantisation: at |ref| >= 4 rms one bf16
+    step is already about 2e-2 * rms, so two correct fp32/fp64 evaluations that
+    round to neighbouring bf16 values would otherwise fail)."""
+    err = np.abs(got - ref)
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    bound = np.maximum(tol * rms, bf16_ulp(ref))
+    bad = err > bound
+    stats = dict(max_err_over_rms=float(err.max() / rms), frac_differing=float((err > 0).mean()),
+                 max_err_in_ulps=float((err / bf16_ulp(ref)).max()))
+    assert not bad.any(), (f"{bad.sum()} elements beyond max({tol}*rms, 1 bf16 step); "
+                           f"first at {np.argwhere(bad)[0]}; {stats}")
+    return stats

@@ -1,6 +1,7 @@
 """GPU parity of latent_moe_forward against the oracle.
 
-Layer outputs: max |gpu - oracle| / rms(oracle) <= 2e-2.  Expert ids,
+Layer outputs: |gpu - oracle| <= max(2e-2 * rms(oracle), one bf16 step at the
+oracle value), elementwise (see tests/gpu_util.assert_layer_close).  Expert ids,
 expert_num_tokens, offsets and the permuted row of every (token, slot): bit-exact.
 Routing weights: 1e-6 relative.
 """
@@ -35,7 +36,7 @@ def check_routing_and_permutation(d, dbg, logits, bias):
 
 
 def tiny_case(d, seed=0, gamma_noise=False, shared=True, zipf=False):
-    from tests.gpu_util import weights_to_device, run_layer, host_bits, rms_rel_err
+    from tests.gpu_util import weights_to_device, run_layer, host_bits, assert_layer_close
     wts = W.layer_weights(d, seed, gamma_noise)
     if not shared:
         wts["ws13"] = wts["ws2"] = None
@@ -44,7 +45,7 @@ def tiny_case(d, seed=0, gamma_noise=False, shared=True, zipf=False):
     out, dbg = run_layer(lm, d, weights_to_device(wts), x, lg)
     ref = O.bf16_to_f64(O.latent_moe_forward(d, wts, x, lg))
     got = O.bf16_to_f64(host_bits(out))
-    assert rms_rel_err(got, ref) <= TOL, rms_rel_err(got, ref)
+    assert_layer_close(got, ref, TOL)
     check_routing_and_permutation(d, dbg, lg, wts["bias"])
     assert lm.lmoe_device_error() == 0
 
@@ -91,7 +92,7 @@ def big_weights():
 
 
 def test_decode_layer_full(big_weights):
-    from tests.gpu_util import run_layer, host_bits, rms_rel_err
+    from tests.gpu_util import run_layer, host_bits, assert_layer_close
     d = W.DECODE
     wdev, wor = big_weights
     x = W.hidden_states(d, 0)
@@ -100,12 +101,12 @@ def test_decode_layer_full(big_weights):
     check_routing_and_permutation(d, dbg, lg, wor["bias"])
     ref = O.bf16_to_f64(O.latent_moe_forward(d, wor, x, lg))
     got = O.bf16_to_f64(host_bits(out))
-    assert rms_rel_err(got, ref) <= TOL, rms_rel_err(got, ref)
+    print(assert_layer_close(got, ref, TOL))
     assert lm.lmoe_device_error() == 0
 
 
 def test_prefill_layer_zipf_sampled(big_weights):
-    from tests.gpu_util import run_layer, host_bits, rms_rel_err
+    from tests.gpu_util import run_layer, host_bits, assert_layer_close
     d = W.PREFILL
     wdev, wor = big_weights
     x = W.hidden_states(d, 0)
@@ -117,7 +118,7 @@ def test_prefill_layer_zipf_sampled(big_weights):
     toks = np.concatenate([[0, d.T - 1], np.random.default_rng(3).choice(d.T, 10, replace=False)])
     ref = O.bf16_to_f64(O.latent_moe_forward(d, wor, x[toks], lg[toks]))
     got = O.bf16_to_f64(host_bits(out))[toks]
-    assert rms_rel_err(got, ref) <= TOL, rms_rel_err(got, ref)
+    print(assert_layer_close(got, ref, TOL))
     # every output finite
     assert torch.isfinite(out.float()).all()
     assert lm.lmoe_device_error() == 0
