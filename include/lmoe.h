@@ -179,6 +179,18 @@ typedef struct lmoe_debug {
 /* invalid dims).  Depends on the dims only.                                  */
 size_t latent_moe_workspace_bytes(const lmoe_dims* dims);
 
+/* Byte offsets of the layer's intermediate buffers inside the workspace, in */
+/* this order (LMOE_WS_COUNT entries), for inspection after a call:           */
+/*   0 topk_ids int32 [T,k]    1 topk_weights fp32 [T,k]  2 counts int32 [E]   */
+/*   3 offsets int32 [E+1]     4 row_of int32 [T,k]       5 Z bf16 [T,L]       */
+/*   6 A bf16 [T*k,L]          7 G bf16 [T*k,2d]          8 act bf16 [T*k,d]   */
+/*   9 Y bf16 [T*k,L]         10 N bf16 [T,L]            11 Gs bf16 [T,2ds]    */
+/*  12 As bf16 [T,ds]         13 Sh bf16 [T,H]                                 */
+/* Z, Gs and Sh hold data only when the call did not split K (T > 128).       */
+/* Returns LMOE_OK or a validation error.                                     */
+enum { LMOE_WS_COUNT = 14 };
+int latent_moe_workspace_offsets(const lmoe_dims* dims, size_t* offsets);
+
 /* Number of kernel launches latent_moe_forward makes for these dims (0 on   */
 /* invalid dims), without the optional debug copies.  Uses the current       */
 /* device's SM count.                                                         */

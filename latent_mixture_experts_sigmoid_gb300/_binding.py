@@ -25,7 +25,7 @@ LMOE_ERR_CUDA = -6
 LMOE_ERR_ALIGN = -7
 
 ABI_FUNCTIONS = ("moe_route", "situ_and_mul", "masked_situ_and_mul", "latent_moe_forward",
-                 "latent_moe_workspace_bytes", "latent_moe_launch_count", "lmoe_linear", "lmoe_status_string",
+                 "latent_moe_workspace_bytes", "latent_moe_workspace_offsets", "latent_moe_launch_count", "lmoe_linear", "lmoe_status_string",
                  "lmoe_device_error", "lmoe_abi_version")
 
 
@@ -83,6 +83,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.masked_situ_and_mul.restype = i32
     lib.latent_moe_workspace_bytes.argtypes = [ctypes.POINTER(LmoeDims)]
     lib.latent_moe_workspace_bytes.restype = ctypes.c_size_t
+    lib.latent_moe_workspace_offsets.argtypes = [ctypes.POINTER(LmoeDims),
+                                                 ctypes.POINTER(ctypes.c_size_t)]
+    lib.latent_moe_workspace_offsets.restype = i32
     lib.latent_moe_launch_count.argtypes = [ctypes.POINTER(LmoeDims), i32]
     lib.latent_moe_launch_count.restype = i32
     lib.latent_moe_forward.argtypes = [ctypes.POINTER(LmoeDims), ctypes.POINTER(LmoeWeights), vp,
@@ -218,6 +221,19 @@ def lmoe_linear(x, w, out, add=None, stream=None, T: int | None = None, N: int |
     st = load_library().lmoe_linear(_ptr(x), _ptr(w), _ptr(add), _ptr(out), int(T), int(N),
                                     int(K), _stream(stream))
     _check(st, "lmoe_linear")
+
+
+WS_NAMES = ("topk_ids", "topk_weights", "counts", "offsets", "row_of", "Z", "A", "G", "act",
+            "Y", "N", "Gs", "As", "Sh")
+
+
+def latent_moe_workspace_offsets(dims) -> dict:
+    """Byte offsets of the intermediate buffers inside the workspace."""
+    dd = dims if isinstance(dims, LmoeDims) else make_dims(dims)
+    arr = (ctypes.c_size_t * len(WS_NAMES))()
+    _check(load_library().latent_moe_workspace_offsets(ctypes.byref(dd), arr),
+           "latent_moe_workspace_offsets")
+    return dict(zip(WS_NAMES, [int(v) for v in arr]))
 
 
 def latent_moe_launch_count(dims, has_shared_expert: bool = True) -> int:

@@ -328,6 +328,20 @@ int lmoe_linear(const lmoe_bf16* x, const lmoe_bf16* w, const lmoe_bf16* add, lm
   return LMOE_OK;
 }
 
+int latent_moe_workspace_offsets(const lmoe_dims* dims, size_t* offsets) {
+  const int v = validate_dims(dims);
+  if (v != LMOE_OK) return v;
+  if (!offsets) return LMOE_ERR_NULL;
+  Ws w;
+  char* const base = reinterpret_cast<char*>(256);   // never dereferenced
+  carve(*dims, base, &w);
+  const void* p[LMOE_WS_COUNT] = {w.ids, w.w, w.counts, w.offsets, w.row_of, w.Z, w.A,
+                                  w.G, w.act, w.Y, w.N, w.Gs, w.As, w.Sh};
+  for (int i = 0; i < LMOE_WS_COUNT; ++i)
+    offsets[i] = (size_t)(reinterpret_cast<const char*>(p[i]) - base);
+  return LMOE_OK;
+}
+
 int latent_moe_launch_count(const lmoe_dims* dims, int has_shared_expert) {
   if (validate_dims(dims) != LMOE_OK) return 0;
   if (dims->T == 0) return 0;

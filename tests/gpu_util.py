@@ -104,17 +104,55 @@ def bf16_ulp(v: np.ndarray) -> np.ndarray:
     return np.ldexp(1.0, np.maximum(e - 1, -126) - 7)
 
 
-def assert_layer_close(got: np.ndarray, ref: np.ndarray, tol: float = 2e-2) -> dict:
-    """Layer parity: every element within tol * rms(ref), or within one bf16
-    step of ref (the output's own quantisation: at |ref| >= 4 rms one bf16
-    step is already about 2e-2 * rms, so two correct fp32/fp64 evaluations that
-    round to neighbouring bf16 values would otherwise fail)."""
+def assert_layer_close(got: np.ndarray, ref: np.ndarray, tol: float = 2e-2,
+                       steps: int = 2) -> dict:
+    """Layer parity: every element within tol * rms(ref), or within `steps`
+    bf16 steps of ref.  Both sides round nine intermediate stages to bf16; a
+    one-step disagreement in an intermediate (each stage, fed identical inputs,
+    agrees to one step on >= 99.9% of its elements) moves the output by up to
+    about two steps, and at |ref| >= 2.5 rms two bf16 steps exceed 2e-2 rms."""
     err = np.abs(got - ref)
     rms = float(np.sqrt(np.mean(ref ** 2)))
-    bound = np.maximum(tol * rms, bf16_ulp(ref))
+    bound = np.maximum(tol * rms, steps * bf16_ulp(ref))
     bad = err > bound
     stats = dict(max_err_over_rms=float(err.max() / rms), frac_differing=float((err > 0).mean()),
                  max_err_in_ulps=float((err / bf16_ulp(ref)).max()))
-    assert not bad.any(), (f"{bad.sum()} elements beyond max({tol}*rms, 1 bf16 step); "
+    assert not bad.any(), (f"{bad.sum()} elements beyond max({tol}*rms, {steps} bf16 steps); "
                            f"first at {np.argwhere(bad)[0]}; {stats}")
     return stats
+
+
+def assert_stage_close(got: np.ndarray, ref: np.ndarray, name: str, max_mismatch: float = 0.01):
+    """One stage fed identical inputs: the bf16 results differ on at most
+    max_mismatch of the elements, by one bf16 step at the 99.9th percentile,
+    and never by more than max(2 steps, 1e-3 * rms) (near-cancelling sums
+    have tiny |ref| and so tiny steps)."""
+    err = np.abs(got - ref)
+    u = bf16_ulp(ref)
+    rms = float(np.sqrt(np.mean(ref ** 2))) or 1.0
+    mism = float((err > 0).mean())
+    p999 = float(np.quantile(err / u, 0.999))
+    worst = float((err / np.maximum(2 * u, 1e-3 * rms)).max())
+    assert mism <= max_mismatch and p999 <= 1.0 and worst <= 1.0, (name, mism, p999, worst)
+    return dict(stage=name, mismatch=mism, p999_steps=p999)
+
+
+def workspace_view(lm, d, ws: torch.Tensor):
+    """Host copies of the layer's intermediates from the workspace."""
+    off = lm.latent_moe_workspace_offsets(d)
+    wsn = ws.cpu().numpy()
+    T, k, L, H, dI, ds = d.T, d.topk, d.latent, d.hidden, d.inter, d.shared_inter
+
+    def bf(name, rows, cols):
+        o = off[name]
+        return wsn[o:o + rows * cols * 2].view(np.uint16).reshape(rows, cols)
+
+    def i32(name, n):
+        o = off[name]
+        return wsn[o:o + n * 4].view(np.int32)
+
+    return dict(row_of=i32("row_of", T * k).reshape(T, k),
+                w=wsn[off["topk_weights"]:off["topk_weights"] + T * k * 4].view(np.float32).reshape(T, k),
+                Z=bf("Z", T, L), A=bf("A", T * k, L), G=bf("G", T * k, 2 * dI),
+                act=bf("act", T * k, dI), Y=bf("Y", T * k, L), N=bf("N", T, L),
+                Gs=bf("Gs", T, 2 * ds), As=bf("As", T, ds), Sh=bf("Sh", T, H))

@@ -101,7 +101,9 @@ def test_decode_layer_full(big_weights):
     check_routing_and_permutation(d, dbg, lg, wor["bias"])
     ref = O.bf16_to_f64(O.latent_moe_forward(d, wor, x, lg))
     got = O.bf16_to_f64(host_bits(out))
-    print(assert_layer_close(got, ref, TOL))
+    stats = assert_layer_close(got, ref, TOL)
+    print(stats)
+    assert stats["frac_differing"] < 0.5 and stats["max_err_over_rms"] < 5e-2
     assert lm.lmoe_device_error() == 0
 
 
@@ -118,7 +120,9 @@ def test_prefill_layer_zipf_sampled(big_weights):
     toks = np.concatenate([[0, d.T - 1], np.random.default_rng(3).choice(d.T, 10, replace=False)])
     ref = O.bf16_to_f64(O.latent_moe_forward(d, wor, x[toks], lg[toks]))
     got = O.bf16_to_f64(host_bits(out))[toks]
-    print(assert_layer_close(got, ref, TOL))
+    stats = assert_layer_close(got, ref, TOL)
+    print(stats)
+    assert stats["frac_differing"] < 0.5 and stats["max_err_over_rms"] < 5e-2
     # every output finite
     assert torch.isfinite(out.float()).all()
     assert lm.lmoe_device_error() == 0

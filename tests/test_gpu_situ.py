@@ -45,7 +45,7 @@ def test_situ_dense_full_size_sampled(lb):
     o = out.float()
     assert torch.isfinite(o).all()
     if lb > 0:
-        assert (o.abs() < 4.0 * 8.0).all()
+        assert (o.abs() <= 4.0 * 8.0).all()   # bf16 rounding can reach the bound
     rows = np.random.default_rng(1).choice(N, 96, replace=False)
     rows = np.concatenate([[0, N - 1], rows])
     got = O.bf16_to_f64(host_bits(out[torch.from_numpy(rows).cuda()]))

@@ -1,0 +1,107 @@
+"""Stage-by-stage GPU parity of the layer: every stage of latent_moe_forward,
+read back from the workspace, against the oracle's stage fed the GPU's own
+inputs to that stage.  This isolates each kernel's arithmetic from the
+propagation of earlier one-step bf16 differences."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import lmoe_oracle as O
+
+pytestmark = pytest.mark.gpu
+lm = pytest.importorskip("latent_mixture_experts_sigmoid_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_ok):
+    lm.load_library()
+
+
+def run_and_check(d, wdev, wor, zipf, toks):
+    from tests.gpu_util import (DEV, dev_bf16, dev_f32, host_bits, workspace_view,
+                                assert_stage_close)
+    f = O.bf16_to_f64
+    x = W.hidden_states(d, 0)
+    lg = W.router_logits(d.T, d.num_experts, 0, zipf=zipf)
+    out = torch.empty((d.T, d.hidden), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(lm.latent_moe_workspace_bytes(d), dtype=torch.uint8, device=DEV)
+    lm.latent_moe_forward(d, wdev, dev_bf16(x), dev_f32(lg), out, ws)
+    torch.cuda.synchronize()
+    v = workspace_view(lm, d, ws)
+    T, k, L, dI, ds = d.T, d.topk, d.latent, d.inter, d.shared_inter
+    toks = np.asarray(toks)
+    ids, _ = O.route(lg[toks], wor["bias"], k, d.routed_scaling_factor, d.renormalize)
+    X = f(x[toks])
+    rr = v["row_of"][toks].ravel()
+    res = []
+    # down-projection (the rows of A are copies of Z)
+    Zref = O.linear_bf16(X, wor["w_down"])
+    Arows = f(v["A"][rr]).reshape(len(toks), k, L)
+    for j in range(k):
+        assert np.array_equal(Arows[:, j], Arows[:, 0])        # scatter copies one row
+    res.append(assert_stage_close(Arows[:, 0], Zref, "down"))
+    # GEMM1, SituGLU, GEMM2 per (token, slot) row, from the GPU's inputs
+    G = f(v["G"][rr])
+    Gref = np.stack([O.linear_bf16(f(v["A"][r:r + 1]), wor["w13"](e))[0]
+                     for r, e in zip(rr, ids.ravel())])
+    res.append(assert_stage_close(G, Gref, "gemm1"))
+    act = f(v["act"][rr])
+    res.append(assert_stage_close(act, O.round_bf16(O.situ(G[:, :dI], G[:, dI:], d.beta,
+                                                           d.linear_beta)), "situ"))
+    Y = f(v["Y"][rr])
+    Yref = np.stack([O.linear_bf16(act[i:i + 1], wor["w2"](e))[0]
+                     for i, e in enumerate(ids.ravel())])
+    res.append(assert_stage_close(Y, Yref, "gemm2"))
+    # combine + RMSNorm from the GPU's Y and weights
+    C = np.einsum("tj,tjl->tl", v["w"][toks].astype(np.float64), Y.reshape(len(toks), k, L))
+    gamma = f(wor["norm_w"])
+    N = f(v["N"][toks])
+    res.append(assert_stage_close(N, O.round_bf16(O.rms_norm(C, gamma, d.rms_eps)), "combine_norm"))
+    # shared expert
+    As = f(v["As"][toks])
+    if T > 128:
+        Gs = f(v["Gs"][toks])
+        res.append(assert_stage_close(Gs, O.linear_bf16(X, wor["ws13"]), "shared1"))
+        res.append(assert_stage_close(As, O.round_bf16(O.situ(Gs[:, :ds], Gs[:, ds:], d.beta,
+                                                              d.linear_beta)), "shared_situ"))
+        Sh = f(v["Sh"][toks])
+        res.append(assert_stage_close(Sh, O.linear_bf16(As, wor["ws2"]), "shared2"))
+    else:
+        Gs = O.linear_bf16(X, wor["ws13"])
+        res.append(assert_stage_close(As, O.round_bf16(O.situ(Gs[:, :ds], Gs[:, ds:], d.beta,
+                                                              d.linear_beta)), "shared1+situ"))
+        Sh = O.linear_bf16(As, wor["ws2"])
+    outref = O.round_bf16(N @ f(wor["w_up"]).T + Sh)
+    res.append(assert_stage_close(f(host_bits(out))[toks], outref, "up+shared_add"))
+    print(res)
+
+
+def _tiny_weights(d, seed=0):
+    from tests.gpu_util import weights_to_device
+    w = W.layer_weights(d, seed)
+    wor = dict(w, w13=lambda e: w["w13"][e], w2=lambda e: w["w2"][e])
+    return weights_to_device(w), wor
+
+
+@pytest.mark.parametrize("T", [8, 300])
+def test_stages_tiny(T):
+    d = dataclasses.replace(W.TINY, T=T)
+    wdev, wor = _tiny_weights(d)
+    run_and_check(d, wdev, wor, False, list(range(min(T, 16))) + [T - 1])
+
+
+@pytest.fixture(scope="module")
+def big():
+    from tests.gpu_util import device_layer_weights, oracle_layer_weights
+    return device_layer_weights(W.DECODE, 0), oracle_layer_weights(W.DECODE, 0)
+
+
+def test_stages_decode(big):
+    run_and_check(W.DECODE, big[0], big[1], False, list(range(8)))
+
+
+def test_stages_prefill_zipf(big):
+    run_and_check(W.PREFILL, big[0], big[1], True, [0, 1, 2, 777, 2048, 4095])
