@@ -171,8 +171,11 @@ __device__ __forceinline__ int total_units(const GemmParams& p, int tok_tile, in
   return tiles * nfeat * p.splits;
 }
 
+// A CTA visits its units in increasing order, so the group of a unit never
+// decreases: `gcur` is a per-thread cursor that only moves forward (over empty
+// groups too), O(1) amortised per unit instead of a search.
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int tok_tile,
-                                            int feat_tile, int nfeat, int nkb) {
+                                            int feat_tile, int nfeat, int nkb, int& gcur) {
   Unit x;
   x.split = u % p.splits;
   const int v = u / p.splits;
@@ -180,12 +183,8 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int tok_
   const int gt = v / nfeat;
   int g = 0, t_in_g = gt, count = p.T_dense, first = 0;
   if (p.tile_prefix) {
-    int lo = 0, hi = p.num_groups - 1;   // last g with tile_prefix[g] <= gt
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(p.tile_prefix + mid) <= gt) lo = mid; else hi = mid - 1;
-    }
-    g = lo;
+    while (gcur + 1 < p.num_groups && __ldg(p.tile_prefix + gcur + 1) <= gt) ++gcur;
+    g = gcur;
     t_in_g = gt - __ldg(p.tile_prefix + g);
     count = __ldg(p.grp_count + g);
     first = __ldg(p.grp_offset + g);
@@ -222,6 +221,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
   const uint32_t done_bar = bar0 + 8u * (2 * S + 4);
 
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
@@ -252,26 +252,56 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int feat_tile = p.tok_on_m ? bn : BM;
   const int nfeat = p.M_feat / feat_tile;
   const int nkb = p.K / BK;
-  const int U = total_units(p, tok_tile, nfeat);
+  const bool dense = p.tile_prefix == nullptr;
+  // the weight operand is B when tokens are on M, A otherwise
+  const CUtensorMap* mapW = p.tok_on_m ? &tmB : &tmA;
+  const CUtensorMap* mapX = p.tok_on_m ? &tmA : &tmB;
+  const uint32_t offW = p.tok_on_m ? a_bytes : 0u;
+  const uint32_t offX = p.tok_on_m ? 0u : a_bytes;
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
+      // Dense GEMMs know their units without reading device data, so the
+      // weight tiles of the first ring of stages are requested before the
+      // wait for the previous kernel (weights are constant).
+      uint32_t pre = 0;
+      if (dense) {
+        const int U0 = total_units(p, tok_tile, nfeat);
+        int gc0 = 0;
+        for (int u = blockIdx.x; u < U0 && pre < (uint32_t)S; u += gridDim.x) {
+          const Unit x = decode_unit(p, u, tok_tile, feat_tile, nfeat, nkb, gc0);
+          for (int kb = x.kb0; kb < x.kb1 && pre < (uint32_t)S; ++kb, ++pre) {
+            const uint32_t sa = smem_u32(smem + (size_t)pre * stage_bytes);
+            mbar_arrive_expect_tx(full_bar((int)pre), stage_bytes);
+            tma_load_2d(mapW, sa + offW, full_bar((int)pre), kb * BK, x.w_row0);
+          }
+        }
+      }
+      pdl_wait();
+      const int U = total_units(p, tok_tile, nfeat);
       uint32_t it = 0;
       bool ok = true;
+      int gc = 0;
       for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-        const Unit x = decode_unit(p, u, tok_tile, feat_tile, nfeat, nkb);
-        const int rowA = p.tok_on_m ? x.tok_row0 : x.w_row0;
-        const int rowB = p.tok_on_m ? x.w_row0 : x.tok_row0;
+        const Unit x = decode_unit(p, u, tok_tile, feat_tile, nfeat, nkb, gc);
         for (int kb = x.kb0; kb < x.kb1; ++kb, ++it) {
           const int s = (int)(it % (uint32_t)S);
-          const uint32_t ph = (it / (uint32_t)S) & 1u;
-          if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kErrProducer)) { ok = false; break; }
           const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-          mbar_arrive_expect_tx(full_bar(s), stage_bytes);
-          tma_load_2d(&tmA, sa, full_bar(s), kb * BK, rowA);
-          tma_load_2d(&tmB, sa + a_bytes, full_bar(s), kb * BK, rowB);
+          if (it >= pre) {
+            const uint32_t ph = (it / (uint32_t)S) & 1u;
+            if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kErrProducer)) { ok = false; break; }
+            mbar_arrive_expect_tx(full_bar(s), stage_bytes);
+            tma_load_2d(mapW, sa + offW, full_bar(s), kb * BK, x.w_row0);
+          }
+          tma_load_2d(mapX, sa + offX, full_bar(s), kb * BK, x.tok_row0);
         }
+      }
+      // stages armed before the wait but never reached (abort) still get their
+      // token tile so that every armed phase can complete
+      for (; it < pre; ++it) {
+        const int s = (int)it;
+        tma_load_2d(mapX, smem_u32(smem + (size_t)s * stage_bytes) + offX, full_bar(s), 0, 0);
       }
       // drain: every copy this thread issued has landed before the CTA exits
       const uint32_t first = it > (uint32_t)S ? it - (uint32_t)S : 0u;
@@ -285,11 +315,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
+      pdl_wait();
+      const int U = total_units(p, tok_tile, nfeat);
       const uint32_t idesc = idesc_bf16(BM, bn);
       uint32_t it = 0, uit = 0;
       bool ok = true;
+      int gc = 0;
       for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++uit) {
-        const Unit x = decode_unit(p, u, tok_tile, feat_tile, nfeat, nkb);
+        const Unit x = decode_unit(p, u, tok_tile, feat_tile, nfeat, nkb, gc);
         const int acc = (int)(uit & 1u);
         if (!wait_bounded(tempty_bar(acc), ((uit >> 1) & 1u) ^ 1u, abort_flag, kErrMmaTmem)) {
           ok = false;
@@ -322,9 +355,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ---------------- epilogue (warps 2..5) ----------------
     const int q = warp & 3;                  // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;             // accumulator row of this thread
+    pdl_wait();
+    const int U = total_units(p, tok_tile, nfeat);
     uint32_t uit = 0;
+    int gc = 0;
     for (int u = blockIdx.x; u < U; u += gridDim.x, ++uit) {
-      const Unit x = decode_unit(p, u, tok_tile, feat_tile, nfeat, nkb);
+      const Unit x = decode_unit(p, u, tok_tile, feat_tile, nfeat, nkb, gc);
       const int acc = (int)(uit & 1u);
       if (!wait_bounded(tfull_bar(acc), (uit >> 1) & 1u, abort_flag, kErrEpilogue)) break;
       tc_fence_after();
@@ -493,11 +529,8 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
   int grid = num_sms();
   if (g.max_units > 0 && g.max_units < grid) grid = g.max_units;
   if (grid < 1) grid = 1;
-  if (g.tok_on_m)
-    gemm_tc_kernel<<<grid, kThreads, smem, stream>>>(mx, mw, p);
-  else
-    gemm_tc_kernel<<<grid, kThreads, smem, stream>>>(mw, mx, p);
-  return cudaGetLastError();
+  if (g.tok_on_m) return launch_k(gemm_tc_kernel, dim3(grid), dim3(kThreads), smem, stream, mx, mw, p);
+  return launch_k(gemm_tc_kernel, dim3(grid), dim3(kThreads), smem, stream, mw, mx, p);
 }
 
 int read_device_error(int clear) {

@@ -29,6 +29,8 @@ constexpr int kWords = kBlkTok / 32;
 __global__ void __launch_bounds__(kBlkTok)
 perm_count_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
                   uint32_t* __restrict__ bitmaps, int32_t* __restrict__ blk_cnt) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint32_t bm[];   // [E][kWords]
   const int b = blockIdx.x;
   for (int i = threadIdx.x; i < E * kWords; i += blockDim.x) bm[i] = 0u;
@@ -86,6 +88,8 @@ __global__ void __launch_bounds__(1024)
 perm_scan_kernel(const int32_t* __restrict__ blk_cnt, int nblk, int E, int tile,
                  int32_t* __restrict__ blk_base, int32_t* __restrict__ counts,
                  int32_t* __restrict__ offsets, int32_t* __restrict__ tile_prefix) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int sh[33];
   const int e = threadIdx.x;
   int total = 0;
@@ -117,6 +121,8 @@ __global__ void __launch_bounds__(kBlkTok)
 perm_rows_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
                  const uint32_t* __restrict__ bitmaps, const int32_t* __restrict__ blk_base,
                  int32_t* __restrict__ row_of, int32_t* __restrict__ tok_of_row) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x;
   const int tl = threadIdx.x;
   const int t = b * kBlkTok + tl;
@@ -142,6 +148,8 @@ __global__ void __launch_bounds__(256)
 scatter_rows_kernel(const uint16_t* __restrict__ Zb, const float* __restrict__ Zp, int S,
                     long long split_stride, int L, int k, const int32_t* __restrict__ row_of,
                     uint16_t* __restrict__ A) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   const int nv = L / 8;
   for (int v = threadIdx.x; v < nv; v += blockDim.x) {
@@ -172,6 +180,8 @@ __global__ void __launch_bounds__(256)
 combine_norm_kernel(const uint16_t* __restrict__ Y, const float* __restrict__ w,
                     const int32_t* __restrict__ row_of, int k, int L,
                     const uint16_t* __restrict__ gamma, float eps, uint16_t* __restrict__ N) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float red[32];
   const int t = blockIdx.x;
   const int nv = L / 8;
@@ -244,6 +254,8 @@ __global__ void __launch_bounds__(256)
 reduce_splits_kernel(const float* __restrict__ P, int S, long long sstride,
                      const float* __restrict__ Q, int S2, long long qstride,
                      const uint16_t* __restrict__ add, long long n8, uint16_t* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < n8;
        v += (long long)gridDim.x * blockDim.x) {
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -284,6 +296,8 @@ reduce_splits_kernel(const float* __restrict__ P, int S, long long sstride,
 __global__ void __launch_bounds__(256)
 reduce_situ_kernel(const float* __restrict__ P, int S, long long sstride, int T, int d,
                    SituParams sp, uint16_t* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const long long n8 = (long long)T * (d / 8);
   for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < n8;
        v += (long long)gridDim.x * blockDim.x) {
@@ -336,19 +350,21 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int tile, vo
   cudaError_t e = cudaFuncSetAttribute(perm_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)sm);
   if (e != cudaSuccess) return e;
-  perm_count_kernel<<<nblk, kBlkTok, sm, s>>>(ids, T, k, E, bitmaps, blk_cnt);
-  perm_scan_kernel<<<1, 1024, 0, s>>>(blk_cnt, nblk, E, tile, blk_base, counts, offsets,
-                                      tile_prefix);
-  perm_rows_kernel<<<nblk, kBlkTok, 0, s>>>(ids, T, k, E, bitmaps, blk_base, row_of, tok_of_row);
-  return cudaGetLastError();
+  e = launch_k(perm_count_kernel, dim3(nblk), dim3(kBlkTok), sm, s, ids, T, k, E, bitmaps, blk_cnt);
+  if (e != cudaSuccess) return e;
+  e = launch_k(perm_scan_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)blk_cnt, nblk, E,
+               tile, blk_base, counts, offsets, tile_prefix);
+  if (e != cudaSuccess) return e;
+  return launch_k(perm_rows_kernel, dim3(nblk), dim3(kBlkTok), 0, s, ids, T, k, E,
+                  (const uint32_t*)bitmaps, (const int32_t*)blk_base, row_of, tok_of_row);
 }
 
 cudaError_t launch_scatter_rows(const uint16_t* Zb, const float* Zp, int S, long long split_stride,
                                 int T, int L, int k, const int32_t* row_of, uint16_t* A,
                                 cudaStream_t s) {
   const int threads = L / 8 < 256 ? ((L / 8 + 31) / 32) * 32 : 256;
-  scatter_rows_kernel<<<T, threads, 0, s>>>(Zb, Zp, S, split_stride, L, k, row_of, A);
-  return cudaGetLastError();
+  return launch_k(scatter_rows_kernel, dim3(T), dim3(threads), 0, s, Zb, Zp, S, split_stride, L, k,
+                  row_of, A);
 }
 
 cudaError_t launch_combine_norm(const uint16_t* Y, const float* w, const int32_t* row_of, int T,
@@ -356,25 +372,23 @@ cudaError_t launch_combine_norm(const uint16_t* Y, const float* w, const int32_t
                                 cudaStream_t s) {
   const int nv = L / 8;
   int threads = nv < 256 ? ((nv + 31) / 32) * 32 : 256;
-  combine_norm_kernel<<<T, threads, 0, s>>>(Y, w, row_of, k, L, gamma, eps, N);
-  return cudaGetLastError();
+  return launch_k(combine_norm_kernel, dim3(T), dim3(threads), 0, s, Y, w, row_of, k, L, gamma, eps,
+                  N);
 }
 
 cudaError_t launch_reduce_splits(const float* P, int S, long long sstride, const float* Q, int S2,
                                  long long qstride, const uint16_t* add, long long n,
                                  uint16_t* out, cudaStream_t s) {
   const long long n8 = n / 8;
-  reduce_splits_kernel<<<grid_for(n8, 256), 256, 0, s>>>(P, S, sstride, Q, S2, qstride, add, n8,
-                                                         out);
-  return cudaGetLastError();
+  return launch_k(reduce_splits_kernel, dim3(grid_for(n8, 256)), dim3(256), 0, s, P, S, sstride, Q,
+                  S2, qstride, add, n8, out);
 }
 
 cudaError_t launch_reduce_situ(const float* P, int S, long long sstride, int T, int d, float beta,
                                float lbeta, uint16_t* out, cudaStream_t s) {
   const long long n8 = (long long)T * (d / 8);
-  reduce_situ_kernel<<<grid_for(n8, 256), 256, 0, s>>>(P, S, sstride, T, d,
-                                                       make_situ_params(beta, lbeta), out);
-  return cudaGetLastError();
+  return launch_k(reduce_situ_kernel, dim3(grid_for(n8, 256)), dim3(256), 0, s, P, S, sstride, T, d,
+                  make_situ_params(beta, lbeta), out);
 }
 
 }  // namespace lmoe

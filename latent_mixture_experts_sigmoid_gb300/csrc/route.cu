@@ -123,6 +123,8 @@ route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bi
                   float* __restrict__ weights) {
   __shared__ float sbias[EPL * 32];
   __shared__ int scand[kWarpsPerBlock][32];
+  pdl_trigger();
+  pdl_wait();
   for (int i = threadIdx.x; i < EPL * 32; i += blockDim.x)
     sbias[i] = (i < E && bias != nullptr) ? bias[i] : 0.0f;
   __syncthreads();
@@ -258,9 +260,8 @@ template <int EPL>
 cudaError_t launch_tier(const float* logits, const float* bias, int T, int E, int k, int renorm,
                         float rsf, int32_t* ids, float* w, cudaStream_t s) {
   const int blocks = ceil_div(T, kWarpsPerBlock);
-  route_warp_kernel<EPL><<<blocks, kWarpsPerBlock * 32, 0, s>>>(logits, bias, T, E, k, renorm,
-                                                                rsf, ids, w);
-  return cudaGetLastError();
+  return launch_k(route_warp_kernel<EPL>, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, s, logits,
+                  bias, T, E, k, renorm, rsf, ids, w);
 }
 
 }  // namespace

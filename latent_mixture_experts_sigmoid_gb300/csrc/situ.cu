@@ -66,6 +66,8 @@ __device__ __forceinline__ void situ_rows(const uint16_t* __restrict__ in, uint1
 __global__ void __launch_bounds__(kThreads)
 situ_dense_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out, long long N,
                   int d, int rows_per_block, SituParams p) {
+  pdl_trigger();
+  pdl_wait();
   const long long row0 = (long long)blockIdx.x * rows_per_block;
   if (row0 >= N) return;
   const int nrows = (int)min((long long)rows_per_block, N - row0);
@@ -76,6 +78,8 @@ __global__ void __launch_bounds__(kThreads)
 situ_masked_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out,
                    const int32_t* __restrict__ counts, int T_max, int d, int rows_per_block,
                    SituParams p) {
+  pdl_trigger();
+  pdl_wait();
   const int e = blockIdx.y;
   const int n = min(max(__ldg(counts + e), 0), T_max);
   const int r0 = blockIdx.x * rows_per_block;
@@ -97,9 +101,8 @@ cudaError_t launch_situ(const uint16_t* in, uint16_t* out, long long N, int d, f
   if (N <= 0) return cudaSuccess;
   const int rpb = rows_for(d);
   const long long blocks = (N + rpb - 1) / rpb;
-  situ_dense_kernel<<<(unsigned)blocks, kThreads, 0, s>>>(in, out, N, d, rpb,
-                                                          make_situ_params(beta, lbeta));
-  return cudaGetLastError();
+  return launch_k(situ_dense_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, s, in, out, N, d,
+                  rpb, make_situ_params(beta, lbeta));
 }
 
 cudaError_t launch_masked_situ(const uint16_t* in, uint16_t* out, const int32_t* counts, int E,
@@ -107,9 +110,8 @@ cudaError_t launch_masked_situ(const uint16_t* in, uint16_t* out, const int32_t*
   if (E <= 0 || T_max <= 0) return cudaSuccess;
   const int rpb = min(rows_for(d), T_max);
   dim3 grid((unsigned)ceil_div(T_max, rpb), (unsigned)E);
-  situ_masked_kernel<<<grid, kThreads, 0, s>>>(in, out, counts, T_max, d, rpb,
-                                               make_situ_params(beta, lbeta));
-  return cudaGetLastError();
+  return launch_k(situ_masked_kernel, grid, dim3(kThreads), 0, s, in, out, counts, T_max, d, rpb,
+                  make_situ_params(beta, lbeta));
 }
 
 }  // namespace lmoe

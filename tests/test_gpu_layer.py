@@ -36,16 +36,18 @@ def check_routing_and_permutation(d, dbg, logits, bias):
 
 
 def tiny_case(d, seed=0, gamma_noise=False, shared=True, zipf=False):
-    from tests.gpu_util import weights_to_device, run_layer, host_bits, assert_layer_close
+    from tests.gpu_util import (weights_to_device, run_layer, host_bits, assert_layer_close,
+                                addend_scale)
     wts = W.layer_weights(d, seed, gamma_noise)
     if not shared:
         wts["ws13"] = wts["ws2"] = None
     x = W.hidden_states(d, seed)
     lg = W.router_logits(d.T, d.num_experts, seed, zipf=zipf)
     out, dbg = run_layer(lm, d, weights_to_device(wts), x, lg)
-    ref = O.bf16_to_f64(O.latent_moe_forward(d, wts, x, lg))
+    ref_bits, mid = O.latent_moe_forward(d, wts, x, lg, intermediates=True)
+    ref = O.bf16_to_f64(ref_bits)
     got = O.bf16_to_f64(host_bits(out))
-    assert_layer_close(got, ref, TOL)
+    assert_layer_close(got, ref, TOL, scale=addend_scale(ref, mid, wts["w_up"]))
     check_routing_and_permutation(d, dbg, lg, wts["bias"])
     assert lm.lmoe_device_error() == 0
 
@@ -92,23 +94,24 @@ def big_weights():
 
 
 def test_decode_layer_full(big_weights):
-    from tests.gpu_util import run_layer, host_bits, assert_layer_close
+    from tests.gpu_util import run_layer, host_bits, assert_layer_close, addend_scale
     d = W.DECODE
     wdev, wor = big_weights
     x = W.hidden_states(d, 0)
     lg = W.router_logits(d.T, d.num_experts, 0)
     out, dbg = run_layer(lm, d, wdev, x, lg)
     check_routing_and_permutation(d, dbg, lg, wor["bias"])
-    ref = O.bf16_to_f64(O.latent_moe_forward(d, wor, x, lg))
+    ref_bits, mid = O.latent_moe_forward(d, wor, x, lg, intermediates=True)
+    ref = O.bf16_to_f64(ref_bits)
     got = O.bf16_to_f64(host_bits(out))
-    stats = assert_layer_close(got, ref, TOL)
+    stats = assert_layer_close(got, ref, TOL, scale=addend_scale(ref, mid, wor["w_up"]))
     print(stats)
     assert stats["frac_differing"] < 0.5 and stats["max_err_over_rms"] < 5e-2
     assert lm.lmoe_device_error() == 0
 
 
 def test_prefill_layer_zipf_sampled(big_weights):
-    from tests.gpu_util import run_layer, host_bits, assert_layer_close
+    from tests.gpu_util import run_layer, host_bits, assert_layer_close, addend_scale
     d = W.PREFILL
     wdev, wor = big_weights
     x = W.hidden_states(d, 0)
@@ -118,9 +121,10 @@ def test_prefill_layer_zipf_sampled(big_weights):
     counts = dbg["expert_num_tokens"]
     assert counts.max() > 500 and (counts == 0).sum() > 100     # the skew is real
     toks = np.concatenate([[0, d.T - 1], np.random.default_rng(3).choice(d.T, 10, replace=False)])
-    ref = O.bf16_to_f64(O.latent_moe_forward(d, wor, x[toks], lg[toks]))
+    ref_bits, mid = O.latent_moe_forward(d, wor, x[toks], lg[toks], intermediates=True)
+    ref = O.bf16_to_f64(ref_bits)
     got = O.bf16_to_f64(host_bits(out))[toks]
-    stats = assert_layer_close(got, ref, TOL)
+    stats = assert_layer_close(got, ref, TOL, scale=addend_scale(ref, mid, wor["w_up"]))
     print(stats)
     assert stats["frac_differing"] < 0.5 and stats["max_err_over_rms"] < 5e-2
     # every output finite
