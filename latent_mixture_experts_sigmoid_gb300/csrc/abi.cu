@@ -213,6 +213,7 @@ cudaError_t gemm_grouped(const uint16_t* W, int E, int M_feat, const uint16_t* X
 }
 
 struct Plan {
+  int T;
   bool decode;
   int tile;          // token tile of the grouped GEMMs
   int g1_bn, g2_bn;  // MMA N of the grouped GEMMs
@@ -221,6 +222,7 @@ struct Plan {
 
 Plan make_plan(const lmoe_dims& d, int nsm) {
   Plan p;
+  p.T = d.T;
   p.decode = d.T <= kDecodeMaxT;
   p.tile = p.decode ? round_up(d.T, 16) : 128;
   p.g1_bn = p.decode ? p.tile : ((2 * d.inter) % 256 == 0 ? 256 : 128);
@@ -233,7 +235,8 @@ Plan make_plan(const lmoe_dims& d, int nsm) {
 }
 
 int plan_launches(const Plan& p, bool shared) {
-  int n = 1 + 1 + 3 + 1 + 3 + 1;        // route, down, permute, scatter, experts, combine
+  const int perm = p.T <= 256 ? 1 : 3;  // one fused permutation kernel for T <= 256
+  int n = 1 + 1 + perm + 1 + 3 + 1;     // route, down, permute, scatter, experts, combine
   if (shared) n += 3;                   // shared GEMM1 + SituGLU, shared GEMM2
   n += 1;                               // up-projection GEMM
   const bool sh_part = shared && p.s2.splits > 1;

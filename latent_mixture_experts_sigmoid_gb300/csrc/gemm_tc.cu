@@ -171,11 +171,17 @@ __device__ __forceinline__ int total_units(const GemmParams& p, int tok_tile, in
   return tiles * nfeat * p.splits;
 }
 
-// A CTA visits its units in increasing order, so the group of a unit never
-// decreases: `gcur` is a per-thread cursor that only moves forward (over empty
-// groups too), O(1) amortised per unit instead of a search.
-__device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int tok_tile,
-                                            int feat_tile, int nfeat, int nkb, int& gcur) {
+// Grouped GEMMs keep the per-group tables (tile prefix, token count, first
+// row) in shared memory, copied once per CTA; a unit's group is found by a
+// binary search there (the last g with tile_prefix[g] <= tile index).
+struct GroupTables {
+  const int* prefix;   // [G+1]
+  const int* count;    // [G]
+  const int* first;    // [G]
+};
+
+__device__ __forceinline__ Unit decode_unit(const GemmParams& p, const GroupTables& gt_tab, int u,
+                                            int tok_tile, int feat_tile, int nfeat, int nkb) {
   Unit x;
   x.split = u % p.splits;
   const int v = u / p.splits;
@@ -183,11 +189,15 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, int u, int tok_
   const int gt = v / nfeat;
   int g = 0, t_in_g = gt, count = p.T_dense, first = 0;
   if (p.tile_prefix) {
-    while (gcur + 1 < p.num_groups && __ldg(p.tile_prefix + gcur + 1) <= gt) ++gcur;
-    g = gcur;
-    t_in_g = gt - __ldg(p.tile_prefix + g);
-    count = __ldg(p.grp_count + g);
-    first = __ldg(p.grp_offset + g);
+    int lo = 0, hi = p.num_groups - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (gt_tab.prefix[mid] <= gt) lo = mid; else hi = mid - 1;
+    }
+    g = lo;
+    t_in_g = gt - gt_tab.prefix[g];
+    count = gt_tab.count[g];
+    first = gt_tab.first[g];
   }
   x.tok_row0 = first + t_in_g * tok_tile;
   x.nvalid = min(tok_tile, count - t_in_g * tok_tile);
@@ -211,6 +221,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   // bars: full[S], empty[S], tfull[2], tempty[2], done
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* tab = reinterpret_cast<int*>(tmem_holder + 4);   // grouped: prefix | count | first
+  GroupTables tabs{tab, tab + p.num_groups + 1, tab + 2 * p.num_groups + 1};
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -243,6 +255,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  if (p.tile_prefix) {
+    // the tables are produced by the previous kernels: wait for them first
+    pdl_wait();
+    const int G = p.num_groups;
+    for (int i = threadIdx.x; i <= G; i += blockDim.x) tab[i] = __ldg(p.tile_prefix + i);
+    for (int i = threadIdx.x; i < G; i += blockDim.x) {
+      tab[G + 1 + i] = __ldg(p.grp_count + i);
+      tab[2 * G + 1 + i] = __ldg(p.grp_offset + i);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -268,9 +290,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t pre = 0;
       if (dense) {
         const int U0 = total_units(p, tok_tile, nfeat);
-        int gc0 = 0;
         for (int u = blockIdx.x; u < U0 && pre < (uint32_t)S; u += gridDim.x) {
-          const Unit x = decode_unit(p, u, tok_tile, feat_tile, nfeat, nkb, gc0);
+          const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb);
           for (int kb = x.kb0; kb < x.kb1 && pre < (uint32_t)S; ++kb, ++pre) {
             const uint32_t sa = smem_u32(smem + (size_t)pre * stage_bytes);
             mbar_arrive_expect_tx(full_bar((int)pre), stage_bytes);
@@ -282,9 +303,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int U = total_units(p, tok_tile, nfeat);
       uint32_t it = 0;
       bool ok = true;
-      int gc = 0;
       for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-        const Unit x = decode_unit(p, u, tok_tile, feat_tile, nfeat, nkb, gc);
+        const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb);
         for (int kb = x.kb0; kb < x.kb1; ++kb, ++it) {
           const int s = (int)(it % (uint32_t)S);
           const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
@@ -320,9 +340,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t idesc = idesc_bf16(BM, bn);
       uint32_t it = 0, uit = 0;
       bool ok = true;
-      int gc = 0;
       for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++uit) {
-        const Unit x = decode_unit(p, u, tok_tile, feat_tile, nfeat, nkb, gc);
+        const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb);
         const int acc = (int)(uit & 1u);
         if (!wait_bounded(tempty_bar(acc), ((uit >> 1) & 1u) ^ 1u, abort_flag, kErrMmaTmem)) {
           ok = false;
@@ -358,9 +377,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     pdl_wait();
     const int U = total_units(p, tok_tile, nfeat);
     uint32_t uit = 0;
-    int gc = 0;
     for (int u = blockIdx.x; u < U; u += gridDim.x, ++uit) {
-      const Unit x = decode_unit(p, u, tok_tile, feat_tile, nfeat, nkb, gc);
+      const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb);
       const int acc = (int)(uit & 1u);
       if (!wait_bounded(tfull_bar(acc), (uit >> 1) & 1u, abort_flag, kErrEpilogue)) break;
       tc_fence_after();
@@ -487,9 +505,9 @@ int stages_for(int bn) {
   return s > 12 ? 12 : (s < 2 ? 2 : s);
 }
 
-size_t smem_for(int bn, int stages) {
+size_t smem_for(int bn, int stages, int groups) {
   const size_t stage = (size_t)BM * BK * 2 + (size_t)bn * BK * 2;
-  return 1024 + stages * stage + (2 * stages + 5) * 8 + 16;
+  return 1024 + stages * stage + (2 * stages + 5) * 8 + 16 + (size_t)(3 * groups + 1) * 4;
 }
 
 }  // namespace
@@ -522,7 +540,7 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
   if (!make_map(&mw, g.W, (long long)g.G * g.M_feat, g.K, w_box)) return cudaErrorInvalidValue;
   if (!make_map(&mx, g.X, g.x_rows, g.K, x_box)) return cudaErrorInvalidValue;
 
-  const size_t smem = smem_for(g.bn, p.stages);
+  const size_t smem = smem_for(g.bn, p.stages, g.grp_count ? g.G : 0);
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;

@@ -116,6 +116,64 @@ perm_scan_kernel(const int32_t* __restrict__ blk_cnt, int nblk, int E, int tile,
   }
 }
 
+// ---- permutation in one block, for T <= 256 (one bitmap block) ---------------
+// The three passes above fused: bitmaps, counts/offsets/tile prefix by a
+// block scan, then every (token, slot) row.  1024 threads, E <= 1024.
+__global__ void __launch_bounds__(1024)
+perm_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int tile,
+                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                  int32_t* __restrict__ tile_prefix, int32_t* __restrict__ row_of,
+                  int32_t* __restrict__ tok_of_row) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ uint32_t bm[1024 * kWords];
+  __shared__ int soff[1024];
+  __shared__ int sh[33];
+  for (int i = threadIdx.x; i < E * kWords; i += blockDim.x) bm[i] = 0u;
+  __syncthreads();
+  const int t = threadIdx.x;
+  if (t < T) {
+    for (int j = 0; j < k; ++j) {
+      const int e = __ldg(ids + (long long)t * k + j);
+      atomicOr(&bm[e * kWords + (t >> 5)], 1u << (t & 31));
+    }
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  int c = 0;
+  if (e < E) {
+#pragma unroll
+    for (int w = 0; w < kWords; ++w) c += __popc(bm[e * kWords + w]);
+  }
+  int all = 0, all_tiles = 0;
+  const int off = block_exclusive_scan(c, sh, &all);
+  const int toff = block_exclusive_scan(e < E ? (c + tile - 1) / tile : 0, sh, &all_tiles);
+  if (e < E) {
+    counts[e] = c;
+    offsets[e] = off;
+    tile_prefix[e] = toff;
+    soff[e] = off;
+  }
+  if (e == 0) {
+    offsets[E] = all;
+    tile_prefix[E] = all_tiles;
+  }
+  __syncthreads();
+  if (t < T) {
+    const int w = t >> 5;
+    const uint32_t below = (1u << (t & 31)) - 1u;
+    for (int j = 0; j < k; ++j) {
+      const int ej = __ldg(ids + (long long)t * k + j);
+      const uint32_t* m = bm + ej * kWords;
+      int rank = __popc(m[w] & below);
+      for (int i = 0; i < w; ++i) rank += __popc(m[i]);
+      const int row = soff[ej] + rank;
+      row_of[(long long)t * k + j] = row;
+      tok_of_row[row] = t;
+    }
+  }
+}
+
 // ---- permutation, pass 3: row of every (token, slot) -------------------------
 __global__ void __launch_bounds__(kBlkTok)
 perm_rows_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
@@ -343,6 +401,9 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int tile, vo
                            int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
                            int32_t* row_of, int32_t* tok_of_row, cudaStream_t s) {
   const int nblk = (T + kBlkTok - 1) / kBlkTok;
+  if (nblk == 1)
+    return launch_k(perm_small_kernel, dim3(1), dim3(1024), 0, s, ids, T, k, E, tile, counts,
+                    offsets, tile_prefix, row_of, tok_of_row);
   uint32_t* bitmaps = reinterpret_cast<uint32_t*>(scratch);
   int32_t* blk_cnt = reinterpret_cast<int32_t*>(bitmaps + (size_t)nblk * E * kWords);
   int32_t* blk_base = blk_cnt + (size_t)nblk * E;

@@ -99,7 +99,9 @@ int rows_for(int d) {
 cudaError_t launch_situ(const uint16_t* in, uint16_t* out, long long N, int d, float beta,
                         float lbeta, cudaStream_t s) {
   if (N <= 0) return cudaSuccess;
-  const int rpb = rows_for(d);
+  // at least two blocks per SM when there are enough rows
+  const long long spread = (N + 2LL * num_sms() - 1) / (2LL * num_sms());
+  const int rpb = (int)(spread < rows_for(d) ? (spread < 1 ? 1 : spread) : rows_for(d));
   const long long blocks = (N + rpb - 1) / rpb;
   return launch_k(situ_dense_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, s, in, out, N, d,
                   rpb, make_situ_params(beta, lbeta));
