@@ -185,12 +185,17 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
         # one forward captured in a CUDA graph (the calls are capturable): the
         # timed steps replay it, so host launch overhead is not on the clock
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            lm.latent_moe_forward(d, w, x, lgd, out, ws, stream=stream)
+        if args.no_graph:
+            def replay():
+                lm.latent_moe_forward(d, w, x, lgd, out, ws, stream=stream)
+        else:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                lm.latent_moe_forward(d, w, x, lgd, out, ws, stream=stream)
+            replay = graph.replay
         for _ in range(warmup):
             with torch.cuda.stream(stream):
-                graph.replay()
+                replay()
         torch.cuda.synchronize()
         n_used = int((counts.cpu().numpy() > 0).sum())
         # device-timed region: K steps, one event pair around each forward
@@ -202,7 +207,7 @@ def run_ours(args, rank, world):
             with torch.cuda.stream(stream):
                 flush_l2()
                 e_a.record(stream)
-                graph.replay()
+                replay()
                 e_b.record(stream)
             stream.synchronize()
             per_step.append(e_a.elapsed_time(e_b))
@@ -305,7 +310,8 @@ def run_ours(args, rank, world):
                    "num_experts": dP.num_experts, "topk": dP.topk, "inter": dP.inter,
                    "shared_inter": dP.shared_inter, "experts_used": pre["n_used"],
                    "l2": "flushed between timed steps (512 MiB write, then 256 MiB read, untimed)",
-                   "timing": "CUDA-graph replay of one latent_moe_forward per step",
+                   "timing": ("eager latent_moe_forward calls" if args.no_graph else
+                              "CUDA-graph replay of one latent_moe_forward per step"),
                    "parallelism": f"replicas x{world}"},
         "e2e": {"value": round(world * dP.T * K / (pre_e2e / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": pre["h2d"], "d2h_bytes_per_step": pre["d2h"]},
@@ -410,6 +416,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager calls instead of CUDA-graph replays (for profiler runs)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
