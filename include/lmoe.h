@@ -204,6 +204,28 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* weights,
                        lmoe_bf16* out, void* workspace, size_t workspace_bytes,
                        const lmoe_debug* dbg, void* stream);
 
+/* The layer forward without a caller workspace.  The pages have no          */
+/* counterpart to this entry point; it exists for callers that cannot         */
+/* allocate device memory: a plugin that an inference runtime calls with only */
+/* its input and output buffers (the runtime owns every allocation), host     */
+/* code with no allocator of its own, or a latency path where cudaMalloc is   */
+/* not allowed because it may synchronise the device.                         */
+/* Same computation, arguments and errors as latent_moe_forward, except that  */
+/* the scratch is a 32 MiB array held by the library in device memory (every */
+/* GPU that loads the library keeps it until the process exits).  Calls whose */
+/* latent_moe_workspace_bytes exceeds 32 MiB return LMOE_ERR_WORKSPACE and    */
+/* launch nothing (the 896-expert, hidden-7168 layer fits up to T = 15).      */
+/* The first call on a device looks up the array's device address           */
+/* (cudaGetSymbolAddress) with that device current; make that first call     */
+/* before any stream capture.  No call allocates.  Every call on a device     */
+/* shares the one array, which keeps the previous call's contents (nothing in */
+/* it has to start at zero: each call writes every scratch value it reads), */
+/* so calls that may overlap on the GPU (different streams, or host threads) */
+/* race; serialise them on one stream.                                        */
+int latent_moe_forward_noalloc(const lmoe_dims* dims, const lmoe_weights* weights,
+                               const lmoe_bf16* hidden, const float* router_logits,
+                               lmoe_bf16* out, const lmoe_debug* dbg, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Dense linear layer on the same tensor-core GEMM engine (the up-projection */
 /* with its shared-output add, [vLLM-runner] _shard_up_proj_tail:             */

@@ -25,7 +25,8 @@ LMOE_ERR_CUDA = -6
 LMOE_ERR_ALIGN = -7
 
 ABI_FUNCTIONS = ("moe_route", "situ_and_mul", "masked_situ_and_mul", "latent_moe_forward",
-                 "latent_moe_workspace_bytes", "latent_moe_workspace_offsets", "latent_moe_launch_count", "lmoe_linear", "lmoe_status_string",
+                 "latent_moe_forward_noalloc", "latent_moe_workspace_bytes", "latent_moe_workspace_offsets",
+                 "latent_moe_launch_count", "lmoe_linear", "lmoe_status_string",
                  "lmoe_device_error", "lmoe_abi_version")
 
 
@@ -86,6 +87,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.latent_moe_workspace_offsets.argtypes = [ctypes.POINTER(LmoeDims),
                                                  ctypes.POINTER(ctypes.c_size_t)]
     lib.latent_moe_workspace_offsets.restype = i32
+    lib.latent_moe_forward_noalloc.argtypes = [ctypes.POINTER(LmoeDims),
+                                               ctypes.POINTER(LmoeWeights), vp, vp, vp,
+                                               ctypes.POINTER(LmoeDebug), vp]
+    lib.latent_moe_forward_noalloc.restype = i32
     lib.latent_moe_launch_count.argtypes = [ctypes.POINTER(LmoeDims), i32]
     lib.latent_moe_launch_count.restype = i32
     lib.latent_moe_forward.argtypes = [ctypes.POINTER(LmoeDims), ctypes.POINTER(LmoeWeights), vp,
@@ -221,6 +226,19 @@ def lmoe_linear(x, w, out, add=None, stream=None, T: int | None = None, N: int |
     st = load_library().lmoe_linear(_ptr(x), _ptr(w), _ptr(add), _ptr(out), int(T), int(N),
                                     int(K), _stream(stream))
     _check(st, "lmoe_linear")
+
+
+def latent_moe_forward_noalloc(dims, weights, hidden, router_logits, out, stream=None):
+    """The layer forward with the library's own 32 MiB device scratch instead
+    of a caller workspace, for callers that cannot allocate device memory.
+    Calls that need more scratch raise LmoeError (LMOE_ERR_WORKSPACE); calls
+    that overlap on the GPU share the scratch and race."""
+    dd = dims if isinstance(dims, LmoeDims) else make_dims(dims)
+    ww = weights if isinstance(weights, LmoeWeights) else make_weights(weights)
+    st = load_library().latent_moe_forward_noalloc(ctypes.byref(dd), ctypes.byref(ww),
+                                                   _ptr(hidden), _ptr(router_logits), _ptr(out),
+                                                   None, _stream(stream))
+    _check(st, "latent_moe_forward_noalloc")
 
 
 WS_NAMES = ("topk_ids", "topk_weights", "counts", "offsets", "row_of", "Z", "A", "G", "act",
