@@ -180,15 +180,21 @@ struct GroupTables {
   const int* first;    // [G]
 };
 
+// Dense GEMMs with tokens on M walk their tiles in bands of kBand feature
+// tiles: inside a band the feature tile changes fastest, then the token tile,
+// so the 152 concurrent tiles share a band of weight tiles and a run of token
+// tiles that both stay in L2 (for K = 7168: 8 x 3.7 MB + 19 x 1.8 MB).
+constexpr int kBand = 8;
+
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const GroupTables& gt_tab, int u,
                                             int tok_tile, int feat_tile, int nfeat, int nkb) {
   Unit x;
   x.split = u % p.splits;
   const int v = u / p.splits;
-  x.feat_tile = v % nfeat;
-  const int gt = v / nfeat;
-  int g = 0, t_in_g = gt, count = p.T_dense, first = 0;
+  int g = 0, t_in_g, count = p.T_dense, first = 0;
   if (p.tile_prefix) {
+    x.feat_tile = v % nfeat;
+    const int gt = v / nfeat;
     int lo = 0, hi = p.num_groups - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -198,6 +204,17 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const GroupTabl
     t_in_g = gt - gt_tab.prefix[g];
     count = gt_tab.count[g];
     first = gt_tab.first[g];
+  } else if (p.tok_on_m) {
+    const int ntok = (p.T_dense + tok_tile - 1) / tok_tile;
+    const int nbands = (nfeat + kBand - 1) / kBand;
+    const int b = min(v / (ntok * kBand), nbands - 1);
+    const int rem = v - b * ntok * kBand;
+    const int fb = (b == nbands - 1) ? nfeat - kBand * (nbands - 1) : kBand;
+    t_in_g = rem / fb;
+    x.feat_tile = b * kBand + rem % fb;
+  } else {
+    x.feat_tile = v % nfeat;
+    t_in_g = v / nfeat;
   }
   x.tok_row0 = first + t_in_g * tok_tile;
   x.nvalid = min(tok_tile, count - t_in_g * tok_tile);

@@ -1,15 +1,18 @@
 // Single-group sigmoid top-k routing (DeepSeekV3 style).
 //
 // vLLM PR #50088, commit 1: with n_group == 1 and topk_group == 1, grouped
-// top-k is plain top-k over all experts; commit 4: sigmoid scores of FP32
-// logits, e_score_correction_bias added for the selection only, weights from
-// the unbiased scores, renormalised, times routed_scaling_factor.
+// top-k is plain top-k over all experts; two kernels are dispatched from a
+// compile-time (num_experts) tier list: block-per-token for few tokens (a
+// hierarchical per-warp reduction), warp-per-token for large batches.
+// Commit 4: sigmoid scores of FP32 logits, e_score_correction_bias added for
+// the selection only, weights from the unbiased scores, renormalised, times
+// routed_scaling_factor.
 //
-// One warp per token.  The selection key must be reproducible to the bit (the
-// expert ids are compared exactly), so the sigmoid that decides it is a fixed
-// sequence of IEEE fp32 operations (exact_sigmoid below).  Evaluating that
-// sequence for all E experts would make the kernel issue-bound, so the kernel
-// selects in two passes:
+// The selection key must be reproducible to the bit (the expert ids are
+// compared exactly), so the sigmoid that decides it is a fixed sequence of
+// IEEE fp32 operations (exact_sigmoid below).  Evaluating that sequence for
+// all E experts would make the kernel issue-bound, so selection takes two
+// passes:
 //   A. a cheap key ka = fast_sigmoid(x) + b for every expert, packed with the
 //      expert index into one u32 (key truncated to 22 bits, index below), and
 //      the top-k of those by per-lane sorted lists merged with warp max
@@ -27,7 +30,7 @@
 // error of __expf (2 + floor(1.173|x|) ulp, |x| <= 87) and __fdividef (2 ulp):
 // |s_fast - s| <= s(1-s) * 1.24e-5 + 3 ulp <= 3.5e-6, plus the exact
 // sigmoid's own error (<= 3 ulp) and the rounding of the two bias additions
-// (<= 2^-23 |key|).  The kernel uses 2D = 1e-5 + 2^-20 * max(|A|, 1), about
+// (<= 2^-23 |key|).  The kernels use 2D = 1e-5 + 2^-20 * max(|A|, 1), about
 // 2.5x that bound.
 #include "lmoe_internal.cuh"
 
@@ -88,6 +91,7 @@ __device__ __forceinline__ float from_orderable(uint32_t o) {
 
 constexpr uint32_t kIdxBits = 10;  // E <= 1024
 constexpr uint32_t kIdxMask = (1u << kIdxBits) - 1u;
+constexpr unsigned FULL = 0xFFFFFFFFu;
 
 __device__ __forceinline__ uint32_t pack_cheap(float ka, int e) {
   return (orderable(ka) & ~kIdxMask) | (kIdxMask - (uint32_t)e);
@@ -96,12 +100,16 @@ __device__ __forceinline__ uint32_t pack_cheap(float ka, int e) {
 // Exact key packed with the index: larger key first, then lower index first.
 __device__ __forceinline__ unsigned long long pack_exact(float key, int e) {
   key = __fadd_rn(key, 0.0f);  // -0 -> +0
-  return ((unsigned long long)orderable(key) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
+  return ((unsigned long long)orderable(key) << 32) |
+         (unsigned long long)(0xFFFFFFFFu - (uint32_t)e);
+}
+__device__ __forceinline__ int expert_of(unsigned long long P) {
+  return (int)(0xFFFFFFFFu - (uint32_t)P);
 }
 
 __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
-  const uint32_t hi = __reduce_max_sync(0xFFFFFFFFu, (uint32_t)(v >> 32));
-  const uint32_t lo = __reduce_max_sync(0xFFFFFFFFu, ((uint32_t)(v >> 32) == hi) ? (uint32_t)v : 0u);
+  const uint32_t hi = __reduce_max_sync(FULL, (uint32_t)(v >> 32));
+  const uint32_t lo = __reduce_max_sync(FULL, ((uint32_t)(v >> 32) == hi) ? (uint32_t)v : 0u);
   return ((unsigned long long)hi << 32) | lo;
 }
 
@@ -113,9 +121,132 @@ __device__ __forceinline__ void insert4(uint32_t v, uint32_t& l0, uint32_t& l1, 
   l3 = max(l3, v);
 }
 
+// Threshold of pass B from the (truncated) cheap key of the k-th pick.
+__device__ __forceinline__ float candidate_threshold(uint32_t a_k) {
+  const float trunc_k = from_orderable(a_k & ~kIdxMask);
+  return trunc_k - (1.0e-5f + 0x1p-20f * fmaxf(fabsf(trunc_k), 1.0f));
+}
+
+// ---- pass A for one warp: experts e = base + lane + stride * i ---------------
+// Fills ka[] with the cheap keys of this lane's experts (-inf where e >= E)
+// and returns in lane r (r < k) the warp's r-th largest packed cheap key.
+template <int EPL>
+__device__ __forceinline__ uint32_t warp_cheap_topk(const float* __restrict__ row,
+                                                    const float* sbias, int E, int k, int base,
+                                                    int stride, int lane, float (&ka)[EPL]) {
+  uint32_t l0 = 0, l1 = 0, l2 = 0, l3 = 0;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = base + lane + stride * i;
+    ka[i] = -INFINITY;
+    if (e < E) {
+      ka[i] = fmaxf(fast_sigmoid(__ldg(row + e)) + sbias[e], -3.0e38f);
+      insert4(pack_cheap(ka[i], e), l0, l1, l2, l3);
+    }
+  }
+  uint32_t mysel = 0, last = 0;
+  int popped = 0;
+  for (int r = 0; r < k; ++r) {
+    const uint32_t m = __reduce_max_sync(FULL, l0);
+    if (lane == r) mysel = m;
+    if (l0 == m && m != 0u) {
+      l0 = l1; l1 = l2; l2 = l3; l3 = 0; ++popped; last = m;
+    }
+    if (EPL > 4) {
+      // a lane that handed out its whole list may hold further large keys
+      const bool refill = (popped == 4);
+      if (__any_sync(FULL, refill) && refill) {
+        popped = 0;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          const int e = base + lane + stride * i;
+          if (e < E) {
+            const uint32_t p = pack_cheap(ka[i], e);
+            if (p < last) insert4(p, l0, l1, l2, l3);
+          }
+        }
+      }
+    }
+  }
+  return mysel;
+}
+
+// ---- pass B exact stage for one warp -----------------------------------------
+// `cand[0..total)` are the candidate experts (total <= 32).  Writes the top-k
+// ids and weights of token t.
+__device__ __forceinline__ void exact_order_and_write(const float* __restrict__ row,
+                                                      const float* sbias, const int* cand,
+                                                      int total, int k, int renorm, float rsf,
+                                                      long long t, int lane,
+                                                      int32_t* __restrict__ ids,
+                                                      float* __restrict__ weights) {
+  unsigned long long P = 0ull;
+  float s = 0.0f;
+  if (lane < total) {
+    const int e = cand[lane];
+    s = exact_sigmoid(__ldg(row + e));
+    P = pack_exact(__fadd_rn(s, sbias[e]), e);
+  }
+  // bitonic sort of 32 (P, s) pairs, descending
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const unsigned long long Po = __shfl_xor_sync(FULL, P, stride);
+      const float so = __shfl_xor_sync(FULL, s, stride);
+      const bool up = ((lane & size) == 0);        // this pair sorts descending
+      const bool lower = ((lane & stride) == 0);   // this lane keeps the larger
+      const bool take = (lower == up) ? (Po > P) : (Po < P);
+      if (take) { P = Po; s = so; }
+    }
+  }
+  float sum = (lane < k) ? s : 0.0f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
+  if (lane < k) {
+    const float wv = renorm ? __fmul_rn(__fdiv_rn(s, sum), rsf) : __fmul_rn(s, rsf);
+    ids[t * k + lane] = expert_of(P);
+    weights[t * k + lane] = wv;
+  }
+}
+
+// Weights and outputs of an exact selection already held as lane r = r-th pick.
+__device__ __forceinline__ void write_selected(const float* __restrict__ row,
+                                               unsigned long long P, int k, int renorm, float rsf,
+                                               long long t, int lane, int32_t* __restrict__ ids,
+                                               float* __restrict__ weights) {
+  const float s = (lane < k) ? exact_sigmoid(__ldg(row + expert_of(P))) : 0.0f;
+  float sum = s;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
+  if (lane < k) {
+    const float wv = renorm ? __fmul_rn(__fdiv_rn(s, sum), rsf) : __fmul_rn(s, rsf);
+    ids[t * k + lane] = expert_of(P);
+    weights[t * k + lane] = wv;
+  }
+}
+
+// Largest exact packed key below `lastP` among this lane's experts.
+template <int EPL>
+__device__ __forceinline__ unsigned long long lane_best_exact(const float* __restrict__ row,
+                                                              const float* sbias, int E, int base,
+                                                              int stride, int lane,
+                                                              unsigned long long lastP) {
+  unsigned long long best = 0ull;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = base + lane + stride * i;
+    if (e < E) {
+      const unsigned long long p = pack_exact(__fadd_rn(exact_sigmoid(__ldg(row + e)), sbias[e]), e);
+      if (p < lastP && p > best) best = p;
+    }
+  }
+  return best;
+}
+
+// ---- warp per token (large batches) ------------------------------------------
 constexpr int kWarpsPerBlock = 8;
 
-// EPL = experts per lane; expert e = lane + 32*i lives in lane e%32, slot e/32.
 template <int EPL>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
@@ -128,69 +259,21 @@ route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bi
   for (int i = threadIdx.x; i < EPL * 32; i += blockDim.x)
     sbias[i] = (i < E && bias != nullptr) ? bias[i] : 0.0f;
   __syncthreads();
-
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const unsigned FULL = 0xFFFFFFFFu;
 
   for (long long t = (long long)blockIdx.x * kWarpsPerBlock + warp; t < T;
        t += (long long)gridDim.x * kWarpsPerBlock) {
     const float* row = logits + t * (long long)E;
-
-    // ---- pass A: cheap keys and per-lane top-4 lists -----------------------
     float ka[EPL];
-    uint32_t l0 = 0, l1 = 0, l2 = 0, l3 = 0;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      ka[i] = -INFINITY;
-      if (e < E) {
-        ka[i] = fast_sigmoid(__ldg(row + e)) + sbias[e];
-        ka[i] = fmaxf(ka[i], -3.0e38f);
-        insert4(pack_cheap(ka[i], e), l0, l1, l2, l3);
-      }
-    }
-
-    // ---- merge: k rounds of warp max over the list heads -------------------
-    uint32_t mysel = 0, last = 0;
-    int popped = 0;
-    for (int r = 0; r < k; ++r) {
-      const uint32_t m = __reduce_max_sync(FULL, l0);
-      if (lane == r) mysel = m;
-      if (l0 == m) {
-        l0 = l1; l1 = l2; l2 = l3; l3 = 0; ++popped; last = m;
-      }
-      if (EPL > 4) {
-        // a lane that handed out its whole list may hold further large keys
-        const bool refill = (popped == 4);
-        if (__any_sync(FULL, refill) && refill) {
-          popped = 0;
-#pragma unroll
-          for (int i = 0; i < EPL; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E) {
-              const uint32_t p = pack_cheap(ka[i], e);
-              if (p < last) insert4(p, l0, l1, l2, l3);
-            }
-          }
-        }
-      }
-    }
-    const uint32_t a_k = __shfl_sync(FULL, mysel, k - 1);
-    const float trunc_k = from_orderable(a_k & ~kIdxMask);
-    const float thr = trunc_k - (1.0e-5f + 0x1p-20f * fmaxf(fabsf(trunc_k), 1.0f));
-
-    // ---- pass B: candidates within the bound --------------------------------
+    const uint32_t mysel = warp_cheap_topk<EPL>(row, sbias, E, k, 0, 32, lane, ka);
+    const float thr = candidate_threshold(__shfl_sync(FULL, mysel, k - 1));
     uint32_t cmask = 0;
     int ccount = 0;
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
+    for (int i = 0; i < EPL; ++i)
       if (ka[i] >= thr) { cmask |= 1u << i; ++ccount; }
-    }
     const int total = (int)__reduce_add_sync(FULL, (uint32_t)ccount);
-
-    unsigned long long P = 0ull;
-    float s = 0.0f;
     if (total <= 32) {
       int incl = ccount;
 #pragma unroll
@@ -203,79 +286,154 @@ route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bi
       for (int i = 0; i < EPL; ++i)
         if (cmask & (1u << i)) scand[warp][pos++] = lane + 32 * i;
       __syncwarp();
-      if (lane < total) {
-        const int e = scand[warp][lane];
-        s = exact_sigmoid(__ldg(row + e));
-        P = pack_exact(__fadd_rn(s, sbias[e]), e);
-      }
-      // bitonic sort of 32 (P, s) pairs, descending
-#pragma unroll
-      for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          const unsigned long long Po = __shfl_xor_sync(FULL, P, stride);
-          const float so = __shfl_xor_sync(FULL, s, stride);
-          const bool up = ((lane & size) == 0);        // this pair sorts descending
-          const bool lower = ((lane & stride) == 0);   // this lane keeps the larger
-          const bool take = (lower == up) ? (Po > P) : (Po < P);
-          if (take) { P = Po; s = so; }
-        }
-      }
+      exact_order_and_write(row, sbias, scand[warp], total, k, renorm, rsf, t, lane, ids, weights);
       __syncwarp();
     } else {
-      // ---- fallback: exact selection over all experts ----------------------
-      unsigned long long lastP = ~0ull;
+      // fallback: exact selection over all experts, one pick per round
+      unsigned long long lastP = ~0ull, P = 0ull;
       for (int r = 0; r < k; ++r) {
-        unsigned long long best = 0ull;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-          const int e = lane + 32 * i;
-          if (e < E) {
-            const unsigned long long p =
-                pack_exact(__fadd_rn(exact_sigmoid(__ldg(row + e)), sbias[e]), e);
-            if (p < lastP && p > best) best = p;
-          }
-        }
-        const unsigned long long m = warp_max_u64(best);
+        const unsigned long long m =
+            warp_max_u64(lane_best_exact<EPL>(row, sbias, E, 0, 32, lane, lastP));
         if (lane == r) P = m;
         lastP = m;
       }
-      if (lane < k) s = exact_sigmoid(__ldg(row + (int)(0xFFFFFFFFu - (uint32_t)P)));
-    }
-
-    // ---- weights and outputs -------------------------------------------------
-    const int e = (int)(0xFFFFFFFFu - (uint32_t)P);
-    float sum = (lane < k) ? s : 0.0f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
-    if (lane < k) {
-      const float wv = renorm ? __fmul_rn(__fdiv_rn(s, sum), rsf) : __fmul_rn(s, rsf);
-      ids[t * k + lane] = e;
-      weights[t * k + lane] = wv;
+      write_selected(row, P, k, renorm, rsf, t, lane, ids, weights);
     }
   }
 }
 
+// ---- block per token (few tokens, many experts) --------------------------------
+// W warps per token; warp w owns experts e = 32*w + lane + 32*W*i.  Each warp
+// finds its own cheap top-k, warp 0 merges the W sorted lists, every warp marks
+// its candidates, and warp 0 runs the exact stage.
+template <int EPL, int W>
+__global__ void __launch_bounds__(W * 32)
+route_block_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
+                   int k, int renorm, float rsf, int32_t* __restrict__ ids,
+                   float* __restrict__ weights) {
+  __shared__ float sbias[EPL * 32 * W];
+  __shared__ uint32_t slist[W][32];
+  __shared__ int scnt[W];
+  __shared__ int scand[32];
+  __shared__ float sthr;
+  __shared__ unsigned long long spick[W];
+  pdl_trigger();
+  pdl_wait();
+  for (int i = threadIdx.x; i < EPL * 32 * W; i += blockDim.x)
+    sbias[i] = (i < E && bias != nullptr) ? bias[i] : 0.0f;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int base = 32 * warp, stride = 32 * W;
+
+  for (long long t = blockIdx.x; t < T; t += gridDim.x) {
+    const float* row = logits + t * (long long)E;
+    float ka[EPL];
+    const uint32_t mysel = warp_cheap_topk<EPL>(row, sbias, E, k, base, stride, lane, ka);
+    slist[warp][lane] = (lane < k) ? mysel : 0u;
+    __syncthreads();
+    if (warp == 0) {
+      // merge W descending lists of k entries: lane w < W owns list w
+      int ptr = 0;
+      uint32_t head = (lane < W) ? slist[lane][0] : 0u;
+      uint32_t a_k = 0;
+      for (int r = 0; r < k; ++r) {
+        const uint32_t m = __reduce_max_sync(FULL, head);
+        a_k = m;
+        if (lane < W && head == m && m != 0u) {
+          ++ptr;
+          head = (ptr < k) ? slist[lane][ptr] : 0u;
+        }
+      }
+      if (lane == 0) sthr = candidate_threshold(a_k);
+    }
+    __syncthreads();
+    const float thr = sthr;
+    uint32_t cmask = 0;
+    int ccount = 0;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (ka[i] >= thr) { cmask |= 1u << i; ++ccount; }
+    int incl = ccount;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) scnt[warp] = incl;
+    __syncthreads();
+    int total = 0, before = 0;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      if (w < warp) before += scnt[w];
+      total += scnt[w];
+    }
+    if (total <= 32) {
+      int pos = before + incl - ccount;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i)
+        if (cmask & (1u << i)) scand[pos++] = base + lane + stride * i;
+      __syncthreads();
+      if (warp == 0)
+        exact_order_and_write(row, sbias, scand, total, k, renorm, rsf, t, lane, ids, weights);
+    } else {
+      // fallback: exact selection over all experts, one pick per round
+      unsigned long long lastP = ~0ull, P = 0ull;
+      for (int r = 0; r < k; ++r) {
+        const unsigned long long m =
+            warp_max_u64(lane_best_exact<EPL>(row, sbias, E, base, stride, lane, lastP));
+        if (lane == 0) spick[warp] = m;
+        __syncthreads();
+        unsigned long long best = 0ull;
+#pragma unroll
+        for (int w = 0; w < W; ++w) best = spick[w] > best ? spick[w] : best;
+        __syncthreads();
+        if (lane == r) P = best;
+        lastP = best;
+      }
+      if (warp == 0) write_selected(row, P, k, renorm, rsf, t, lane, ids, weights);
+    }
+    __syncthreads();
+  }
+}
+
 template <int EPL>
-cudaError_t launch_tier(const float* logits, const float* bias, int T, int E, int k, int renorm,
-                        float rsf, int32_t* ids, float* w, cudaStream_t s) {
+cudaError_t launch_warp_tier(const float* logits, const float* bias, int T, int E, int k,
+                             int renorm, float rsf, int32_t* ids, float* w, cudaStream_t s) {
   const int blocks = ceil_div(T, kWarpsPerBlock);
   return launch_k(route_warp_kernel<EPL>, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, s, logits,
                   bias, T, E, k, renorm, rsf, ids, w);
 }
 
+template <int EPL, int W>
+cudaError_t launch_block_tier(const float* logits, const float* bias, int T, int E, int k,
+                              int renorm, float rsf, int32_t* ids, float* w, cudaStream_t s) {
+  return launch_k(route_block_kernel<EPL, W>, dim3(T), dim3(W * 32), 0, s, logits, bias, T, E, k,
+                  renorm, rsf, ids, w);
+}
+
 }  // namespace
 
-// Compile-time tier list of experts-per-lane; E <= 32 * EPL.
+// Tokens up to this count get a block each (4 warps); larger batches a warp each.
+constexpr int kBlockPerTokenMaxT = 1024;
+
+// Compile-time tier list: experts per lane (EPL) for E <= 32 * EPL (warp per
+// token) or E <= 128 * EPL (block of 4 warps per token, E > 128 only).
 cudaError_t launch_route(const float* logits, const float* bias, int T, int E, int k, int renorm,
                          float rsf, int32_t* ids, float* w, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  if (E <= 64) return launch_tier<2>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  if (E <= 128) return launch_tier<4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  if (E <= 256) return launch_tier<8>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  if (E <= 512) return launch_tier<16>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  if (E <= 896) return launch_tier<28>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  return launch_tier<32>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (T <= kBlockPerTokenMaxT && E > 128) {
+    if (E <= 256) return launch_block_tier<2, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+    if (E <= 512) return launch_block_tier<4, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+    if (E <= 896) return launch_block_tier<7, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+    return launch_block_tier<8, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  }
+  if (E <= 64) return launch_warp_tier<2>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 128) return launch_warp_tier<4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 256) return launch_warp_tier<8>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 512) return launch_warp_tier<16>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 896) return launch_warp_tier<28>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  return launch_warp_tier<32>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
 }
 
 }  // namespace lmoe
