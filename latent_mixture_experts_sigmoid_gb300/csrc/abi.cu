@@ -190,7 +190,8 @@ cudaError_t gemm_dense(const uint16_t* W, int M_feat, const uint16_t* X, int T, 
 
 cudaError_t gemm_grouped(const uint16_t* W, int E, int M_feat, const uint16_t* X, long long rows,
                          int K, int tok_on_m, int bn, const Ws& ws, int tile, void* out,
-                         cudaStream_t s) {
+                         cudaStream_t s, int fuse_situ = 0, float beta = 1.0f,
+                         float linear_beta = 0.0f) {
   GemmDesc g{};
   g.W = W;
   g.X = X;
@@ -205,8 +206,11 @@ cudaError_t gemm_grouped(const uint16_t* W, int E, int M_feat, const uint16_t* X
   g.bn = bn;
   g.splits = 1;
   g.out = out;
-  g.ldo = M_feat;
-  const int feat_tile = tok_on_m ? bn : 128;
+  g.ldo = fuse_situ ? M_feat / 2 : M_feat;
+  g.fuse_situ = fuse_situ;
+  g.beta = beta;
+  g.linear_beta = linear_beta;
+  const int feat_tile = fuse_situ ? 256 : (tok_on_m ? bn : 128);
   const long long nonempty = rows < E ? rows : E;
   g.max_units = (int)(((rows + tile - 1) / tile + nonempty) * (M_feat / feat_tile));
   return launch_gemm(g, s);
@@ -215,6 +219,7 @@ cudaError_t gemm_grouped(const uint16_t* W, int E, int M_feat, const uint16_t* X
 struct Plan {
   int T;
   bool decode;
+  bool fuse_g1;      // GEMM1 with SituGLU in its epilogue (tokens on M, 2*inter % 256 == 0)
   int tile;          // token tile of the grouped GEMMs
   int g1_bn, g2_bn;  // MMA N of the grouped GEMMs
   DenseCfg down, s1, s2, up;
@@ -226,6 +231,8 @@ Plan make_plan(const lmoe_dims& d, int nsm) {
   p.decode = d.T <= kDecodeMaxT;
   p.tile = p.decode ? round_up(d.T, 16) : 128;
   p.g1_bn = p.decode ? p.tile : ((2 * d.inter) % 256 == 0 ? 256 : 128);
+  p.fuse_g1 = !p.decode && d.inter % 128 == 0;
+  if (p.fuse_g1) p.g1_bn = 256;
   p.g2_bn = p.decode ? p.tile : (d.latent % 256 == 0 ? 256 : 128);
   p.down = dense_cfg(d.T, d.latent, d.hidden, nsm);
   p.s1 = dense_cfg(d.T, 2 * d.shared_inter, d.hidden, nsm);
@@ -236,7 +243,8 @@ Plan make_plan(const lmoe_dims& d, int nsm) {
 
 int plan_launches(const Plan& p, bool shared) {
   const int perm = p.T <= 256 ? 1 : 3;  // one fused permutation kernel for T <= 256
-  int n = 1 + 1 + perm + 1 + 3 + 1;     // route, down, permute, scatter, experts, combine
+  const int experts = p.fuse_g1 ? 2 : 3;  // GEMM1 (+ SituGLU unless fused), GEMM2
+  int n = 1 + 1 + perm + 1 + experts + 1;  // route, down, permute, scatter, experts, combine
   if (shared) n += 3;                   // shared GEMM1 + SituGLU, shared GEMM2
   n += 1;                               // up-projection GEMM
   const bool sh_part = shared && p.s2.splits > 1;
@@ -418,9 +426,17 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
                                cdown.splits, down_stride, T, L, k, ws.row_of, ws.A, s));
   if (!mark(LMOE_STAGE_SCATTER + 1)) return LMOE_ERR_CUDA;
   // 5-7. experts
-  LMOE_TRY(gemm_grouped(wt->w13, E, 2 * dI, ws.A, rows, L, !decode, pl.g1_bn, ws, tile, ws.G, s));
-  if (!mark(LMOE_STAGE_GEMM1 + 1)) return LMOE_ERR_CUDA;
-  LMOE_TRY(launch_situ(ws.G, ws.act, rows, dI, d.beta, d.linear_beta, s));
+  if (pl.fuse_g1) {
+    // act = bf16(SituGLU(bf16(A W13_e^T))) straight from GEMM1's epilogue
+    LMOE_TRY(gemm_grouped(wt->w13, E, 2 * dI, ws.A, rows, L, 1, 256, ws, tile, ws.act, s, 1,
+                          d.beta, d.linear_beta));
+    if (!mark(LMOE_STAGE_GEMM1 + 1)) return LMOE_ERR_CUDA;
+  } else {
+    LMOE_TRY(gemm_grouped(wt->w13, E, 2 * dI, ws.A, rows, L, !decode, pl.g1_bn, ws, tile, ws.G,
+                          s));
+    if (!mark(LMOE_STAGE_GEMM1 + 1)) return LMOE_ERR_CUDA;
+    LMOE_TRY(launch_situ(ws.G, ws.act, rows, dI, d.beta, d.linear_beta, s));
+  }
   if (!mark(LMOE_STAGE_SITU + 1)) return LMOE_ERR_CUDA;
   LMOE_TRY(gemm_grouped(wt->w2, E, L, ws.act, rows, dI, !decode, pl.g2_bn, ws, tile, ws.Y, s));
   if (!mark(LMOE_STAGE_GEMM2 + 1)) return LMOE_ERR_CUDA;

@@ -218,7 +218,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const GroupTabl
   }
   x.tok_row0 = first + t_in_g * tok_tile;
   x.nvalid = min(tok_tile, count - t_in_g * tok_tile);
-  x.w_row0 = g * p.M_feat + x.feat_tile * feat_tile;
+  x.w_row0 = g * p.M_feat + x.feat_tile * (p.fuse_situ ? BM : feat_tile);
   x.kb0 = (int)((long long)x.split * nkb / p.splits);
   x.kb1 = (int)((long long)(x.split + 1) * nkb / p.splits);
   return x;
@@ -240,6 +240,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* tab = reinterpret_cast<int*>(tmem_holder + 4);   // grouped: prefix | count | first
   GroupTables tabs{tab, tab + p.num_groups + 1, tab + 2 * p.num_groups + 1};
+  // epilogue staging: 4 warps x [32 rows][32 fp32], 16-byte chunks XOR-swizzled by row
+  float* stage_out = reinterpret_cast<float*>(
+      (reinterpret_cast<uintptr_t>(tab + (p.tile_prefix ? 3 * p.num_groups + 1 : 0)) + 15) &
+      ~uintptr_t(15));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -289,7 +293,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   const int tok_tile = p.tok_on_m ? BM : bn;
   const int feat_tile = p.tok_on_m ? bn : BM;
-  const int nfeat = p.M_feat / feat_tile;
+  const int nfeat = p.fuse_situ ? (p.M_feat / 2) / BM : p.M_feat / feat_tile;
   const int nkb = p.K / BK;
   const bool dense = p.tile_prefix == nullptr;
   // the weight operand is B when tokens are on M, A otherwise
@@ -297,6 +301,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const CUtensorMap* mapX = p.tok_on_m ? &tmA : &tmB;
   const uint32_t offW = p.tok_on_m ? a_bytes : 0u;
   const uint32_t offX = p.tok_on_m ? 0u : a_bytes;
+  // the weight tile: one box, or (fused SituGLU) 128 gate rows and the 128 up
+  // rows of the same features, stacked into one 256-row operand
+  auto load_w = [&](uint32_t dst, uint32_t bar, int kb, int row) {
+    if (p.fuse_situ) {
+      tma_load_2d(mapW, dst, bar, kb * BK, row);
+      tma_load_2d(mapW, dst + BM * BK * 2, bar, kb * BK, row + p.M_feat / 2);
+    } else {
+      tma_load_2d(mapW, dst, bar, kb * BK, row);
+    }
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -312,7 +326,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           for (int kb = x.kb0; kb < x.kb1 && pre < (uint32_t)S; ++kb, ++pre) {
             const uint32_t sa = smem_u32(smem + (size_t)pre * stage_bytes);
             mbar_arrive_expect_tx(full_bar((int)pre), stage_bytes);
-            tma_load_2d(mapW, sa + offW, full_bar((int)pre), kb * BK, x.w_row0);
+            load_w(sa + offW, full_bar((int)pre), kb, x.w_row0);
           }
         }
       }
@@ -329,7 +343,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t ph = (it / (uint32_t)S) & 1u;
             if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kErrProducer)) { ok = false; break; }
             mbar_arrive_expect_tx(full_bar(s), stage_bytes);
-            tma_load_2d(mapW, sa + offW, full_bar(s), kb * BK, x.w_row0);
+            load_w(sa + offW, full_bar(s), kb, x.w_row0);
           }
           tma_load_2d(mapX, sa + offX, full_bar(s), kb * BK, x.tok_row0);
         }
@@ -400,8 +414,72 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (!wait_bounded(tfull_bar(acc), (uit >> 1) & 1u, abort_flag, kErrEpilogue)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * bn);
-      if (p.tok_on_m) {
-        // row r = token, columns = features
+      if (p.tok_on_m && !p.out_fp32) {
+        // row r = token, columns = features.  Per 32-column chunk: each thread
+        // puts its row's fp32 results into its warp's staging buffer; the warp
+        // then writes 4 rows x 32 columns per store instruction (the shared
+        // output add happens here in fp32, before the single bf16 rounding).
+        float* st = stage_out + (size_t)q * 32 * 32;
+        const int width = p.fuse_situ ? BM : bn;           // output columns of this tile
+        const int fcol0 = x.feat_tile * width;
+        const int ldo = p.fuse_situ ? p.M_feat / 2 : p.ldo;
+        for (int c0 = 0; c0 < width; c0 += 32) {
+          float f[32];
+          {
+            uint32_t v[16];
+            tmem_ld16(tbase + (uint32_t)c0, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
+            tmem_ld16(tbase + (uint32_t)(c0 + 16), v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) f[16 + j] = __uint_as_float(v[j]);
+          }
+          if (p.fuse_situ) {
+            // gate = f, up = the same features 128 columns further; both
+            // rounded to bf16 first, as the stored GEMM output would be
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t v[16];
+              tmem_ld16(tbase + (uint32_t)(BM + c0 + 16 * h), v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; j += 2) {
+                const uint32_t gb = pack_bf16x2(f[16 * h + j], f[16 * h + j + 1]);
+                const uint32_t ub = pack_bf16x2(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+                f[16 * h + j] = situ1(bf16_lo(gb), bf16_lo(ub), p.sp);
+                f[16 * h + j + 1] = situ1(bf16_hi(gb), bf16_hi(ub), p.sp);
+              }
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4*>(st + lane * 32 + ((c ^ (lane & 7)) * 4)) =
+                make_float4(f[4 * c], f[4 * c + 1], f[4 * c + 2], f[4 * c + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = i * 4 + (lane >> 3);            // row within this warp's 32
+            const int c = lane & 7;                        // 4-column chunk
+            const float4 a = *reinterpret_cast<const float4*>(st + rr * 32 + ((c ^ (rr & 7)) * 4));
+            const int row_in_tile = q * 32 + rr;
+            if (row_in_tile < x.nvalid) {
+              const long long orow = (long long)(x.tok_row0 + row_in_tile);
+              const long long off = orow * ldo + fcol0 + c0 + c * 4;
+              float o0 = a.x, o1 = a.y, o2 = a.z, o3 = a.w;
+              if (p.add) {
+                const uint2 ad = *reinterpret_cast<const uint2*>(p.add + off);
+                o0 += bf16_lo(ad.x); o1 += bf16_hi(ad.x); o2 += bf16_lo(ad.y); o3 += bf16_hi(ad.y);
+              }
+              *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) + off) =
+                  make_uint2(pack_bf16x2(o0, o1), pack_bf16x2(o2, o3));
+            }
+          }
+          __syncwarp();
+        }
+      } else if (p.tok_on_m) {
+        // fp32 split partials, row r = token
         const bool valid = r < x.nvalid;
         const long long orow = (long long)(x.tok_row0 + r);
         const int fcol0 = x.feat_tile * bn;
@@ -410,34 +488,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           tmem_ld16(tbase + (uint32_t)c0, v);
           tmem_wait_ld();
           if (!valid) continue;
-          if (p.out_fp32) {
-            float* o = reinterpret_cast<float*>(p.out) + (long long)x.split * p.split_stride +
-                       orow * p.ldo + fcol0 + c0;
+          float* o = reinterpret_cast<float*>(p.out) + (long long)x.split * p.split_stride +
+                     orow * p.ldo + fcol0 + c0;
 #pragma unroll
-            for (int j = 0; j < 16; j += 4)
-              *reinterpret_cast<uint4*>(o + j) = make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-          } else {
-            float f[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
-            if (p.add) {
-              const uint16_t* a = p.add + orow * p.ldo + fcol0 + c0;
-              const uint4 a0 = *reinterpret_cast<const uint4*>(a);
-              const uint4 a1 = *reinterpret_cast<const uint4*>(a + 8);
-              const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                f[2 * j] += bf16_lo(aw[j]);
-                f[2 * j + 1] += bf16_hi(aw[j]);
-              }
-            }
-            uint32_t pk[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) pk[j] = pack_bf16x2(f[2 * j], f[2 * j + 1]);
-            uint16_t* o = reinterpret_cast<uint16_t*>(p.out) + orow * p.ldo + fcol0 + c0;
-            *reinterpret_cast<uint4*>(o) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            *reinterpret_cast<uint4*>(o + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          }
+          for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<uint4*>(o + j) = make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]);
         }
       } else {
         // row r = feature, columns = tokens
@@ -522,9 +577,12 @@ int stages_for(int bn) {
   return s > 12 ? 12 : (s < 2 ? 2 : s);
 }
 
-size_t smem_for(int bn, int stages, int groups) {
+// ring of stages, barriers, TMEM holder/abort flag, group tables, and (tokens
+// on M only) the epilogue staging buffers; at most 227 KB
+size_t smem_for(int bn, int stages, int groups, int tok_on_m) {
   const size_t stage = (size_t)BM * BK * 2 + (size_t)bn * BK * 2;
-  return 1024 + stages * stage + (2 * stages + 5) * 8 + 16 + (size_t)(3 * groups + 1) * 4;
+  return 1024 + stages * stage + (2 * stages + 5) * 8 + 16 + (size_t)(3 * groups + 1) * 4 + 16 +
+         (tok_on_m ? 4 * 32 * 32 * 4 : 0);
 }
 
 }  // namespace
@@ -547,17 +605,20 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
   p.out_fp32 = g.out_fp32;
   p.add = g.add;
   p.stages = stages_for(g.bn);
+  p.fuse_situ = g.fuse_situ;
+  p.sp = make_situ_params(g.beta > 0.0f ? g.beta : 1.0f, g.linear_beta);
   uint32_t cols = 32;
   while (cols < (uint32_t)(2 * g.bn)) cols <<= 1;
   p.tmem_cols = cols;
 
   CUtensorMap mw, mx;
-  const int w_box = g.tok_on_m ? g.bn : BM;
+  const int w_box = g.fuse_situ ? BM : (g.tok_on_m ? g.bn : BM);
   const int x_box = g.tok_on_m ? BM : g.bn;
   if (!make_map(&mw, g.W, (long long)g.G * g.M_feat, g.K, w_box)) return cudaErrorInvalidValue;
   if (!make_map(&mx, g.X, g.x_rows, g.K, x_box)) return cudaErrorInvalidValue;
 
-  const size_t smem = smem_for(g.bn, p.stages, g.grp_count ? g.G : 0);
+  const size_t smem = smem_for(g.bn, p.stages, g.grp_count ? g.G : 0, g.tok_on_m);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;

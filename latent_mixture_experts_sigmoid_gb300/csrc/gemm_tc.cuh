@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "lmoe_internal.cuh"
+
 namespace lmoe {
 
 // Kernel parameters (passed by value).
@@ -25,6 +27,9 @@ struct GemmParams {
   const uint16_t* add;     // bf16 [rows, ldo] added before rounding, or NULL
   int stages;
   uint32_t tmem_cols;
+  int fuse_situ;           // tokens on M only: W tile = 128 gate rows + the matching 128 up
+                           // rows; the epilogue writes bf16(SituGLU(bf16(G))) [rows, M_feat/2]
+  SituParams sp;
 };
 
 // One GEMM launch:  out[tok, f] = sum_c X[tok, c] W[g*M_feat + f, c] (+ add).
@@ -44,6 +49,8 @@ struct GemmDesc {
   long long split_stride;
   const uint16_t* add;
   int max_units;           // > 0: known upper bound on work units (caps the grid)
+  int fuse_situ;           // see GemmParams; requires tok_on_m, bn == 256, splits == 1
+  float beta, linear_beta;
 };
 
 cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream);
