@@ -423,6 +423,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int width = p.fuse_situ ? BM : bn;           // output columns of this tile
         const int fcol0 = x.feat_tile * width;
         const int ldo = p.fuse_situ ? p.M_feat / 2 : p.ldo;
+        if (p.add && r < x.nvalid) {
+          // pull this thread's row of the addend into L2 while the tile drains
+          const uint16_t* arow = p.add + (long long)(x.tok_row0 + r) * ldo + fcol0;
+          for (int b = 0; b < width * 2; b += 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(arow) + b));
+        }
         for (int c0 = 0; c0 < width; c0 += 32) {
           float f[32];
           {
@@ -458,6 +464,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             *reinterpret_cast<float4*>(st + lane * 32 + ((c ^ (lane & 7)) * 4)) =
                 make_float4(f[4 * c], f[4 * c + 1], f[4 * c + 2], f[4 * c + 3]);
           __syncwarp();
+          // the shared-output add: all eight loads first (the stores below
+          // may alias them as far as the compiler knows)
+          uint2 ad[8];
+          if (p.add) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = i * 4 + (lane >> 3);
+              const int row_in_tile = q * 32 + rr;
+              ad[i] = make_uint2(0u, 0u);
+              if (row_in_tile < x.nvalid)
+                ad[i] = __ldg(reinterpret_cast<const uint2*>(
+                    p.add + (long long)(x.tok_row0 + row_in_tile) * ldo + fcol0 + c0 +
+                    (lane & 7) * 4));
+            }
+          }
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int rr = i * 4 + (lane >> 3);            // row within this warp's 32
@@ -469,8 +490,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               const long long off = orow * ldo + fcol0 + c0 + c * 4;
               float o0 = a.x, o1 = a.y, o2 = a.z, o3 = a.w;
               if (p.add) {
-                const uint2 ad = *reinterpret_cast<const uint2*>(p.add + off);
-                o0 += bf16_lo(ad.x); o1 += bf16_hi(ad.x); o2 += bf16_lo(ad.y); o3 += bf16_hi(ad.y);
+                o0 += bf16_lo(ad[i].x); o1 += bf16_hi(ad[i].x);
+                o2 += bf16_lo(ad[i].y); o3 += bf16_hi(ad[i].y);
               }
               *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) + off) =
                   make_uint2(pack_bf16x2(o0, o1), pack_bf16x2(o2, o3));

@@ -185,7 +185,7 @@ __device__ __forceinline__ void exact_order_and_write(const float* __restrict__ 
   if (lane < total) {
     const int e = cand[lane];
     s = exact_sigmoid(__ldg(row + e));
-    P = pack_exact(__fadd_rn(s, sbias[e]), e);
+    P = pack_exact(__fadd_rn(s, sbias ? sbias[e] : 0.0f), e);
   }
   // bitonic sort of 32 (P, s) pairs, descending
 #pragma unroll
@@ -237,7 +237,8 @@ __device__ __forceinline__ unsigned long long lane_best_exact(const float* __res
   for (int i = 0; i < EPL; ++i) {
     const int e = base + lane + stride * i;
     if (e < E) {
-      const unsigned long long p = pack_exact(__fadd_rn(exact_sigmoid(__ldg(row + e)), sbias[e]), e);
+      const unsigned long long p =
+          pack_exact(__fadd_rn(exact_sigmoid(__ldg(row + e)), sbias ? sbias[e] : 0.0f), e);
       if (p < lastP && p > best) best = p;
     }
   }
@@ -302,53 +303,56 @@ route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bi
   }
 }
 
-// ---- block per token (few tokens, many experts) --------------------------------
-// W warps per token; warp w owns experts e = 32*w + lane + 32*W*i.  Each warp
-// finds its own cheap top-k, warp 0 merges the W sorted lists, every warp marks
-// its candidates, and warp 0 runs the exact stage.
+// ---- block per token ---------------------------------------------------------
+// W warps per token; warp w owns experts e = 32*w + lane + 32*W*i.  Instead of
+// merging sorted lists round by round, the block takes as its pass-B bound the
+// k-th largest of the W*32 lane maxima of the cheap keys: at least k experts
+// reach it, which is all the candidate argument above needs, and when the
+// top-k sit in distinct lanes it equals the k-th largest cheap key.  It is
+// found in parallel: every thread counts the lane maxima above its own.
 template <int EPL, int W>
 __global__ void __launch_bounds__(W * 32)
 route_block_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
                    int k, int renorm, float rsf, int32_t* __restrict__ ids,
                    float* __restrict__ weights) {
-  __shared__ float sbias[EPL * 32 * W];
-  __shared__ uint32_t slist[W][32];
+  __shared__ __align__(16) uint32_t smax[W * 32];
   __shared__ int scnt[W];
   __shared__ int scand[32];
-  __shared__ float sthr;
+  __shared__ uint32_t sak;
   __shared__ unsigned long long spick[W];
   pdl_trigger();
   pdl_wait();
-  for (int i = threadIdx.x; i < EPL * 32 * W; i += blockDim.x)
-    sbias[i] = (i < E && bias != nullptr) ? bias[i] : 0.0f;
-  __syncthreads();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int base = 32 * warp, stride = 32 * W;
 
   for (long long t = blockIdx.x; t < T; t += gridDim.x) {
     const float* row = logits + t * (long long)E;
+    // pass A: cheap keys and this lane's maximum (every lane owns >= 1 expert: E > 32*W)
     float ka[EPL];
-    const uint32_t mysel = warp_cheap_topk<EPL>(row, sbias, E, k, base, stride, lane, ka);
-    slist[warp][lane] = (lane < k) ? mysel : 0u;
-    __syncthreads();
-    if (warp == 0) {
-      // merge W descending lists of k entries: lane w < W owns list w
-      int ptr = 0;
-      uint32_t head = (lane < W) ? slist[lane][0] : 0u;
-      uint32_t a_k = 0;
-      for (int r = 0; r < k; ++r) {
-        const uint32_t m = __reduce_max_sync(FULL, head);
-        a_k = m;
-        if (lane < W && head == m && m != 0u) {
-          ++ptr;
-          head = (ptr < k) ? slist[lane][ptr] : 0u;
-        }
+    uint32_t cmax = 0;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = base + lane + stride * i;
+      ka[i] = -INFINITY;
+      if (e < E) {
+        const float b = bias ? __ldg(bias + e) : 0.0f;
+        ka[i] = fmaxf(fast_sigmoid(__ldg(row + e)) + b, -3.0e38f);
+        cmax = max(cmax, pack_cheap(ka[i], e));
       }
-      if (lane == 0) sthr = candidate_threshold(a_k);
     }
+    smax[threadIdx.x] = cmax;
     __syncthreads();
-    const float thr = sthr;
+    // rank of this lane maximum among all W*32 (packed values are distinct)
+    int above = 0;
+#pragma unroll 8
+    for (int j = 0; j < W * 32; j += 4) {
+      const uint4 v = *reinterpret_cast<const uint4*>(smax + j);
+      above += (v.x > cmax) + (v.y > cmax) + (v.z > cmax) + (v.w > cmax);
+    }
+    if (above == k - 1) sak = cmax;
+    __syncthreads();
+    const float thr = candidate_threshold(sak);
     uint32_t cmask = 0;
     int ccount = 0;
 #pragma unroll
@@ -375,13 +379,13 @@ route_block_kernel(const float* __restrict__ logits, const float* __restrict__ b
         if (cmask & (1u << i)) scand[pos++] = base + lane + stride * i;
       __syncthreads();
       if (warp == 0)
-        exact_order_and_write(row, sbias, scand, total, k, renorm, rsf, t, lane, ids, weights);
+        exact_order_and_write(row, bias, scand, total, k, renorm, rsf, t, lane, ids, weights);
     } else {
       // fallback: exact selection over all experts, one pick per round
       unsigned long long lastP = ~0ull, P = 0ull;
       for (int r = 0; r < k; ++r) {
         const unsigned long long m =
-            warp_max_u64(lane_best_exact<EPL>(row, sbias, E, base, stride, lane, lastP));
+            warp_max_u64(lane_best_exact<EPL>(row, bias, E, base, stride, lane, lastP));
         if (lane == 0) spick[warp] = m;
         __syncthreads();
         unsigned long long best = 0ull;
@@ -414,8 +418,11 @@ cudaError_t launch_block_tier(const float* logits, const float* bias, int T, int
 
 }  // namespace
 
-// Tokens up to this count get a block each (4 warps); larger batches a warp each.
-constexpr int kBlockPerTokenMaxT = 1024;
+// Tokens up to this count get a block each (4 warps); larger batches a warp
+// each.  Measured on GB300 at 896 experts the block kernel is faster at every
+// batch size up to 16384 tokens (more warps in flight hide the serial merge
+// rounds), so the warp kernel serves only beyond that.
+constexpr int kBlockPerTokenMaxT = 1 << 20;
 
 // Compile-time tier list: experts per lane (EPL) for E <= 32 * EPL (warp per
 // token) or E <= 128 * EPL (block of 4 warps per token, E > 128 only).
