@@ -11,6 +11,7 @@ CASE is one of
            ~2 GB on the device;
   decode   one decode forward (T=8) of the same 128-expert variant;
   route    routing of [16384, 896] fp32 logits, top-16;
+  route8   routing of [8, 896] fp32 logits, top-16 (decode);
   situ     dense SituGLU of bf16 [16384, 8192].
 Inputs are seeded (workloads/); each case runs `reps` times after one warm-up.
 """
@@ -72,13 +73,21 @@ def case_decode(reps):
     _layer(dataclasses.replace(W.DECODE, num_experts=128), False, reps)
 
 
-def case_route(reps):
-    lg = torch.from_numpy(W.router_logits(16384, 896, 0, tie_every=64)).to(DEV)
+def _route(T, reps):
+    lg = torch.from_numpy(W.router_logits(T, 896, 0, tie_every=64)).to(DEV)
     b = torch.from_numpy(W.score_bias(896, 0)).to(DEV)
-    ids = torch.empty((16384, 16), dtype=torch.int32, device=DEV)
-    wt = torch.empty((16384, 16), dtype=torch.float32, device=DEV)
+    ids = torch.empty((T, 16), dtype=torch.int32, device=DEV)
+    wt = torch.empty((T, 16), dtype=torch.float32, device=DEV)
     for _ in range(reps + 1):
         lm.moe_route(lg, b, 16, 2.5, ids, wt)
+
+
+def case_route(reps):
+    _route(16384, reps)
+
+
+def case_route8(reps):
+    _route(8, reps)
 
 
 def case_situ(reps):
@@ -89,7 +98,7 @@ def case_situ(reps):
 
 
 CASES = dict(linear=case_linear, layer=case_layer, decode=case_decode, route=case_route,
-             situ=case_situ)
+             route8=case_route8, situ=case_situ)
 
 
 def main():
