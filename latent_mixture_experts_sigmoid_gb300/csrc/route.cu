@@ -1,9 +1,11 @@
 // Single-group sigmoid top-k routing (DeepSeekV3 style).
 //
 // vLLM PR #50088, commit 1: with n_group == 1 and topk_group == 1, grouped
-// top-k is plain top-k over all experts; two kernels are dispatched from a
-// compile-time (num_experts) tier list: block-per-token for few tokens (a
-// hierarchical per-warp reduction), warp-per-token for large batches.
+// top-k is plain top-k over all experts; kernels are dispatched from a
+// compile-time (num_experts) tier list.  Here: a block per token whenever the
+// experts outnumber one warp's lanes several times (4 warps for few tokens,
+// 2 for large batches; a shared-memory reduction across the warps), and a
+// warp per token for up to 128 experts.
 // Commit 4: sigmoid scores of FP32 logits, e_score_correction_bias added for
 // the selection only, weights from the unbiased scores, renormalised, times
 // routed_scaling_factor.
@@ -304,7 +306,7 @@ route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bi
 }
 
 // ---- block per token ---------------------------------------------------------
-// W warps per token; warp w owns experts e = 32*w + lane + 32*W*i.  Instead of
+// W warps per token (E > 32*W); warp w owns experts e = 32*w + lane + 32*W*i.  Instead of
 // merging sorted lists round by round, the block takes as its pass-B bound the
 // k-th largest of the W*32 lane maxima of the cheap keys: at least k experts
 // reach it, which is all the candidate argument above needs, and when the
@@ -325,10 +327,21 @@ route_block_kernel(const float* __restrict__ logits, const float* __restrict__ b
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int base = 32 * warp, stride = 32 * W;
+  // per-lane constants for every token of this block: bias and packed index
+  float lb[EPL];
+  uint32_t lidx[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = base + lane + stride * i;
+    lb[i] = (e < E && bias) ? __ldg(bias + e) : 0.0f;
+    lidx[i] = kIdxMask - (uint32_t)e;
+  }
 
   for (long long t = blockIdx.x; t < T; t += gridDim.x) {
     const float* row = logits + t * (long long)E;
-    // pass A: cheap keys and this lane's maximum (every lane owns >= 1 expert: E > 32*W)
+    // pass A: cheap keys and this lane's maximum (every lane owns >= 1 expert: E > 32*W).
+    // No clamp is needed: __expf saturates to 0 or inf beyond |x| ~ 88 and the
+    // key then differs from the exact one by less than 1e-38.
     float ka[EPL];
     uint32_t cmax = 0;
 #pragma unroll
@@ -336,16 +349,15 @@ route_block_kernel(const float* __restrict__ logits, const float* __restrict__ b
       const int e = base + lane + stride * i;
       ka[i] = -INFINITY;
       if (e < E) {
-        const float b = bias ? __ldg(bias + e) : 0.0f;
-        ka[i] = fmaxf(fast_sigmoid(__ldg(row + e)) + b, -3.0e38f);
-        cmax = max(cmax, pack_cheap(ka[i], e));
+        ka[i] = __fdividef(1.0f, 1.0f + __expf(-__ldg(row + e))) + lb[i];
+        cmax = max(cmax, (orderable(ka[i]) & ~kIdxMask) | lidx[i]);
       }
     }
     smax[threadIdx.x] = cmax;
     __syncthreads();
     // rank of this lane maximum among all W*32 (packed values are distinct)
     int above = 0;
-#pragma unroll 8
+#pragma unroll
     for (int j = 0; j < W * 32; j += 4) {
       const uint4 v = *reinterpret_cast<const uint4*>(smax + j);
       above += (v.x > cmax) + (v.y > cmax) + (v.z > cmax) + (v.w > cmax);
@@ -412,35 +424,38 @@ cudaError_t launch_warp_tier(const float* logits, const float* bias, int T, int 
 template <int EPL, int W>
 cudaError_t launch_block_tier(const float* logits, const float* bias, int T, int E, int k,
                               int renorm, float rsf, int32_t* ids, float* w, cudaStream_t s) {
-  return launch_k(route_block_kernel<EPL, W>, dim3(T), dim3(W * 32), 0, s, logits, bias, T, E, k,
-                  renorm, rsf, ids, w);
+  // persistent: a few blocks per SM loop over the tokens (bias loaded once per block)
+  const int cap = num_sms() * (64 / W);
+  const int grid = T < cap ? T : cap;
+  return launch_k(route_block_kernel<EPL, W>, dim3(grid), dim3(W * 32), 0, s, logits, bias, T, E,
+                  k, renorm, rsf, ids, w);
 }
 
 }  // namespace
 
-// Tokens up to this count get a block each (4 warps); larger batches a warp
-// each.  Measured on GB300 at 896 experts the block kernel is faster at every
-// batch size up to 16384 tokens (more warps in flight hide the serial merge
-// rounds), so the warp kernel serves only beyond that.
-constexpr int kBlockPerTokenMaxT = 1 << 20;
+// Dispatch.  E > 128: a block per token, 4 warps for few tokens (latency),
+// 2 warps per token for large batches (half the rank count per token).  Up to
+// E = 128 one warp holds every expert of a token.
+constexpr int kFourWarpsMaxT = 512;
 
-// Compile-time tier list: experts per lane (EPL) for E <= 32 * EPL (warp per
-// token) or E <= 128 * EPL (block of 4 warps per token, E > 128 only).
+// Compile-time tier list: experts per lane (EPL) for E <= 32 * W * EPL.
 cudaError_t launch_route(const float* logits, const float* bias, int T, int E, int k, int renorm,
                          float rsf, int32_t* ids, float* w, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  if (T <= kBlockPerTokenMaxT && E > 128) {
+  if (E > 128 && T <= kFourWarpsMaxT) {
     if (E <= 256) return launch_block_tier<2, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
     if (E <= 512) return launch_block_tier<4, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
     if (E <= 896) return launch_block_tier<7, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
     return launch_block_tier<8, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
   }
+  if (E > 128) {
+    if (E <= 256) return launch_block_tier<4, 2>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+    if (E <= 512) return launch_block_tier<8, 2>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+    if (E <= 896) return launch_block_tier<14, 2>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+    return launch_block_tier<16, 2>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  }
   if (E <= 64) return launch_warp_tier<2>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  if (E <= 128) return launch_warp_tier<4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  if (E <= 256) return launch_warp_tier<8>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  if (E <= 512) return launch_warp_tier<16>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  if (E <= 896) return launch_warp_tier<28>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  return launch_warp_tier<32>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  return launch_warp_tier<4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
 }
 
 }  // namespace lmoe
