@@ -454,8 +454,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               for (int j = 0; j < 16; j += 2) {
                 const uint32_t gb = pack_bf16x2(f[16 * h + j], f[16 * h + j + 1]);
                 const uint32_t ub = pack_bf16x2(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
-                f[16 * h + j] = situ1(bf16_lo(gb), bf16_lo(ub), p.sp);
-                f[16 * h + j + 1] = situ1(bf16_hi(gb), bf16_hi(ub), p.sp);
+                const f32x2 o = situ2_f32(gb, ub, p.sp);
+                f[16 * h + j] = f2_lo(o);
+                f[16 * h + j + 1] = f2_hi(o);
               }
             }
           }

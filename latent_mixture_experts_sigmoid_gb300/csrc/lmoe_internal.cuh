@@ -83,8 +83,88 @@ __device__ __forceinline__ float situ1(float g, float u, const SituParams& p) {
   return __fdividef(num, den);
 }
 
+// Two elements at a time on the packed fp32 pipe (sm_100 f32x2 FMA/MUL/ADD,
+// each lane rounded to nearest like the scalar form); the hardware 2^x and
+// reciprocal stay per element.  Same formulation and accuracy as situ1.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 f2_make(uint32_t lo_bits, uint32_t hi_bits) {
+  f32x2 d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo_bits), "r"(hi_bits));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_splat(float x) {
+  return f2_make(__float_as_uint(x), __float_as_uint(x));
+}
+__device__ __forceinline__ float f2_lo(f32x2 v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2_hi(f32x2 v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float rcp_fast(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// e^z - 1 for a pair of z <= 0 (Taylor series to z^5 above -0.2, else 2^x - 1)
+__device__ __forceinline__ f32x2 expm1_neg2(f32x2 z) {
+  f32x2 p = f2_fma(z, f2_splat(1.0f / 120.0f), f2_splat(1.0f / 24.0f));
+  p = f2_fma(p, z, f2_splat(1.0f / 6.0f));
+  p = f2_fma(p, z, f2_splat(0.5f));
+  p = f2_fma(p, z, f2_splat(1.0f));
+  const f32x2 small = f2_mul(p, z);
+  const f32x2 t = f2_mul(z, f2_splat(1.4426950408889634f));
+  const f32x2 big = f2_add(f2_make(__float_as_uint(ex2_fast(f2_lo(t))),
+                                   __float_as_uint(ex2_fast(f2_hi(t)))),
+                           f2_splat(-1.0f));
+  const uint32_t lo = f2_lo(z) > -0.2f ? (uint32_t)small : (uint32_t)big;
+  const uint32_t hi = f2_hi(z) > -0.2f ? (uint32_t)(small >> 32) : (uint32_t)(big >> 32);
+  return f2_make(lo, hi);
+}
+
+// bf16x2 gate / up in, fp32 pair out (lo, hi)
+__device__ __forceinline__ f32x2 situ2_f32(uint32_t g2, uint32_t u2, const SituParams& p) {
+  const f32x2 g = f2_make(g2 << 16, g2 & 0xFFFF0000u);
+  const f32x2 gabs = g & 0x7FFFFFFF7FFFFFFFull;
+  const f32x2 m1 = expm1_neg2(f2_mul(gabs, f2_splat(-2.0f * p.inv_beta)));
+  const f32x2 t = f2_mul(g, f2_splat(-1.4426950408889634f));
+  const f32x2 e = f2_make(__float_as_uint(ex2_fast(f2_lo(t))), __float_as_uint(ex2_fast(f2_hi(t))));
+  // -beta with the sign of g flipped: num = sgn(g) * beta * (-m1)
+  const f32x2 nb = (g & 0x8000000080000000ull) ^ f2_splat(-p.beta);
+  f32x2 num = f2_mul(nb, m1);
+  f32x2 den = f2_mul(f2_add(m1, f2_splat(2.0f)), f2_add(e, f2_splat(1.0f)));
+  const f32x2 u = f2_make(u2 << 16, u2 & 0xFFFF0000u);
+  if (p.has_lbeta) {
+    const f32x2 uabs = u & 0x7FFFFFFF7FFFFFFFull;
+    const f32x2 m2 = expm1_neg2(f2_mul(uabs, f2_splat(-2.0f * p.inv_lbeta)));
+    const f32x2 nl = (u & 0x8000000080000000ull) ^ f2_splat(-p.lbeta);
+    num = f2_mul(num, f2_mul(nl, m2));
+    den = f2_mul(den, f2_add(m2, f2_splat(2.0f)));
+  } else {
+    num = f2_mul(num, u);
+  }
+  // a denominator beyond 2^126 (gate below about -87) flushes its reciprocal
+  // to 0, the value to bf16 precision
+  const f32x2 r = f2_make(__float_as_uint(rcp_fast(f2_lo(den))),
+                          __float_as_uint(rcp_fast(f2_hi(den))));
+  return f2_mul(num, r);
+}
+
 __device__ __forceinline__ uint32_t situ2(uint32_t g2, uint32_t u2, const SituParams& p) {
-  return pack_bf16x2(situ1(bf16_lo(g2), bf16_lo(u2), p), situ1(bf16_hi(g2), bf16_hi(u2), p));
+  const f32x2 o = situ2_f32(g2, u2, p);
+  return pack_bf16x2(f2_lo(o), f2_hi(o));
 }
 
 inline SituParams make_situ_params(float beta, float lbeta) {

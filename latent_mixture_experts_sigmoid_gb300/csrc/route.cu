@@ -337,8 +337,23 @@ route_block_kernel(const float* __restrict__ logits, const float* __restrict__ b
     lidx[i] = kIdxMask - (uint32_t)e;
   }
 
+  // this lane's logits of the block's next token are loaded one token ahead
+  float xn[EPL];
+  auto load_row = [&](long long tt) {
+    const float* rr = logits + tt * (long long)E;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = base + lane + stride * i;
+      xn[i] = (tt < T && e < E) ? __ldg(rr + e) : 0.0f;
+    }
+  };
+  load_row(blockIdx.x);
   for (long long t = blockIdx.x; t < T; t += gridDim.x) {
     const float* row = logits + t * (long long)E;
+    float xv[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) xv[i] = xn[i];
+    load_row(t + gridDim.x);
     // pass A: cheap keys and this lane's maximum (every lane owns >= 1 expert: E > 32*W).
     // No clamp is needed: __expf saturates to 0 or inf beyond |x| ~ 88 and the
     // key then differs from the exact one by less than 1e-38.
@@ -349,7 +364,7 @@ route_block_kernel(const float* __restrict__ logits, const float* __restrict__ b
       const int e = base + lane + stride * i;
       ka[i] = -INFINITY;
       if (e < E) {
-        ka[i] = __fdividef(1.0f, 1.0f + __expf(-__ldg(row + e))) + lb[i];
+        ka[i] = __fdividef(1.0f, 1.0f + __expf(-xv[i])) + lb[i];
         cmax = max(cmax, (orderable(ka[i]) & ~kIdxMask) | lidx[i]);
       }
     }
