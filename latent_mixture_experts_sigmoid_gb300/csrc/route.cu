@@ -439,9 +439,18 @@ cudaError_t launch_warp_tier(const float* logits, const float* bias, int T, int 
 template <int EPL, int W>
 cudaError_t launch_block_tier(const float* logits, const float* bias, int T, int E, int k,
                               int renorm, float rsf, int32_t* ids, float* w, cudaStream_t s) {
-  // persistent: a few blocks per SM loop over the tokens (bias loaded once per block)
-  const int cap = num_sms() * (64 / W);
-  const int grid = T < cap ? T : cap;
+  // persistent: as many blocks as fit on the GPU at once loop over the tokens
+  // (bias loaded once per block, next token's logits prefetched)
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, route_block_kernel<EPL, W>, W * 32, 0) !=
+            cudaSuccess || n < 1)
+      n = 4;
+    per_sm = n;
+  }
+  const long long cap = (long long)num_sms() * per_sm;
+  const int grid = (int)(T < cap ? T : cap);
   return launch_k(route_block_kernel<EPL, W>, dim3(grid), dim3(W * 32), 0, s, logits, bias, T, E,
                   k, renorm, rsf, ids, w);
 }
