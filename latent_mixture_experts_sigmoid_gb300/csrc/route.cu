@@ -15,20 +15,22 @@
 // IEEE fp32 operations (exact_sigmoid below).  Evaluating that sequence for
 // all E experts would make the kernel issue-bound, so selection takes two
 // passes:
-//   A. a cheap key ka = fast_sigmoid(x) + b for every expert, packed with the
-//      expert index into one u32 (key truncated to 22 bits, index below), and
-//      the top-k of those by per-lane sorted lists merged with warp max
-//      (redux.sync.max.u32);
-//   B. every expert whose cheap key lies within a proven error bound of the
-//      k-th cheap key is a candidate; candidates (normally k or k+1 of them)
-//      get the exact key and are ordered by a 32-lane bitonic network on
-//      (exact key, lower index first).  More than 32 candidates (a row of tied
-//      logits) fall back to an exact selection over all experts.
+//   A. a cheap key ka = 1/(1 + __expf(-x)) + b for every expert, packed with
+//      the expert index into one u32 (key truncated to 22 bits, index below),
+//      and a bound A: the k-th largest of a small set of per-lane maxima of
+//      those packed keys (so at least k experts reach A), found by a parallel
+//      rank count in shared memory;
+//   B. every expert whose cheap key lies within a proven error bound below A
+//      is a candidate; candidates (normally k to k+4 of them) get the exact
+//      key, and each one's output slot is the number of candidates with a
+//      larger exact key (ties go to the lower index).  More than 32
+//      candidates (a row of tied logits) fall back to an exact selection over
+//      all experts.
 // Why the candidate set always holds the exact top-k: let |ka - key| <= D for
-// every expert and let A be the (truncated) cheap key of the k-th pick.  At
-// least k experts have ka >= A, so at least k have key >= A - D; hence the
-// k-th largest exact key K satisfies K >= A - D, and every member of the exact
-// top-k has ka >= key - D >= K - D >= A - 2D.  D is bounded from the documented
+// every expert and let A be the truncated key of a packed value that at least
+// k experts reach.  Those k have ka >= A, so at least k have key >= A - D;
+// hence the k-th largest exact key K satisfies K >= A - D, and every member of
+// the exact top-k has ka >= key - D >= K - D >= A - 2D.  D is bounded from the documented
 // error of __expf (2 + floor(1.173|x|) ulp, |x| <= 87) and __fdividef (2 ulp):
 // |s_fast - s| <= s(1-s) * 1.24e-5 + 3 ulp <= 3.5e-6, plus the exact
 // sigmoid's own error (<= 3 ulp) and the rounding of the two bias additions
@@ -76,10 +78,6 @@ __device__ __forceinline__ float exact_sigmoid(float x) {
   return __fdiv_rn(1.0f, __fadd_rn(1.0f, e));
 }
 
-__device__ __forceinline__ float fast_sigmoid(float x) {
-  const float xc = fminf(fmaxf(x, -87.0f), 87.0f);
-  return __fdividef(1.0f, 1.0f + __expf(-xc));
-}
 
 // Monotone map float -> u32 (larger float -> larger integer; -0 < +0).
 __device__ __forceinline__ uint32_t orderable(float f) {
@@ -95,9 +93,6 @@ constexpr uint32_t kIdxBits = 10;  // E <= 1024
 constexpr uint32_t kIdxMask = (1u << kIdxBits) - 1u;
 constexpr unsigned FULL = 0xFFFFFFFFu;
 
-__device__ __forceinline__ uint32_t pack_cheap(float ka, int e) {
-  return (orderable(ka) & ~kIdxMask) | (kIdxMask - (uint32_t)e);
-}
 
 // Exact key packed with the index: larger key first, then lower index first.
 __device__ __forceinline__ unsigned long long pack_exact(float key, int e) {
@@ -115,13 +110,6 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
   return ((unsigned long long)hi << 32) | lo;
 }
 
-__device__ __forceinline__ void insert4(uint32_t v, uint32_t& l0, uint32_t& l1, uint32_t& l2,
-                                        uint32_t& l3) {
-  uint32_t t = max(l0, v); v = min(l0, v); l0 = t;
-  t = max(l1, v); v = min(l1, v); l1 = t;
-  t = max(l2, v); v = min(l2, v); l2 = t;
-  l3 = max(l3, v);
-}
 
 // Threshold of pass B from the (truncated) cheap key of the k-th pick.
 __device__ __forceinline__ float candidate_threshold(uint32_t a_k) {
@@ -129,87 +117,42 @@ __device__ __forceinline__ float candidate_threshold(uint32_t a_k) {
   return trunc_k - (1.0e-5f + 0x1p-20f * fmaxf(fabsf(trunc_k), 1.0f));
 }
 
-// ---- pass A for one warp: experts e = base + lane + stride * i ---------------
-// Fills ka[] with the cheap keys of this lane's experts (-inf where e >= E)
-// and returns in lane r (r < k) the warp's r-th largest packed cheap key.
-template <int EPL>
-__device__ __forceinline__ uint32_t warp_cheap_topk(const float* __restrict__ row,
-                                                    const float* sbias, int E, int k, int base,
-                                                    int stride, int lane, float (&ka)[EPL]) {
-  uint32_t l0 = 0, l1 = 0, l2 = 0, l3 = 0;
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    const int e = base + lane + stride * i;
-    ka[i] = -INFINITY;
-    if (e < E) {
-      ka[i] = fmaxf(fast_sigmoid(__ldg(row + e)) + sbias[e], -3.0e38f);
-      insert4(pack_cheap(ka[i], e), l0, l1, l2, l3);
-    }
-  }
-  uint32_t mysel = 0, last = 0;
-  int popped = 0;
-  for (int r = 0; r < k; ++r) {
-    const uint32_t m = __reduce_max_sync(FULL, l0);
-    if (lane == r) mysel = m;
-    if (l0 == m && m != 0u) {
-      l0 = l1; l1 = l2; l2 = l3; l3 = 0; ++popped; last = m;
-    }
-    if (EPL > 4) {
-      // a lane that handed out its whole list may hold further large keys
-      const bool refill = (popped == 4);
-      if (__any_sync(FULL, refill) && refill) {
-        popped = 0;
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-          const int e = base + lane + stride * i;
-          if (e < E) {
-            const uint32_t p = pack_cheap(ka[i], e);
-            if (p < last) insert4(p, l0, l1, l2, l3);
-          }
-        }
-      }
-    }
-  }
-  return mysel;
-}
-
 // ---- pass B exact stage for one warp -----------------------------------------
-// `cand[0..total)` are the candidate experts (total <= 32).  Writes the top-k
-// ids and weights of token t.
+// `cand[0..total)` are the candidate experts (total <= 32).  Every candidate
+// gets its exact key; its output position is the number of candidates with a
+// larger key (keys are distinct: the index breaks ties), so no sort network
+// is needed.  Writes the top-k ids and weights of token t.  `skey` is a
+// 32-entry scratch of this warp.
 __device__ __forceinline__ void exact_order_and_write(const float* __restrict__ row,
                                                       const float* sbias, const int* cand,
                                                       int total, int k, int renorm, float rsf,
                                                       long long t, int lane,
+                                                      unsigned long long* skey,
                                                       int32_t* __restrict__ ids,
                                                       float* __restrict__ weights) {
   unsigned long long P = 0ull;
   float s = 0.0f;
+  int e = 0;
   if (lane < total) {
-    const int e = cand[lane];
+    e = cand[lane];
     s = exact_sigmoid(__ldg(row + e));
     P = pack_exact(__fadd_rn(s, sbias ? sbias[e] : 0.0f), e);
   }
-  // bitonic sort of 32 (P, s) pairs, descending
-#pragma unroll
-  for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const unsigned long long Po = __shfl_xor_sync(FULL, P, stride);
-      const float so = __shfl_xor_sync(FULL, s, stride);
-      const bool up = ((lane & size) == 0);        // this pair sorts descending
-      const bool lower = ((lane & stride) == 0);   // this lane keeps the larger
-      const bool take = (lower == up) ? (Po > P) : (Po < P);
-      if (take) { P = Po; s = so; }
-    }
-  }
-  float sum = (lane < k) ? s : 0.0f;
+  skey[lane] = P;
+  __syncwarp();
+  int rank = 0;
+#pragma unroll 8
+  for (int j = 0; j < 32; ++j) rank += (skey[j] > P) ? 1 : 0;
+  const bool sel = lane < total && rank < k;
+  float sum = sel ? s : 0.0f;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
-  if (lane < k) {
+  if (sel) {
     const float wv = renorm ? __fmul_rn(__fdiv_rn(s, sum), rsf) : __fmul_rn(s, rsf);
-    ids[t * k + lane] = expert_of(P);
-    weights[t * k + lane] = wv;
+    ids[t * k + rank] = e;
+    weights[t * k + rank] = wv;
   }
+  __syncwarp();
 }
 
 // Weights and outputs of an exact selection already held as lane r = r-th pick.
@@ -247,30 +190,81 @@ __device__ __forceinline__ unsigned long long lane_best_exact(const float* __res
   return best;
 }
 
-// ---- warp per token (large batches) ------------------------------------------
-constexpr int kWarpsPerBlock = 8;
+// ---- warp per token --------------------------------------------------------------
+// One warp per token, EPL experts per lane (e = lane + 32*i), tokens visited
+// with a stride of all warps of the grid, the next token's logits loaded one
+// token ahead.  The pass-B bound is the k-th largest of the 64 per-lane top-2
+// cheap keys: at least k experts reach it, and it equals the k-th largest
+// cheap key unless a lane holds three of the top k.  It is found by a
+// warp-local rank count in shared memory (no block barrier).
+constexpr int kWarpsPerBlock = 4;
 
 template <int EPL>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
                   int k, int renorm, float rsf, int32_t* __restrict__ ids,
                   float* __restrict__ weights) {
-  __shared__ float sbias[EPL * 32];
+  __shared__ __align__(16) uint32_t stop2[kWarpsPerBlock][64];
   __shared__ int scand[kWarpsPerBlock][32];
+  __shared__ unsigned long long skey[kWarpsPerBlock][32];
   pdl_trigger();
   pdl_wait();
-  for (int i = threadIdx.x; i < EPL * 32; i += blockDim.x)
-    sbias[i] = (i < E && bias != nullptr) ? bias[i] : 0.0f;
-  __syncthreads();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-
-  for (long long t = (long long)blockIdx.x * kWarpsPerBlock + warp; t < T;
-       t += (long long)gridDim.x * kWarpsPerBlock) {
+  float lb[EPL];
+  uint32_t lidx[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    lb[i] = (e < E && bias) ? __ldg(bias + e) : 0.0f;
+    lidx[i] = kIdxMask - (uint32_t)e;
+  }
+  const long long step = (long long)gridDim.x * kWarpsPerBlock;
+  float xn[EPL];
+  auto load_row = [&](long long tt) {
+    const float* rr = logits + tt * (long long)E;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      xn[i] = (tt < T && e < E) ? __ldg(rr + e) : 0.0f;
+    }
+  };
+  const long long t0 = (long long)blockIdx.x * kWarpsPerBlock + warp;
+  load_row(t0);
+  for (long long t = t0; t < T; t += step) {
     const float* row = logits + t * (long long)E;
     float ka[EPL];
-    const uint32_t mysel = warp_cheap_topk<EPL>(row, sbias, E, k, 0, 32, lane, ka);
-    const float thr = candidate_threshold(__shfl_sync(FULL, mysel, k - 1));
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) ka[i] = xn[i];
+    load_row(t + step);
+    // pass A: cheap keys (no clamp needed, see route_block_kernel) and top-2 per lane
+    uint32_t m1 = 0, m2 = 0;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) {
+        ka[i] = __fdividef(1.0f, 1.0f + __expf(-ka[i])) + lb[i];
+        const uint32_t v = (orderable(ka[i]) & ~kIdxMask) | lidx[i];
+        m2 = max(m2, min(m1, v));
+        m1 = max(m1, v);
+      } else {
+        ka[i] = -INFINITY;
+      }
+    }
+    stop2[warp][lane] = m1;
+    stop2[warp][32 + lane] = m2;
+    __syncwarp();
+    int r1 = 0, r2 = 0;
+#pragma unroll
+    for (int j = 0; j < 64; j += 4) {
+      const uint4 v = *reinterpret_cast<const uint4*>(&stop2[warp][j]);
+      r1 += (v.x > m1) + (v.y > m1) + (v.z > m1) + (v.w > m1);
+      r2 += (v.x > m2) + (v.y > m2) + (v.z > m2) + (v.w > m2);
+    }
+    // exactly one of the 64 (nonzero, distinct) values has rank k-1
+    uint32_t mine = (r1 == k - 1 && m1 != 0u) ? m1 : ((r2 == k - 1 && m2 != 0u) ? m2 : 0u);
+    const uint32_t a_k = __reduce_max_sync(FULL, mine);
+    const float thr = candidate_threshold(a_k);
     uint32_t cmask = 0;
     int ccount = 0;
 #pragma unroll
@@ -289,19 +283,20 @@ route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bi
       for (int i = 0; i < EPL; ++i)
         if (cmask & (1u << i)) scand[warp][pos++] = lane + 32 * i;
       __syncwarp();
-      exact_order_and_write(row, sbias, scand[warp], total, k, renorm, rsf, t, lane, ids, weights);
-      __syncwarp();
+      exact_order_and_write(row, bias, scand[warp], total, k, renorm, rsf, t, lane, skey[warp],
+                            ids, weights);
     } else {
       // fallback: exact selection over all experts, one pick per round
       unsigned long long lastP = ~0ull, P = 0ull;
       for (int r = 0; r < k; ++r) {
         const unsigned long long m =
-            warp_max_u64(lane_best_exact<EPL>(row, sbias, E, 0, 32, lane, lastP));
+            warp_max_u64(lane_best_exact<EPL>(row, bias, E, 0, 32, lane, lastP));
         if (lane == r) P = m;
         lastP = m;
       }
       write_selected(row, P, k, renorm, rsf, t, lane, ids, weights);
     }
+    __syncwarp();
   }
 }
 
@@ -322,6 +317,7 @@ route_block_kernel(const float* __restrict__ logits, const float* __restrict__ b
   __shared__ int scand[32];
   __shared__ uint32_t sak;
   __shared__ unsigned long long spick[W];
+  __shared__ unsigned long long skey[32];
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
@@ -406,7 +402,8 @@ route_block_kernel(const float* __restrict__ logits, const float* __restrict__ b
         if (cmask & (1u << i)) scand[pos++] = base + lane + stride * i;
       __syncthreads();
       if (warp == 0)
-        exact_order_and_write(row, bias, scand, total, k, renorm, rsf, t, lane, ids, weights);
+        exact_order_and_write(row, bias, scand, total, k, renorm, rsf, t, lane, skey, ids,
+                              weights);
     } else {
       // fallback: exact selection over all experts, one pick per round
       unsigned long long lastP = ~0ull, P = 0ull;
@@ -431,7 +428,18 @@ route_block_kernel(const float* __restrict__ logits, const float* __restrict__ b
 template <int EPL>
 cudaError_t launch_warp_tier(const float* logits, const float* bias, int T, int E, int k,
                              int renorm, float rsf, int32_t* ids, float* w, cudaStream_t s) {
-  const int blocks = ceil_div(T, kWarpsPerBlock);
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, route_warp_kernel<EPL>,
+                                                      kWarpsPerBlock * 32, 0) != cudaSuccess ||
+        n < 1)
+      n = 4;
+    per_sm = n;
+  }
+  const long long need = ((long long)T + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  const long long cap = (long long)num_sms() * per_sm;
+  const int blocks = (int)(need < cap ? need : cap);
   return launch_k(route_warp_kernel<EPL>, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, s, logits,
                   bias, T, E, k, renorm, rsf, ids, w);
 }
@@ -457,29 +465,25 @@ cudaError_t launch_block_tier(const float* logits, const float* bias, int T, int
 
 }  // namespace
 
-// Dispatch.  E > 128: a block per token, 4 warps for few tokens (latency),
-// 2 warps per token for large batches (half the rank count per token).  Up to
-// E = 128 one warp holds every expert of a token.
-constexpr int kFourWarpsMaxT = 512;
+// Dispatch.  E > 128 and few tokens: a block of 4 warps per token (latency);
+// otherwise a warp per token, EPL = ceil(E / 32) from the tier list.
+constexpr int kBlockMaxT = 512;
 
-// Compile-time tier list: experts per lane (EPL) for E <= 32 * W * EPL.
 cudaError_t launch_route(const float* logits, const float* bias, int T, int E, int k, int renorm,
                          float rsf, int32_t* ids, float* w, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  if (E > 128 && T <= kFourWarpsMaxT) {
+  if (E > 128 && T <= kBlockMaxT) {
     if (E <= 256) return launch_block_tier<2, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
     if (E <= 512) return launch_block_tier<4, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
     if (E <= 896) return launch_block_tier<7, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
     return launch_block_tier<8, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
   }
-  if (E > 128) {
-    if (E <= 256) return launch_block_tier<4, 2>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-    if (E <= 512) return launch_block_tier<8, 2>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-    if (E <= 896) return launch_block_tier<14, 2>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-    return launch_block_tier<16, 2>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  }
   if (E <= 64) return launch_warp_tier<2>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  return launch_warp_tier<4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 128) return launch_warp_tier<4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 256) return launch_warp_tier<8>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 512) return launch_warp_tier<16>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 896) return launch_warp_tier<28>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  return launch_warp_tier<32>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
 }
 
 }  // namespace lmoe
