@@ -27,6 +27,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "gemm_tc.cuh"
 #include "lmoe_internal.cuh"
 #include "moe_data.cuh"
@@ -252,6 +254,37 @@ int plan_launches(const Plan& p, bool shared) {
   return n;
 }
 
+// The second stream of the decode forward: the shared expert runs there,
+// forked from and joined back to the caller's stream by two events (so the
+// fork is also recorded by a stream capture).  One per device, created by the
+// first decode call on it; the mutex keeps the fork/join event pair of one
+// call from interleaving with another host thread's.
+struct AuxStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+AuxStream g_aux[64];
+std::mutex g_aux_mu;
+
+bool aux_for_current_device(AuxStream** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  AuxStream& a = g_aux[dev];
+  if (a.stream == nullptr) {
+    cudaStream_t st = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return false;
+    if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess)
+      return false;
+    a.stream = st;
+    a.fork = f;
+    a.join = j;
+  }
+  *out = &a;
+  return true;
+}
+
 #define LMOE_TRY(x)                                  \
   do {                                               \
     if ((x) != cudaSuccess) return LMOE_ERR_CUDA;    \
@@ -405,6 +438,60 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
     return ev == nullptr || cudaEventRecord((cudaEvent_t)ev[i], s) == cudaSuccess;
   };
   if (!mark(0)) return LMOE_ERR_CUDA;
+  // decode sizes: the shared expert gets the second stream (not when per-stage
+  // timing was asked for, which needs the stages one after another)
+  const bool concurrent = shared && decode && ev == nullptr;
+  AuxStream* aux = nullptr;
+  std::unique_lock<std::mutex> aux_lock(g_aux_mu, std::defer_lock);
+  if (concurrent) {
+    aux_lock.lock();
+    if (!aux_for_current_device(&aux)) return LMOE_ERR_CUDA;
+    if (cudaEventRecord(aux->fork, s) != cudaSuccess) return LMOE_ERR_CUDA;
+  }
+  // 9-11. shared expert on the original hidden states (enqueued by a lambda:
+  // on the caller's stream, or at decode sizes first thing on the second
+  // stream so that it overlaps the routed path)
+  const float* sh_part = nullptr;
+  int sh_splits = 0;
+  long long sh_stride = 0;
+  const uint16_t* sh_bf16 = nullptr;
+  auto shared_expert = [&](cudaStream_t ss, bool marks) -> int {
+    if (shared) {
+      const DenseCfg c1 = pl.s1;
+      const long long s1_stride = (long long)T * 2 * ds;
+      if (c1.splits > 1) {
+        LMOE_TRY(gemm_dense(wt->ws13, 2 * ds, X, T, H, c1, ws.Pb, 1, s1_stride, nullptr, ss));
+        LMOE_TRY(launch_reduce_situ(ws.Pb, c1.splits, s1_stride, T, ds, d.beta, d.linear_beta,
+                                    ws.As, ss));
+      } else {
+        LMOE_TRY(gemm_dense(wt->ws13, 2 * ds, X, T, H, c1, ws.Gs, 0, 0, nullptr, ss));
+        LMOE_TRY(launch_situ(ws.Gs, ws.As, T, ds, d.beta, d.linear_beta, ss));
+      }
+    }
+    if (marks && !mark(LMOE_STAGE_SHARED1 + 1)) return LMOE_ERR_CUDA;
+    if (shared) {
+      const DenseCfg c2 = pl.s2;
+      sh_stride = (long long)T * H;
+      if (c2.splits > 1) {
+        LMOE_TRY(gemm_dense(wt->ws2, H, ws.As, T, ds, c2, ws.Pb, 1, sh_stride, nullptr, ss));
+        sh_part = ws.Pb;
+        sh_splits = c2.splits;
+      } else {
+        LMOE_TRY(gemm_dense(wt->ws2, H, ws.As, T, ds, c2, ws.Sh, 0, 0, nullptr, ss));
+        sh_bf16 = ws.Sh;
+      }
+    }
+    if (marks && !mark(LMOE_STAGE_SHARED2 + 1)) return LMOE_ERR_CUDA;
+    return LMOE_OK;
+  };
+  int st = LMOE_OK;
+  if (concurrent) {
+    if (cudaStreamWaitEvent(aux->stream, aux->fork, 0) != cudaSuccess) return LMOE_ERR_CUDA;
+    st = shared_expert(aux->stream, false);
+    if (st != LMOE_OK) return st;
+    if (cudaEventRecord(aux->join, aux->stream) != cudaSuccess) return LMOE_ERR_CUDA;
+  }
+
 
   // 1. routing
   LMOE_TRY(launch_route(router_logits, wt->e_score_correction_bias, T, E, k, d.renormalize,
@@ -443,45 +530,20 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
   // 8. combine + RMSNorm
   LMOE_TRY(launch_combine_norm(ws.Y, ws.w, ws.row_of, T, k, L, wt->norm_w, d.rms_eps, ws.N, s));
   if (!mark(LMOE_STAGE_COMBINE + 1)) return LMOE_ERR_CUDA;
-  // 9-11. shared expert on the original hidden states
-  const float* sh_part = nullptr;
-  int sh_splits = 0;
-  long long sh_stride = 0;
-  const uint16_t* sh_bf16 = nullptr;
-  if (shared) {
-    const DenseCfg c1 = pl.s1;
-    const long long s1_stride = (long long)T * 2 * ds;
-    if (c1.splits > 1) {
-      LMOE_TRY(gemm_dense(wt->ws13, 2 * ds, X, T, H, c1, ws.Pb, 1, s1_stride, nullptr, s));
-      LMOE_TRY(launch_reduce_situ(ws.Pb, c1.splits, s1_stride, T, ds, d.beta, d.linear_beta,
-                                  ws.As, s));
-    } else {
-      LMOE_TRY(gemm_dense(wt->ws13, 2 * ds, X, T, H, c1, ws.Gs, 0, 0, nullptr, s));
-      LMOE_TRY(launch_situ(ws.Gs, ws.As, T, ds, d.beta, d.linear_beta, s));
-    }
-  }
-  if (!mark(LMOE_STAGE_SHARED1 + 1)) return LMOE_ERR_CUDA;
-  if (shared) {
-    const DenseCfg c2 = pl.s2;
-    sh_stride = (long long)T * H;
-    if (c2.splits > 1) {
-      LMOE_TRY(gemm_dense(wt->ws2, H, ws.As, T, ds, c2, ws.Pb, 1, sh_stride, nullptr, s));
-      sh_part = ws.Pb;
-      sh_splits = c2.splits;
-    } else {
-      LMOE_TRY(gemm_dense(wt->ws2, H, ws.As, T, ds, c2, ws.Sh, 0, 0, nullptr, s));
-      sh_bf16 = ws.Sh;
-    }
-  }
-  if (!mark(LMOE_STAGE_SHARED2 + 1)) return LMOE_ERR_CUDA;
   // 12. up-projection with the shared output added in the epilogue
   const DenseCfg cup = pl.up;
+  if (!concurrent) {
+    st = shared_expert(s, true);
+    if (st != LMOE_OK) return st;
+  }
   if (cup.splits > 1) {
     const long long up_stride = (long long)T * H;
     LMOE_TRY(gemm_dense(wt->w_up, H, ws.N, T, L, cup, ws.Pa, 1, up_stride, nullptr, s));
+    if (concurrent && cudaStreamWaitEvent(s, aux->join, 0) != cudaSuccess) return LMOE_ERR_CUDA;
     LMOE_TRY(launch_reduce_splits(ws.Pa, cup.splits, up_stride, sh_part, sh_splits, sh_stride,
                                   sh_bf16, (long long)T * H, out, s));
   } else {
+    if (concurrent && cudaStreamWaitEvent(s, aux->join, 0) != cudaSuccess) return LMOE_ERR_CUDA;
     if (sh_part) {
       // shared output still in partials: materialise it in bf16 first
       LMOE_TRY(launch_reduce_splits(sh_part, sh_splits, sh_stride, nullptr, 0, 0, nullptr,
