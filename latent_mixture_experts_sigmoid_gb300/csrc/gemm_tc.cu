@@ -42,6 +42,7 @@ __device__ int g_device_error = 0;
 namespace {
 
 constexpr int BK = 64;                 // K elements per stage (128 bytes of bf16)
+static_assert(BK == 64, "the MMA issue loop unrolls four K=16 steps per stage");
 constexpr int BM = 128;                // MMA M
 constexpr int kThreads = 192;          // 6 warps
 constexpr long long kWaitCycles = 1ll << 32;   // ~2 s at 2 GHz
@@ -90,6 +91,12 @@ __device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatil
       return false;
     }
   }
+}
+
+// Fast path inline (the phase is usually complete already), bounded loop out of line.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int code) {
+  return mbar_try_wait(bar, parity) || wait_bounded(bar, parity, abort_flag, code);
 }
 
 __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint32_t dst, uint32_t bar,
@@ -332,20 +339,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
       pdl_wait();
       const int U = total_units(p, tok_tile, nfeat);
-      uint32_t it = 0;
+      // ring position kept incrementally: stage s, its smem address, parity
+      uint32_t it = 0, s = 0, ph = 0;
+      uint32_t sa = smem_u32(smem);
+      const uint32_t sa0 = sa;
       bool ok = true;
       for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
         const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb);
         for (int kb = x.kb0; kb < x.kb1; ++kb, ++it) {
-          const int s = (int)(it % (uint32_t)S);
-          const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
           if (it >= pre) {
-            const uint32_t ph = (it / (uint32_t)S) & 1u;
-            if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kErrProducer)) { ok = false; break; }
-            mbar_arrive_expect_tx(full_bar(s), stage_bytes);
-            load_w(sa + offW, full_bar(s), kb, x.w_row0);
+            if (!wait_phase(empty_bar((int)s), ph ^ 1u, abort_flag, kErrProducer)) { ok = false; break; }
+            mbar_arrive_expect_tx(full_bar((int)s), stage_bytes);
+            load_w(sa + offW, full_bar((int)s), kb, x.w_row0);
           }
-          tma_load_2d(mapX, sa + offX, full_bar(s), kb * BK, x.tok_row0);
+          tma_load_2d(mapX, sa + offX, full_bar((int)s), kb * BK, x.tok_row0);
+          if (++s == (uint32_t)S) { s = 0; ph ^= 1u; sa = sa0; } else { sa += stage_bytes; }
         }
       }
       // stages armed before the wait but never reached (abort) still get their
@@ -369,30 +377,35 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       pdl_wait();
       const int U = total_units(p, tok_tile, nfeat);
       const uint32_t idesc = idesc_bf16(BM, bn);
-      uint32_t it = 0, uit = 0;
+      // descriptors of stage 0; stage s adds s*stage_bytes, each K=16 step adds
+      // 32 bytes (+2 in the 16-byte address field, which never carries out)
+      const uint64_t da0 = sdesc(smem_u32(smem));
+      const uint64_t db0 = sdesc(smem_u32(smem) + a_bytes);
+      const uint64_t dstep = stage_bytes >> 4;
+      uint32_t uit = 0, s = 0, ph = 0;
+      uint64_t da = da0, db = db0;
       bool ok = true;
       for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++uit) {
         const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb);
         const int acc = (int)(uit & 1u);
-        if (!wait_bounded(tempty_bar(acc), ((uit >> 1) & 1u) ^ 1u, abort_flag, kErrMmaTmem)) {
+        if (!wait_phase(tempty_bar(acc), ((uit >> 1) & 1u) ^ 1u, abort_flag, kErrMmaTmem)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * bn);
-        for (int kb = x.kb0; kb < x.kb1; ++kb, ++it) {
-          const int s = (int)(it % (uint32_t)S);
-          const uint32_t ph = (it / (uint32_t)S) & 1u;
-          if (!wait_bounded(full_bar(s), ph, abort_flag, kErrMmaFull)) { ok = false; break; }
+        uint32_t accumulate = 0u;
+        for (int kb = x.kb0; kb < x.kb1; ++kb) {
+          if (!wait_phase(full_bar((int)s), ph, abort_flag, kErrMmaFull)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-          const uint32_t sb = sa + a_bytes;
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            mma_bf16(d_tmem, sdesc(sa + kk * 32), sdesc(sb + kk * 32), idesc,
-                     (kb > x.kb0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(empty_bar(s));
+          mma_bf16(d_tmem, da, db, idesc, accumulate);
+          mma_bf16(d_tmem, da + 2, db + 2, idesc, 1u);
+          mma_bf16(d_tmem, da + 4, db + 4, idesc, 1u);
+          mma_bf16(d_tmem, da + 6, db + 6, idesc, 1u);
+          accumulate = 1u;
+          mma_commit(empty_bar((int)s));
+          if (++s == (uint32_t)S) { s = 0; ph ^= 1u; da = da0; db = db0; }
+          else { da += dstep; db += dstep; }
         }
         if (ok) mma_commit(tfull_bar(acc));
       }
