@@ -191,106 +191,161 @@ __device__ __forceinline__ unsigned long long lane_best_exact(const float* __res
 }
 
 // ---- warp per token --------------------------------------------------------------
-// One warp per token, EPL experts per lane (e = lane + 32*i), tokens visited
-// with a stride of all warps of the grid, the next token's logits loaded one
-// token ahead.  The pass-B bound is the k-th largest of the 64 per-lane top-2
-// cheap keys: at least k experts reach it, and it equals the k-th largest
-// cheap key unless a lane holds three of the top k.  It is found by a
-// warp-local rank count in shared memory (no block barrier).
+// One warp per token, tokens visited with a stride of all warps of the grid and
+// the next token's logits loaded one token ahead.  Lane l owns the experts
+// e = 128*c + 4*l + j (chunk c < C, j < 4), so every load of a row is one 16-byte
+// vector per lane when E is a multiple of 4.  Pass A keeps plain float keys
+// (padding is NaN, which neither a maximum nor a candidate test picks up) and
+// two group maxima per lane (j < 2 and j >= 2 over all chunks): the 64 group
+// maxima are keys of 64 distinct experts, so the k-th largest of them is a
+// bound that at least k experts reach.  It is found by a bitonic sort of the 64
+// values across the warp (shuffles, no shared memory); on N(0,1) logits it
+// sits near the 18th largest key, leaving 17-20 candidates for the exact stage.
 constexpr int kWarpsPerBlock = 4;
 
-template <int EPL>
+// Ascending bitonic sort of the 64 values (v0, v1) of a warp, element index 2*lane + g.
+__device__ __forceinline__ void warp_sort64(float& v0, float& v1, int lane) {
+  const int i2 = 2 * lane;
+#pragma unroll
+  for (int size = 2; size <= 64; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 1; stride >>= 1) {
+      const float p0 = __shfl_xor_sync(FULL, v0, stride >> 1);
+      const float p1 = __shfl_xor_sync(FULL, v1, stride >> 1);
+      // keep the smaller value where (lower half) == (ascending block)
+      const bool kmin = ((i2 & stride) == 0) == ((i2 & size) == 0);
+      v0 = kmin ? fminf(v0, p0) : fmaxf(v0, p0);
+      v1 = kmin ? fminf(v1, p1) : fmaxf(v1, p1);
+    }
+    // stride 1: the lane's own pair
+    const float lo = fminf(v0, v1), hi = fmaxf(v0, v1);
+    const bool asc = (i2 & size) == 0;
+    v0 = asc ? lo : hi;
+    v1 = asc ? hi : lo;
+  }
+}
+
+__device__ __forceinline__ float candidate_threshold_f(float a) {
+  return a - (1.0e-5f + 0x1p-20f * fmaxf(fabsf(a), 1.0f));
+}
+
+template <int C>
+__device__ __forceinline__ int chunk_expert(int i, int lane) {
+  return 128 * (i >> 2) + 4 * lane + (i & 3);
+}
+
+// Largest exact packed key below `lastP` among this lane's experts (chunk layout).
+template <int C>
+__device__ __forceinline__ unsigned long long lane_best_exact_chunk(const float* __restrict__ row,
+                                                                    const float* sbias, int E,
+                                                                    int lane,
+                                                                    unsigned long long lastP) {
+  unsigned long long best = 0ull;
+#pragma unroll
+  for (int i = 0; i < 4 * C; ++i) {
+    const int e = chunk_expert<C>(i, lane);
+    if (e < E) {
+      const unsigned long long p = pack_exact(__fadd_rn(exact_sigmoid(__ldg(row + e)), sbias[e]), e);
+      if (p < lastP && p > best) best = p;
+    }
+  }
+  return best;
+}
+
+template <int C, bool VEC>
+__device__ __forceinline__ void load_chunks(const float* __restrict__ logits, long long t, int T,
+                                            int E, int lane, float (&x)[4 * C]) {
+  const float* rr = logits + t * (long long)E;
+#pragma unroll
+  for (int c = 0; c < C; ++c) {
+    const int e0 = 128 * c + 4 * lane;
+    if (VEC) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < T && e0 < E) v = __ldg(reinterpret_cast<const float4*>(rr + e0));
+      x[4 * c] = v.x; x[4 * c + 1] = v.y; x[4 * c + 2] = v.z; x[4 * c + 3] = v.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) x[4 * c + j] = (t < T && e0 + j < E) ? __ldg(rr + e0 + j) : 0.0f;
+    }
+  }
+}
+
+template <int C, bool VEC>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
                   int k, int renorm, float rsf, int32_t* __restrict__ ids,
                   float* __restrict__ weights) {
-  __shared__ __align__(16) uint32_t stop2[kWarpsPerBlock][64];
+  constexpr int EPL = 4 * C;
+  __shared__ __align__(16) float sbias[128 * C];
   __shared__ int scand[kWarpsPerBlock][32];
   __shared__ unsigned long long skey[kWarpsPerBlock][32];
   pdl_trigger();
+  for (int e = threadIdx.x; e < 128 * C; e += blockDim.x) sbias[e] = 0.0f;
   pdl_wait();
+  if (bias)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) sbias[e] = __ldg(bias + e);
+  __syncthreads();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  float lb[EPL];
-  uint32_t lidx[EPL];
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    const int e = lane + 32 * i;
-    lb[i] = (e < E && bias) ? __ldg(bias + e) : 0.0f;
-    lidx[i] = kIdxMask - (uint32_t)e;
-  }
   const long long step = (long long)gridDim.x * kWarpsPerBlock;
-  float xn[EPL];
-  auto load_row = [&](long long tt) {
-    const float* rr = logits + tt * (long long)E;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      xn[i] = (tt < T && e < E) ? __ldg(rr + e) : 0.0f;
-    }
-  };
   const long long t0 = (long long)blockIdx.x * kWarpsPerBlock + warp;
-  load_row(t0);
+  // ascending sorted position of the k-th largest group maximum
+  const int kpos = 64 - k, klane = kpos >> 1, kodd = kpos & 1;
+  float xn[EPL];
+  load_chunks<C, VEC>(logits, t0, T, E, lane, xn);
   for (long long t = t0; t < T; t += step) {
     const float* row = logits + t * (long long)E;
     float ka[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) ka[i] = xn[i];
-    load_row(t + step);
-    // pass A: cheap keys (no clamp needed, see route_block_kernel) and top-2 per lane
-    uint32_t m1 = 0, m2 = 0;
+    load_chunks<C, VEC>(logits, t + step, T, E, lane, xn);
+    // pass A: cheap keys and the two group maxima of this lane
+    float g0 = -INFINITY, g1 = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) {
-        ka[i] = __fdividef(1.0f, 1.0f + __expf(-ka[i])) + lb[i];
-        const uint32_t v = (orderable(ka[i]) & ~kIdxMask) | lidx[i];
-        m2 = max(m2, min(m1, v));
-        m1 = max(m1, v);
-      } else {
-        ka[i] = -INFINITY;
+    for (int c = 0; c < C; ++c) {
+      const float4 b = *reinterpret_cast<const float4*>(&sbias[128 * c + 4 * lane]);
+      const float bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = 4 * c + j;
+        // no clamp: __expf saturates to 0 or inf beyond |x| ~ 88, where the
+        // cheap key differs from the exact one by less than 1e-38
+        const float key = __fdividef(1.0f, 1.0f + __expf(-ka[i])) + bb[j];
+        ka[i] = (128 * c + 4 * lane + j < E) ? key : __int_as_float(0x7fc00000);
+        if (j < 2) g0 = fmaxf(g0, ka[i]); else g1 = fmaxf(g1, ka[i]);
       }
     }
-    stop2[warp][lane] = m1;
-    stop2[warp][32 + lane] = m2;
-    __syncwarp();
-    int r1 = 0, r2 = 0;
-#pragma unroll
-    for (int j = 0; j < 64; j += 4) {
-      const uint4 v = *reinterpret_cast<const uint4*>(&stop2[warp][j]);
-      r1 += (v.x > m1) + (v.y > m1) + (v.z > m1) + (v.w > m1);
-      r2 += (v.x > m2) + (v.y > m2) + (v.z > m2) + (v.w > m2);
-    }
-    // exactly one of the 64 (nonzero, distinct) values has rank k-1
-    uint32_t mine = (r1 == k - 1 && m1 != 0u) ? m1 : ((r2 == k - 1 && m2 != 0u) ? m2 : 0u);
-    const uint32_t a_k = __reduce_max_sync(FULL, mine);
-    const float thr = candidate_threshold(a_k);
+    warp_sort64(g0, g1, lane);
+    const float a_k = __shfl_sync(FULL, kodd ? g1 : g0, klane);
+    const float thr = candidate_threshold_f(a_k);
     uint32_t cmask = 0;
-    int ccount = 0;
 #pragma unroll
     for (int i = 0; i < EPL; ++i)
-      if (ka[i] >= thr) { cmask |= 1u << i; ++ccount; }
-    const int total = (int)__reduce_add_sync(FULL, (uint32_t)ccount);
+      if (ka[i] >= thr) cmask |= 1u << i;
+    const int ccount = __popc(cmask);
+    int incl = ccount;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int total = __shfl_sync(FULL, incl, 31);
     if (total <= 32) {
-      int incl = ccount;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(FULL, incl, o);
-        if (lane >= o) incl += v;
-      }
       int pos = incl - ccount;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i)
-        if (cmask & (1u << i)) scand[warp][pos++] = lane + 32 * i;
+      while (cmask) {
+        const int i = __ffs(cmask) - 1;
+        cmask &= cmask - 1u;
+        scand[warp][pos++] = 128 * (i >> 2) + 4 * lane + (i & 3);
+      }
       __syncwarp();
-      exact_order_and_write(row, bias, scand[warp], total, k, renorm, rsf, t, lane, skey[warp],
+      exact_order_and_write(row, sbias, scand[warp], total, k, renorm, rsf, t, lane, skey[warp],
                             ids, weights);
     } else {
-      // fallback: exact selection over all experts, one pick per round
+      // fallback (rows of tied logits): exact selection over all experts, one pick per round
       unsigned long long lastP = ~0ull, P = 0ull;
       for (int r = 0; r < k; ++r) {
         const unsigned long long m =
-            warp_max_u64(lane_best_exact<EPL>(row, bias, E, 0, 32, lane, lastP));
+            warp_max_u64(lane_best_exact_chunk<C>(row, sbias, E, lane, lastP));
         if (lane == r) P = m;
         lastP = m;
       }
@@ -425,13 +480,13 @@ route_block_kernel(const float* __restrict__ logits, const float* __restrict__ b
   }
 }
 
-template <int EPL>
+template <int C, bool VEC>
 cudaError_t launch_warp_tier(const float* logits, const float* bias, int T, int E, int k,
                              int renorm, float rsf, int32_t* ids, float* w, cudaStream_t s) {
   static int per_sm = 0;
   if (per_sm == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, route_warp_kernel<EPL>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, route_warp_kernel<C, VEC>,
                                                       kWarpsPerBlock * 32, 0) != cudaSuccess ||
         n < 1)
       n = 4;
@@ -440,8 +495,16 @@ cudaError_t launch_warp_tier(const float* logits, const float* bias, int T, int 
   const long long need = ((long long)T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const long long cap = (long long)num_sms() * per_sm;
   const int blocks = (int)(need < cap ? need : cap);
-  return launch_k(route_warp_kernel<EPL>, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, s, logits,
-                  bias, T, E, k, renorm, rsf, ids, w);
+  return launch_k(route_warp_kernel<C, VEC>, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, s,
+                  logits, bias, T, E, k, renorm, rsf, ids, w);
+}
+
+template <int C>
+cudaError_t launch_warp_chunks(const float* logits, const float* bias, int T, int E, int k,
+                               int renorm, float rsf, int32_t* ids, float* w, cudaStream_t s) {
+  // 16-byte row loads need every row to start on a 16-byte boundary
+  if (E % 4 == 0) return launch_warp_tier<C, true>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  return launch_warp_tier<C, false>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
 }
 
 template <int EPL, int W>
@@ -466,7 +529,7 @@ cudaError_t launch_block_tier(const float* logits, const float* bias, int T, int
 }  // namespace
 
 // Dispatch.  E > 128 and few tokens: a block of 4 warps per token (latency);
-// otherwise a warp per token, EPL = ceil(E / 32) from the tier list.
+// otherwise a warp per token, C = ceil(E / 128) chunks of four experts per lane.
 constexpr int kBlockMaxT = 512;
 
 cudaError_t launch_route(const float* logits, const float* bias, int T, int E, int k, int renorm,
@@ -478,12 +541,11 @@ cudaError_t launch_route(const float* logits, const float* bias, int T, int E, i
     if (E <= 896) return launch_block_tier<7, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
     return launch_block_tier<8, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
   }
-  if (E <= 64) return launch_warp_tier<2>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  if (E <= 128) return launch_warp_tier<4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  if (E <= 256) return launch_warp_tier<8>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  if (E <= 512) return launch_warp_tier<16>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  if (E <= 896) return launch_warp_tier<28>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  return launch_warp_tier<32>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 128) return launch_warp_chunks<1>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 256) return launch_warp_chunks<2>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 512) return launch_warp_chunks<4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 896) return launch_warp_chunks<7>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  return launch_warp_chunks<8>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
 }
 
 }  // namespace lmoe
