@@ -121,8 +121,9 @@ __device__ __forceinline__ float candidate_threshold(uint32_t a_k) {
 // `cand[0..total)` are the candidate experts (total <= 32).  Every candidate
 // gets its exact key; its output position is the number of candidates with a
 // larger key (keys are distinct: the index breaks ties), so no sort network
-// is needed.  Writes the top-k ids and weights of token t.  `skey` is a
-// 32-entry scratch of this warp.
+// is needed.  Writes the top-k ids and weights of token t.  `row` is the
+// token's logits (global or shared memory); `skey` is a 32-entry, 16-byte
+// aligned scratch of this warp.
 __device__ __forceinline__ void exact_order_and_write(const float* __restrict__ row,
                                                       const float* sbias, const int* cand,
                                                       int total, int k, int renorm, float rsf,
@@ -135,14 +136,19 @@ __device__ __forceinline__ void exact_order_and_write(const float* __restrict__ 
   int e = 0;
   if (lane < total) {
     e = cand[lane];
-    s = exact_sigmoid(__ldg(row + e));
+    s = exact_sigmoid(row[e]);
     P = pack_exact(__fadd_rn(s, sbias ? sbias[e] : 0.0f), e);
   }
   skey[lane] = P;
   __syncwarp();
+  // entries of lanes >= total are 0 and count for nothing
   int rank = 0;
-#pragma unroll 8
-  for (int j = 0; j < 32; ++j) rank += (skey[j] > P) ? 1 : 0;
+  const int jn = (total + 3) & ~3;
+  for (int j = 0; j < jn; j += 4) {
+    const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(skey + j);
+    const ulonglong2 b = *reinterpret_cast<const ulonglong2*>(skey + j + 2);
+    rank += (a.x > P) + (a.y > P) + (b.x > P) + (b.y > P);
+  }
   const bool sel = lane < total && rank < k;
   float sum = sel ? s : 0.0f;
 #pragma unroll
@@ -160,7 +166,7 @@ __device__ __forceinline__ void write_selected(const float* __restrict__ row,
                                                unsigned long long P, int k, int renorm, float rsf,
                                                long long t, int lane, int32_t* __restrict__ ids,
                                                float* __restrict__ weights) {
-  const float s = (lane < k) ? exact_sigmoid(__ldg(row + expert_of(P))) : 0.0f;
+  const float s = (lane < k) ? exact_sigmoid(row[expert_of(P)]) : 0.0f;
   float sum = s;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(FULL, sum, o);
@@ -191,17 +197,64 @@ __device__ __forceinline__ unsigned long long lane_best_exact(const float* __res
 }
 
 // ---- warp per token --------------------------------------------------------------
-// One warp per token, tokens visited with a stride of all warps of the grid and
-// the next token's logits loaded one token ahead.  Lane l owns the experts
-// e = 128*c + 4*l + j (chunk c < C, j < 4), so every load of a row is one 16-byte
-// vector per lane when E is a multiple of 4.  Pass A keeps plain float keys
-// (padding is NaN, which neither a maximum nor a candidate test picks up) and
-// two group maxima per lane (j < 2 and j >= 2 over all chunks): the 64 group
-// maxima are keys of 64 distinct experts, so the k-th largest of them is a
-// bound that at least k experts reach.  It is found by a bitonic sort of the 64
-// values across the warp (shuffles, no shared memory); on N(0,1) logits it
-// sits near the 18th largest key, leaving 17-20 candidates for the exact stage.
+// One warp per token, tokens visited with a stride of all warps of the grid.
+// Rows are staged in shared memory by cp.async, the next token's row in flight
+// while the current one is processed (two slots per warp); padding slots hold
+// NaN, which neither a maximum nor a candidate test picks up.  Lane l owns the
+// experts e = 128*c + 4*l + j (chunk c < C, j < 4): one 16-byte copy and one
+// 16-byte shared load per chunk when E is a multiple of 4.
+//
+// Pass A uses a cheaper key than the block kernel, in a doubled scale:
+//   ka2 = tanh(x/2) + (2b + 1)   (= 2 sigmoid(x) + 2b up to the error of tanh)
+// with the hardware tanh (one MUFU operation per expert).  tanh.approx.f32 is
+// documented with a maximum error near 2^-11; the window below allows 2^-9
+// per key (four times that), and an exhaustive run over every finite fp32
+// input on GB300 measured at most 2^-16.9 absolute.  Other error terms: the
+// rounding of 2b + 1 and of the final add (2^-24 |.| each), and the exact key's
+// own error doubled (3 ulp of sigmoid plus the rounding of the bias add), all
+// below 2^-20 max(|ka2|, 1).  So with D2 = 2^-9 + 2^-21 max(|A2|, 1) the
+// candidate argument of the file header holds in the doubled scale.
+//
+// The bound A2 is first the k-th largest of the 32 lane maxima (a bitonic sort
+// across the warp); in the rare case that leaves more than 32 candidates it is
+// refined to the k-th largest of 64 group maxima (j < 2 and j >= 2 of every
+// lane), and only then does the exact fallback run.
 constexpr int kWarpsPerBlock = 4;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(smem)), "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// Ascending bitonic sort of one value per lane across the warp.
+__device__ __forceinline__ float warp_sort32(float v, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const float p = __shfl_xor_sync(FULL, v, stride);
+      const bool kmin = ((lane & stride) == 0) == ((lane & size) == 0);
+      v = kmin ? fminf(v, p) : fmaxf(v, p);
+    }
+  }
+  return v;
+}
 
 // Ascending bitonic sort of the 64 values (v0, v1) of a warp, element index 2*lane + g.
 __device__ __forceinline__ void warp_sort64(float& v0, float& v1, int lane) {
@@ -225,112 +278,128 @@ __device__ __forceinline__ void warp_sort64(float& v0, float& v1, int lane) {
   }
 }
 
-__device__ __forceinline__ float candidate_threshold_f(float a) {
-  return a - (1.0e-5f + 0x1p-20f * fmaxf(fabsf(a), 1.0f));
-}
-
-template <int C>
-__device__ __forceinline__ int chunk_expert(int i, int lane) {
-  return 128 * (i >> 2) + 4 * lane + (i & 3);
+__device__ __forceinline__ float candidate_threshold2(float a2) {
+  return a2 - (0x1p-8f + 0x1p-20f * fmaxf(fabsf(a2), 1.0f));
 }
 
 // Largest exact packed key below `lastP` among this lane's experts (chunk layout).
 template <int C>
-__device__ __forceinline__ unsigned long long lane_best_exact_chunk(const float* __restrict__ row,
+__device__ __forceinline__ unsigned long long lane_best_exact_chunk(const float* row,
                                                                     const float* sbias, int E,
                                                                     int lane,
                                                                     unsigned long long lastP) {
   unsigned long long best = 0ull;
 #pragma unroll
   for (int i = 0; i < 4 * C; ++i) {
-    const int e = chunk_expert<C>(i, lane);
+    const int e = 128 * (i >> 2) + 4 * lane + (i & 3);
     if (e < E) {
-      const unsigned long long p = pack_exact(__fadd_rn(exact_sigmoid(__ldg(row + e)), sbias[e]), e);
+      const unsigned long long p = pack_exact(__fadd_rn(exact_sigmoid(row[e]), sbias[e]), e);
       if (p < lastP && p > best) best = p;
     }
   }
   return best;
 }
 
+// Start the copy of token tt's row into `dst` (nothing for tt >= T), then close the group.
 template <int C, bool VEC>
-__device__ __forceinline__ void load_chunks(const float* __restrict__ logits, long long t, int T,
-                                            int E, int lane, float (&x)[4 * C]) {
-  const float* rr = logits + t * (long long)E;
+__device__ __forceinline__ void stage_row(float* dst, const float* __restrict__ logits,
+                                          long long tt, int T, int E, int lane) {
+  if (tt < T) {
+    const float* rr = logits + tt * (long long)E;
 #pragma unroll
-  for (int c = 0; c < C; ++c) {
-    const int e0 = 128 * c + 4 * lane;
-    if (VEC) {
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (t < T && e0 < E) v = __ldg(reinterpret_cast<const float4*>(rr + e0));
-      x[4 * c] = v.x; x[4 * c + 1] = v.y; x[4 * c + 2] = v.z; x[4 * c + 3] = v.w;
-    } else {
+    for (int c = 0; c < C; ++c) {
+      const int e0 = 128 * c + 4 * lane;
+      if (VEC) {
+        if (e0 < E) cp_async16(dst + e0, rr + e0);
+      } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) x[4 * c + j] = (t < T && e0 + j < E) ? __ldg(rr + e0 + j) : 0.0f;
+        for (int j = 0; j < 4; ++j)
+          if (e0 + j < E) cp_async4(dst + e0 + j, rr + e0 + j);
+      }
     }
   }
+  cp_async_commit();
 }
 
 template <int C, bool VEC>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, 5)
 route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
                   int k, int renorm, float rsf, int32_t* __restrict__ ids,
                   float* __restrict__ weights) {
-  constexpr int EPL = 4 * C;
-  __shared__ __align__(16) float sbias[128 * C];
+  constexpr int EW = 128 * C;
+  __shared__ __align__(16) float srow[kWarpsPerBlock][2][EW];
+  __shared__ __align__(16) float sbias[EW];
+  __shared__ __align__(16) float sc2[EW];     // 2b + 1
   __shared__ int scand[kWarpsPerBlock][32];
-  __shared__ unsigned long long skey[kWarpsPerBlock][32];
+  __shared__ __align__(16) unsigned long long skey[kWarpsPerBlock][32];
   pdl_trigger();
-  for (int e = threadIdx.x; e < 128 * C; e += blockDim.x) sbias[e] = 0.0f;
+  const float qnan = __int_as_float(0x7fc00000);
+  for (int i = threadIdx.x; i < kWarpsPerBlock * 2 * EW; i += blockDim.x) (&srow[0][0][0])[i] = qnan;
   pdl_wait();
-  if (bias)
-    for (int e = threadIdx.x; e < E; e += blockDim.x) sbias[e] = __ldg(bias + e);
+  for (int e = threadIdx.x; e < EW; e += blockDim.x) {
+    const float b = (bias && e < E) ? __ldg(bias + e) : 0.0f;
+    sbias[e] = b;
+    sc2[e] = 2.0f * b + 1.0f;
+  }
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const long long step = (long long)gridDim.x * kWarpsPerBlock;
   const long long t0 = (long long)blockIdx.x * kWarpsPerBlock + warp;
-  // ascending sorted position of the k-th largest group maximum
-  const int kpos = 64 - k, klane = kpos >> 1, kodd = kpos & 1;
-  float xn[EPL];
-  load_chunks<C, VEC>(logits, t0, T, E, lane, xn);
-  for (long long t = t0; t < T; t += step) {
-    const float* row = logits + t * (long long)E;
-    float ka[EPL];
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) ka[i] = xn[i];
-    load_chunks<C, VEC>(logits, t + step, T, E, lane, xn);
-    // pass A: cheap keys and the two group maxima of this lane
+  const f32x2 half2 = f2_splat(0.5f);
+  stage_row<C, VEC>(srow[warp][0], logits, t0, T, E, lane);
+  int slot = 0;
+  for (long long t = t0; t < T; t += step, slot ^= 1) {
+    stage_row<C, VEC>(srow[warp][slot ^ 1], logits, t + step, T, E, lane);
+    cp_async_wait1();
+    __syncwarp();
+    const float* row = srow[warp][slot];
+    // pass A: doubled cheap keys, lane maximum and two group maxima
+    float ka[4 * C];
     float g0 = -INFINITY, g1 = -INFINITY;
 #pragma unroll
     for (int c = 0; c < C; ++c) {
-      const float4 b = *reinterpret_cast<const float4*>(&sbias[128 * c + 4 * lane]);
-      const float bb[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int i = 4 * c + j;
-        // no clamp: __expf saturates to 0 or inf beyond |x| ~ 88, where the
-        // cheap key differs from the exact one by less than 1e-38
-        const float key = __fdividef(1.0f, 1.0f + __expf(-ka[i])) + bb[j];
-        ka[i] = (128 * c + 4 * lane + j < E) ? key : __int_as_float(0x7fc00000);
-        if (j < 2) g0 = fmaxf(g0, ka[i]); else g1 = fmaxf(g1, ka[i]);
-      }
+      const int e0 = 128 * c + 4 * lane;
+      const float4 x = *reinterpret_cast<const float4*>(row + e0);
+      const float4 cb = *reinterpret_cast<const float4*>(sc2 + e0);
+      const f32x2 h01 = f2_mul(f2_make(__float_as_uint(x.x), __float_as_uint(x.y)), half2);
+      const f32x2 h23 = f2_mul(f2_make(__float_as_uint(x.z), __float_as_uint(x.w)), half2);
+      const f32x2 k01 = f2_add(f2_make(__float_as_uint(tanh_fast(f2_lo(h01))),
+                                       __float_as_uint(tanh_fast(f2_hi(h01)))),
+                               f2_make(__float_as_uint(cb.x), __float_as_uint(cb.y)));
+      const f32x2 k23 = f2_add(f2_make(__float_as_uint(tanh_fast(f2_lo(h23))),
+                                       __float_as_uint(tanh_fast(f2_hi(h23)))),
+                               f2_make(__float_as_uint(cb.z), __float_as_uint(cb.w)));
+      ka[4 * c] = f2_lo(k01); ka[4 * c + 1] = f2_hi(k01);
+      ka[4 * c + 2] = f2_lo(k23); ka[4 * c + 3] = f2_hi(k23);
+      g0 = fmaxf(g0, fmaxf(ka[4 * c], ka[4 * c + 1]));
+      g1 = fmaxf(g1, fmaxf(ka[4 * c + 2], ka[4 * c + 3]));
     }
-    warp_sort64(g0, g1, lane);
-    const float a_k = __shfl_sync(FULL, kodd ? g1 : g0, klane);
-    const float thr = candidate_threshold_f(a_k);
+    float thr = candidate_threshold2(__shfl_sync(FULL, warp_sort32(fmaxf(g0, g1), lane), 32 - k));
     uint32_t cmask = 0;
 #pragma unroll
-    for (int i = 0; i < EPL; ++i)
+    for (int i = 0; i < 4 * C; ++i)
       if (ka[i] >= thr) cmask |= 1u << i;
-    const int ccount = __popc(cmask);
-    int incl = ccount;
+    int total = (int)__reduce_add_sync(FULL, (uint32_t)__popc(cmask));
+    if (total > 32) {
+      // refine the bound with the 64 group maxima
+      warp_sort64(g0, g1, lane);
+      const int kpos = 64 - k;
+      thr = candidate_threshold2(__shfl_sync(FULL, (kpos & 1) ? g1 : g0, kpos >> 1));
+      cmask = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(FULL, incl, o);
-      if (lane >= o) incl += v;
+      for (int i = 0; i < 4 * C; ++i)
+        if (ka[i] >= thr) cmask |= 1u << i;
+      total = (int)__reduce_add_sync(FULL, (uint32_t)__popc(cmask));
     }
-    const int total = __shfl_sync(FULL, incl, 31);
     if (total <= 32) {
+      const int ccount = __popc(cmask);
+      int incl = ccount;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += v;
+      }
       int pos = incl - ccount;
       while (cmask) {
         const int i = __ffs(cmask) - 1;
@@ -353,6 +422,7 @@ route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bi
     }
     __syncwarp();
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ---- block per token ---------------------------------------------------------
@@ -372,7 +442,7 @@ route_block_kernel(const float* __restrict__ logits, const float* __restrict__ b
   __shared__ int scand[32];
   __shared__ uint32_t sak;
   __shared__ unsigned long long spick[W];
-  __shared__ unsigned long long skey[32];
+  __shared__ __align__(16) unsigned long long skey[32];
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
