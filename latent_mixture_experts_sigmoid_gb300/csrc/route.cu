@@ -120,24 +120,23 @@ __device__ __forceinline__ float candidate_threshold(uint32_t a_k) {
 // ---- pass B exact stage for one warp -----------------------------------------
 // `cand[0..total)` are the candidate experts (total <= 32).  Every candidate
 // gets its exact key; its output position is the number of candidates with a
-// larger key (keys are distinct: the index breaks ties), so no sort network
-// is needed.  Writes the top-k ids and weights of token t.  `row` is the
-// token's logits (global or shared memory); `skey` is a 32-entry, 16-byte
+// larger key plus the number with an equal key and a lower index, so no sort
+// network is needed.  Writes the top-k ids and weights of token t.  `row` is
+// the token's logits (global or shared memory); `skey` is a 32-entry, 16-byte
 // aligned scratch of this warp.
 __device__ __forceinline__ void exact_order_and_write(const float* __restrict__ row,
                                                       const float* sbias, const int* cand,
                                                       int total, int k, int renorm, float rsf,
-                                                      long long t, int lane,
-                                                      unsigned long long* skey,
+                                                      long long t, int lane, uint32_t* skey,
                                                       int32_t* __restrict__ ids,
                                                       float* __restrict__ weights) {
-  unsigned long long P = 0ull;
+  uint32_t P = 0u;   // no finite key maps to 0
   float s = 0.0f;
   int e = 0;
   if (lane < total) {
     e = cand[lane];
     s = exact_sigmoid(row[e]);
-    P = pack_exact(__fadd_rn(s, sbias ? sbias[e] : 0.0f), e);
+    P = orderable(__fadd_rn(__fadd_rn(s, sbias ? sbias[e] : 0.0f), 0.0f));  // -0 -> +0
   }
   skey[lane] = P;
   __syncwarp();
@@ -145,9 +144,17 @@ __device__ __forceinline__ void exact_order_and_write(const float* __restrict__ 
   int rank = 0;
   const int jn = (total + 3) & ~3;
   for (int j = 0; j < jn; j += 4) {
-    const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(skey + j);
-    const ulonglong2 b = *reinterpret_cast<const ulonglong2*>(skey + j + 2);
-    rank += (a.x > P) + (a.y > P) + (b.x > P) + (b.y > P);
+    const uint4 a = *reinterpret_cast<const uint4*>(skey + j);
+    rank += (a.x > P) + (a.y > P) + (a.z > P) + (a.w > P);
+  }
+  // equal keys (rare): the lower expert index goes first
+  uint32_t same = __match_any_sync(FULL, P) & ~(1u << lane);
+  if (lane < total) {
+    while (same) {
+      const int j = __ffs(same) - 1;
+      same &= same - 1u;
+      rank += cand[j] < e;
+    }
   }
   const bool sel = lane < total && rank < k;
   float sum = sel ? s : 0.0f;
@@ -198,21 +205,24 @@ __device__ __forceinline__ unsigned long long lane_best_exact(const float* __res
 
 // ---- warp per token --------------------------------------------------------------
 // One warp per token, tokens visited with a stride of all warps of the grid.
-// Rows are staged in shared memory by cp.async, the next token's row in flight
-// while the current one is processed (two slots per warp); padding slots hold
-// NaN, which neither a maximum nor a candidate test picks up.  Lane l owns the
+// Rows are staged in shared memory by cp.async in a ring of NSLOT rows per
+// warp, so that NSLOT - 1 rows are in flight while one is processed (a warp
+// handles only a few tokens, and one row in flight per warp leaves the copy
+// latency exposed); padding slots hold NaN, which neither a maximum nor a
+// candidate test picks up.  Lane l owns the
 // experts e = 128*c + 4*l + j (chunk c < C, j < 4): one 16-byte copy and one
 // 16-byte shared load per chunk when E is a multiple of 4.
 //
 // Pass A uses a cheaper key than the block kernel, in a doubled scale:
-//   ka2 = tanh(x/2) + (2b + 1)   (= 2 sigmoid(x) + 2b up to the error of tanh)
-// with the hardware tanh (one MUFU operation per expert).  tanh.approx.f32 is
+//   ka2 = tanh(x/2) + 2b   (= 2 sigmoid(x) + 2b - 1 up to the error of tanh;
+// the constant shift changes no comparison) with the hardware tanh (one MUFU
+// operation per expert) and one fused multiply-add.  tanh.approx.f32 is
 // documented with a maximum error near 2^-11; the window below allows 2^-9
 // per key (four times that), and an exhaustive run over every finite fp32
 // input on GB300 measured at most 2^-16.9 absolute.  Other error terms: the
-// rounding of 2b + 1 and of the final add (2^-24 |.| each), and the exact key's
-// own error doubled (3 ulp of sigmoid plus the rounding of the bias add), all
-// below 2^-20 max(|ka2|, 1).  So with D2 = 2^-9 + 2^-21 max(|A2|, 1) the
+// rounding of the fused add (2^-24 |ka2|) and the exact key's own error
+// doubled (3 ulp of sigmoid plus the rounding of the bias add), all below
+// 2^-20 max(|ka2|, 1).  So with D2 = 2^-9 + 2^-21 max(|A2|, 1) the
 // candidate argument of the file header holds in the doubled scale.
 //
 // The bound A2 is first the k-th largest of the 32 lane maxima (a bitonic sort
@@ -240,17 +250,33 @@ __device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Per-lane direction bits of the 15 compare-exchange steps of a 32-wide
+// ascending bitonic sort: bit s set = keep the smaller value at step s.
+__device__ __forceinline__ uint32_t sort32_directions(int lane) {
+  uint32_t m = 0;
+  int s = 0;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1, ++s)
+      if (((lane & stride) == 0) == ((lane & size) == 0)) m |= 1u << s;
+  return m;
+}
 
 // Ascending bitonic sort of one value per lane across the warp.
-__device__ __forceinline__ float warp_sort32(float v, int lane) {
+__device__ __forceinline__ float warp_sort32(float v, uint32_t dirs) {
+  int s = 0;
 #pragma unroll
   for (int size = 2; size <= 32; size <<= 1) {
 #pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1, ++s) {
       const float p = __shfl_xor_sync(FULL, v, stride);
-      const bool kmin = ((lane & stride) == 0) == ((lane & size) == 0);
-      v = kmin ? fminf(v, p) : fmaxf(v, p);
+      v = ((dirs >> s) & 1u) ? fminf(v, p) : fmaxf(v, p);
     }
   }
   return v;
@@ -289,7 +315,7 @@ __device__ __forceinline__ unsigned long long lane_best_exact_chunk(const float*
                                                                     int lane,
                                                                     unsigned long long lastP) {
   unsigned long long best = 0ull;
-#pragma unroll
+#pragma unroll 1
   for (int i = 0; i < 4 * C; ++i) {
     const int e = 128 * (i >> 2) + 4 * lane + (i & 3);
     if (e < E) {
@@ -321,61 +347,75 @@ __device__ __forceinline__ void stage_row(float* dst, const float* __restrict__ 
   cp_async_commit();
 }
 
-template <int C, bool VEC>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, 5)
+// ring depth and the blocks per SM the register budget is sized for
+constexpr int kRouteSlots = 2;
+constexpr int kRouteMinBlocks = 6;
+
+template <int C, int NSLOT>
+constexpr size_t warp_kernel_smem() {
+  return (size_t)kWarpsPerBlock * NSLOT * 128 * C * sizeof(float);
+}
+
+template <int C, bool VEC, int NSLOT>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, kRouteMinBlocks)
 route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
                   int k, int renorm, float rsf, int32_t* __restrict__ ids,
                   float* __restrict__ weights) {
   constexpr int EW = 128 * C;
-  __shared__ __align__(16) float srow[kWarpsPerBlock][2][EW];
+  extern __shared__ __align__(16) float srow_all[];   // [warp][slot][EW]
   __shared__ __align__(16) float sbias[EW];
-  __shared__ __align__(16) float sc2[EW];     // 2b + 1
   __shared__ int scand[kWarpsPerBlock][32];
-  __shared__ __align__(16) unsigned long long skey[kWarpsPerBlock][32];
+  __shared__ __align__(16) uint32_t skey[kWarpsPerBlock][32];
   pdl_trigger();
-  const float qnan = __int_as_float(0x7fc00000);
-  for (int i = threadIdx.x; i < kWarpsPerBlock * 2 * EW; i += blockDim.x) (&srow[0][0][0])[i] = qnan;
-  pdl_wait();
-  for (int e = threadIdx.x; e < EW; e += blockDim.x) {
-    const float b = (bias && e < E) ? __ldg(bias + e) : 0.0f;
-    sbias[e] = b;
-    sc2[e] = 2.0f * b + 1.0f;
+  if (E < EW) {
+    // padding slots (never written by the copies) read as NaN
+    const float4 qnan4 = make_float4(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000),
+                                     __int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+    for (int i = threadIdx.x; i < kWarpsPerBlock * NSLOT * EW / 4; i += blockDim.x)
+      reinterpret_cast<float4*>(srow_all)[i] = qnan4;
   }
+  pdl_wait();
+  for (int e = threadIdx.x; e < EW; e += blockDim.x) sbias[e] = (bias && e < E) ? __ldg(bias + e) : 0.0f;
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
+  float* const ring = srow_all + (size_t)warp * NSLOT * EW;
   const long long step = (long long)gridDim.x * kWarpsPerBlock;
   const long long t0 = (long long)blockIdx.x * kWarpsPerBlock + warp;
-  const f32x2 half2 = f2_splat(0.5f);
-  stage_row<C, VEC>(srow[warp][0], logits, t0, T, E, lane);
-  int slot = 0;
-  for (long long t = t0; t < T; t += step, slot ^= 1) {
-    stage_row<C, VEC>(srow[warp][slot ^ 1], logits, t + step, T, E, lane);
-    cp_async_wait1();
+  const f32x2 half2 = f2_splat(0.5f), two2 = f2_splat(2.0f);
+  const uint32_t dirs = sort32_directions(lane);
+#pragma unroll
+  for (int p = 0; p < NSLOT - 1; ++p) stage_row<C, VEC>(ring + p * EW, logits, t0 + p * step, T, E, lane);
+  int slot = 0, fill = NSLOT - 1;
+  for (long long t = t0; t < T; t += step) {
+    stage_row<C, VEC>(ring + fill * EW, logits, t + (NSLOT - 1) * step, T, E, lane);
+    cp_async_wait<NSLOT - 1>();
     __syncwarp();
-    const float* row = srow[warp][slot];
-    // pass A: doubled cheap keys, lane maximum and two group maxima
+    const float* row = ring + slot * EW;
+    if (++slot == NSLOT) slot = 0;
+    if (++fill == NSLOT) fill = 0;
+    // pass A: doubled cheap keys, two group maxima per lane
     float ka[4 * C];
     float g0 = -INFINITY, g1 = -INFINITY;
 #pragma unroll
     for (int c = 0; c < C; ++c) {
       const int e0 = 128 * c + 4 * lane;
       const float4 x = *reinterpret_cast<const float4*>(row + e0);
-      const float4 cb = *reinterpret_cast<const float4*>(sc2 + e0);
+      const float4 b = *reinterpret_cast<const float4*>(sbias + e0);
       const f32x2 h01 = f2_mul(f2_make(__float_as_uint(x.x), __float_as_uint(x.y)), half2);
       const f32x2 h23 = f2_mul(f2_make(__float_as_uint(x.z), __float_as_uint(x.w)), half2);
-      const f32x2 k01 = f2_add(f2_make(__float_as_uint(tanh_fast(f2_lo(h01))),
-                                       __float_as_uint(tanh_fast(f2_hi(h01)))),
-                               f2_make(__float_as_uint(cb.x), __float_as_uint(cb.y)));
-      const f32x2 k23 = f2_add(f2_make(__float_as_uint(tanh_fast(f2_lo(h23))),
-                                       __float_as_uint(tanh_fast(f2_hi(h23)))),
-                               f2_make(__float_as_uint(cb.z), __float_as_uint(cb.w)));
+      const f32x2 k01 = f2_fma(f2_make(__float_as_uint(b.x), __float_as_uint(b.y)), two2,
+                               f2_make(__float_as_uint(tanh_fast(f2_lo(h01))),
+                                       __float_as_uint(tanh_fast(f2_hi(h01)))));
+      const f32x2 k23 = f2_fma(f2_make(__float_as_uint(b.z), __float_as_uint(b.w)), two2,
+                               f2_make(__float_as_uint(tanh_fast(f2_lo(h23))),
+                                       __float_as_uint(tanh_fast(f2_hi(h23)))));
       ka[4 * c] = f2_lo(k01); ka[4 * c + 1] = f2_hi(k01);
       ka[4 * c + 2] = f2_lo(k23); ka[4 * c + 3] = f2_hi(k23);
       g0 = fmaxf(g0, fmaxf(ka[4 * c], ka[4 * c + 1]));
       g1 = fmaxf(g1, fmaxf(ka[4 * c + 2], ka[4 * c + 3]));
     }
-    float thr = candidate_threshold2(__shfl_sync(FULL, warp_sort32(fmaxf(g0, g1), lane), 32 - k));
+    float thr = candidate_threshold2(__shfl_sync(FULL, warp_sort32(fmaxf(g0, g1), dirs), 32 - k));
     uint32_t cmask = 0;
 #pragma unroll
     for (int i = 0; i < 4 * C; ++i)
@@ -442,7 +482,7 @@ route_block_kernel(const float* __restrict__ logits, const float* __restrict__ b
   __shared__ int scand[32];
   __shared__ uint32_t sak;
   __shared__ unsigned long long spick[W];
-  __shared__ __align__(16) unsigned long long skey[32];
+  __shared__ __align__(16) uint32_t skey[32];
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
@@ -553,20 +593,24 @@ route_block_kernel(const float* __restrict__ logits, const float* __restrict__ b
 template <int C, bool VEC>
 cudaError_t launch_warp_tier(const float* logits, const float* bias, int T, int E, int k,
                              int renorm, float rsf, int32_t* ids, float* w, cudaStream_t s) {
+  constexpr size_t smem = warp_kernel_smem<C, kRouteSlots>();
   static int per_sm = 0;
   if (per_sm == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, route_warp_kernel<C, VEC>,
-                                                      kWarpsPerBlock * 32, 0) != cudaSuccess ||
+    if (cudaFuncSetAttribute(route_warp_kernel<C, VEC, kRouteSlots>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return cudaGetLastError();
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, route_warp_kernel<C, VEC, kRouteSlots>,
+                                                      kWarpsPerBlock * 32, smem) != cudaSuccess ||
         n < 1)
-      n = 4;
+      n = 1;
     per_sm = n;
   }
   const long long need = ((long long)T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const long long cap = (long long)num_sms() * per_sm;
   const int blocks = (int)(need < cap ? need : cap);
-  return launch_k(route_warp_kernel<C, VEC>, dim3(blocks), dim3(kWarpsPerBlock * 32), 0, s,
-                  logits, bias, T, E, k, renorm, rsf, ids, w);
+  return launch_k(route_warp_kernel<C, VEC, kRouteSlots>, dim3(blocks), dim3(kWarpsPerBlock * 32),
+                  smem, s, logits, bias, T, E, k, renorm, rsf, ids, w);
 }
 
 template <int C>
