@@ -32,35 +32,31 @@ __device__ __forceinline__ uint16_t to_bf16(float x) {
 }
 
 // ---------------------------------------------------------------------------
-// SituGLU scalar math (vLLM PR #50088, commit 2), fp32
+// SituGLU math (vLLM PR #50088, commit 2), fp32
 // ---------------------------------------------------------------------------
-// Written from the identities
-//   tanh(a)    = -m / (2 + m),   m = e^{-2|a|} - 1   (sign restored separately)
-//   sigmoid(g) = 1 / (1 + e^{-g})
-// so that one reciprocal serves the whole product:
-//   out = [beta*sgn(g)*(-m1)] * [linear_beta*sgn(u)*(-m2)  or  u]
-//         / [(2 + m1) * (1 + e^{-g}) * (2 + m2  or  1)]
-// m = e^z - 1 (z <= 0) comes from the hardware 2^x for |z| >= 0.2 and from
-// its Taylor series to z^5 below that (no cancellation); relative error of
-// every factor is about 1e-6, so the bf16 result is almost always the
-// correctly rounded one.  A denominator beyond 2^126 (gate below about -87)
-// gives 0, the value to bf16 precision.
+//   out = beta*tanh(g/beta) * [linear_beta*tanh(u/linear_beta)  or  u] / (1 + e^{-g})
+// Both tanh factors come from the hardware tanh (tanh.approx.f32: documented
+// maximum relative error near 2^-11; an exhaustive run over every finite fp32
+// input on GB300 measured 2^-16.5).  The sigmoid stays 1 / (1 + e^{-g}) from
+// the hardware 2^x and reciprocal: 0.5 + 0.5*tanh(g/2) would cancel for very
+// negative gates, where the output is tiny but must keep its relative
+// accuracy.  Four transcendental ops per element (two tanh, one 2^x, one
+// reciprocal) and about ten other instructions; a denominator beyond 2^126
+// (gate below about -87) gives 0, the value to bf16 precision.
 __device__ __forceinline__ float ex2_fast(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-
-__device__ __forceinline__ float expm1_neg(float z) {   // e^z - 1 for z <= 0
-  if (z > -0.2f) {
-    float p = 1.0f / 120.0f;
-    p = fmaf(p, z, 1.0f / 24.0f);
-    p = fmaf(p, z, 1.0f / 6.0f);
-    p = fmaf(p, z, 0.5f);
-    p = fmaf(p, z, 1.0f);
-    return p * z;
-  }
-  return ex2_fast(z * 1.4426950408889634f) - 1.0f;
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_fast(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 struct SituParams {
@@ -68,24 +64,9 @@ struct SituParams {
   int has_lbeta;
 };
 
-__device__ __forceinline__ float situ1(float g, float u, const SituParams& p) {
-  const float m1 = expm1_neg(-2.0f * fabsf(g * p.inv_beta));
-  const float e = ex2_fast(-g * 1.4426950408889634f);
-  float num = copysignf(p.beta, g) * (-m1);
-  float den = (2.0f + m1) * (1.0f + e);
-  if (p.has_lbeta) {
-    const float m2 = expm1_neg(-2.0f * fabsf(u * p.inv_lbeta));
-    num *= copysignf(p.lbeta, u) * (-m2);
-    den *= (2.0f + m2);
-  } else {
-    num *= u;
-  }
-  return __fdividef(num, den);
-}
-
 // Two elements at a time on the packed fp32 pipe (sm_100 f32x2 FMA/MUL/ADD,
-// each lane rounded to nearest like the scalar form); the hardware 2^x and
-// reciprocal stay per element.  Same formulation and accuracy as situ1.
+// each lane rounded to nearest like the scalar form); the transcendental ops
+// stay per element.
 typedef unsigned long long f32x2;
 __device__ __forceinline__ f32x2 f2_make(uint32_t lo_bits, uint32_t hi_bits) {
   f32x2 d;
@@ -112,53 +93,20 @@ __device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-__device__ __forceinline__ float rcp_fast(float x) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// e^z - 1 for a pair of z <= 0 (Taylor series to z^5 above -0.2, else 2^x - 1)
-__device__ __forceinline__ f32x2 expm1_neg2(f32x2 z) {
-  f32x2 p = f2_fma(z, f2_splat(1.0f / 120.0f), f2_splat(1.0f / 24.0f));
-  p = f2_fma(p, z, f2_splat(1.0f / 6.0f));
-  p = f2_fma(p, z, f2_splat(0.5f));
-  p = f2_fma(p, z, f2_splat(1.0f));
-  const f32x2 small = f2_mul(p, z);
-  const f32x2 t = f2_mul(z, f2_splat(1.4426950408889634f));
-  const f32x2 big = f2_add(f2_make(__float_as_uint(ex2_fast(f2_lo(t))),
-                                   __float_as_uint(ex2_fast(f2_hi(t)))),
-                           f2_splat(-1.0f));
-  const uint32_t lo = f2_lo(z) > -0.2f ? (uint32_t)small : (uint32_t)big;
-  const uint32_t hi = f2_hi(z) > -0.2f ? (uint32_t)(small >> 32) : (uint32_t)(big >> 32);
-  return f2_make(lo, hi);
-}
+// elementwise f(x) of a pair through a scalar transcendental op
+#define LMOE_F2_APPLY(f, v) f2_make(__float_as_uint(f(f2_lo(v))), __float_as_uint(f(f2_hi(v))))
 
 // bf16x2 gate / up in, fp32 pair out (lo, hi)
 __device__ __forceinline__ f32x2 situ2_f32(uint32_t g2, uint32_t u2, const SituParams& p) {
   const f32x2 g = f2_make(g2 << 16, g2 & 0xFFFF0000u);
-  const f32x2 gabs = g & 0x7FFFFFFF7FFFFFFFull;
-  const f32x2 m1 = expm1_neg2(f2_mul(gabs, f2_splat(-2.0f * p.inv_beta)));
-  const f32x2 t = f2_mul(g, f2_splat(-1.4426950408889634f));
-  const f32x2 e = f2_make(__float_as_uint(ex2_fast(f2_lo(t))), __float_as_uint(ex2_fast(f2_hi(t))));
-  // -beta with the sign of g flipped: num = sgn(g) * beta * (-m1)
-  const f32x2 nb = (g & 0x8000000080000000ull) ^ f2_splat(-p.beta);
-  f32x2 num = f2_mul(nb, m1);
-  f32x2 den = f2_mul(f2_add(m1, f2_splat(2.0f)), f2_add(e, f2_splat(1.0f)));
   const f32x2 u = f2_make(u2 << 16, u2 & 0xFFFF0000u);
-  if (p.has_lbeta) {
-    const f32x2 uabs = u & 0x7FFFFFFF7FFFFFFFull;
-    const f32x2 m2 = expm1_neg2(f2_mul(uabs, f2_splat(-2.0f * p.inv_lbeta)));
-    const f32x2 nl = (u & 0x8000000080000000ull) ^ f2_splat(-p.lbeta);
-    num = f2_mul(num, f2_mul(nl, m2));
-    den = f2_mul(den, f2_add(m2, f2_splat(2.0f)));
-  } else {
-    num = f2_mul(num, u);
-  }
-  // a denominator beyond 2^126 (gate below about -87) flushes its reciprocal
-  // to 0, the value to bf16 precision
-  const f32x2 r = f2_make(__float_as_uint(rcp_fast(f2_lo(den))),
-                          __float_as_uint(rcp_fast(f2_hi(den))));
+  const f32x2 tg = LMOE_F2_APPLY(tanh_fast, f2_mul(g, f2_splat(p.inv_beta)));
+  const f32x2 e = LMOE_F2_APPLY(ex2_fast, f2_mul(g, f2_splat(-1.4426950408889634f)));
+  const f32x2 up = p.has_lbeta ? f2_mul(LMOE_F2_APPLY(tanh_fast, f2_mul(u, f2_splat(p.inv_lbeta))),
+                                        f2_splat(p.lbeta))
+                               : u;
+  const f32x2 num = f2_mul(f2_mul(tg, f2_splat(p.beta)), up);
+  const f32x2 r = LMOE_F2_APPLY(rcp_fast, f2_add(e, f2_splat(1.0f)));
   return f2_mul(num, r);
 }
 

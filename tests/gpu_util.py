@@ -133,13 +133,16 @@ def assert_layer_close(got: np.ndarray, ref: np.ndarray, tol: float = 2e-2,
     return stats
 
 
-def assert_stage_close(got: np.ndarray, ref: np.ndarray, name: str, max_mismatch: float = 0.01):
+def assert_stage_close(got: np.ndarray, ref: np.ndarray, name: str, max_mismatch: float = 0.01,
+                       scale=None):
     """One stage fed identical inputs: the bf16 results differ on at most
     max_mismatch of the elements, by one bf16 step at the 99.9th percentile,
     and never by more than max(2 steps, 1e-3 * rms) (near-cancelling sums
-    have tiny |ref| and so tiny steps)."""
+    have tiny |ref| and so tiny steps).  Steps are taken at |ref|, or at
+    `scale` where an input of the stage is not observable and only its
+    rounding scale is known."""
     err = np.abs(got - ref)
-    u = bf16_ulp(ref)
+    u = bf16_ulp(ref if scale is None else np.maximum(np.abs(ref), scale))
     rms = float(np.sqrt(np.mean(ref ** 2))) or 1.0
     mism = float((err > 0).mean())
     p999 = float(np.quantile(err / u, 0.999))

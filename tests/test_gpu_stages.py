@@ -80,7 +80,11 @@ def run_and_check(d, wdev, wor, zipf, toks):
                                                               d.linear_beta)), "shared1+situ"))
         Sh = O.linear_bf16(As, wor["ws2"])
     outref = O.round_bf16(N @ f(wor["w_up"]).T + Sh)
-    res.append(assert_stage_close(f(host_bits(out))[toks], outref, "up+shared_add"))
+    # small T: the GPU forms the bf16 shared output inside the final split-K
+    # reduction and never stores it, so the reference takes the oracle's Sh; a
+    # one-step rounding difference there moves the sum by one step of |Sh|
+    res.append(assert_stage_close(f(host_bits(out))[toks], outref, "up+shared_add",
+                                  scale=None if T > 128 else np.abs(Sh)))
     print(res)
 
 
