@@ -427,8 +427,73 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (!wait_bounded(tfull_bar(acc), (uit >> 1) & 1u, abort_flag, kErrEpilogue)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * bn);
-      if (p.tok_on_m && !p.out_fp32) {
-        // row r = token, columns = features.  Per 32-column chunk: each thread
+      if (p.tok_on_m && !p.out_fp32 && !p.add) {
+        // row r = token, columns = features, no addend.  Per 64-column chunk
+        // each thread rounds its row to bf16 (after SituGLU when fused) into
+        // its warp's staging buffer [32 rows][64 bf16]; the warp then writes 4
+        // rows x 128 bytes per 16-byte store instruction.
+        uint32_t* st = reinterpret_cast<uint32_t*>(stage_out) + (size_t)q * 32 * 32;
+        const int width = p.fuse_situ ? BM : bn;           // output columns of this tile
+        const int fcol0 = x.feat_tile * width;
+        const int ldo = p.fuse_situ ? p.M_feat / 2 : p.ldo;
+        for (int c0 = 0; c0 < width; c0 += 64) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float f[32];
+            {
+              uint32_t v[16];
+              tmem_ld16(tbase + (uint32_t)(c0 + 32 * h), v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
+              tmem_ld16(tbase + (uint32_t)(c0 + 32 * h + 16), v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) f[16 + j] = __uint_as_float(v[j]);
+            }
+            uint32_t pk[16];
+            if (p.fuse_situ) {
+              // gate = f, up = the same features 128 columns further; both
+              // rounded to bf16 first, as the stored GEMM output would be
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                uint32_t v[16];
+                tmem_ld16(tbase + (uint32_t)(BM + c0 + 32 * h + 16 * hh), v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; j += 2) {
+                  const uint32_t gb = pack_bf16x2(f[16 * hh + j], f[16 * hh + j + 1]);
+                  const uint32_t ub = pack_bf16x2(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+                  const f32x2 o = situ2_f32(gb, ub, p.sp);
+                  pk[8 * hh + j / 2] = pack_bf16x2(f2_lo(o), f2_hi(o));
+                }
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(f[2 * j], f[2 * j + 1]);
+            }
+            // 16-byte chunk 4h + c of row `lane`, XOR-swizzled by row
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              *reinterpret_cast<uint4*>(st + lane * 32 + (((4 * h + c) ^ (lane & 7)) * 4)) =
+                  make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = i * 4 + (lane >> 3);            // row within this warp's 32
+            const int c = lane & 7;                        // 8-column chunk
+            const uint4 a = *reinterpret_cast<const uint4*>(st + rr * 32 + ((c ^ (rr & 7)) * 4));
+            const int row_in_tile = q * 32 + rr;
+            if (row_in_tile < x.nvalid) {
+              const long long off = (long long)(x.tok_row0 + row_in_tile) * ldo + fcol0 + c0 + c * 8;
+              *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + off) = a;
+            }
+          }
+          __syncwarp();
+        }
+      } else if (p.tok_on_m && !p.out_fp32) {
+        // row r = token, columns = features, bf16 addend.  Per 32-column chunk: each thread
         // puts its row's fp32 results into its warp's staging buffer; the warp
         // then writes 4 rows x 32 columns per store instruction (the shared
         // output add happens here in fp32, before the single bf16 rounding).
