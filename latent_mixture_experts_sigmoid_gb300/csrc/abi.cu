@@ -167,7 +167,8 @@ int validate_dims(const lmoe_dims* d) {
 
 cudaError_t gemm_dense(const uint16_t* W, int M_feat, const uint16_t* X, int T, int K,
                        const DenseCfg& c, void* out, int out_fp32, long long split_stride,
-                       const uint16_t* add, cudaStream_t s) {
+                       const uint16_t* add, cudaStream_t s, int fuse_situ = 0, float beta = 1.0f,
+                       float linear_beta = 0.0f) {
   GemmDesc g{};
   g.W = W;
   g.X = X;
@@ -180,10 +181,13 @@ cudaError_t gemm_dense(const uint16_t* W, int M_feat, const uint16_t* X, int T, 
   g.bn = c.bn;
   g.splits = c.splits;
   g.out = out;
-  g.ldo = M_feat;
+  g.ldo = fuse_situ ? M_feat / 2 : M_feat;
   g.out_fp32 = out_fp32;
   g.split_stride = split_stride;
   g.add = add;
+  g.fuse_situ = fuse_situ;
+  g.beta = beta;
+  g.linear_beta = linear_beta;
   const int tok_tile = c.tok_on_m ? 128 : c.bn;
   const int feat_tile = c.tok_on_m ? c.bn : 128;
   g.max_units = ((T + tok_tile - 1) / tok_tile) * (M_feat / feat_tile) * c.splits;
@@ -222,6 +226,7 @@ struct Plan {
   int T;
   bool decode;
   bool fuse_g1;      // GEMM1 with SituGLU in its epilogue (tokens on M, 2*inter % 256 == 0)
+  bool fuse_s1;      // shared GEMM1 likewise (tokens on M, no split-K, shared_inter % 128 == 0)
   int tile;          // token tile of the grouped GEMMs
   int g1_bn, g2_bn;  // MMA N of the grouped GEMMs
   DenseCfg down, s1, s2, up;
@@ -238,6 +243,7 @@ Plan make_plan(const lmoe_dims& d, int nsm) {
   p.g2_bn = p.decode ? p.tile : (d.latent % 256 == 0 ? 256 : 128);
   p.down = dense_cfg(d.T, d.latent, d.hidden, nsm);
   p.s1 = dense_cfg(d.T, 2 * d.shared_inter, d.hidden, nsm);
+  p.fuse_s1 = p.s1.tok_on_m && p.s1.splits == 1 && p.s1.bn == 256 && d.shared_inter % 128 == 0;
   p.s2 = dense_cfg(d.T, d.hidden, d.shared_inter, nsm);
   p.up = dense_cfg(d.T, d.hidden, d.latent, nsm);
   return p;
@@ -247,7 +253,7 @@ int plan_launches(const Plan& p, bool shared) {
   const int perm = p.T <= 256 ? 1 : 3;  // one fused permutation kernel for T <= 256
   const int experts = p.fuse_g1 ? 2 : 3;  // GEMM1 (+ SituGLU unless fused), GEMM2
   int n = 1 + 1 + perm + 1 + experts + 1;  // route, down, permute, scatter, experts, combine
-  if (shared) n += 3;                   // shared GEMM1 + SituGLU, shared GEMM2
+  if (shared) n += p.fuse_s1 ? 2 : 3;   // shared GEMM1 (+ SituGLU unless fused), shared GEMM2
   n += 1;                               // up-projection GEMM
   const bool sh_part = shared && p.s2.splits > 1;
   if (p.up.splits > 1 || sh_part) n += 1;   // fixed-order reduction
@@ -463,6 +469,10 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
         LMOE_TRY(gemm_dense(wt->ws13, 2 * ds, X, T, H, c1, ws.Pb, 1, s1_stride, nullptr, ss));
         LMOE_TRY(launch_reduce_situ(ws.Pb, c1.splits, s1_stride, T, ds, d.beta, d.linear_beta,
                                     ws.As, ss));
+      } else if (pl.fuse_s1) {
+        // As = bf16(SituGLU(bf16(X Ws13^T))) straight from the GEMM epilogue
+        LMOE_TRY(gemm_dense(wt->ws13, 2 * ds, X, T, H, c1, ws.As, 0, 0, nullptr, ss, 1, d.beta,
+                            d.linear_beta));
       } else {
         LMOE_TRY(gemm_dense(wt->ws13, 2 * ds, X, T, H, c1, ws.Gs, 0, 0, nullptr, ss));
         LMOE_TRY(launch_situ(ws.Gs, ws.As, T, ds, d.beta, d.linear_beta, ss));

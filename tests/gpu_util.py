@@ -151,6 +151,36 @@ def assert_stage_close(got: np.ndarray, ref: np.ndarray, name: str, max_mismatch
     return dict(stage=name, mismatch=mism, p999_steps=p999)
 
 
+def assert_gemm_situ_close(act: np.ndarray, G: np.ndarray, beta: float, linear_beta: float,
+                           name: str, max_mismatch: float = 0.01, steps: int = 2):
+    """GEMM + SituGLU as one stage (SituGLU in the GEMM epilogue or in the
+    split-K reduction, so the GPU's bf16 GEMM output is not observable).
+
+    G is the oracle's bf16 GEMM output [rows, 2d] (gate | up).  The GPU's may
+    differ from it by up to `steps` rounding steps, as any GEMM stage may, and
+    SituGLU can magnify one step of a large |gate| into several output steps
+    (d log sigmoid / dg ~ 1).  So every output must be within one step (or
+    1e-3 rms) of bf16(SituGLU(g', u')) for some g', u' within `steps` bf16
+    steps of the oracle's gate and up, and at most max_mismatch of the outputs
+    may differ from the value at the oracle's own G."""
+    from oracle import lmoe_oracle as O
+    d = G.shape[1] // 2
+    g, u = G[:, :d], G[:, d:]
+    central = O.round_bf16(O.situ(g, u, beta, linear_beta))
+    rms = float(np.sqrt(np.mean(central ** 2))) or 1.0
+    offs = [i / 2 for i in range(-2 * steps, 2 * steps + 1)]   # half steps cover binade edges
+    best = np.abs(act - central)
+    for a in offs:
+        ga = O.round_bf16(g + a * bf16_ulp(g))
+        for b in offs:
+            ub = O.round_bf16(u + b * bf16_ulp(u))
+            best = np.minimum(best, np.abs(act - O.round_bf16(O.situ(ga, ub, beta, linear_beta))))
+    mism = float((np.abs(act - central) > 0).mean())
+    worst = float((best / np.maximum(bf16_ulp(central), 1e-3 * rms)).max())
+    assert mism <= max_mismatch and worst <= 1.0, (name, mism, worst)
+    return dict(stage=name, mismatch=mism, worst_steps_at_nearest=worst)
+
+
 def workspace_view(lm, d, ws: torch.Tensor):
     """Host copies of the layer's intermediates from the workspace."""
     off = lm.latent_moe_workspace_offsets(d)

@@ -22,7 +22,7 @@ def _lib(cuda_ok):
 
 def run_and_check(d, wdev, wor, zipf, toks):
     from tests.gpu_util import (DEV, dev_bf16, dev_f32, host_bits, workspace_view,
-                                assert_stage_close)
+                                assert_stage_close, assert_gemm_situ_close)
     f = O.bf16_to_f64
     x = W.hidden_states(d, 0)
     lg = W.router_logits(d.T, d.num_experts, 0, zipf=zipf)
@@ -49,8 +49,7 @@ def run_and_check(d, wdev, wor, zipf, toks):
     act = f(v["act"][rr])
     if T > 128 and dI % 128 == 0:
         # prefill: SituGLU runs in GEMM1's epilogue, G is never stored
-        res.append(assert_stage_close(act, O.round_bf16(O.situ(Gref[:, :dI], Gref[:, dI:], d.beta,
-                                                               d.linear_beta)), "gemm1+situ"))
+        res.append(assert_gemm_situ_close(act, Gref, d.beta, d.linear_beta, "gemm1+situ"))
     else:
         G = f(v["G"][rr])
         res.append(assert_stage_close(G, Gref, "gemm1"))
@@ -65,19 +64,22 @@ def run_and_check(d, wdev, wor, zipf, toks):
     gamma = f(wor["norm_w"])
     N = f(v["N"][toks])
     res.append(assert_stage_close(N, O.round_bf16(O.rms_norm(C, gamma, d.rms_eps)), "combine_norm"))
-    # shared expert
+    # shared expert: at T > 128 with shared_inter % 128 == 0 SituGLU runs in the
+    # shared GEMM1's epilogue (no Gs); at T <= 128 it runs in the split-K
+    # reduction; otherwise Gs is stored and a separate kernel applies it
     As = f(v["As"][toks])
-    if T > 128:
+    if T > 128 and ds % 128:
         Gs = f(v["Gs"][toks])
         res.append(assert_stage_close(Gs, O.linear_bf16(X, wor["ws13"]), "shared1"))
         res.append(assert_stage_close(As, O.round_bf16(O.situ(Gs[:, :ds], Gs[:, ds:], d.beta,
                                                               d.linear_beta)), "shared_situ"))
+    else:
+        res.append(assert_gemm_situ_close(As, O.linear_bf16(X, wor["ws13"]), d.beta,
+                                          d.linear_beta, "shared1+situ"))
+    if T > 128:
         Sh = f(v["Sh"][toks])
         res.append(assert_stage_close(Sh, O.linear_bf16(As, wor["ws2"]), "shared2"))
     else:
-        Gs = O.linear_bf16(X, wor["ws13"])
-        res.append(assert_stage_close(As, O.round_bf16(O.situ(Gs[:, :ds], Gs[:, ds:], d.beta,
-                                                              d.linear_beta)), "shared1+situ"))
         Sh = O.linear_bf16(As, wor["ws2"])
     outref = O.round_bf16(N @ f(wor["w_up"]).T + Sh)
     # small T: the GPU forms the bf16 shared output inside the final split-K
