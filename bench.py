@@ -363,6 +363,20 @@ def run_ours(args, rank, world):
                            "unit": "GB/s", "frac": round(dec_gbs / pk["hbm"], 4)},
               "per_stage_ms": per_stage_dec,
               "e2e_tokens_per_s": round(world * dDc.T * K / (dec_e2e / 1e3), 1)}
+    # the layer's own data-movement stages at prefill (per-stage events, algorithmic bytes)
+    T, k, L = dP.T, dP.topk, dP.latent
+    for name, stage, nbytes, what in (
+            ("permute_scatter_prefill", "scatter", T * L * 2 + T * k * L * 2,
+             "token rows into the expert-major layout: read Z [T, L], write A [T*k, L] (bf16)"),
+            ("combine_norm_prefill", "combine_norm", T * k * L * 2 + T * L * 2 + T * k * 8 + L * 2,
+             "top-k combine + RMSNorm: read Y [T*k, L], weights, rows; write N [T, L]"),
+            ("permute_index_prefill", "permute", T * k * 4 * 3,
+             "counting-sort indices (ids in, row_of and tok_of_row out): latency-bound")):
+        ms_st = st[stage]
+        kern[name] = {"workload": what, "us": round(ms_st * 1e3, 2),
+                      "GBps": round(nbytes / ms_st / 1e6, 1),
+                      "frac_hbm": round(nbytes / ms_st / 1e6 / pk["hbm"], 4),
+                      "timing": "per-stage CUDA events of the prefill layer"}
     launches = lm.latent_moe_launch_count(dP) + lm.latent_moe_launch_count(dDc)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
