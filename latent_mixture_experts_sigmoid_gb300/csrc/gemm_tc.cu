@@ -21,6 +21,14 @@
 //               accumulator-ready signals through tcgen05.commit;
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator, optional bf16 add,
 //               bf16 or fp32 stores straight to global memory.
+// Dense GEMMs with tokens on M and 256-row weight tiles run in clusters of two
+// CTAs.  A pair of units shares an operand: token tiles 2t and 2t+1 against the
+// same weight tile (each CTA loads one 128-row half of the weight tile with a
+// TMA multicast into both CTAs' shared memory), or, for the last token tile
+// when the tile count is odd, one token tile against weight tiles 2f and 2f+1
+// (CTA 0 multicasts the token tile).  Each CTA's MMA commit releases the stage
+// in both CTAs.  (Grouped GEMMs measured slower in pairs: a pair advances in
+// lockstep across experts of very different sizes.)
 // The MMA's M side (128 rows) is either the tokens (large token counts) or
 // the weight rows ("swap AB", small token counts where N = 16..64 tokens); the
 // N side is the other operand.  Small dense problems split K across CTAs and
@@ -31,6 +39,8 @@
 // and the CTA drains its own in-flight copies and MMAs (again bounded),
 // frees its TMEM and returns.
 #include <cuda.h>
+
+#include <mutex>
 
 #include "lmoe_internal.cuh"
 #include "gemm_tc.cuh"
@@ -108,6 +118,29 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint32_t dst
       : "memory");
 }
 
+// The same box into the same shared-memory offset of every CTA in `mask`,
+// completing bytes on each CTA's barrier at `bar`'s offset.
+__device__ __forceinline__ void tma_load_2d_mc(const CUtensorMap* map, uint32_t dst, uint32_t bar,
+                                               int c0, int c1, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of every CTA of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -150,6 +183,15 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
+// Arrive on the barrier at `bar`'s offset in every CTA of `mask` once the
+// MMAs this thread issued so far have completed.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar), "h"(mask)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -170,13 +212,8 @@ struct Unit {
   int tok_row0;   // first token row of the tile (in X / out rows)
   int nvalid;     // valid token rows in the tile
   int w_row0;     // first weight row of the tile
+  int shareA;     // multicast: 1 = the pair shares the token tile, 0 = the weight tile
 };
-
-__device__ __forceinline__ int total_units(const GemmParams& p, int tok_tile, int nfeat) {
-  const int tiles = p.tile_prefix ? __ldg(p.tile_prefix + p.num_groups)
-                                  : (p.T_dense + tok_tile - 1) / tok_tile;
-  return tiles * nfeat * p.splits;
-}
 
 // Grouped GEMMs keep the per-group tables (tile prefix, token count, first
 // row) in shared memory, copied once per CTA; a unit's group is found by a
@@ -187,6 +224,16 @@ struct GroupTables {
   const int* first;    // [G]
 };
 
+// Work units of one CTA: with multicast a unit is a pair of token tiles (one
+// per CTA of the cluster), so both CTAs walk the same unit sequence.
+__device__ __forceinline__ int total_units(const GemmParams& p, const GroupTables& gt_tab,
+                                           int tok_tile, int nfeat) {
+  const int tiles = p.tile_prefix ? gt_tab.prefix[p.num_groups]
+                                  : (p.T_dense + tok_tile - 1) / tok_tile;
+  // multicast pairs two units (tiles * nfeat is even: the launcher checks)
+  return p.mcast ? tiles * nfeat / 2 : tiles * nfeat * p.splits;
+}
+
 // Dense GEMMs with tokens on M walk their tiles in bands of kBand feature
 // tiles: inside a band the feature tile changes fastest, then the token tile,
 // so the 152 concurrent tiles share a band of weight tiles and a run of token
@@ -194,12 +241,34 @@ struct GroupTables {
 constexpr int kBand = 8;
 
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const GroupTables& gt_tab, int u,
-                                            int tok_tile, int feat_tile, int nfeat, int nkb) {
+                                            int tok_tile, int feat_tile, int nfeat, int nkb,
+                                            int rank) {
   Unit x;
+  x.shareA = 0;
   x.split = u % p.splits;
   const int v = u / p.splits;
   int g = 0, t_in_g, count = p.T_dense, first = 0;
-  if (p.tile_prefix) {
+  if (p.mcast) {
+    // pair unit v (dense): first floor(t/2) * nfeat pairs of token tiles
+    // (2tp + rank, same feature tile, in bands of kBand feature tiles as
+    // below), then for an odd t the last token tile against feature tiles
+    // 2j + rank
+    const int t = (p.T_dense + tok_tile - 1) / tok_tile;
+    const int nb = (t / 2) * nfeat;
+    if (v < nb) {
+      const int nt = t / 2;
+      const int nbands = (nfeat + kBand - 1) / kBand;
+      const int b = min(v / (nt * kBand), nbands - 1);
+      const int rem = v - b * nt * kBand;
+      const int fb = (b == nbands - 1) ? nfeat - kBand * (nbands - 1) : kBand;
+      t_in_g = 2 * (rem / fb) + rank;
+      x.feat_tile = b * kBand + rem % fb;
+    } else {
+      x.shareA = 1;
+      t_in_g = t - 1;
+      x.feat_tile = 2 * (v - nb) + rank;
+    }
+  } else if (p.tile_prefix) {
     x.feat_tile = v % nfeat;
     const int gt = v / nfeat;
     int lo = 0, hi = p.num_groups - 1;
@@ -223,8 +292,8 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const GroupTabl
     x.feat_tile = v % nfeat;
     t_in_g = v / nfeat;
   }
-  x.tok_row0 = first + t_in_g * tok_tile;
   x.nvalid = min(tok_tile, count - t_in_g * tok_tile);
+  x.tok_row0 = first + t_in_g * tok_tile;
   x.w_row0 = g * p.M_feat + x.feat_tile * (p.fuse_situ ? BM : feat_tile);
   x.kb0 = (int)((long long)x.split * nkb / p.splits);
   x.kb1 = (int)((long long)(x.split + 1) * nkb / p.splits);
@@ -265,7 +334,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), p.mcast ? 2 : 1);   // multicast: both CTAs' MMAs release
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -294,9 +363,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   }
   tc_fence_before();
-  __syncthreads();
+  // with multicast the partner CTA's barriers must be initialised before any
+  // copy or commit reaches them: a cluster-wide barrier (it also syncs this CTA)
+  if (p.mcast) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // CTA-to-unit walk: with multicast both CTAs of a cluster take the same units
+  const int rank = p.mcast ? (int)cluster_rank() : 0;
+  const int cl0 = p.mcast ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ncl = p.mcast ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   const int tok_tile = p.tok_on_m ? BM : bn;
   const int feat_tile = p.tok_on_m ? bn : BM;
@@ -326,10 +401,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       // weight tiles of the first ring of stages are requested before the
       // wait for the previous kernel (weights are constant).
       uint32_t pre = 0;
-      if (dense) {
-        const int U0 = total_units(p, tok_tile, nfeat);
-        for (int u = blockIdx.x; u < U0 && pre < (uint32_t)S; u += gridDim.x) {
-          const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb);
+      if (dense && !p.mcast) {
+        const int U0 = total_units(p, tabs, tok_tile, nfeat);
+        for (int u = cl0; u < U0 && pre < (uint32_t)S; u += ncl) {
+          const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb, rank);
           for (int kb = x.kb0; kb < x.kb1 && pre < (uint32_t)S; ++kb, ++pre) {
             const uint32_t sa = smem_u32(smem + (size_t)pre * stage_bytes);
             mbar_arrive_expect_tx(full_bar((int)pre), stage_bytes);
@@ -338,21 +413,42 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
       }
       pdl_wait();
-      const int U = total_units(p, tok_tile, nfeat);
+      const int U = total_units(p, tabs, tok_tile, nfeat);
       // ring position kept incrementally: stage s, its smem address, parity
       uint32_t it = 0, s = 0, ph = 0;
       uint32_t sa = smem_u32(smem);
       const uint32_t sa0 = sa;
       bool ok = true;
-      for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-        const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb);
+      for (int u = cl0; u < U && ok; u += ncl) {
+        const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb, rank);
         for (int kb = x.kb0; kb < x.kb1; ++kb, ++it) {
-          if (it >= pre) {
+          if (p.mcast) {
             if (!wait_phase(empty_bar((int)s), ph ^ 1u, abort_flag, kErrProducer)) { ok = false; break; }
             mbar_arrive_expect_tx(full_bar((int)s), stage_bytes);
-            load_w(sa + offW, full_bar((int)s), kb, x.w_row0);
+            // the weight tile in two 128-row boxes: gate and up rows (fused
+            // SituGLU) or rows w_row0 and w_row0 + 128
+            const int wstep = p.fuse_situ ? p.M_feat / 2 : BM;
+            if (!x.shareA) {
+              // this CTA's half of the shared weight tile goes to both CTAs,
+              // the token tile to this one only
+              tma_load_2d_mc(mapW, sa + offW + (uint32_t)rank * (BM * BK * 2), full_bar((int)s),
+                             kb * BK, x.w_row0 + rank * wstep, (uint16_t)3u);
+              tma_load_2d(mapX, sa + offX, full_bar((int)s), kb * BK, x.tok_row0);
+            } else {
+              // shared token tile (CTA 0 multicasts it), own weight tile
+              if (rank == 0)
+                tma_load_2d_mc(mapX, sa + offX, full_bar((int)s), kb * BK, x.tok_row0, (uint16_t)3u);
+              tma_load_2d(mapW, sa + offW, full_bar((int)s), kb * BK, x.w_row0);
+              tma_load_2d(mapW, sa + offW + BM * BK * 2, full_bar((int)s), kb * BK, x.w_row0 + wstep);
+            }
+          } else {
+            if (it >= pre) {
+              if (!wait_phase(empty_bar((int)s), ph ^ 1u, abort_flag, kErrProducer)) { ok = false; break; }
+              mbar_arrive_expect_tx(full_bar((int)s), stage_bytes);
+              load_w(sa + offW, full_bar((int)s), kb, x.w_row0);
+            }
+            tma_load_2d(mapX, sa + offX, full_bar((int)s), kb * BK, x.tok_row0);
           }
-          tma_load_2d(mapX, sa + offX, full_bar((int)s), kb * BK, x.tok_row0);
           if (++s == (uint32_t)S) { s = 0; ph ^= 1u; sa = sa0; } else { sa += stage_bytes; }
         }
       }
@@ -375,7 +471,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
       pdl_wait();
-      const int U = total_units(p, tok_tile, nfeat);
+      const int U = total_units(p, tabs, tok_tile, nfeat);
       const uint32_t idesc = idesc_bf16(BM, bn);
       // descriptors of stage 0; stage s adds s*stage_bytes, each K=16 step adds
       // 32 bytes (+2 in the 16-byte address field, which never carries out)
@@ -385,8 +481,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t uit = 0, s = 0, ph = 0;
       uint64_t da = da0, db = db0;
       bool ok = true;
-      for (int u = blockIdx.x; u < U && ok; u += gridDim.x, ++uit) {
-        const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb);
+      for (int u = cl0; u < U && ok; u += ncl, ++uit) {
+        const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb, rank);
         const int acc = (int)(uit & 1u);
         if (!wait_phase(tempty_bar(acc), ((uit >> 1) & 1u) ^ 1u, abort_flag, kErrMmaTmem)) {
           ok = false;
@@ -403,7 +499,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           mma_bf16(d_tmem, da + 4, db + 4, idesc, 1u);
           mma_bf16(d_tmem, da + 6, db + 6, idesc, 1u);
           accumulate = 1u;
-          mma_commit(empty_bar((int)s));
+          if (p.mcast) mma_commit_mc(empty_bar((int)s), (uint16_t)3u);
+          else mma_commit(empty_bar((int)s));
           if (++s == (uint32_t)S) { s = 0; ph ^= 1u; da = da0; db = db0; }
           else { da += dstep; db += dstep; }
         }
@@ -419,10 +516,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int q = warp & 3;                  // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;             // accumulator row of this thread
     pdl_wait();
-    const int U = total_units(p, tok_tile, nfeat);
+    const int U = total_units(p, tabs, tok_tile, nfeat);
     uint32_t uit = 0;
-    for (int u = blockIdx.x; u < U; u += gridDim.x, ++uit) {
-      const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb);
+    for (int u = cl0; u < U; u += ncl, ++uit) {
+      const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb, rank);
       const int acc = (int)(uit & 1u);
       if (!wait_bounded(tfull_bar(acc), (uit >> 1) & 1u, abort_flag, kErrEpilogue)) break;
       tc_fence_after();
@@ -632,6 +729,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                  "r"(p.tmem_cols)
                  : "memory");
   }
+  // no CTA leaves while its partner may still multicast into it or commit to it
+  if (p.mcast) cluster_sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -677,6 +776,35 @@ int stages_for(int bn) {
   return s > 12 ? 12 : (s < 2 ? 2 : s);
 }
 
+// Clusters of two gemm_tc_kernel CTAs that fit on the device at once with
+// `smem` bytes each, cached per size (queried once per size and device).
+int max_pairs_resident(size_t smem) {
+  struct Entry { int dev; size_t smem; int pairs; };
+  static Entry cache[16];
+  static int n = 0;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (cache[i].dev == dev && cache[i].smem == smem) return cache[i].pairs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * num_sms());
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int pairs = 0;
+  if (cudaOccupancyMaxActiveClusters(&pairs, gemm_tc_kernel, &cfg) != cudaSuccess) pairs = 0;
+  if (n < 16) cache[n++] = Entry{dev, smem, pairs};
+  return pairs;
+}
+
 // ring of stages, barriers, TMEM holder/abort flag, group tables, and (tokens
 // on M only) the epilogue staging buffers; at most 227 KB
 size_t smem_for(int bn, int stages, int groups, int tok_on_m) {
@@ -706,13 +834,21 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
   p.add = g.add;
   p.stages = stages_for(g.bn);
   p.fuse_situ = g.fuse_situ;
+  // CTA pairs with a multicast operand: dense, tokens on M, 256-row weight
+  // tiles, and an even count of token tiles or of weight tiles
+  {
+    const int nfeat = g.fuse_situ ? (g.M_feat / 2) / BM : g.M_feat / 256;
+    const int ntok = (g.T_dense + BM - 1) / BM;
+    p.mcast = !g.grp_count && g.tok_on_m && g.bn == 256 && g.splits == 1 &&
+              (nfeat % 2 == 0 || ntok % 2 == 0);
+  }
   p.sp = make_situ_params(g.beta > 0.0f ? g.beta : 1.0f, g.linear_beta);
   uint32_t cols = 32;
   while (cols < (uint32_t)(2 * g.bn)) cols <<= 1;
   p.tmem_cols = cols;
 
   CUtensorMap mw, mx;
-  const int w_box = g.fuse_situ ? BM : (g.tok_on_m ? g.bn : BM);
+  const int w_box = (g.fuse_situ || p.mcast) ? BM : (g.tok_on_m ? g.bn : BM);
   const int x_box = g.tok_on_m ? BM : g.bn;
   if (!make_map(&mw, g.W, (long long)g.G * g.M_feat, g.K, w_box)) return cudaErrorInvalidValue;
   if (!make_map(&mx, g.X, g.x_rows, g.K, x_box)) return cudaErrorInvalidValue;
@@ -722,6 +858,15 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
+  if (p.mcast) {
+    // as many CTA pairs as can be resident at once (pairs share a GPC)
+    const int pairs = max_pairs_resident(smem);
+    if (pairs < 1) return cudaErrorInvalidConfiguration;
+    int np = pairs;
+    if (g.max_units > 0 && g.max_units < np) np = g.max_units;
+    return launch_k_cluster(gemm_tc_kernel, dim3(2 * np), dim3(kThreads), smem, stream, 2, mx, mw,
+                            p);
+  }
   int grid = num_sms();
   if (g.max_units > 0 && g.max_units < grid) grid = g.max_units;
   if (grid < 1) grid = 1;

@@ -20,7 +20,10 @@ def _bits(g, shape, std):
 
 @pytest.mark.parametrize("T,N,K", [
     (1, 128, 64), (8, 256, 128), (16, 128, 512), (37, 384, 192), (128, 256, 1024),
-    (129, 256, 256), (300, 384, 128), (1024, 512, 2048), (4096, 7168, 2048)])
+    (129, 256, 256), (300, 384, 128), (1024, 512, 2048), (4096, 7168, 2048),
+    # CTA pairs: an odd token-tile count puts the last (ragged) tile on pairs of
+    # weight tiles that share it (3 tiles x 2, 5 tiles x 4 weight tiles)
+    (300, 512, 192), (600, 1024, 320)])
 @pytest.mark.parametrize("with_add", [False, True])
 def test_linear_matches_float64(T, N, K, with_add):
     from tests.gpu_util import dev_bf16, host_bits, DEV
