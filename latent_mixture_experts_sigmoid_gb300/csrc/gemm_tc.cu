@@ -21,14 +21,14 @@
 //               accumulator-ready signals through tcgen05.commit;
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator, optional bf16 add,
 //               bf16 or fp32 stores straight to global memory.
-// Dense GEMMs with tokens on M and 256-row weight tiles run in clusters of two
-// CTAs.  A pair of units shares an operand: token tiles 2t and 2t+1 against the
-// same weight tile (each CTA loads one 128-row half of the weight tile with a
-// TMA multicast into both CTAs' shared memory), or, for the last token tile
-// when the tile count is odd, one token tile against weight tiles 2f and 2f+1
-// (CTA 0 multicasts the token tile).  Each CTA's MMA commit releases the stage
-// in both CTAs.  (Grouped GEMMs measured slower in pairs: a pair advances in
-// lockstep across experts of very different sizes.)
+// GEMMs with tokens on M and 256-row weight tiles run in clusters of two CTAs.
+// A pair of units shares an operand: token tiles 2t and 2t+1 of a group
+// against the same weight tile (each CTA loads one 128-row half of the weight
+// tile with a TMA multicast into both CTAs' shared memory), or, for the last
+// token tile of a group with an odd tile count, that token tile against weight
+// tiles 2f and 2f+1 (CTA 0 multicasts the token tile).  A group of t token
+// tiles and nfeat weight tiles thus gives exactly t * nfeat / 2 pair units.
+// Each CTA's MMA commit releases the stage in both CTAs.
 // The MMA's M side (128 rows) is either the tokens (large token counts) or
 // the weight rows ("swap AB", small token counts where N = 16..64 tokens); the
 // N side is the other operand.  Small dense problems split K across CTAs and
@@ -216,18 +216,21 @@ struct Unit {
 };
 
 // Grouped GEMMs keep the per-group tables (tile prefix, token count, first
-// row) in shared memory, copied once per CTA; a unit's group is found by a
-// binary search there (the last g with tile_prefix[g] <= tile index).
+// row, and in pairs the prefix of pair units) in shared memory, copied once
+// per CTA; a unit's group is found by a binary search there (the last g whose
+// prefix is <= the unit's tile or pair index).
 struct GroupTables {
   const int* prefix;   // [G+1]
   const int* count;    // [G]
   const int* first;    // [G]
+  const int* pairs;    // [G+1] prefix of tiles * nfeat / 2 (CTA pairs only)
 };
 
 // Work units of one CTA: with multicast a unit is a pair of token tiles (one
 // per CTA of the cluster), so both CTAs walk the same unit sequence.
 __device__ __forceinline__ int total_units(const GemmParams& p, const GroupTables& gt_tab,
                                            int tok_tile, int nfeat) {
+  if (p.mcast && p.tile_prefix) return gt_tab.pairs[p.num_groups];
   const int tiles = p.tile_prefix ? gt_tab.prefix[p.num_groups]
                                   : (p.T_dense + tok_tile - 1) / tok_tile;
   // multicast pairs two units (tiles * nfeat is even: the launcher checks)
@@ -249,24 +252,43 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const GroupTabl
   const int v = u / p.splits;
   int g = 0, t_in_g, count = p.T_dense, first = 0;
   if (p.mcast) {
-    // pair unit v (dense): first floor(t/2) * nfeat pairs of token tiles
-    // (2tp + rank, same feature tile, in bands of kBand feature tiles as
-    // below), then for an odd t the last token tile against feature tiles
-    // 2j + rank
-    const int t = (p.T_dense + tok_tile - 1) / tok_tile;
+    // pair unit v of group g: first floor(t/2) * nfeat pairs of token tiles
+    // (2tp + rank, same feature tile; dense GEMMs in bands of kBand feature
+    // tiles as below), then for an odd t the last token tile against feature
+    // tiles 2j + rank
+    int t, j = v;
+    if (p.tile_prefix) {
+      int lo = 0, hi = p.num_groups - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (gt_tab.pairs[mid] <= v) lo = mid; else hi = mid - 1;
+      }
+      g = lo;
+      j = v - gt_tab.pairs[g];
+      t = gt_tab.prefix[g + 1] - gt_tab.prefix[g];
+      count = gt_tab.count[g];
+      first = gt_tab.first[g];
+    } else {
+      t = (p.T_dense + tok_tile - 1) / tok_tile;
+    }
     const int nb = (t / 2) * nfeat;
-    if (v < nb) {
-      const int nt = t / 2;
-      const int nbands = (nfeat + kBand - 1) / kBand;
-      const int b = min(v / (nt * kBand), nbands - 1);
-      const int rem = v - b * nt * kBand;
-      const int fb = (b == nbands - 1) ? nfeat - kBand * (nbands - 1) : kBand;
-      t_in_g = 2 * (rem / fb) + rank;
-      x.feat_tile = b * kBand + rem % fb;
+    if (j < nb) {
+      if (p.tile_prefix) {
+        t_in_g = 2 * (j / nfeat) + rank;
+        x.feat_tile = j % nfeat;
+      } else {
+        const int nt = t / 2;
+        const int nbands = (nfeat + kBand - 1) / kBand;
+        const int b = min(j / (nt * kBand), nbands - 1);
+        const int rem = j - b * nt * kBand;
+        const int fb = (b == nbands - 1) ? nfeat - kBand * (nbands - 1) : kBand;
+        t_in_g = 2 * (rem / fb) + rank;
+        x.feat_tile = b * kBand + rem % fb;
+      }
     } else {
       x.shareA = 1;
       t_in_g = t - 1;
-      x.feat_tile = 2 * (v - nb) + rank;
+      x.feat_tile = 2 * (j - nb) + rank;
     }
   } else if (p.tile_prefix) {
     x.feat_tile = v % nfeat;
@@ -314,11 +336,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   // bars: full[S], empty[S], tfull[2], tempty[2], done
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int* tab = reinterpret_cast<int*>(tmem_holder + 4);   // grouped: prefix | count | first
-  GroupTables tabs{tab, tab + p.num_groups + 1, tab + 2 * p.num_groups + 1};
+  int* tab = reinterpret_cast<int*>(tmem_holder + 4);   // grouped: prefix | count | first | pairs
+  GroupTables tabs{tab, tab + p.num_groups + 1, tab + 2 * p.num_groups + 1,
+                   tab + 3 * p.num_groups + 1};
   // epilogue staging: 4 warps x [32 rows][32 fp32], 16-byte chunks XOR-swizzled by row
   float* stage_out = reinterpret_cast<float*>(
-      (reinterpret_cast<uintptr_t>(tab + (p.tile_prefix ? 3 * p.num_groups + 1 : 0)) + 15) &
+      (reinterpret_cast<uintptr_t>(tab + (p.tile_prefix ? 4 * p.num_groups + 2 : 0)) + 15) &
       ~uintptr_t(15));
 
   const int warp = threadIdx.x >> 5;
@@ -360,6 +383,30 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     for (int i = threadIdx.x; i < G; i += blockDim.x) {
       tab[G + 1 + i] = __ldg(p.grp_count + i);
       tab[2 * G + 1 + i] = __ldg(p.grp_offset + i);
+    }
+    if (p.mcast) {
+      // prefix of pair units per group (tiles * nfeat / 2), by warp 0 (G <= 1024: a run per lane)
+      __syncthreads();
+      if (warp == 0) {
+        const int nf = p.fuse_situ ? (p.M_feat / 2) / BM : p.M_feat / bn;
+        const int per = (G + 31) / 32;
+        const int g0 = min(G, lane * per), g1 = min(G, g0 + per);
+        int sum = 0;
+        for (int g = g0; g < g1; ++g) sum += (tab[g + 1] - tab[g]) * nf / 2;
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        int run = incl - sum;
+        int* pairs = tab + 3 * G + 1;
+        for (int g = g0; g < g1; ++g) {
+          pairs[g] = run;
+          run += (tab[g + 1] - tab[g]) * nf / 2;
+        }
+        if (lane == 31) pairs[G] = incl;
+      }
     }
   }
   tc_fence_before();
@@ -809,7 +856,7 @@ int max_pairs_resident(size_t smem) {
 // on M only) the epilogue staging buffers; at most 227 KB
 size_t smem_for(int bn, int stages, int groups, int tok_on_m) {
   const size_t stage = (size_t)BM * BK * 2 + (size_t)bn * BK * 2;
-  return 1024 + stages * stage + (2 * stages + 5) * 8 + 16 + (size_t)(3 * groups + 1) * 4 + 16 +
+  return 1024 + stages * stage + (2 * stages + 5) * 8 + 16 + (size_t)(4 * groups + 2) * 4 + 16 +
          (tok_on_m ? 4 * 32 * 32 * 4 : 0);
 }
 
@@ -834,13 +881,13 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
   p.add = g.add;
   p.stages = stages_for(g.bn);
   p.fuse_situ = g.fuse_situ;
-  // CTA pairs with a multicast operand: dense, tokens on M, 256-row weight
-  // tiles, and an even count of token tiles or of weight tiles
+  // CTA pairs with a multicast operand: tokens on M, 256-row weight tiles, and
+  // an even count of weight tiles (or, dense, of token tiles)
   {
     const int nfeat = g.fuse_situ ? (g.M_feat / 2) / BM : g.M_feat / 256;
     const int ntok = (g.T_dense + BM - 1) / BM;
-    p.mcast = !g.grp_count && g.tok_on_m && g.bn == 256 && g.splits == 1 &&
-              (nfeat % 2 == 0 || ntok % 2 == 0);
+    p.mcast = g.tok_on_m && g.bn == 256 && g.splits == 1 &&
+              (nfeat % 2 == 0 || (!g.grp_count && ntok % 2 == 0));
   }
   p.sp = make_situ_params(g.beta > 0.0f ? g.beta : 1.0f, g.linear_beta);
   uint32_t cols = 32;
