@@ -228,13 +228,14 @@ struct GroupTables {
 
 // Work units of one CTA: with multicast a unit is a pair of token tiles (one
 // per CTA of the cluster), so both CTAs walk the same unit sequence.
+template <bool kPairs>
 __device__ __forceinline__ int total_units(const GemmParams& p, const GroupTables& gt_tab,
                                            int tok_tile, int nfeat) {
-  if (p.mcast && p.tile_prefix) return gt_tab.pairs[p.num_groups];
+  if (kPairs && p.tile_prefix) return gt_tab.pairs[p.num_groups];
   const int tiles = p.tile_prefix ? gt_tab.prefix[p.num_groups]
                                   : (p.T_dense + tok_tile - 1) / tok_tile;
   // multicast pairs two units (tiles * nfeat is even: the launcher checks)
-  return p.mcast ? tiles * nfeat / 2 : tiles * nfeat * p.splits;
+  return kPairs ? tiles * nfeat / 2 : tiles * nfeat * p.splits;
 }
 
 // Dense GEMMs with tokens on M walk their tiles in bands of kBand feature
@@ -243,6 +244,7 @@ __device__ __forceinline__ int total_units(const GemmParams& p, const GroupTable
 // tiles that both stay in L2 (for K = 7168: 8 x 3.7 MB + 19 x 1.8 MB).
 constexpr int kBand = 8;
 
+template <bool kPairs>
 __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const GroupTables& gt_tab, int u,
                                             int tok_tile, int feat_tile, int nfeat, int nkb,
                                             int rank) {
@@ -251,7 +253,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const GroupTabl
   x.split = u % p.splits;
   const int v = u / p.splits;
   int g = 0, t_in_g, count = p.T_dense, first = 0;
-  if (p.mcast) {
+  if (kPairs) {
     // pair unit v of group g: first floor(t/2) * nfeat pairs of token tiles
     // (2tp + rank, same feature tile; dense GEMMs in bands of kBand feature
     // tiles as below), then for an odd t the last token tile against feature
@@ -322,6 +324,8 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const GroupTabl
   return x;
 }
 
+// kPairs: the CTA-pair form (launched in clusters of two; p.mcast is set)
+template <bool kPairs>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const GemmParams p) {
@@ -357,7 +361,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), p.mcast ? 2 : 1);   // multicast: both CTAs' MMAs release
+      mbar_init(empty_bar(s), kPairs ? 2 : 1);   // multicast: both CTAs' MMAs release
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -384,7 +388,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tab[G + 1 + i] = __ldg(p.grp_count + i);
       tab[2 * G + 1 + i] = __ldg(p.grp_offset + i);
     }
-    if (p.mcast) {
+    if (kPairs) {
       // prefix of pair units per group (tiles * nfeat / 2), by warp 0 (G <= 1024: a run per lane)
       __syncthreads();
       if (warp == 0) {
@@ -412,13 +416,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   tc_fence_before();
   // with multicast the partner CTA's barriers must be initialised before any
   // copy or commit reaches them: a cluster-wide barrier (it also syncs this CTA)
-  if (p.mcast) cluster_sync(); else __syncthreads();
+  if (kPairs) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   // CTA-to-unit walk: with multicast both CTAs of a cluster take the same units
-  const int rank = p.mcast ? (int)cluster_rank() : 0;
-  const int cl0 = p.mcast ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int ncl = p.mcast ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int rank = kPairs ? (int)cluster_rank() : 0;
+  const int cl0 = kPairs ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ncl = kPairs ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   const int tok_tile = p.tok_on_m ? BM : bn;
   const int feat_tile = p.tok_on_m ? bn : BM;
@@ -448,10 +452,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       // weight tiles of the first ring of stages are requested before the
       // wait for the previous kernel (weights are constant).
       uint32_t pre = 0;
-      if (dense && !p.mcast) {
-        const int U0 = total_units(p, tabs, tok_tile, nfeat);
+      if (dense && !kPairs) {
+        const int U0 = total_units<kPairs>(p, tabs, tok_tile, nfeat);
         for (int u = cl0; u < U0 && pre < (uint32_t)S; u += ncl) {
-          const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb, rank);
+          const Unit x = decode_unit<kPairs>(p, tabs, u, tok_tile, feat_tile, nfeat, nkb, rank);
           for (int kb = x.kb0; kb < x.kb1 && pre < (uint32_t)S; ++kb, ++pre) {
             const uint32_t sa = smem_u32(smem + (size_t)pre * stage_bytes);
             mbar_arrive_expect_tx(full_bar((int)pre), stage_bytes);
@@ -460,16 +464,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
       }
       pdl_wait();
-      const int U = total_units(p, tabs, tok_tile, nfeat);
+      const int U = total_units<kPairs>(p, tabs, tok_tile, nfeat);
       // ring position kept incrementally: stage s, its smem address, parity
       uint32_t it = 0, s = 0, ph = 0;
       uint32_t sa = smem_u32(smem);
       const uint32_t sa0 = sa;
       bool ok = true;
       for (int u = cl0; u < U && ok; u += ncl) {
-        const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb, rank);
+        const Unit x = decode_unit<kPairs>(p, tabs, u, tok_tile, feat_tile, nfeat, nkb, rank);
         for (int kb = x.kb0; kb < x.kb1; ++kb, ++it) {
-          if (p.mcast) {
+          if (kPairs) {
             if (!wait_phase(empty_bar((int)s), ph ^ 1u, abort_flag, kErrProducer)) { ok = false; break; }
             mbar_arrive_expect_tx(full_bar((int)s), stage_bytes);
             // the weight tile in two 128-row boxes: gate and up rows (fused
@@ -518,7 +522,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
       pdl_wait();
-      const int U = total_units(p, tabs, tok_tile, nfeat);
+      const int U = total_units<kPairs>(p, tabs, tok_tile, nfeat);
       const uint32_t idesc = idesc_bf16(BM, bn);
       // descriptors of stage 0; stage s adds s*stage_bytes, each K=16 step adds
       // 32 bytes (+2 in the 16-byte address field, which never carries out)
@@ -529,7 +533,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint64_t da = da0, db = db0;
       bool ok = true;
       for (int u = cl0; u < U && ok; u += ncl, ++uit) {
-        const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb, rank);
+        const Unit x = decode_unit<kPairs>(p, tabs, u, tok_tile, feat_tile, nfeat, nkb, rank);
         const int acc = (int)(uit & 1u);
         if (!wait_phase(tempty_bar(acc), ((uit >> 1) & 1u) ^ 1u, abort_flag, kErrMmaTmem)) {
           ok = false;
@@ -546,7 +550,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           mma_bf16(d_tmem, da + 4, db + 4, idesc, 1u);
           mma_bf16(d_tmem, da + 6, db + 6, idesc, 1u);
           accumulate = 1u;
-          if (p.mcast) mma_commit_mc(empty_bar((int)s), (uint16_t)3u);
+          if (kPairs) mma_commit_mc(empty_bar((int)s), (uint16_t)3u);
           else mma_commit(empty_bar((int)s));
           if (++s == (uint32_t)S) { s = 0; ph ^= 1u; da = da0; db = db0; }
           else { da += dstep; db += dstep; }
@@ -563,10 +567,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int q = warp & 3;                  // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;             // accumulator row of this thread
     pdl_wait();
-    const int U = total_units(p, tabs, tok_tile, nfeat);
+    const int U = total_units<kPairs>(p, tabs, tok_tile, nfeat);
     uint32_t uit = 0;
     for (int u = cl0; u < U; u += ncl, ++uit) {
-      const Unit x = decode_unit(p, tabs, u, tok_tile, feat_tile, nfeat, nkb, rank);
+      const Unit x = decode_unit<kPairs>(p, tabs, u, tok_tile, feat_tile, nfeat, nkb, rank);
       const int acc = (int)(uit & 1u);
       if (!wait_bounded(tfull_bar(acc), (uit >> 1) & 1u, abort_flag, kErrEpilogue)) break;
       tc_fence_after();
@@ -777,7 +781,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                  : "memory");
   }
   // no CTA leaves while its partner may still multicast into it or commit to it
-  if (p.mcast) cluster_sync();
+  if (kPairs) cluster_sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -847,7 +851,7 @@ int max_pairs_resident(size_t smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int pairs = 0;
-  if (cudaOccupancyMaxActiveClusters(&pairs, gemm_tc_kernel, &cfg) != cudaSuccess) pairs = 0;
+  if (cudaOccupancyMaxActiveClusters(&pairs, gemm_tc_kernel<true>, &cfg) != cudaSuccess) pairs = 0;
   if (n < 16) cache[n++] = Entry{dev, smem, pairs};
   return pairs;
 }
@@ -902,8 +906,8 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
 
   const size_t smem = smem_for(g.bn, p.stages, g.grp_count ? g.G : 0, g.tok_on_m);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(p.mcast ? gemm_tc_kernel<true> : gemm_tc_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (p.mcast) {
     // as many CTA pairs as can be resident at once (pairs share a GPC)
@@ -911,14 +915,15 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
     if (pairs < 1) return cudaErrorInvalidConfiguration;
     int np = pairs;
     if (g.max_units > 0 && g.max_units < np) np = g.max_units;
-    return launch_k_cluster(gemm_tc_kernel, dim3(2 * np), dim3(kThreads), smem, stream, 2, mx, mw,
-                            p);
+    return launch_k_cluster(gemm_tc_kernel<true>, dim3(2 * np), dim3(kThreads), smem, stream, 2, mx,
+                            mw, p);
   }
   int grid = num_sms();
   if (g.max_units > 0 && g.max_units < grid) grid = g.max_units;
   if (grid < 1) grid = 1;
-  if (g.tok_on_m) return launch_k(gemm_tc_kernel, dim3(grid), dim3(kThreads), smem, stream, mx, mw, p);
-  return launch_k(gemm_tc_kernel, dim3(grid), dim3(kThreads), smem, stream, mw, mx, p);
+  if (g.tok_on_m)
+    return launch_k(gemm_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, stream, mx, mw, p);
+  return launch_k(gemm_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, stream, mw, mx, p);
 }
 
 int read_device_error(int clear) {
