@@ -186,7 +186,9 @@ size_t latent_moe_workspace_bytes(const lmoe_dims* dims);
 /*   6 A bf16 [T*k,L]          7 G bf16 [T*k,2d]          8 act bf16 [T*k,d]   */
 /*   9 Y bf16 [T*k,L]         10 N bf16 [T,L]            11 Gs bf16 [T,2ds]    */
 /*  12 As bf16 [T,ds]         13 Sh bf16 [T,H]                                 */
-/* Z, Gs and Sh hold data only when the call did not split K (T > 128).       */
+/* Z and Sh hold data only when the call did not split K (T > 128).  At      */
+/* T > 128, G holds data only if inter % 128 != 0 and Gs only if            */
+/* shared_inter % 128 != 0 (otherwise SituGLU runs in the GEMM's epilogue).   */
 /* Returns LMOE_OK or a validation error.                                     */
 enum { LMOE_WS_COUNT = 14 };
 int latent_moe_workspace_offsets(const lmoe_dims* dims, size_t* offsets);
@@ -198,7 +200,11 @@ int latent_moe_launch_count(const lmoe_dims* dims, int has_shared_expert);
 
 /* hidden [T, H] bf16, router_logits [T, E] fp32, out [T, H] bf16; workspace  */
 /* at least latent_moe_workspace_bytes(dims) bytes, 256-byte aligned, not     */
-/* shared with a concurrent call.  dbg may be NULL.                           */
+/* shared with a concurrent call.  dbg may be NULL.  The shared expert runs  */
+/* on a library-owned second stream of the device, forked from `stream` and  */
+/* joined back to it by events (also inside a stream capture), so all of the */
+/* call's work is ordered after earlier work on `stream` and before later.    */
+/* With dbg->stage_events every stage runs on `stream`, one after another.    */
 int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* weights,
                        const lmoe_bf16* hidden, const float* router_logits,
                        lmoe_bf16* out, void* workspace, size_t workspace_bytes,

@@ -260,10 +260,10 @@ int plan_launches(const Plan& p, bool shared) {
   return n;
 }
 
-// The second stream of the decode forward: the shared expert runs there,
+// The second stream of the forward: the shared expert runs there,
 // forked from and joined back to the caller's stream by two events (so the
 // fork is also recorded by a stream capture).  One per device, created by the
-// first decode call on it; the mutex keeps the fork/join event pair of one
+// first call on it; the mutex keeps the fork/join event pair of one
 // call from interleaving with another host thread's.
 struct AuxStream {
   cudaStream_t stream = nullptr;
@@ -444,9 +444,10 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
     return ev == nullptr || cudaEventRecord((cudaEvent_t)ev[i], s) == cudaSuccess;
   };
   if (!mark(0)) return LMOE_ERR_CUDA;
-  // decode sizes: the shared expert gets the second stream (not when per-stage
-  // timing was asked for, which needs the stages one after another)
-  const bool concurrent = shared && decode && ev == nullptr;
+  // the shared expert gets the second stream, where it fills the gaps the
+  // routed path's latency-bound stages leave (not when per-stage timing was
+  // asked for, which needs the stages one after another)
+  const bool concurrent = shared && ev == nullptr;
   AuxStream* aux = nullptr;
   std::unique_lock<std::mutex> aux_lock(g_aux_mu, std::defer_lock);
   if (concurrent) {

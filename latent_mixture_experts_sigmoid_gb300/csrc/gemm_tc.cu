@@ -575,18 +575,32 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (!wait_bounded(tfull_bar(acc), (uit >> 1) & 1u, abort_flag, kErrEpilogue)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * bn);
-      if (p.tok_on_m && !p.out_fp32 && !p.add) {
-        // row r = token, columns = features, no addend.  Per 64-column chunk
-        // each thread rounds its row to bf16 (after SituGLU when fused) into
-        // its warp's staging buffer [32 rows][64 bf16]; the warp then writes 4
-        // rows x 128 bytes per 16-byte store instruction.
+      if (p.tok_on_m && !p.out_fp32) {
+        // row r = token, columns = features.  Per 64-column chunk each thread
+        // rounds its row to bf16 (after SituGLU when fused, after adding the
+        // bf16 addend in fp32 when there is one) into its warp's staging
+        // buffer [32 rows][64 bf16]; the warp then writes 4 rows x 128 bytes
+        // per 16-byte store instruction.
         uint32_t* st = reinterpret_cast<uint32_t*>(stage_out) + (size_t)q * 32 * 32;
         const int width = p.fuse_situ ? BM : bn;           // output columns of this tile
         const int fcol0 = x.feat_tile * width;
         const int ldo = p.fuse_situ ? p.M_feat / 2 : p.ldo;
+        const bool row_ok = r < x.nvalid;
+        const uint16_t* arow =
+            p.add ? p.add + (long long)(x.tok_row0 + (row_ok ? r : 0)) * ldo + fcol0 : nullptr;
+        if (p.add && row_ok)   // pull this thread's addend row into L2 while the tile drains
+          for (int b = 0; b < width * 2; b += 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(arow) + b));
         for (int c0 = 0; c0 < width; c0 += 64) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
+            // the addend's 32 columns, loaded before the accumulator
+            uint4 ad[4] = {};
+            if (p.add && row_ok) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                ad[i] = __ldg(reinterpret_cast<const uint4*>(arow + c0 + 32 * h) + i);
+            }
             float f[32];
             {
               uint32_t v[16];
@@ -617,6 +631,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
               }
             } else {
+              if (p.add) {
+                const uint32_t aw[16] = {ad[0].x, ad[0].y, ad[0].z, ad[0].w, ad[1].x, ad[1].y,
+                                         ad[1].z, ad[1].w, ad[2].x, ad[2].y, ad[2].z, ad[2].w,
+                                         ad[3].x, ad[3].y, ad[3].z, ad[3].w};
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  f[2 * j] += bf16_lo(aw[j]);
+                  f[2 * j + 1] += bf16_hi(aw[j]);
+                }
+              }
 #pragma unroll
               for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(f[2 * j], f[2 * j + 1]);
             }
@@ -636,92 +660,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (row_in_tile < x.nvalid) {
               const long long off = (long long)(x.tok_row0 + row_in_tile) * ldo + fcol0 + c0 + c * 8;
               *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + off) = a;
-            }
-          }
-          __syncwarp();
-        }
-      } else if (p.tok_on_m && !p.out_fp32) {
-        // row r = token, columns = features, bf16 addend.  Per 32-column chunk: each thread
-        // puts its row's fp32 results into its warp's staging buffer; the warp
-        // then writes 4 rows x 32 columns per store instruction (the shared
-        // output add happens here in fp32, before the single bf16 rounding).
-        float* st = stage_out + (size_t)q * 32 * 32;
-        const int width = p.fuse_situ ? BM : bn;           // output columns of this tile
-        const int fcol0 = x.feat_tile * width;
-        const int ldo = p.fuse_situ ? p.M_feat / 2 : p.ldo;
-        if (p.add && r < x.nvalid) {
-          // pull this thread's row of the addend into L2 while the tile drains
-          const uint16_t* arow = p.add + (long long)(x.tok_row0 + r) * ldo + fcol0;
-          for (int b = 0; b < width * 2; b += 128)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(arow) + b));
-        }
-        for (int c0 = 0; c0 < width; c0 += 32) {
-          float f[32];
-          {
-            uint32_t v[16];
-            tmem_ld16(tbase + (uint32_t)c0, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) f[j] = __uint_as_float(v[j]);
-            tmem_ld16(tbase + (uint32_t)(c0 + 16), v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) f[16 + j] = __uint_as_float(v[j]);
-          }
-          if (p.fuse_situ) {
-            // gate = f, up = the same features 128 columns further; both
-            // rounded to bf16 first, as the stored GEMM output would be
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint32_t v[16];
-              tmem_ld16(tbase + (uint32_t)(BM + c0 + 16 * h), v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int j = 0; j < 16; j += 2) {
-                const uint32_t gb = pack_bf16x2(f[16 * h + j], f[16 * h + j + 1]);
-                const uint32_t ub = pack_bf16x2(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
-                const f32x2 o = situ2_f32(gb, ub, p.sp);
-                f[16 * h + j] = f2_lo(o);
-                f[16 * h + j + 1] = f2_hi(o);
-              }
-            }
-          }
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<float4*>(st + lane * 32 + ((c ^ (lane & 7)) * 4)) =
-                make_float4(f[4 * c], f[4 * c + 1], f[4 * c + 2], f[4 * c + 3]);
-          __syncwarp();
-          // the shared-output add: all eight loads first (the stores below
-          // may alias them as far as the compiler knows)
-          uint2 ad[8];
-          if (p.add) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int rr = i * 4 + (lane >> 3);
-              const int row_in_tile = q * 32 + rr;
-              ad[i] = make_uint2(0u, 0u);
-              if (row_in_tile < x.nvalid)
-                ad[i] = __ldg(reinterpret_cast<const uint2*>(
-                    p.add + (long long)(x.tok_row0 + row_in_tile) * ldo + fcol0 + c0 +
-                    (lane & 7) * 4));
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rr = i * 4 + (lane >> 3);            // row within this warp's 32
-            const int c = lane & 7;                        // 4-column chunk
-            const float4 a = *reinterpret_cast<const float4*>(st + rr * 32 + ((c ^ (rr & 7)) * 4));
-            const int row_in_tile = q * 32 + rr;
-            if (row_in_tile < x.nvalid) {
-              const long long orow = (long long)(x.tok_row0 + row_in_tile);
-              const long long off = orow * ldo + fcol0 + c0 + c * 4;
-              float o0 = a.x, o1 = a.y, o2 = a.z, o3 = a.w;
-              if (p.add) {
-                o0 += bf16_lo(ad[i].x); o1 += bf16_hi(ad[i].x);
-                o2 += bf16_lo(ad[i].y); o3 += bf16_hi(ad[i].y);
-              }
-              *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.out) + off) =
-                  make_uint2(pack_bf16x2(o0, o1), pack_bf16x2(o2, o3));
             }
           }
           __syncwarp();
