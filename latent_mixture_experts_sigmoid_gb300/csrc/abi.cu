@@ -267,7 +267,7 @@ int plan_launches(const Plan& p, bool shared) {
 // call from interleaving with another host thread's.
 struct AuxStream {
   cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, routed = nullptr;
 };
 AuxStream g_aux[64];
 std::mutex g_aux_mu;
@@ -278,14 +278,16 @@ bool aux_for_current_device(AuxStream** out) {
   AuxStream& a = g_aux[dev];
   if (a.stream == nullptr) {
     cudaStream_t st = nullptr;
-    cudaEvent_t f = nullptr, j = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr, r = nullptr;
     if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return false;
     if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess)
+        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&r, cudaEventDisableTiming) != cudaSuccess)
       return false;
     a.stream = st;
     a.fork = f;
     a.join = j;
+    a.routed = r;
   }
   *out = &a;
   return true;
@@ -456,8 +458,8 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
     if (cudaEventRecord(aux->fork, s) != cudaSuccess) return LMOE_ERR_CUDA;
   }
   // 9-11. shared expert on the original hidden states (enqueued by a lambda:
-  // on the caller's stream, or at decode sizes first thing on the second
-  // stream so that it overlaps the routed path)
+  // on the caller's stream, or on the second stream so that it overlaps the
+  // routed path)
   const float* sh_part = nullptr;
   int sh_splits = 0;
   long long sh_stride = 0;
@@ -495,19 +497,40 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
     if (marks && !mark(LMOE_STAGE_SHARED2 + 1)) return LMOE_ERR_CUDA;
     return LMOE_OK;
   };
+  // 1. routing and 3. permutation: at large T they run first on the second
+  // stream, beside the down-projection (which leaves SMs idle in its last
+  // wave), and the caller's stream waits for them before the scatter (at
+  // decode sizes this measured slower: they stay on the caller's stream)
+  auto route_and_permute = [&](cudaStream_t rs, bool marks) -> int {
+    LMOE_TRY(launch_route(router_logits, wt->e_score_correction_bias, T, E, k, d.renormalize,
+                          d.routed_scaling_factor, ws.ids, ws.w, rs));
+    if (marks && !mark(LMOE_STAGE_ROUTE + 1)) return LMOE_ERR_CUDA;
+    return LMOE_OK;
+  };
+  auto permute = [&](cudaStream_t rs) -> int {
+    LMOE_TRY(launch_permute(ws.ids, T, k, E, tile, ws.perm_scratch, ws.counts, ws.offsets,
+                            ws.tile_prefix, ws.row_of, ws.tok_of_row, rs));
+    return LMOE_OK;
+  };
   int st = LMOE_OK;
+  const bool side_route = concurrent && !decode;
   if (concurrent) {
     if (cudaStreamWaitEvent(aux->stream, aux->fork, 0) != cudaSuccess) return LMOE_ERR_CUDA;
+    if (side_route) {
+      st = route_and_permute(aux->stream, false);
+      if (st != LMOE_OK) return st;
+      st = permute(aux->stream);
+      if (st != LMOE_OK) return st;
+      if (cudaEventRecord(aux->routed, aux->stream) != cudaSuccess) return LMOE_ERR_CUDA;
+    }
     st = shared_expert(aux->stream, false);
     if (st != LMOE_OK) return st;
     if (cudaEventRecord(aux->join, aux->stream) != cudaSuccess) return LMOE_ERR_CUDA;
   }
-
-
-  // 1. routing
-  LMOE_TRY(launch_route(router_logits, wt->e_score_correction_bias, T, E, k, d.renormalize,
-                        d.routed_scaling_factor, ws.ids, ws.w, s));
-  if (!mark(LMOE_STAGE_ROUTE + 1)) return LMOE_ERR_CUDA;
+  if (!side_route) {
+    st = route_and_permute(s, true);
+    if (st != LMOE_OK) return st;
+  }
   // 2. latent down-projection
   const DenseCfg cdown = pl.down;
   const bool down_split = cdown.splits > 1;
@@ -515,9 +538,12 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
   LMOE_TRY(gemm_dense(wt->w_down, L, X, T, H, cdown, down_split ? (void*)ws.Pa : (void*)ws.Z,
                       down_split, down_stride, nullptr, s));
   if (!mark(LMOE_STAGE_DOWN + 1)) return LMOE_ERR_CUDA;
-  // 3. permutation
-  LMOE_TRY(launch_permute(ws.ids, T, k, E, tile, ws.perm_scratch, ws.counts, ws.offsets,
-                          ws.tile_prefix, ws.row_of, ws.tok_of_row, s));
+  if (side_route) {
+    if (cudaStreamWaitEvent(s, aux->routed, 0) != cudaSuccess) return LMOE_ERR_CUDA;
+  } else {
+    st = permute(s);
+    if (st != LMOE_OK) return st;
+  }
   if (!mark(LMOE_STAGE_PERMUTE + 1)) return LMOE_ERR_CUDA;
   // 4. routed input into the expert-major rows
   LMOE_TRY(launch_scatter_rows(down_split ? nullptr : ws.Z, down_split ? ws.Pa : nullptr,
