@@ -66,6 +66,20 @@ def test_route_shapes(E, k):
     check(logits, bias, k, 1.5, renorm=0)
 
 
+@pytest.mark.parametrize("E,k,renorm", [(600, 16, 1), (1001, 16, 1), (896, 8, 0), (130, 32, 1),
+                                         (257, 3, 1)])
+def test_route_warp_kernel_shapes(E, k, renorm):
+    # T > 512: the warp-per-token kernel.  E = 600 leaves padded chunks (NaN
+    # slots), E = 1001 and 257 are not multiples of 4 (4-byte row copies),
+    # k = 32 fills the candidate window, renorm = 0 keeps the raw scores
+    T = 700
+    g = np.random.default_rng(E * 7 + k)
+    logits = g.standard_normal((T, E)).astype(np.float32)
+    logits[::64] = logits[::64, :1]          # every 64th row tied
+    bias = (g.standard_normal(E) * 0.1).astype(np.float32)
+    check(logits, bias, k, 2.5, renorm=renorm)
+
+
 def test_route_sigmoid_bit_exact():
     # E = 1, k = 1, no renormalisation, rsf = 1: the weight IS the fp32 sigmoid
     x = np.concatenate([np.linspace(-120, 120, 200001, dtype=np.float32),
