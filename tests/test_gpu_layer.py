@@ -63,7 +63,7 @@ def test_tiny_layer_token_counts(T):
 
 
 @pytest.mark.parametrize("variant", ["no_shared", "linear_beta_unset", "gamma_noise", "top1",
-                                     "no_renorm", "zipf_prefill", "wide"])
+                                     "no_renorm", "zipf_prefill", "wide", "pairs"])
 def test_tiny_layer_variants(variant):
     d = W.TINY
     kw = {}
@@ -83,6 +83,10 @@ def test_tiny_layer_variants(variant):
     elif variant == "wide":
         d = dataclasses.replace(d, T=200, hidden=384, latent=256, inter=192, shared_inter=320,
                                 num_experts=40, topk=8)
+    elif variant == "pairs":
+        # every GEMM in CTA pairs: even weight-tile counts everywhere, 5 token
+        # tiles (the dense GEMMs' odd last tile is shared by two weight tiles)
+        d = dataclasses.replace(d, T=600, hidden=512, latent=512, inter=256, shared_inter=256)
     tiny_case(d, seed=11, **kw)
 
 
