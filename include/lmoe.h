@@ -22,6 +22,13 @@
  *   - On a validation error nothing is launched and a negative lmoe_status is
  *     returned.  A zero-sized problem (T == 0, N == 0, E == 0) returns LMOE_OK
  *     and launches nothing.
+ *   - Weights (the members of lmoe_weights, the `w` of lmoe_linear and the
+ *     e_score_correction_bias of moe_route) are read-only model parameters.
+ *     Kernels launch with programmatic dependent launch and may start reading
+ *     them before the preceding work on `stream` has finished; work that
+ *     writes a weight must be separated from the call by an event or a
+ *     synchronisation, not by stream order alone.  Activations (hidden states,
+ *     router logits) are read only after the preceding work has finished.
  *   - bf16 values are carried as raw 16-bit patterns (lmoe_bf16).
  *   - Internal waits in the tensor-core kernels are bounded; if one ever gives
  *     up, the kernel records a code in a device error word and returns early

@@ -368,8 +368,9 @@ route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bi
     for (int i = threadIdx.x; i < kWarpsPerBlock * NSLOT * EW / 4; i += blockDim.x)
       reinterpret_cast<float4*>(srow_all)[i] = qnan4;
   }
-  pdl_wait();
+  // the bias is a model parameter: read while the preceding kernel drains
   for (int e = threadIdx.x; e < EW; e += blockDim.x) sbias[e] = (bias && e < E) ? __ldg(bias + e) : 0.0f;
+  pdl_wait();
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
