@@ -19,8 +19,11 @@
 //               (kind::f16, bf16 in, fp32 accumulate, M = 128) into one of
 //               two TMEM accumulators, committing stage releases and
 //               accumulator-ready signals through tcgen05.commit;
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, optional bf16 add,
-//               bf16 or fp32 stores straight to global memory.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator; with tokens on M the
+//               rows are rounded to bf16 (after SituGLU or the bf16 addend
+//               where asked) into a swizzled shared-memory staging buffer and
+//               written 4 rows x 128 bytes per 16-byte store instruction;
+//               otherwise fp32 partials or bf16 values go straight out.
 // GEMMs with tokens on M and 256-row weight tiles run in clusters of two CTAs.
 // A pair of units shares an operand: token tiles 2t and 2t+1 of a group
 // against the same weight tile (each CTA loads one 128-row half of the weight
@@ -37,7 +40,8 @@
 // Every wait on an mbarrier is bounded (clock64 deadline).  A wait that gives
 // up records a code in the device error word, raises a CTA-wide abort flag,
 // and the CTA drains its own in-flight copies and MMAs (again bounded),
-// frees its TMEM and returns.
+// frees its TMEM and returns (CTA pairs meet at a cluster barrier first, so
+// that neither leaves while the other may still write into it).
 #include <cuda.h>
 
 #include <mutex>

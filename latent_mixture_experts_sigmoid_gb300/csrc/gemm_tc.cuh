@@ -29,9 +29,9 @@ struct GemmParams {
   uint32_t tmem_cols;
   int fuse_situ;           // tokens on M only: W tile = 128 gate rows + the matching 128 up
                            // rows; the epilogue writes bf16(SituGLU(bf16(G))) [rows, M_feat/2]
-  int mcast;               // 1: clusters of two CTAs take token tiles 2t and 2t+1 of the
-                           // same weight tile (tokens on M, bn == 256, no split-K); each
-                           // loads one 128-row half of the weight tile into both CTAs
+  int mcast;               // 1: launched in clusters of two CTAs (the gemm_tc_kernel<true>
+                           // form) that share an operand tile by TMA multicast; dense or
+                           // grouped, tokens on M, 256-row weight tiles, no split-K
   SituParams sp;
 };
 
