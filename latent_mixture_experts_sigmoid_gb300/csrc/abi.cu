@@ -250,9 +250,12 @@ Plan make_plan(const lmoe_dims& d, int nsm) {
 }
 
 int plan_launches(const Plan& p, bool shared) {
-  const int perm = p.T <= 256 ? 1 : 3;  // one fused permutation kernel for T <= 256
+  // one permutation kernel for T <= 256; at decode sizes it also does the scatter
+  const int perm = p.T <= 256 ? 1 : 3;
   const int experts = p.fuse_g1 ? 2 : 3;  // GEMM1 (+ SituGLU unless fused), GEMM2
-  int n = 1 + 1 + perm + 1 + experts + 1;  // route, down, permute, scatter, experts, combine
+  // route, down, permute, scatter (fused into the permutation at decode sizes),
+  // experts, combine
+  int n = 1 + 1 + perm + (p.decode ? 0 : 1) + experts + 1;
   if (shared) n += p.fuse_s1 ? 2 : 3;   // shared GEMM1 (+ SituGLU unless fused), shared GEMM2
   n += 1;                               // up-projection GEMM
   const bool sh_part = shared && p.s2.splits > 1;
@@ -538,16 +541,26 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
   LMOE_TRY(gemm_dense(wt->w_down, L, X, T, H, cdown, down_split ? (void*)ws.Pa : (void*)ws.Z,
                       down_split, down_stride, nullptr, s));
   if (!mark(LMOE_STAGE_DOWN + 1)) return LMOE_ERR_CUDA;
+  // small T: permutation and scatter in one launch (every block rebuilds the
+  // small counting sort); large T: the scatter after the separate permutation
+  const bool fused_scatter = decode;
   if (side_route) {
     if (cudaStreamWaitEvent(s, aux->routed, 0) != cudaSuccess) return LMOE_ERR_CUDA;
+  } else if (fused_scatter) {
+    LMOE_TRY(launch_permute_scatter_small(ws.ids, T, k, E, tile, ws.counts, ws.offsets,
+                                          ws.tile_prefix, ws.row_of, ws.tok_of_row,
+                                          down_split ? nullptr : ws.Z,
+                                          down_split ? ws.Pa : nullptr, cdown.splits, down_stride,
+                                          L, ws.A, s));
   } else {
     st = permute(s);
     if (st != LMOE_OK) return st;
   }
   if (!mark(LMOE_STAGE_PERMUTE + 1)) return LMOE_ERR_CUDA;
   // 4. routed input into the expert-major rows
-  LMOE_TRY(launch_scatter_rows(down_split ? nullptr : ws.Z, down_split ? ws.Pa : nullptr,
-                               cdown.splits, down_stride, T, L, k, ws.row_of, ws.A, s));
+  if (!fused_scatter)
+    LMOE_TRY(launch_scatter_rows(down_split ? nullptr : ws.Z, down_split ? ws.Pa : nullptr,
+                                 cdown.splits, down_stride, T, L, k, ws.row_of, ws.A, s));
   if (!mark(LMOE_STAGE_SCATTER + 1)) return LMOE_ERR_CUDA;
   // 5-7. experts
   if (pl.fuse_g1) {

@@ -199,6 +199,92 @@ perm_rows_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
   }
 }
 
+// ---- permutation and scatter in one kernel, for small T (decode) -------------
+// T blocks of 1024 threads (T <= 256, E <= 1024).  Every block rebuilds the
+// whole counting sort of the T*k (token, slot) pairs in shared memory (bitmaps,
+// counts, a block scan for the offsets), which for so few pairs costs less than
+// a second launch; block 0 publishes counts, offsets, tile prefix and every
+// row; block t then writes Z[t] (the fixed-order sum of the S fp32 split
+// partials, or a bf16 row) into its k expert-major rows.
+__global__ void __launch_bounds__(1024)
+perm_scatter_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int tile,
+                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                          int32_t* __restrict__ tile_prefix, int32_t* __restrict__ row_of,
+                          int32_t* __restrict__ tok_of_row, const uint16_t* __restrict__ Zb,
+                          const float* __restrict__ Zp, int S, long long split_stride, int L,
+                          uint16_t* __restrict__ A) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ uint32_t bm[1024 * kWords];
+  __shared__ int soff[1024];
+  __shared__ int sh[33];
+  __shared__ int srow[32];
+  for (int i = threadIdx.x; i < E * kWords; i += blockDim.x) bm[i] = 0u;
+  __syncthreads();
+  if ((int)threadIdx.x < T) {
+    const int tt = threadIdx.x;
+    for (int j = 0; j < k; ++j) {
+      const int e = __ldg(ids + (long long)tt * k + j);
+      atomicOr(&bm[e * kWords + (tt >> 5)], 1u << (tt & 31));
+    }
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  int c = 0;
+  if (e < E) {
+#pragma unroll
+    for (int w = 0; w < kWords; ++w) c += __popc(bm[e * kWords + w]);
+  }
+  int all = 0, all_tiles = 0;
+  const int off = block_exclusive_scan(c, sh, &all);
+  const int toff = block_exclusive_scan(e < E ? (c + tile - 1) / tile : 0, sh, &all_tiles);
+  if (e < E) soff[e] = off;
+  if (blockIdx.x == 0) {
+    if (e < E) {
+      counts[e] = c;
+      offsets[e] = off;
+      tile_prefix[e] = toff;
+    }
+    if (e == 0) {
+      offsets[E] = all;
+      tile_prefix[E] = all_tiles;
+    }
+  }
+  __syncthreads();
+  const int t = blockIdx.x;
+  if ((int)threadIdx.x < k) {
+    const int j = threadIdx.x;
+    const int ej = __ldg(ids + (long long)t * k + j);
+    const uint32_t* m = bm + ej * kWords;
+    const int w = t >> 5;
+    int rank = __popc(m[w] & ((1u << (t & 31)) - 1u));
+    for (int i = 0; i < w; ++i) rank += __popc(m[i]);
+    const int row = soff[ej] + rank;
+    row_of[(long long)t * k + j] = row;
+    tok_of_row[row] = t;
+    srow[j] = row;
+  }
+  __syncthreads();
+  for (int v = threadIdx.x; v < L / 8; v += blockDim.x) {
+    uint4 o;
+    if (Zp) {
+      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int sp = 0; sp < S; ++sp) {
+        const float4* p = reinterpret_cast<const float4*>(Zp + sp * split_stride +
+                                                          (long long)t * L + v * 8);
+        const float4 a = __ldg(p), b = __ldg(p + 1);
+        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+      }
+      o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                     pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    } else {
+      o = __ldg(reinterpret_cast<const uint4*>(Zb + (long long)t * L) + v);
+    }
+    for (int j = 0; j < k; ++j) reinterpret_cast<uint4*>(A + (long long)srow[j] * L)[v] = o;
+  }
+}
+
 // ---- scatter of the routed input into the expert-major rows ------------------
 // A[row_of[t, j], :] = Z[t, :] for every slot j, where Z[t] is either a bf16
 // row or the bf16 rounding of the fixed-order sum of S fp32 split partials.
@@ -418,6 +504,16 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int tile, vo
   if (e != cudaSuccess) return e;
   return launch_k(perm_rows_kernel, dim3(nblk), dim3(kBlkTok), 0, s, ids, T, k, E,
                   (const uint32_t*)bitmaps, (const int32_t*)blk_base, row_of, tok_of_row);
+}
+
+cudaError_t launch_permute_scatter_small(const int32_t* ids, int T, int k, int E, int tile,
+                                         int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
+                                         int32_t* row_of, int32_t* tok_of_row, const uint16_t* Zb,
+                                         const float* Zp, int S, long long split_stride, int L,
+                                         uint16_t* A, cudaStream_t s) {
+  if (T > kBlkTok || E > 1024 || k > 32) return cudaErrorInvalidValue;
+  return launch_k(perm_scatter_small_kernel, dim3(T), dim3(1024), 0, s, ids, T, k, E, tile, counts,
+                  offsets, tile_prefix, row_of, tok_of_row, Zb, Zp, S, split_stride, L, A);
 }
 
 cudaError_t launch_scatter_rows(const uint16_t* Zb, const float* Zp, int S, long long split_stride,

@@ -15,6 +15,14 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int tile, vo
                            int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
                            int32_t* row_of, int32_t* tok_of_row, cudaStream_t s);
 
+// launch_permute followed by launch_scatter_rows in one launch of T blocks,
+// for T <= 256, E <= 1024, k <= 32 (the small-T path).
+cudaError_t launch_permute_scatter_small(const int32_t* ids, int T, int k, int E, int tile,
+                                         int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
+                                         int32_t* row_of, int32_t* tok_of_row, const uint16_t* Zb,
+                                         const float* Zp, int S, long long split_stride, int L,
+                                         uint16_t* A, cudaStream_t s);
+
 // A[row_of[t,j]] = Z[t] for j < k; Z from bf16 rows Zb or from the sum of S
 // fp32 partials Zp (split_stride elements apart).  L % 8 == 0.
 cudaError_t launch_scatter_rows(const uint16_t* Zb, const float* Zp, int S, long long split_stride,
