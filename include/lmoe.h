@@ -265,6 +265,22 @@ int lmoe_device_error(int clear);
 /* ABI version of this header (major * 100 + minor).                          */
 int lmoe_abi_version(void);
 
+/* Work-unit walk of the grouped expert GEMM with tokens on M (the prefill    */
+/* form), for inspection and tests; host only, launches nothing.  G groups   */
+/* (experts) of count[g] >= 0 token rows, stored consecutively in group order */
+/* (group g starts at the sum of the earlier counts); token tiles of 128 rows */
+/* and nfeat feature tiles of 256 weight rows per group (M_feat = 256*nfeat). */
+/* paired = 1: the CTA-pair form (two CTAs share one operand tile; nfeat    */
+/* even), paired = 0: one CTA per unit.  Writes, for unit u in walk order and */
+/* CTA rank r < 1 + paired, five ints at out[(u * (1 + paired) + r) * 5]:    */
+/* first token row, valid token rows, first weight row, feature tile, and 1  */
+/* if the pair shares its token tile (0 if it shares the weight tile).  A     */
+/* persistent launch of n CTAs (or pairs) gives unit u to CTA (pair) u % n.  */
+/* Writes at most max_units units (nothing if out is NULL); returns the unit  */
+/* count, or LMOE_ERR_DIM for G outside 1..1024, a negative count, nfeat < 1  */
+/* or odd with paired = 1, or more than 2^30 rows.                            */
+int lmoe_gemm_unit_walk(int G, const int* count, int nfeat, int paired, int* out, int max_units);
+
 #ifdef __cplusplus
 }
 #endif

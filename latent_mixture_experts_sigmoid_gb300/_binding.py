@@ -27,7 +27,7 @@ LMOE_ERR_ALIGN = -7
 ABI_FUNCTIONS = ("moe_route", "situ_and_mul", "masked_situ_and_mul", "latent_moe_forward",
                  "latent_moe_forward_noalloc", "latent_moe_workspace_bytes", "latent_moe_workspace_offsets",
                  "latent_moe_launch_count", "lmoe_linear", "lmoe_status_string",
-                 "lmoe_device_error", "lmoe_abi_version")
+                 "lmoe_device_error", "lmoe_abi_version", "lmoe_gemm_unit_walk")
 
 
 class LmoeError(RuntimeError):
@@ -104,6 +104,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.lmoe_device_error.restype = i32
     lib.lmoe_abi_version.argtypes = []
     lib.lmoe_abi_version.restype = i32
+    lib.lmoe_gemm_unit_walk.argtypes = [i32, vp, i32, i32, vp, i32]
+    lib.lmoe_gemm_unit_walk.restype = i32
     _lib = lib
     return lib
 
@@ -265,3 +267,19 @@ def lmoe_device_error(clear: bool = False) -> int:
 
 def lmoe_abi_version() -> int:
     return int(load_library().lmoe_abi_version())
+
+
+def gemm_unit_walk(counts, nfeat: int, paired: bool):
+    """Work-unit walk of the grouped GEMM (tokens on M) for per-group token
+    counts: int32 [units, 1 + paired, 5] of (first token row, valid rows,
+    first weight row, feature tile, shares-token-tile).  Host only."""
+    import numpy as np
+    c = np.ascontiguousarray(counts, dtype=np.int32)
+    lib = load_library()
+    n = lib.lmoe_gemm_unit_walk(len(c), c.ctypes.data, nfeat, int(paired), None, 0)
+    if n < 0:
+        raise LmoeError(n, "lmoe_gemm_unit_walk")
+    out = np.zeros((n, 1 + int(paired), 5), dtype=np.int32)
+    _check(min(0, lib.lmoe_gemm_unit_walk(len(c), c.ctypes.data, nfeat, int(paired),
+                                          out.ctypes.data, n)), "lmoe_gemm_unit_walk")
+    return out

@@ -308,7 +308,7 @@ using namespace lmoe;
 
 extern "C" {
 
-int lmoe_abi_version(void) { return 100; }
+int lmoe_abi_version(void) { return 101; }
 
 const char* lmoe_status_string(int status) {
   switch (status) {

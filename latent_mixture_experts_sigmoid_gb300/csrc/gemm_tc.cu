@@ -45,6 +45,7 @@
 #include <cuda.h>
 
 #include <mutex>
+#include <vector>
 
 #include "lmoe_internal.cuh"
 #include "gemm_tc.cuh"
@@ -230,11 +231,24 @@ struct GroupTables {
   const int* pairs;    // [G+1] prefix of tiles * nfeat / 2 (CTA pairs only)
 };
 
+// Ints of shared memory the grouped tables take.
+__host__ __device__ constexpr int group_table_ints(int G) { return 4 * G + 2; }
+
+// Largest i in [0, n) with a[i] <= v (a non-decreasing, a[0] <= v).
+__host__ __device__ __forceinline__ int last_leq(const int* a, int n, int v) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a[mid] <= v) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // Work units of one CTA: with multicast a unit is a pair of token tiles (one
 // per CTA of the cluster), so both CTAs walk the same unit sequence.
 template <bool kPairs>
-__device__ __forceinline__ int total_units(const GemmParams& p, const GroupTables& gt_tab,
-                                           int tok_tile, int nfeat) {
+__host__ __device__ __forceinline__ int total_units(const GemmParams& p, const GroupTables& gt_tab,
+                                                    int tok_tile, int nfeat) {
   if (kPairs && p.tile_prefix) return gt_tab.pairs[p.num_groups];
   const int tiles = p.tile_prefix ? gt_tab.prefix[p.num_groups]
                                   : (p.T_dense + tok_tile - 1) / tok_tile;
@@ -249,9 +263,9 @@ __device__ __forceinline__ int total_units(const GemmParams& p, const GroupTable
 constexpr int kBand = 8;
 
 template <bool kPairs>
-__device__ __forceinline__ Unit decode_unit(const GemmParams& p, const GroupTables& gt_tab, int u,
-                                            int tok_tile, int feat_tile, int nfeat, int nkb,
-                                            int rank) {
+__host__ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const GroupTables& gt_tab,
+                                                     int u, int tok_tile, int feat_tile, int nfeat,
+                                                     int nkb, int rank) {
   Unit x;
   x.shareA = 0;
   x.split = u % p.splits;
@@ -264,12 +278,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const GroupTabl
     // tiles 2j + rank
     int t, j = v;
     if (p.tile_prefix) {
-      int lo = 0, hi = p.num_groups - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (gt_tab.pairs[mid] <= v) lo = mid; else hi = mid - 1;
-      }
-      g = lo;
+      g = last_leq(gt_tab.pairs, p.num_groups, v);
       j = v - gt_tab.pairs[g];
       t = gt_tab.prefix[g + 1] - gt_tab.prefix[g];
       count = gt_tab.count[g];
@@ -299,12 +308,7 @@ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const GroupTabl
   } else if (p.tile_prefix) {
     x.feat_tile = v % nfeat;
     const int gt = v / nfeat;
-    int lo = 0, hi = p.num_groups - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (gt_tab.prefix[mid] <= gt) lo = mid; else hi = mid - 1;
-    }
-    g = lo;
+    g = last_leq(gt_tab.prefix, p.num_groups, gt);
     t_in_g = gt - gt_tab.prefix[g];
     count = gt_tab.count[g];
     first = gt_tab.first[g];
@@ -344,12 +348,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   // bars: full[S], empty[S], tfull[2], tempty[2], done
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int* tab = reinterpret_cast<int*>(tmem_holder + 4);   // grouped: prefix | count | first | pairs
+  // grouped: prefix | count | first | pairs
+  int* tab = reinterpret_cast<int*>(tmem_holder + 4);
   GroupTables tabs{tab, tab + p.num_groups + 1, tab + 2 * p.num_groups + 1,
                    tab + 3 * p.num_groups + 1};
   // epilogue staging: 4 warps x [32 rows][32 fp32], 16-byte chunks XOR-swizzled by row
   float* stage_out = reinterpret_cast<float*>(
-      (reinterpret_cast<uintptr_t>(tab + (p.tile_prefix ? 4 * p.num_groups + 2 : 0)) + 15) &
+      (reinterpret_cast<uintptr_t>(tab + (p.tile_prefix ? group_table_ints(p.num_groups) : 0)) +
+       15) &
       ~uintptr_t(15));
 
   const int warp = threadIdx.x >> 5;
@@ -802,7 +808,8 @@ int max_pairs_resident(size_t smem) {
 // on M only) the epilogue staging buffers; at most 227 KB
 size_t smem_for(int bn, int stages, int groups, int tok_on_m) {
   const size_t stage = (size_t)BM * BK * 2 + (size_t)bn * BK * 2;
-  return 1024 + stages * stage + (2 * stages + 5) * 8 + 16 + (size_t)(4 * groups + 2) * 4 + 16 +
+  return 1024 + stages * stage + (2 * stages + 5) * 8 + 16 +
+         (groups ? (size_t)group_table_ints(groups) * 4 : 0) + 16 +
          (tok_on_m ? 4 * 32 * 32 * 4 : 0);
 }
 
@@ -880,3 +887,53 @@ int read_device_error(int clear) {
 }
 
 }  // namespace lmoe
+
+extern "C" int lmoe_gemm_unit_walk(int G, const int* count, int nfeat, int paired, int* out,
+                                   int max_units) {
+  using namespace lmoe;
+  if (G < 1 || G > 1024 || !count || nfeat < 1 || (paired != 0 && paired != 1) ||
+      (paired && nfeat % 2) || max_units < 0)
+    return LMOE_ERR_DIM;
+  // the tables the kernel builds in its prologue, built here in order
+  std::vector<int> tab(group_table_ints(G));
+  int* prefix = tab.data();
+  int* cnt = prefix + G + 1;
+  int* first = cnt + G;
+  int* pairs = first + G;
+  prefix[0] = pairs[0] = 0;
+  long long row = 0;
+  for (int g = 0; g < G; ++g) {
+    if (count[g] < 0) return LMOE_ERR_DIM;
+    const int t = (count[g] + BM - 1) / BM;
+    cnt[g] = count[g];
+    first[g] = (int)row;
+    row += count[g];
+    prefix[g + 1] = prefix[g] + t;
+    pairs[g + 1] = pairs[g] + t * nfeat / 2;
+  }
+  if (row > (1LL << 30)) return LMOE_ERR_DIM;
+  GemmParams p{};
+  p.tok_on_m = 1;
+  p.bn = 256;
+  p.M_feat = 256 * nfeat;
+  p.num_groups = G;
+  p.tile_prefix = prefix;   // marks the grouped walk; the walk reads the tables only
+  p.splits = 1;
+  const GroupTables tabs{prefix, cnt, first, pairs};
+  const int U = paired ? total_units<true>(p, tabs, BM, nfeat)
+                       : total_units<false>(p, tabs, BM, nfeat);
+  if (!out) return U;
+  const int nr = 1 + paired;
+  for (int u = 0; u < U && u < max_units; ++u)
+    for (int r = 0; r < nr; ++r) {
+      const Unit x = paired ? decode_unit<true>(p, tabs, u, BM, 256, nfeat, 1, r)
+                            : decode_unit<false>(p, tabs, u, BM, 256, nfeat, 1, r);
+      int* o = out + ((size_t)u * nr + r) * 5;
+      o[0] = x.tok_row0;
+      o[1] = x.nvalid;
+      o[2] = x.w_row0;
+      o[3] = x.feat_tile;
+      o[4] = x.shareA;
+    }
+  return U;
+}

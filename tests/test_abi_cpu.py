@@ -44,7 +44,7 @@ def test_status_strings(lib):
     for st in range(-7, 1):
         assert lib.lmoe_status_string(st)
     assert lib.lmoe_status_string(-99) == b"unknown status"
-    assert lib.lmoe_abi_version() == 100
+    assert lib.lmoe_abi_version() == 101
 
 
 def test_route_validation(lib):
