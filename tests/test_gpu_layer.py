@@ -90,6 +90,27 @@ def test_tiny_layer_variants(variant):
     tiny_case(d, seed=11, **kw)
 
 
+@pytest.mark.parametrize("T", [8, 300])
+def test_tiny_layer_max_experts_and_topk(T):
+    # the largest expert count and top-k the library accepts (1024, 32), in the
+    # decode (fused permutation + scatter) and prefill regimes
+    tiny_case(dataclasses.replace(W.TINY, T=T, num_experts=1024, topk=32), seed=5)
+
+
+def test_zero_tokens_is_a_no_op():
+    from tests.gpu_util import DEV, weights_to_device
+    d = dataclasses.replace(W.TINY, T=0)
+    assert lm.latent_moe_launch_count(d) == 0
+    wdev = weights_to_device(W.layer_weights(W.TINY, 0))
+    x = torch.empty((0, d.hidden), dtype=torch.bfloat16, device=DEV)
+    lg = torch.empty((0, d.num_experts), dtype=torch.float32, device=DEV)
+    out = torch.empty((0, d.hidden), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(max(256, lm.latent_moe_workspace_bytes(d)), dtype=torch.uint8, device=DEV)
+    lm.latent_moe_forward(d, wdev, x, lg, out, ws)
+    torch.cuda.synchronize()
+    assert lm.lmoe_device_error() == 0
+
+
 @pytest.fixture(scope="module")
 def big_weights():
     from tests.gpu_util import device_layer_weights, oracle_layer_weights
