@@ -217,6 +217,24 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* weights,
                        lmoe_bf16* out, void* workspace, size_t workspace_bytes,
                        const lmoe_debug* dbg, void* stream);
 
+/* The layer forward on a routing done ahead of it (pre-routing: the         */
+/* TensorRT-LLM PR #20541 launches the routing of a decode step early on its */
+/* own stream and the MoE layer consumes its result after an event join).    */
+/* topk_ids [T, k] int32 and topk_weights [T, k] fp32 as moe_route writes    */
+/* them (same dims; the weights already renormalised and scaled) replace     */
+/* router_logits; the layer skips its routing kernel and otherwise runs as    */
+/* latent_moe_forward (same arguments, workspace and errors; one launch      */
+/* fewer than latent_moe_launch_count).  The routing must be complete on the */
+/* GPU before the call's work starts (same stream, or an event the caller    */
+/* waits on).  The ids of a token must be distinct, as moe_route writes     */
+/* them.  An id outside [0, E) is read as expert 0 and the device error word */
+/* records 7 (the output is then wrong, but no memory outside the call's     */
+/* buffers is touched).                                                       */
+int latent_moe_forward_routed(const lmoe_dims* dims, const lmoe_weights* weights,
+                              const lmoe_bf16* hidden, const int32_t* topk_ids,
+                              const float* topk_weights, lmoe_bf16* out, void* workspace,
+                              size_t workspace_bytes, const lmoe_debug* dbg, void* stream);
+
 /* The layer forward without a caller workspace.  The pages have no          */
 /* counterpart to this entry point; it exists for callers that cannot         */
 /* allocate device memory: a plugin that an inference runtime calls with only */
@@ -258,7 +276,10 @@ int lmoe_linear(const lmoe_bf16* x, const lmoe_bf16* w, const lmoe_bf16* add, lm
 const char* lmoe_status_string(int status);
 
 /* Reads (and with clear != 0 resets) the device error word of the current    */
-/* device.  0 = no bounded wait has given up.  Synchronises the device.      */
+/* device: 0 = nothing went wrong; 1-6 = a bounded wait of the tensor-core    */
+/* GEMM gave up; 7 = latent_moe_forward_routed met an expert id outside      */
+/* [0, E).  The first code written stays until cleared.  Synchronises the    */
+/* device.                                                                    */
 /* Returns the word, or LMOE_ERR_CUDA if it cannot be read.                   */
 int lmoe_device_error(int clear);
 

@@ -5,6 +5,7 @@ marshal torch tensors (device memory, streams) into the library.
 """
 from ._binding import (  # noqa: F401
     ABI_FUNCTIONS, LIB_PATH, LmoeDebug, LmoeDims, LmoeError, LmoeWeights, latent_moe_forward, latent_moe_forward_noalloc,
+    latent_moe_forward_routed,
     latent_moe_launch_count, latent_moe_workspace_offsets, NUM_STAGES, STAGE_NAMES, WS_NAMES,
     latent_moe_workspace_bytes, lmoe_abi_version, lmoe_linear, lmoe_device_error, load_library, make_dims,
     make_weights, masked_situ_and_mul, moe_route, situ_and_mul, status_string, gemm_unit_walk,

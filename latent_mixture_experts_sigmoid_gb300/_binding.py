@@ -25,6 +25,7 @@ LMOE_ERR_CUDA = -6
 LMOE_ERR_ALIGN = -7
 
 ABI_FUNCTIONS = ("moe_route", "situ_and_mul", "masked_situ_and_mul", "latent_moe_forward",
+                 "latent_moe_forward_routed",
                  "latent_moe_forward_noalloc", "latent_moe_workspace_bytes", "latent_moe_workspace_offsets",
                  "latent_moe_launch_count", "lmoe_linear", "lmoe_status_string",
                  "lmoe_device_error", "lmoe_abi_version", "lmoe_gemm_unit_walk")
@@ -96,6 +97,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.latent_moe_forward.argtypes = [ctypes.POINTER(LmoeDims), ctypes.POINTER(LmoeWeights), vp,
                                        vp, vp, vp, ctypes.c_size_t, ctypes.POINTER(LmoeDebug), vp]
     lib.latent_moe_forward.restype = i32
+    lib.latent_moe_forward_routed.argtypes = [ctypes.POINTER(LmoeDims), ctypes.POINTER(LmoeWeights),
+                                              vp, vp, vp, vp, vp, ctypes.c_size_t,
+                                              ctypes.POINTER(LmoeDebug), vp]
+    lib.latent_moe_forward_routed.restype = i32
     lib.lmoe_linear.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp]
     lib.lmoe_linear.restype = i32
     lib.lmoe_status_string.argtypes = [i32]
@@ -198,25 +203,49 @@ def latent_moe_forward(dims, weights, hidden, router_logits, out, workspace,
     ww = weights if isinstance(weights, LmoeWeights) else make_weights(weights)
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
-    dbg = None
-    if debug:
-        ev = debug.get("stage_events")
-        ev_arr = None
-        if ev is not None:
-            for e in ev:                  # torch creates the CUDA event on first record
-                if not e.cuda_event:
-                    e.record()
-            ev_arr = (ctypes.c_void_p * len(ev))(*[e.cuda_event for e in ev])
-        dbg = LmoeDebug(_ptr(debug.get("topk_ids")), _ptr(debug.get("topk_weights")),
-                        _ptr(debug.get("expert_num_tokens")), _ptr(debug.get("expert_offsets")),
-                        _ptr(debug.get("row_of")),
-                        ctypes.cast(ev_arr, ctypes.c_void_p) if ev_arr is not None else None)
+    dbg, keep = _debug_struct(debug)
     st = load_library().latent_moe_forward(ctypes.byref(dd), ctypes.byref(ww), _ptr(hidden),
                                            _ptr(router_logits), _ptr(out), _ptr(workspace),
                                            int(workspace_bytes),
                                            ctypes.byref(dbg) if dbg is not None else None,
                                            _stream(stream))
     _check(st, "latent_moe_forward")
+
+
+def _debug_struct(debug):
+    """LmoeDebug for a dict of optional outputs (and the event array it points to)."""
+    if not debug:
+        return None, None
+    ev = debug.get("stage_events")
+    ev_arr = None
+    if ev is not None:
+        for e in ev:                  # torch creates the CUDA event on first record
+            if not e.cuda_event:
+                e.record()
+        ev_arr = (ctypes.c_void_p * len(ev))(*[e.cuda_event for e in ev])
+    dbg = LmoeDebug(_ptr(debug.get("topk_ids")), _ptr(debug.get("topk_weights")),
+                    _ptr(debug.get("expert_num_tokens")), _ptr(debug.get("expert_offsets")),
+                    _ptr(debug.get("row_of")),
+                    ctypes.cast(ev_arr, ctypes.c_void_p) if ev_arr is not None else None)
+    return dbg, ev_arr
+
+
+def latent_moe_forward_routed(dims, weights, hidden, topk_ids, topk_weights, out, workspace,
+                              workspace_bytes: int | None = None, debug: dict | None = None,
+                              stream=None):
+    """The layer forward on routing done ahead (topk_ids [T,k] int32 and
+    topk_weights [T,k] fp32 as moe_route writes them); skips the routing kernel."""
+    dd = dims if isinstance(dims, LmoeDims) else make_dims(dims)
+    ww = weights if isinstance(weights, LmoeWeights) else make_weights(weights)
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    dbg, keep = _debug_struct(debug)
+    st = load_library().latent_moe_forward_routed(ctypes.byref(dd), ctypes.byref(ww), _ptr(hidden),
+                                                  _ptr(topk_ids), _ptr(topk_weights), _ptr(out),
+                                                  _ptr(workspace), int(workspace_bytes),
+                                                  ctypes.byref(dbg) if dbg is not None else None,
+                                                  _stream(stream))
+    _check(st, "latent_moe_forward_routed")
 
 
 def lmoe_linear(x, w, out, add=None, stream=None, T: int | None = None, N: int | None = None,

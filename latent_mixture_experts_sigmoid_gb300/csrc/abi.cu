@@ -408,21 +408,26 @@ size_t latent_moe_workspace_bytes(const lmoe_dims* dims) {
   return carve(*dims, nullptr, nullptr);
 }
 
-int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe_bf16* hidden,
-                       const float* router_logits, lmoe_bf16* out, void* workspace,
-                       size_t workspace_bytes, const lmoe_debug* dbg, void* stream) {
+// The layer forward.  Exactly one of router_logits (the layer routes) and
+// pre_ids/pre_w (routing done ahead by the caller) is given.
+static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe_bf16* hidden,
+                        const float* router_logits, const int32_t* pre_ids, const float* pre_w,
+                        lmoe_bf16* out, void* workspace, size_t workspace_bytes,
+                        const lmoe_debug* dbg, void* stream) {
   const int v = validate_dims(dims);
   if (v != LMOE_OK) return v;
   if (!wt) return LMOE_ERR_NULL;
   const lmoe_dims d = *dims;
   if (d.T == 0) return LMOE_OK;
-  if (!hidden || !router_logits || !out || !wt->w_down || !wt->w13 || !wt->w2 || !wt->w_up)
+  const bool pre_routed = router_logits == nullptr;
+  if (!hidden || (pre_routed && (!pre_ids || !pre_w)) || !out || !wt->w_down || !wt->w13 ||
+      !wt->w2 || !wt->w_up)
     return LMOE_ERR_NULL;
   const bool shared = wt->ws13 != nullptr;
   if (shared != (wt->ws2 != nullptr)) return LMOE_ERR_NULL;
   if (shared && d.shared_inter <= 0) return LMOE_ERR_DIM;
-  const void* ptrs[] = {hidden, router_logits, out, wt->w_down, wt->w13, wt->w2, wt->w_up,
-                        wt->ws13, wt->ws2, wt->norm_w, wt->e_score_correction_bias};
+  const void* ptrs[] = {hidden, router_logits, pre_ids, pre_w, out, wt->w_down, wt->w13, wt->w2,
+                        wt->w_up, wt->ws13, wt->ws2, wt->norm_w, wt->e_score_correction_bias};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return LMOE_ERR_ALIGN;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return LMOE_ERR_WORKSPACE;
@@ -438,6 +443,12 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
 
   cudaStream_t s = (cudaStream_t)stream;
   const int T = d.T, k = d.topk, E = d.num_experts, H = d.hidden, L = d.latent;
+  // the routing result: the layer's own, or the caller's (whose ids the
+  // permutation checks against [0, E), recording kErrExpertId)
+  const int32_t* ids = pre_routed ? pre_ids : ws.ids;
+  const float* topw = pre_routed ? pre_w : ws.w;
+  int* id_err = pre_routed ? device_error_word() : nullptr;
+  if (pre_routed && !id_err) return LMOE_ERR_CUDA;
   const int dI = d.inter, ds = d.shared_inter;
   const long long rows = (long long)T * k;
   const Plan pl = make_plan(d, num_sms());
@@ -505,14 +516,15 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
   // wave), and the caller's stream waits for them before the scatter (at
   // decode sizes this measured slower: they stay on the caller's stream)
   auto route_and_permute = [&](cudaStream_t rs, bool marks) -> int {
-    LMOE_TRY(launch_route(router_logits, wt->e_score_correction_bias, T, E, k, d.renormalize,
-                          d.routed_scaling_factor, ws.ids, ws.w, rs));
+    if (!pre_routed)
+      LMOE_TRY(launch_route(router_logits, wt->e_score_correction_bias, T, E, k, d.renormalize,
+                            d.routed_scaling_factor, ws.ids, ws.w, rs));
     if (marks && !mark(LMOE_STAGE_ROUTE + 1)) return LMOE_ERR_CUDA;
     return LMOE_OK;
   };
   auto permute = [&](cudaStream_t rs) -> int {
-    LMOE_TRY(launch_permute(ws.ids, T, k, E, tile, ws.perm_scratch, ws.counts, ws.offsets,
-                            ws.tile_prefix, ws.row_of, ws.tok_of_row, rs));
+    LMOE_TRY(launch_permute(ids, T, k, E, tile, ws.perm_scratch, ws.counts, ws.offsets,
+                            ws.tile_prefix, ws.row_of, ws.tok_of_row, id_err, rs));
     return LMOE_OK;
   };
   int st = LMOE_OK;
@@ -547,11 +559,11 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
   if (side_route) {
     if (cudaStreamWaitEvent(s, aux->routed, 0) != cudaSuccess) return LMOE_ERR_CUDA;
   } else if (fused_scatter) {
-    LMOE_TRY(launch_permute_scatter_small(ws.ids, T, k, E, tile, ws.counts, ws.offsets,
+    LMOE_TRY(launch_permute_scatter_small(ids, T, k, E, tile, ws.counts, ws.offsets,
                                           ws.tile_prefix, ws.row_of, ws.tok_of_row,
                                           down_split ? nullptr : ws.Z,
                                           down_split ? ws.Pa : nullptr, cdown.splits, down_stride,
-                                          L, ws.A, s));
+                                          L, ws.A, id_err, s));
   } else {
     st = permute(s);
     if (st != LMOE_OK) return st;
@@ -578,7 +590,7 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
   LMOE_TRY(gemm_grouped(wt->w2, E, L, ws.act, rows, dI, !decode, pl.g2_bn, ws, tile, ws.Y, s));
   if (!mark(LMOE_STAGE_GEMM2 + 1)) return LMOE_ERR_CUDA;
   // 8. combine + RMSNorm
-  LMOE_TRY(launch_combine_norm(ws.Y, ws.w, ws.row_of, T, k, L, wt->norm_w, d.rms_eps, ws.N, s));
+  LMOE_TRY(launch_combine_norm(ws.Y, topw, ws.row_of, T, k, L, wt->norm_w, d.rms_eps, ws.N, s));
   if (!mark(LMOE_STAGE_COMBINE + 1)) return LMOE_ERR_CUDA;
   // 12. up-projection with the shared output added in the epilogue
   const DenseCfg cup = pl.up;
@@ -606,9 +618,9 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
   // optional copies of the routing and permutation
   if (dbg) {
     if (dbg->topk_ids)
-      LMOE_TRY(cudaMemcpyAsync(dbg->topk_ids, ws.ids, rows * 4, cudaMemcpyDeviceToDevice, s));
+      LMOE_TRY(cudaMemcpyAsync(dbg->topk_ids, ids, rows * 4, cudaMemcpyDeviceToDevice, s));
     if (dbg->topk_weights)
-      LMOE_TRY(cudaMemcpyAsync(dbg->topk_weights, ws.w, rows * 4, cudaMemcpyDeviceToDevice, s));
+      LMOE_TRY(cudaMemcpyAsync(dbg->topk_weights, topw, rows * 4, cudaMemcpyDeviceToDevice, s));
     if (dbg->expert_num_tokens)
       LMOE_TRY(cudaMemcpyAsync(dbg->expert_num_tokens, ws.counts, (size_t)E * 4,
                                cudaMemcpyDeviceToDevice, s));
@@ -619,6 +631,21 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
       LMOE_TRY(cudaMemcpyAsync(dbg->row_of, ws.row_of, rows * 4, cudaMemcpyDeviceToDevice, s));
   }
   return LMOE_OK;
+}
+
+int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe_bf16* hidden,
+                       const float* router_logits, lmoe_bf16* out, void* workspace,
+                       size_t workspace_bytes, const lmoe_debug* dbg, void* stream) {
+  return forward_impl(dims, wt, hidden, router_logits, nullptr, nullptr, out, workspace,
+                      workspace_bytes, dbg, stream);
+}
+
+int latent_moe_forward_routed(const lmoe_dims* dims, const lmoe_weights* wt,
+                              const lmoe_bf16* hidden, const int32_t* topk_ids,
+                              const float* topk_weights, lmoe_bf16* out, void* workspace,
+                              size_t workspace_bytes, const lmoe_debug* dbg, void* stream) {
+  return forward_impl(dims, wt, hidden, nullptr, topk_ids, topk_weights, out, workspace,
+                      workspace_bytes, dbg, stream);
 }
 
 }  // extern "C"

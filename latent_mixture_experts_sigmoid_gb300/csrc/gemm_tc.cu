@@ -65,6 +65,7 @@ constexpr long long kWaitCycles = 1ll << 32;   // ~2 s at 2 GHz
 // error codes written to g_device_error
 enum : int { kErrProducer = 1, kErrMmaFull = 2, kErrMmaTmem = 3, kErrEpilogue = 4,
              kErrDrain = 5, kErrDone = 6 };
+static_assert(kErrExpertId > kErrDone, "error codes are distinct");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -873,6 +874,20 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
   if (g.tok_on_m)
     return launch_k(gemm_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, stream, mx, mw, p);
   return launch_k(gemm_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, stream, mw, mx, p);
+}
+
+int* device_error_word() {
+  static int* cache[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<int*>(p);
+  }
+  return cache[dev];
 }
 
 int read_device_error(int clear) {

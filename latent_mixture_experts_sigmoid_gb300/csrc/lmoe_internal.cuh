@@ -13,6 +13,14 @@ namespace lmoe {
 
 constexpr int kNumSmsDefault = 152;
 
+// Codes of the device error word (the first one written stays): 1-6 are the
+// tensor-core GEMM's bounded waits; kErrExpertId is an expert id outside
+// [0, E) handed to the pre-routed forward.
+constexpr int kErrExpertId = 7;
+
+// Device address of the error word of the current device.
+int* device_error_word();
+
 // ---------------------------------------------------------------------------
 // bf16 <-> fp32 on raw 16-bit patterns (round to nearest even on the way down)
 // ---------------------------------------------------------------------------

@@ -25,10 +25,21 @@ namespace {
 constexpr int kBlkTok = 256;     // tokens per permutation block
 constexpr int kWords = kBlkTok / 32;
 
+// Expert id of pair i.  Ids the library did not write itself (the pre-routed
+// forward) may be out of range: such an id is read as expert 0, the same way
+// by every pass, and the device error word records kErrExpertId.
+__device__ __forceinline__ int expert_id(const int32_t* __restrict__ ids, long long i, int E,
+                                         int* err) {
+  const int e = __ldg(ids + i);
+  if ((unsigned)e < (unsigned)E) return e;
+  if (err) atomicCAS(err, 0, kErrExpertId);
+  return 0;
+}
+
 // ---- permutation, pass 1: bitmaps and per-block counts -----------------------
 __global__ void __launch_bounds__(kBlkTok)
 perm_count_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
-                  uint32_t* __restrict__ bitmaps, int32_t* __restrict__ blk_cnt) {
+                  uint32_t* __restrict__ bitmaps, int32_t* __restrict__ blk_cnt, int* err) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ uint32_t bm[];   // [E][kWords]
@@ -38,7 +49,7 @@ perm_count_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
   const int t = b * kBlkTok + threadIdx.x;
   if (t < T) {
     for (int j = 0; j < k; ++j) {
-      const int e = __ldg(ids + (long long)t * k + j);
+      const int e = expert_id(ids, (long long)t * k + j, E, err);
       atomicOr(&bm[e * kWords + (threadIdx.x >> 5)], 1u << (threadIdx.x & 31));
     }
   }
@@ -123,7 +134,7 @@ __global__ void __launch_bounds__(1024)
 perm_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int tile,
                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                   int32_t* __restrict__ tile_prefix, int32_t* __restrict__ row_of,
-                  int32_t* __restrict__ tok_of_row) {
+                  int32_t* __restrict__ tok_of_row, int* err) {
   pdl_trigger();
   pdl_wait();
   __shared__ uint32_t bm[1024 * kWords];
@@ -134,7 +145,7 @@ perm_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int tile
   const int t = threadIdx.x;
   if (t < T) {
     for (int j = 0; j < k; ++j) {
-      const int e = __ldg(ids + (long long)t * k + j);
+      const int e = expert_id(ids, (long long)t * k + j, E, err);
       atomicOr(&bm[e * kWords + (t >> 5)], 1u << (t & 31));
     }
   }
@@ -163,7 +174,7 @@ perm_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int tile
     const int w = t >> 5;
     const uint32_t below = (1u << (t & 31)) - 1u;
     for (int j = 0; j < k; ++j) {
-      const int ej = __ldg(ids + (long long)t * k + j);
+      const int ej = expert_id(ids, (long long)t * k + j, E, nullptr);
       const uint32_t* m = bm + ej * kWords;
       int rank = __popc(m[w] & below);
       for (int i = 0; i < w; ++i) rank += __popc(m[i]);
@@ -189,7 +200,7 @@ perm_rows_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
   const int w = tl >> 5;
   const uint32_t below = (1u << (tl & 31)) - 1u;
   for (int j = 0; j < k; ++j) {
-    const int e = __ldg(ids + (long long)t * k + j);
+    const int e = expert_id(ids, (long long)t * k + j, E, nullptr);
     const uint32_t* m = gbm + e * kWords;
     int rank = __popc(__ldg(m + w) & below);
     for (int i = 0; i < w; ++i) rank += __popc(__ldg(m + i));
@@ -212,7 +223,7 @@ perm_scatter_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, 
                           int32_t* __restrict__ tile_prefix, int32_t* __restrict__ row_of,
                           int32_t* __restrict__ tok_of_row, const uint16_t* __restrict__ Zb,
                           const float* __restrict__ Zp, int S, long long split_stride, int L,
-                          uint16_t* __restrict__ A) {
+                          uint16_t* __restrict__ A, int* err) {
   pdl_trigger();
   pdl_wait();
   __shared__ uint32_t bm[1024 * kWords];
@@ -224,7 +235,7 @@ perm_scatter_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, 
   if ((int)threadIdx.x < T) {
     const int tt = threadIdx.x;
     for (int j = 0; j < k; ++j) {
-      const int e = __ldg(ids + (long long)tt * k + j);
+      const int e = expert_id(ids, (long long)tt * k + j, E, blockIdx.x == 0 ? err : nullptr);
       atomicOr(&bm[e * kWords + (tt >> 5)], 1u << (tt & 31));
     }
   }
@@ -254,7 +265,7 @@ perm_scatter_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, 
   const int t = blockIdx.x;
   if ((int)threadIdx.x < k) {
     const int j = threadIdx.x;
-    const int ej = __ldg(ids + (long long)t * k + j);
+    const int ej = expert_id(ids, (long long)t * k + j, E, nullptr);
     const uint32_t* m = bm + ej * kWords;
     const int w = t >> 5;
     int rank = __popc(m[w] & ((1u << (t & 31)) - 1u));
@@ -485,11 +496,11 @@ size_t permute_scratch_bytes(int T, int E) {
 
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int tile, void* scratch,
                            int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
-                           int32_t* row_of, int32_t* tok_of_row, cudaStream_t s) {
+                           int32_t* row_of, int32_t* tok_of_row, int* err, cudaStream_t s) {
   const int nblk = (T + kBlkTok - 1) / kBlkTok;
   if (nblk == 1)
     return launch_k(perm_small_kernel, dim3(1), dim3(1024), 0, s, ids, T, k, E, tile, counts,
-                    offsets, tile_prefix, row_of, tok_of_row);
+                    offsets, tile_prefix, row_of, tok_of_row, err);
   uint32_t* bitmaps = reinterpret_cast<uint32_t*>(scratch);
   int32_t* blk_cnt = reinterpret_cast<int32_t*>(bitmaps + (size_t)nblk * E * kWords);
   int32_t* blk_base = blk_cnt + (size_t)nblk * E;
@@ -497,7 +508,8 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int tile, vo
   cudaError_t e = cudaFuncSetAttribute(perm_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)sm);
   if (e != cudaSuccess) return e;
-  e = launch_k(perm_count_kernel, dim3(nblk), dim3(kBlkTok), sm, s, ids, T, k, E, bitmaps, blk_cnt);
+  e = launch_k(perm_count_kernel, dim3(nblk), dim3(kBlkTok), sm, s, ids, T, k, E, bitmaps, blk_cnt,
+               err);
   if (e != cudaSuccess) return e;
   e = launch_k(perm_scan_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)blk_cnt, nblk, E,
                tile, blk_base, counts, offsets, tile_prefix);
@@ -510,10 +522,10 @@ cudaError_t launch_permute_scatter_small(const int32_t* ids, int T, int k, int E
                                          int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
                                          int32_t* row_of, int32_t* tok_of_row, const uint16_t* Zb,
                                          const float* Zp, int S, long long split_stride, int L,
-                                         uint16_t* A, cudaStream_t s) {
+                                         uint16_t* A, int* err, cudaStream_t s) {
   if (T > kBlkTok || E > 1024 || k > 32) return cudaErrorInvalidValue;
   return launch_k(perm_scatter_small_kernel, dim3(T), dim3(1024), 0, s, ids, T, k, E, tile, counts,
-                  offsets, tile_prefix, row_of, tok_of_row, Zb, Zp, S, split_stride, L, A);
+                  offsets, tile_prefix, row_of, tok_of_row, Zb, Zp, S, split_stride, L, A, err);
 }
 
 cudaError_t launch_scatter_rows(const uint16_t* Zb, const float* Zp, int S, long long split_stride,

@@ -10,10 +10,12 @@ namespace lmoe {
 size_t permute_scratch_bytes(int T, int E);
 
 // ids [T,k] -> counts [E], offsets [E+1], tile_prefix [E+1] (prefix of
-// ceil(count/tile)), row_of [T,k], tok_of_row [T*k].  E <= 1024.
+// ceil(count/tile)), row_of [T,k], tok_of_row [T*k].  E <= 1024.  An id
+// outside [0, E) is read as 0 and, if err is given, recorded there
+// (kErrExpertId) by the first pass.
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int tile, void* scratch,
                            int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
-                           int32_t* row_of, int32_t* tok_of_row, cudaStream_t s);
+                           int32_t* row_of, int32_t* tok_of_row, int* err, cudaStream_t s);
 
 // launch_permute followed by launch_scatter_rows in one launch of T blocks,
 // for T <= 256, E <= 1024, k <= 32 (the small-T path).
@@ -21,7 +23,7 @@ cudaError_t launch_permute_scatter_small(const int32_t* ids, int T, int k, int E
                                          int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
                                          int32_t* row_of, int32_t* tok_of_row, const uint16_t* Zb,
                                          const float* Zp, int S, long long split_stride, int L,
-                                         uint16_t* A, cudaStream_t s);
+                                         uint16_t* A, int* err, cudaStream_t s);
 
 // A[row_of[t,j]] = Z[t] for j < k; Z from bf16 rows Zb or from the sum of S
 // fp32 partials Zp (split_stride elements apart).  L % 8 == 0.

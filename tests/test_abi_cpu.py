@@ -105,6 +105,15 @@ def test_layer_validation_and_workspace(lib):
     z.T = 0
     assert lib.latent_moe_forward(ctypes.byref(z), ctypes.byref(w), None, None, None, None, 0,
                                   None, None) == 0
+    # pre-routed form: ids and weights replace the logits
+    fr = lib.latent_moe_forward_routed
+    assert fr(ctypes.byref(d), ctypes.byref(w2), p, None, p, p, p, n, None, None) == -1
+    assert fr(ctypes.byref(d), ctypes.byref(w2), p, p, None, p, p, n, None, None) == -1
+    assert fr(ctypes.byref(d), ctypes.byref(w2), p, ctypes.c_void_p(260), p, p, p, n, None,
+              None) == -7
+    assert fr(ctypes.byref(d), ctypes.byref(w2), p, p, p, p, ctypes.c_void_p(272), n, None,
+              None) == -5
+    assert fr(ctypes.byref(z), ctypes.byref(w), None, None, None, None, None, 0, None, None) == 0
 
 
 def test_linear_validation(lib):

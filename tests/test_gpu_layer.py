@@ -111,6 +111,63 @@ def test_zero_tokens_is_a_no_op():
     assert lm.lmoe_device_error() == 0
 
 
+def _routed_case(T, seed=3):
+    from tests.gpu_util import DEV, weights_to_device, dev_bf16, dev_f32
+    d = dataclasses.replace(W.TINY, T=T)
+    wdev = weights_to_device(W.layer_weights(d, seed))
+    x = dev_bf16(W.hidden_states(d, seed))
+    lg = dev_f32(W.router_logits(d.T, d.num_experts, seed))
+    ids = torch.empty((T, d.topk), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, d.topk), dtype=torch.float32, device=DEV)
+    return d, wdev, x, lg, ids, w
+
+
+@pytest.mark.parametrize("T", [8, 300])
+def test_pre_routed_forward_is_bit_identical(T):
+    # TensorRT-LLM PR #20541, commit 1: the routing runs as its own op on
+    # another stream and the MoE op consumes its outputs after an event join;
+    # the output is bit-identical to the op routing itself
+    from tests.gpu_util import DEV
+    d, wdev, x, lg, ids, w = _routed_case(T)
+    ws = torch.empty(lm.latent_moe_workspace_bytes(d), dtype=torch.uint8, device=DEV)
+    ref = torch.empty((T, d.hidden), dtype=torch.bfloat16, device=DEV)
+    lm.latent_moe_forward(d, wdev, x, lg, ref, ws)
+    side, main = torch.cuda.Stream(), torch.cuda.Stream()
+    routed = torch.cuda.Event()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        lm.moe_route(lg, wdev["bias"], d.topk, d.routed_scaling_factor, ids, w,
+                     renormalize=d.renormalize, stream=side)
+        routed.record(side)
+    out = torch.empty_like(ref)
+    ws2 = torch.empty_like(ws)
+    main.wait_event(routed)
+    with torch.cuda.stream(main):
+        lm.latent_moe_forward_routed(d, wdev, x, ids, w, out, ws2, stream=main)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert lm.lmoe_device_error() == 0
+
+
+@pytest.mark.parametrize("T", [8, 300])
+def test_pre_routed_out_of_range_id_is_recorded(T):
+    # an expert id outside [0, E) is read as expert 0 (no access outside the
+    # buffers) and recorded as code 7 in the device error word
+    from tests.gpu_util import DEV
+    d, wdev, x, lg, ids, w = _routed_case(T)
+    lm.moe_route(lg, wdev["bias"], d.topk, d.routed_scaling_factor, ids, w,
+                 renormalize=d.renormalize)
+    ids[T // 2, 1] = d.num_experts + 5
+    ids[T - 1, 0] = -1
+    ws = torch.empty(lm.latent_moe_workspace_bytes(d), dtype=torch.uint8, device=DEV)
+    out = torch.empty((T, d.hidden), dtype=torch.bfloat16, device=DEV)
+    assert lm.lmoe_device_error(clear=True) == 0
+    lm.latent_moe_forward_routed(d, wdev, x, ids, w, out, ws)
+    torch.cuda.synchronize()
+    assert lm.lmoe_device_error(clear=True) == 7
+    assert lm.lmoe_device_error() == 0
+
+
 @pytest.fixture(scope="module")
 def big_weights():
     from tests.gpu_util import device_layer_weights, oracle_layer_weights
