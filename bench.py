@@ -37,6 +37,10 @@ import workloads as W  # noqa: E402
 
 METRIC = "latent-MoE layer tokens/s at T=8 and T=4096; % of HBM / bf16 TC roofline"
 UNIT = "tokens/s"
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum, one ncu capture) of
+# the six GEMM launches of one prefill forward of this workload, summed; valid
+# for the GEMM kernel as it was when captured, and for this workload only.
+GEMM_SET_DRAM_BYTES = 2271430912
 
 
 def peaks():
@@ -419,7 +423,10 @@ def run_ours(args, rank, world):
     roof = {"kernel": "gemm_tc_kernel (all GEMM launches of one prefill forward)",
             "bound": "tensor", "achieved": round(ach_tf, 1), "peak": pk["bf16_sus"],
             "unit": "TFLOP/s", "frac": round(ach_tf / pk["bf16_sus"], 4),
-            "peak_source": f"{pk['source']} bf16 sustained", "traffic": None,
+            "peak_source": f"{pk['source']} bf16 sustained",
+            "traffic": GEMM_SET_DRAM_BYTES,
+            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the six GEMM "
+                              "launches of one prefill forward (algorithmic: 2042.8 MB)",
             "flops_per_launch_set": fl["total"], "ms_per_launch_set": round(gemm_ms, 4)}
     per_stage_pre = {n: round(v, 4) for n, v in st.items()}
     per_stage_dec = {n: round(v, 4) for n, v in zip(names, dec["per_stage"])}
