@@ -35,12 +35,15 @@ def check_routing_and_permutation(d, dbg, logits, bias):
     assert np.array_equal(dbg["row_of"], row_of)
 
 
-def tiny_case(d, seed=0, gamma_noise=False, shared=True, zipf=False):
+def tiny_case(d, seed=0, gamma_noise=False, shared=True, zipf=False, defaults=False):
     from tests.gpu_util import (weights_to_device, run_layer, host_bits, assert_layer_close,
                                 addend_scale)
     wts = W.layer_weights(d, seed, gamma_noise)
     if not shared:
         wts["ws13"] = wts["ws2"] = None
+    if defaults:
+        # the optional weights left out: gamma = ones, selection bias = zeros
+        wts["norm_w"] = wts["bias"] = None
     x = W.hidden_states(d, seed)
     lg = W.router_logits(d.T, d.num_experts, seed, zipf=zipf)
     out, dbg = run_layer(lm, d, weights_to_device(wts), x, lg)
@@ -63,7 +66,8 @@ def test_tiny_layer_token_counts(T):
 
 
 @pytest.mark.parametrize("variant", ["no_shared", "linear_beta_unset", "gamma_noise", "top1",
-                                     "no_renorm", "zipf_prefill", "wide", "pairs"])
+                                     "no_renorm", "zipf_prefill", "wide", "pairs",
+                                     "no_gamma_no_bias", "no_gamma_no_bias_prefill"])
 def test_tiny_layer_variants(variant):
     d = W.TINY
     kw = {}
@@ -83,6 +87,11 @@ def test_tiny_layer_variants(variant):
     elif variant == "wide":
         d = dataclasses.replace(d, T=200, hidden=384, latent=256, inter=192, shared_inter=320,
                                 num_experts=40, topk=8)
+    elif variant == "no_gamma_no_bias":
+        kw["defaults"] = True
+    elif variant == "no_gamma_no_bias_prefill":
+        d = dataclasses.replace(d, T=300)
+        kw["defaults"] = True
     elif variant == "pairs":
         # every GEMM in CTA pairs: even weight-tile counts everywhere, 5 token
         # tiles (the dense GEMMs' odd last tile is shared by two weight tiles)
