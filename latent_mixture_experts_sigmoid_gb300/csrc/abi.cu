@@ -1,16 +1,20 @@
 // The C ABI of liblmoe.so (declared in include/lmoe.h): argument validation,
 // the workspace layout and the schedule of kernels of one layer forward.
 //
-// Layer schedule (one stream, no host synchronisation), following the data
+// Layer schedule (no host synchronisation, no allocation), following the data
 // flow of the vLLM latent_moe_runner page (ROCmLatentMoERunner._fused_forward
-// and _shard_up_proj_tail) on one device, with the decode order of
-// TensorRT-LLM PR #20541, Commit 2:
+// and _shard_up_proj_tail) on one device, with the stream layout of
+// TensorRT-LLM PR #20541, Commit 2: the shared expert (steps 9-11) runs on a
+// second stream forked from and joined back to the caller's by events, and at
+// large T so do steps 1 and 3, beside the down-projection.  The pre-routed
+// entry point (that PR's Commit 1) skips step 1.
 //   1 route             ids, w                        (routing kernel)
 //   2 down-projection   Z = X W_down^T                (tcgen05 GEMM)
 //   3 permute           counts, offsets, row_of       (bitmap counting sort)
 //   4 scatter           A[row_of[t,j]] = bf16(Z[t])
 //   5 GEMM1 (grouped)   G = A W13_e^T                 (tcgen05 GEMM)
-//   6 SituGLU           act = SituGLU(G)
+//   6 SituGLU           act = SituGLU(G)              (in GEMM1's epilogue at
+//                                                      large T)
 //   7 GEMM2 (grouped)   Y = act W2_e^T                (tcgen05 GEMM)
 //   8 combine + norm    N = RMSNorm(sum_j w Y) * gamma
 //   9 shared GEMM1      Gs = X Ws13^T                 (tcgen05 GEMM)
@@ -21,12 +25,14 @@
 // Two regimes.  Small T (<= 128 tokens, decode): every GEMM puts the weight
 // rows on the MMA's M side and the tokens on N (16..128), dense GEMMs split K
 // so that all SMs stream weights, and the split partials are summed in a fixed
-// order by the consumer (the scatter of step 4, the SituGLU of step 10, and
-// the final reduction that also adds Sh).  Large T (prefill): tokens on M,
-// 128 x (128|256) tiles, no split, bf16 stored straight from the epilogue.
+// order by the consumer (the scatter of step 4, fused with the permutation of
+// step 3, the SituGLU of step 10, and the final reduction that also adds Sh).
+// Large T (prefill): tokens on M, 128 x (128|256) tiles (CTA pairs sharing
+// operand tiles), no split, bf16 stored straight from the epilogue.
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "gemm_tc.cuh"
@@ -36,16 +42,16 @@
 namespace lmoe {
 
 int num_sms() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];   // 0 = not queried yet
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kNumSmsDefault;
-  if (cache[dev] == 0) {
-    int n = 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       n = kNumSmsDefault;
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return n;
 }
 
 namespace {

@@ -36,6 +36,8 @@
 // sigmoid's own error (<= 3 ulp) and the rounding of the two bias additions
 // (<= 2^-23 |key|).  The kernels use 2D = 1e-5 + 2^-20 * max(|A|, 1), about
 // 2.5x that bound.
+#include <atomic>
+
 #include "lmoe_internal.cuh"
 
 namespace lmoe {
@@ -589,7 +591,12 @@ template <int C, bool VEC>
 cudaError_t launch_warp_tier(const float* logits, const float* bias, int T, int E, int k,
                              int renorm, float rsf, int32_t* ids, float* w, cudaStream_t s) {
   constexpr size_t smem = warp_kernel_smem<C, kRouteSlots>();
-  static int per_sm = 0;
+  // resident blocks per SM, per device (the shared-memory attribute is set on
+  // each device once, before its first launch)
+  static std::atomic<int> per_sm_of[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int per_sm = per_sm_of[dev].load(std::memory_order_relaxed);
   if (per_sm == 0) {
     int n = 0;
     if (cudaFuncSetAttribute(route_warp_kernel<C, VEC, kRouteSlots>,
@@ -600,6 +607,7 @@ cudaError_t launch_warp_tier(const float* logits, const float* bias, int T, int 
         n < 1)
       n = 1;
     per_sm = n;
+    per_sm_of[dev].store(n, std::memory_order_relaxed);
   }
   const long long need = ((long long)T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const long long cap = (long long)num_sms() * per_sm;
@@ -621,13 +629,17 @@ cudaError_t launch_block_tier(const float* logits, const float* bias, int T, int
                               int renorm, float rsf, int32_t* ids, float* w, cudaStream_t s) {
   // persistent: as many blocks as fit on the GPU at once loop over the tokens
   // (bias loaded once per block, next token's logits prefetched)
-  static int per_sm = 0;
+  static std::atomic<int> per_sm_of[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int per_sm = per_sm_of[dev].load(std::memory_order_relaxed);
   if (per_sm == 0) {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, route_block_kernel<EPL, W>, W * 32, 0) !=
             cudaSuccess || n < 1)
       n = 4;
     per_sm = n;
+    per_sm_of[dev].store(n, std::memory_order_relaxed);
   }
   const long long cap = (long long)num_sms() * per_sm;
   const int grid = (int)(T < cap ? T : cap);
