@@ -127,6 +127,32 @@ def _ptr(t) -> int | None:
     return t.data_ptr()
 
 
+_BF16 = (torch.bfloat16, torch.int16)   # bf16 values, or their raw 16-bit patterns
+
+
+def _dev(t, name: str, dtypes, numel: int) -> int | None:
+    """Device address of a tensor argument, after checking that the kernels can
+    access it as the C ABI describes: a contiguous tensor on the current CUDA
+    device, of one of `dtypes`, holding at least `numel` elements.  None and raw
+    integer addresses pass through unchecked (the caller vouches for them)."""
+    if t is None or isinstance(t, int):
+        return t
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch tensor, an address or None")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor (got device {t.device})")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name}: on {t.device}, but the current device is "
+                         f"cuda:{torch.cuda.current_device()}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.dtype not in (dtypes if isinstance(dtypes, tuple) else (dtypes,)):
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtypes}")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: {t.numel()} elements, needs at least {numel}")
+    return t.data_ptr()
+
+
 def _stream(stream) -> int | None:
     if stream is None:
         if torch.cuda.is_available():
@@ -148,10 +174,15 @@ def moe_route(router_logits, e_score_correction_bias, topk: int, routed_scaling_
     """Single-group sigmoid top-k routing; writes topk_ids [T,k] and topk_weights [T,k]."""
     if T is None:
         T, E = router_logits.shape
-    st = load_library().moe_route(_ptr(router_logits), _ptr(e_score_correction_bias), int(T),
-                                  int(E), int(topk), int(n_group), int(topk_group),
-                                  int(renormalize), float(routed_scaling_factor), _ptr(topk_ids),
-                                  _ptr(topk_weights), _stream(stream))
+    T, E, k = int(T), int(E), int(topk)
+    st = load_library().moe_route(_dev(router_logits, "router_logits", torch.float32, T * E),
+                                  _dev(e_score_correction_bias, "e_score_correction_bias",
+                                       torch.float32, E),
+                                  T, E, k, int(n_group), int(topk_group),
+                                  int(renormalize), float(routed_scaling_factor),
+                                  _dev(topk_ids, "topk_ids", torch.int32, T * k),
+                                  _dev(topk_weights, "topk_weights", torch.float32, T * k),
+                                  _stream(stream))
     _check(st, "moe_route")
 
 
@@ -161,7 +192,9 @@ def situ_and_mul(inp, out, beta: float, linear_beta: float, stream=None,
     if N is None:
         d = inp.shape[-1] // 2
         N = inp.numel() // (2 * d)
-    st = load_library().situ_and_mul(_ptr(inp), _ptr(out), int(N), int(d), float(beta),
+    N, d = int(N), int(d)
+    st = load_library().situ_and_mul(_dev(inp, "input", _BF16, N * 2 * d),
+                                      _dev(out, "out", _BF16, N * d), N, d, float(beta),
                                       float(linear_beta), _stream(stream))
     _check(st, "situ_and_mul")
 
@@ -169,10 +202,12 @@ def situ_and_mul(inp, out, beta: float, linear_beta: float, stream=None,
 def masked_situ_and_mul(inp, out, expert_num_tokens, beta: float, linear_beta: float,
                         stream=None, shape: tuple | None = None):
     """SituGLU over the batched [E, T_max, 2d] layout; padded rows untouched."""
-    E, T_max, two_d = shape if shape is not None else tuple(inp.shape)
-    st = load_library().masked_situ_and_mul(_ptr(inp), _ptr(out), _ptr(expert_num_tokens),
-                                            int(E), int(T_max), int(two_d // 2), float(beta),
-                                            float(linear_beta), _stream(stream))
+    E, T_max, two_d = (int(v) for v in (shape if shape is not None else tuple(inp.shape)))
+    st = load_library().masked_situ_and_mul(
+        _dev(inp, "input", _BF16, E * T_max * two_d),
+        _dev(out, "out", _BF16, E * T_max * (two_d // 2)),
+        _dev(expert_num_tokens, "expert_num_tokens", torch.int32, E),
+        E, T_max, two_d // 2, float(beta), float(linear_beta), _stream(stream))
     _check(st, "masked_situ_and_mul")
 
 
@@ -184,10 +219,33 @@ def make_dims(d) -> LmoeDims:
                     float(d.linear_beta), float(d.rms_eps))
 
 
-def make_weights(w: dict) -> LmoeWeights:
-    g = lambda k: _ptr(w.get(k))  # noqa: E731
-    return LmoeWeights(g("w_down"), g("w13"), g("w2"), g("ws13"), g("ws2"), g("norm_w"),
-                       g("w_up"), g("bias"))
+def make_weights(w: dict, dims=None) -> LmoeWeights:
+    """LmoeWeights from a dict of tensors (or addresses); with `dims` every
+    tensor is checked against the size lmoe_weights documents for it."""
+    if dims is None:
+        g = lambda k: _ptr(w.get(k))  # noqa: E731
+        return LmoeWeights(g("w_down"), g("w13"), g("w2"), g("ws13"), g("ws2"), g("norm_w"),
+                           g("w_up"), g("bias"))
+    H, L, E, dI, ds = (int(dims.hidden), int(dims.latent), int(dims.num_experts),
+                       int(dims.inter), int(dims.shared_inter))
+    need = {"w_down": L * H, "w13": E * 2 * dI * L, "w2": E * L * dI, "ws13": 2 * ds * H,
+            "ws2": H * ds, "norm_w": L, "w_up": H * L}
+    g = {k: _dev(w.get(k), k, _BF16, n) for k, n in need.items()}
+    return LmoeWeights(g["w_down"], g["w13"], g["w2"], g["ws13"], g["ws2"], g["norm_w"],
+                       g["w_up"], _dev(w.get("bias"), "bias", torch.float32, E))
+
+
+def _workspace(workspace, workspace_bytes):
+    """(address, byte count) of a workspace tensor, checked to hold the bytes
+    claimed for it (the whole tensor when workspace_bytes is None)."""
+    if workspace is None or isinstance(workspace, int):
+        return workspace, int(workspace_bytes or 0)
+    have = workspace.numel() * workspace.element_size()
+    n = have if workspace_bytes is None else int(workspace_bytes)
+    if n > have:
+        raise ValueError(f"workspace: {have} bytes, {n} claimed")
+    _dev(workspace, "workspace", (workspace.dtype,), 0)
+    return workspace.data_ptr(), n
 
 
 def latent_moe_workspace_bytes(dims) -> int:
@@ -200,22 +258,23 @@ def latent_moe_forward(dims, weights, hidden, router_logits, out, workspace,
                        stream=None):
     """The latent-MoE layer forward; writes out [T, hidden] bf16."""
     dd = dims if isinstance(dims, LmoeDims) else make_dims(dims)
-    ww = weights if isinstance(weights, LmoeWeights) else make_weights(weights)
-    if workspace_bytes is None:
-        workspace_bytes = workspace.numel() * workspace.element_size()
-    dbg, keep = _debug_struct(debug)
-    st = load_library().latent_moe_forward(ctypes.byref(dd), ctypes.byref(ww), _ptr(hidden),
-                                           _ptr(router_logits), _ptr(out), _ptr(workspace),
-                                           int(workspace_bytes),
-                                           ctypes.byref(dbg) if dbg is not None else None,
-                                           _stream(stream))
+    ww = weights if isinstance(weights, LmoeWeights) else make_weights(weights, dd)
+    T, H, E = int(dd.T), int(dd.hidden), int(dd.num_experts)
+    wsp, wsn = _workspace(workspace, workspace_bytes)
+    dbg, keep = _debug_struct(debug, dd)
+    st = load_library().latent_moe_forward(
+        ctypes.byref(dd), ctypes.byref(ww), _dev(hidden, "hidden", _BF16, T * H),
+        _dev(router_logits, "router_logits", torch.float32, T * E),
+        _dev(out, "out", _BF16, T * H), wsp, wsn,
+        ctypes.byref(dbg) if dbg is not None else None, _stream(stream))
     _check(st, "latent_moe_forward")
 
 
-def _debug_struct(debug):
+def _debug_struct(debug, dd):
     """LmoeDebug for a dict of optional outputs (and the event array it points to)."""
     if not debug:
         return None, None
+    T, k, E = int(dd.T), int(dd.topk), int(dd.num_experts)
     ev = debug.get("stage_events")
     ev_arr = None
     if ev is not None:
@@ -223,9 +282,11 @@ def _debug_struct(debug):
             if not e.cuda_event:
                 e.record()
         ev_arr = (ctypes.c_void_p * len(ev))(*[e.cuda_event for e in ev])
-    dbg = LmoeDebug(_ptr(debug.get("topk_ids")), _ptr(debug.get("topk_weights")),
-                    _ptr(debug.get("expert_num_tokens")), _ptr(debug.get("expert_offsets")),
-                    _ptr(debug.get("row_of")),
+    dbg = LmoeDebug(_dev(debug.get("topk_ids"), "topk_ids", torch.int32, T * k),
+                    _dev(debug.get("topk_weights"), "topk_weights", torch.float32, T * k),
+                    _dev(debug.get("expert_num_tokens"), "expert_num_tokens", torch.int32, E),
+                    _dev(debug.get("expert_offsets"), "expert_offsets", torch.int32, E + 1),
+                    _dev(debug.get("row_of"), "row_of", torch.int32, T * k),
                     ctypes.cast(ev_arr, ctypes.c_void_p) if ev_arr is not None else None)
     return dbg, ev_arr
 
@@ -236,15 +297,16 @@ def latent_moe_forward_routed(dims, weights, hidden, topk_ids, topk_weights, out
     """The layer forward on routing done ahead (topk_ids [T,k] int32 and
     topk_weights [T,k] fp32 as moe_route writes them); skips the routing kernel."""
     dd = dims if isinstance(dims, LmoeDims) else make_dims(dims)
-    ww = weights if isinstance(weights, LmoeWeights) else make_weights(weights)
-    if workspace_bytes is None:
-        workspace_bytes = workspace.numel() * workspace.element_size()
-    dbg, keep = _debug_struct(debug)
-    st = load_library().latent_moe_forward_routed(ctypes.byref(dd), ctypes.byref(ww), _ptr(hidden),
-                                                  _ptr(topk_ids), _ptr(topk_weights), _ptr(out),
-                                                  _ptr(workspace), int(workspace_bytes),
-                                                  ctypes.byref(dbg) if dbg is not None else None,
-                                                  _stream(stream))
+    ww = weights if isinstance(weights, LmoeWeights) else make_weights(weights, dd)
+    T, H, k = int(dd.T), int(dd.hidden), int(dd.topk)
+    wsp, wsn = _workspace(workspace, workspace_bytes)
+    dbg, keep = _debug_struct(debug, dd)
+    st = load_library().latent_moe_forward_routed(
+        ctypes.byref(dd), ctypes.byref(ww), _dev(hidden, "hidden", _BF16, T * H),
+        _dev(topk_ids, "topk_ids", torch.int32, T * k),
+        _dev(topk_weights, "topk_weights", torch.float32, T * k),
+        _dev(out, "out", _BF16, T * H), wsp, wsn,
+        ctypes.byref(dbg) if dbg is not None else None, _stream(stream))
     _check(st, "latent_moe_forward_routed")
 
 
@@ -254,8 +316,10 @@ def lmoe_linear(x, w, out, add=None, stream=None, T: int | None = None, N: int |
     if T is None:
         T, K = x.shape
         N = w.shape[0]
-    st = load_library().lmoe_linear(_ptr(x), _ptr(w), _ptr(add), _ptr(out), int(T), int(N),
-                                    int(K), _stream(stream))
+    T, N, K = int(T), int(N), int(K)
+    st = load_library().lmoe_linear(_dev(x, "x", _BF16, T * K), _dev(w, "w", _BF16, N * K),
+                                    _dev(add, "add", _BF16, T * N), _dev(out, "out", _BF16, T * N),
+                                    T, N, K, _stream(stream))
     _check(st, "lmoe_linear")
 
 
@@ -265,10 +329,12 @@ def latent_moe_forward_noalloc(dims, weights, hidden, router_logits, out, stream
     Calls that need more scratch raise LmoeError (LMOE_ERR_WORKSPACE); calls
     that overlap on the GPU share the scratch and race."""
     dd = dims if isinstance(dims, LmoeDims) else make_dims(dims)
-    ww = weights if isinstance(weights, LmoeWeights) else make_weights(weights)
-    st = load_library().latent_moe_forward_noalloc(ctypes.byref(dd), ctypes.byref(ww),
-                                                   _ptr(hidden), _ptr(router_logits), _ptr(out),
-                                                   None, _stream(stream))
+    ww = weights if isinstance(weights, LmoeWeights) else make_weights(weights, dd)
+    T, H, E = int(dd.T), int(dd.hidden), int(dd.num_experts)
+    st = load_library().latent_moe_forward_noalloc(
+        ctypes.byref(dd), ctypes.byref(ww), _dev(hidden, "hidden", _BF16, T * H),
+        _dev(router_logits, "router_logits", torch.float32, T * E),
+        _dev(out, "out", _BF16, T * H), None, _stream(stream))
     _check(st, "latent_moe_forward_noalloc")
 
 

@@ -252,9 +252,22 @@ def test_invalid_arguments_are_rejected():
     ws = torch.empty(16, dtype=torch.uint8, device=DEV)
     x = torch.zeros((d.T, d.hidden), dtype=torch.bfloat16, device=DEV)
     lg = torch.zeros((d.T, d.num_experts), device=DEV)
+    # placeholder weights, unchecked by the binding: the library refuses first
+    pw = lm.make_weights({"w_down": x, "w13": x, "w2": x, "w_up": x})
     with pytest.raises(lm.LmoeError) as e:
-        lm.latent_moe_forward(d, {"w_down": x, "w13": x, "w2": x, "w_up": x}, x, lg, x, ws)
+        lm.latent_moe_forward(d, pw, x, lg, x, ws)
     assert e.value.status == -5   # workspace too small
+    # the binding refuses tensors the kernels could not use as the ABI says
+    wts = {"w_down": x, "w13": x, "w2": x, "w_up": x}
+    with pytest.raises(ValueError, match="w_down"):
+        lm.latent_moe_forward(d, wts, x, lg, x, ws)
+    full = lm.make_weights({})   # no weights at all: the library reports the missing ones
+    with pytest.raises(ValueError, match="router_logits"):
+        lm.latent_moe_forward(d, full, x, lg.double(), x, ws)
+    with pytest.raises(ValueError, match="contiguous"):
+        lm.latent_moe_forward(d, full, x.t(), lg, x, ws)
+    with pytest.raises(ValueError, match="workspace"):
+        lm.latent_moe_forward(d, full, x, lg, x, ws, workspace_bytes=1 << 20)
     for bad, st in [(dict(beta=0.0), -4), (dict(n_group=4), -3), (dict(hidden=200), -2),
                     (dict(topk=65), -2)]:
         with pytest.raises(lm.LmoeError) as e:

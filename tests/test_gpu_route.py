@@ -111,5 +111,12 @@ def test_route_invalid_arguments_launch_nothing():
         with pytest.raises(lm.LmoeError) as e:
             lm.moe_route(x, None, 2, 1.0, ids, w, **kw)
         assert e.value.status == st
-    with pytest.raises(lm.LmoeError):
-        lm.moe_route(x, None, 9, 1.0, ids, w)
+    # k > E: raw addresses reach the library's own check
+    with pytest.raises(lm.LmoeError) as e:
+        lm.moe_route(x, None, 9, 1.0, ids.data_ptr(), w.data_ptr())
+    assert e.value.status == -2
+    # tensors too small for k = 3, or of the wrong dtype: refused by the binding
+    with pytest.raises(ValueError):
+        lm.moe_route(x, None, 3, 1.0, ids, w)
+    with pytest.raises(ValueError):
+        lm.moe_route(x.half(), None, 2, 1.0, ids, w)

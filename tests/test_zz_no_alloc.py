@@ -66,7 +66,8 @@ def test_noalloc_rejects_calls_beyond_its_scratch(cuda_ok):
     assert lm.latent_moe_workspace_bytes(d) > 32 * 2 ** 20
     x = torch.zeros((d.T, d.hidden), dtype=torch.bfloat16, device=DEV)
     lg = torch.zeros((d.T, d.num_experts), device=DEV)
-    w = {k: x for k in ("w_down", "w13", "w2", "w_up")}
+    # placeholder weights, unchecked by the binding: the library refuses first
+    w = lm.make_weights({k: x for k in ("w_down", "w13", "w2", "w_up")})
     with pytest.raises(lm.LmoeError) as e:
         lm.latent_moe_forward_noalloc(d, w, x, lg, x)
     assert e.value.status == -5
