@@ -141,7 +141,7 @@ def _dev(t, name: str, dtypes, numel: int) -> int | None:
         raise TypeError(f"{name}: expected a torch tensor, an address or None")
     if not t.is_cuda:
         raise ValueError(f"{name}: must be a CUDA tensor (got device {t.device})")
-    if t.device.index != torch.cuda.current_device():
+    if t.get_device() != torch.cuda.current_device():
         raise ValueError(f"{name}: on {t.device}, but the current device is "
                          f"cuda:{torch.cuda.current_device()}")
     if not t.is_contiguous():
