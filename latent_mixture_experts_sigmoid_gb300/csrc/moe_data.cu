@@ -331,6 +331,10 @@ scatter_rows_kernel(const uint16_t* __restrict__ Zb, const float* __restrict__ Z
 }
 
 // ---- combine + RMSNorm -------------------------------------------------------
+// kMaxV: 8-element vectors per thread (L <= 8 * blockDim * kMaxV), a template
+// parameter so that the accumulators of the common L <= 2048 take 8 registers
+// and eight 256-thread blocks fit per SM.
+template <int kMaxV>
 __global__ void __launch_bounds__(256)
 combine_norm_kernel(const uint16_t* __restrict__ Y, const float* __restrict__ w,
                     const int32_t* __restrict__ row_of, int k, int L,
@@ -340,7 +344,6 @@ combine_norm_kernel(const uint16_t* __restrict__ Y, const float* __restrict__ w,
   __shared__ float red[32];
   const int t = blockIdx.x;
   const int nv = L / 8;
-  constexpr int kMaxV = 4;   // vectors per thread (L <= 8 * 256 * 4)
   float acc[kMaxV][8];
   float ss = 0.0f;
 #pragma unroll
@@ -541,8 +544,15 @@ cudaError_t launch_combine_norm(const uint16_t* Y, const float* w, const int32_t
                                 cudaStream_t s) {
   const int nv = L / 8;
   int threads = nv < 256 ? ((nv + 31) / 32) * 32 : 256;
-  return launch_k(combine_norm_kernel, dim3(T), dim3(threads), 0, s, Y, w, row_of, k, L, gamma, eps,
-                  N);
+  const int per = (nv + threads - 1) / threads;   // vectors per thread, <= 4 (L <= 8192)
+  if (per <= 1)
+    return launch_k(combine_norm_kernel<1>, dim3(T), dim3(threads), 0, s, Y, w, row_of, k, L,
+                    gamma, eps, N);
+  if (per == 2)
+    return launch_k(combine_norm_kernel<2>, dim3(T), dim3(threads), 0, s, Y, w, row_of, k, L,
+                    gamma, eps, N);
+  return launch_k(combine_norm_kernel<4>, dim3(T), dim3(threads), 0, s, Y, w, row_of, k, L, gamma,
+                  eps, N);
 }
 
 cudaError_t launch_reduce_splits(const float* P, int S, long long sstride, const float* Q, int S2,
