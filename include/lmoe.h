@@ -121,9 +121,10 @@ int masked_situ_and_mul(const lmoe_bf16* in, lmoe_bf16* out,
 /*   Sh     = bf16(bf16(SituGLU(bf16(hidden Ws13^T))) Ws2^T)  shared expert    */
 /*   out    = bf16(N W_up^T + Sh)                (Sh added in the GEMM epilogue) */
 /*                                                                            */
-/* Limits: hidden % 128 == 0, latent % 128 == 0, inter % 64 == 0,             */
-/* shared_inter % 64 == 0 (when the shared expert is present), the routing    */
-/* limits above, T >= 0.                                                      */
+/* Limits: hidden % 128 == 0, latent % 128 == 0, latent <= 8192,            */
+/* inter % 64 == 0, shared_inter % 64 == 0 (when the shared expert is        */
+/* present), the routing limits above, T >= 0, T * topk <= 2^30 and          */
+/* T * topk * max(2 * inter, latent) <= 2^40 (LMOE_ERR_DIM otherwise).        */
 /* ------------------------------------------------------------------------ */
 typedef struct lmoe_dims {
   int T;                 /* tokens                                           */

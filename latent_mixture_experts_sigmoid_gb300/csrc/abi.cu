@@ -165,8 +165,10 @@ int validate_dims(const lmoe_dims* d) {
   if (!isfinite(d->linear_beta) || !isfinite(d->routed_scaling_factor) || !isfinite(d->rms_eps) ||
       d->rms_eps < 0.0f)
     return LMOE_ERR_DIM;
-  if ((long long)d->T * d->topk * (long long)(2 * d->inter > d->latent ? 2 * d->inter : d->latent) >
-      (1ll << 40))
+  // expert-major rows are indexed with 32-bit integers, elements with 64-bit
+  if ((long long)d->T * d->topk > (1ll << 30) ||
+      (long long)d->T * d->topk * (long long)(2 * d->inter > d->latent ? 2 * d->inter : d->latent) >
+          (1ll << 40))
     return LMOE_ERR_DIM;
   return LMOE_OK;
 }

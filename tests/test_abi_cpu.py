@@ -88,6 +88,9 @@ def test_layer_validation_and_workspace(lib):
     bad.n_group = 8
     assert lib.latent_moe_forward(ctypes.byref(bad), ctypes.byref(w), p, p, p, p, n, None, None) == -3
     bad = lm.make_dims(W.TINY)
+    bad.T = (1 << 30) // bad.topk + 1          # more expert-major rows than 2^30
+    assert lib.latent_moe_workspace_bytes(ctypes.byref(bad)) == 0
+    bad = lm.make_dims(W.TINY)
     bad.latent = 100
     assert lib.latent_moe_forward(ctypes.byref(bad), ctypes.byref(w), p, p, p, p, n, None, None) == -2
     # missing weights
