@@ -11,7 +11,8 @@ combine + RMSNorm, shared expert, up-projection with the shared add).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Inputs are seeded synthetic tensors (workloads/), resident in HBM before the
-timed region; L2 is flushed (a 512 MiB write) between timed steps.  --impl
+timed region; L2 is flushed between timed steps (a 512 MiB write, then a
+256 MiB read, so that no dirty line is written back inside the timed step).  --impl
 reference times the CPU oracle (oracle/) on a bounded sample of tokens of the
 same workload on the host cores.  With N > 1 (torchrun) every rank runs an
 independent replica (no collective on the data path) and rank 0 reports the
