@@ -33,9 +33,10 @@
 // tiles and nfeat weight tiles thus gives exactly t * nfeat / 2 pair units.
 // Each CTA's MMA commit releases the stage in both CTAs.
 // The MMA's M side (128 rows) is either the tokens (large token counts) or
-// the weight rows ("swap AB", small token counts where N = 16..64 tokens); the
-// N side is the other operand.  Small dense problems split K across CTAs and
-// write fp32 partials that a reduction kernel sums in a fixed order.
+// the weight rows ("swap AB", up to 128 tokens: N = 16..128); the N side is
+// the other operand.  Small dense problems split K across CTAs and write fp32
+// partials that a reduction kernel sums in a fixed order.  The unit walk
+// (decode_unit) also compiles for the host: lmoe_gemm_unit_walk lists it.
 //
 // Every wait on an mbarrier is bounded (clock64 deadline).  A wait that gives
 // up records a code in the device error word, raises a CTA-wide abort flag,
