@@ -2,10 +2,10 @@
 //
 // vLLM PR #50088, commit 1: with n_group == 1 and topk_group == 1, grouped
 // top-k is plain top-k over all experts; kernels are dispatched from a
-// compile-time (num_experts) tier list.  Here: a block per token whenever the
-// experts outnumber one warp's lanes several times (4 warps for few tokens,
-// 2 for large batches; a shared-memory reduction across the warps), and a
-// warp per token for up to 128 experts.
+// compile-time (num_experts) tier list.  Here: a block of 4 warps per token
+// for more than 128 experts and at most 512 tokens (latency: the decode
+// sizes), and otherwise a warp per token, persistent, with the token rows
+// staged in shared memory (throughput: the large batches).
 // Commit 4: sigmoid scores of FP32 logits, e_score_correction_bias added for
 // the selection only, weights from the unbiased scores, renormalised, times
 // routed_scaling_factor.
@@ -15,13 +15,15 @@
 // IEEE fp32 operations (exact_sigmoid below).  Evaluating that sequence for
 // all E experts would make the kernel issue-bound, so selection takes two
 // passes:
-//   A. a cheap key ka = 1/(1 + __expf(-x)) + b for every expert, packed with
-//      the expert index into one u32 (key truncated to 22 bits, index below),
-//      and a bound A: the k-th largest of a small set of per-lane maxima of
-//      those packed keys (so at least k experts reach A), found by a parallel
-//      rank count in shared memory;
+//   A. a cheap key for every expert (in the block kernel ka = 1/(1 +
+//      __expf(-x)) + b, packed with the expert index into one u32, key
+//      truncated to 22 bits, index below; the warp kernel's tanh key is
+//      described at that kernel), and a bound A: the k-th largest of a small
+//      set of per-lane maxima of those keys (so at least k experts reach A),
+//      found by a parallel rank count in shared memory (block kernel) or a
+//      sort across the warp (warp kernel);
 //   B. every expert whose cheap key lies within a proven error bound below A
-//      is a candidate; candidates (normally k to k+4 of them) get the exact
+//      is a candidate; candidates (a few more than k) get the exact
 //      key, and each one's output slot is the number of candidates with a
 //      larger exact key (ties go to the lower index).  More than 32
 //      candidates (a row of tied logits) fall back to an exact selection over
@@ -34,8 +36,8 @@
 // error of __expf (2 + floor(1.173|x|) ulp, |x| <= 87) and __fdividef (2 ulp):
 // |s_fast - s| <= s(1-s) * 1.24e-5 + 3 ulp <= 3.5e-6, plus the exact
 // sigmoid's own error (<= 3 ulp) and the rounding of the two bias additions
-// (<= 2^-23 |key|).  The kernels use 2D = 1e-5 + 2^-20 * max(|A|, 1), about
-// 2.5x that bound.
+// (<= 2^-23 |key|).  The block kernel uses 2D = 1e-5 + 2^-20 * max(|A|, 1),
+// about 2.5x that bound.
 #include <atomic>
 
 #include "lmoe_internal.cuh"
