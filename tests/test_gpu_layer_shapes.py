@@ -17,13 +17,13 @@ pytestmark = pytest.mark.gpu
 lm = pytest.importorskip("latent_mixture_experts_sigmoid_gb300")
 
 
-def _cases(n=14, seed=20261202):
+def _cases(n=22, seed=20261202):
     g = np.random.default_rng(seed)
     out = []
     for i in range(n):
         E = int(g.choice([5, 33, 67, 130, 257, 511, 1000]))
         k = int(min(E, g.choice([1, 2, 6, 8, 16, 32])))
-        T = int(g.choice([1, 7, 64, 127, 128, 129, 200, 257]))
+        T = int(g.choice([1, 7, 64, 127, 128, 129, 200, 257, 520]))
         d = W.LayerDims(T=T, hidden=int(128 * g.integers(1, 5)), latent=int(128 * g.integers(1, 4)),
                         num_experts=E, topk=k, inter=int(64 * g.integers(1, 5)),
                         shared_inter=int(64 * g.integers(0, 5)),
@@ -40,7 +40,7 @@ def _lib(cuda_ok):
     lm.load_library()
 
 
-@pytest.mark.parametrize("i", range(14))
+@pytest.mark.parametrize("i", range(22))
 def test_layer_shape_sample(i):
     from tests.test_gpu_layer import tiny_case
     d = _cases()[i]

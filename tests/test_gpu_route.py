@@ -120,3 +120,27 @@ def test_route_invalid_arguments_launch_nothing():
         lm.moe_route(x, None, 3, 1.0, ids, w)
     with pytest.raises(ValueError):
         lm.moe_route(x.half(), None, 2, 1.0, ids, w)
+
+
+def _route_cases(n=16, seed=7):
+    g = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        E = int(g.integers(1, 1025))
+        k = int(g.integers(1, min(E, 32) + 1))
+        T = int(g.choice([1, 3, 31, 200, 513, 700, 2049]))
+        cases.append((T, E, k, int(g.integers(0, 2)), bool(g.integers(0, 2)),
+                      float(g.choice([1.0, 2.5])), float(g.choice([0.1, 1.0, 4.0]))))
+    return cases
+
+
+@pytest.mark.parametrize("case", _route_cases())
+def test_route_random_shapes(case):
+    # seeded random (T, E, k, renormalise, bias present, rsf, logit scale):
+    # both kernels (block per token up to 512 tokens, warp per token above),
+    # every chunk count and the scalar loads of E % 4 != 0
+    T, E, k, renorm, with_bias, rsf, scale = case
+    g = np.random.default_rng(T * 7919 + E * 31 + k)
+    logits = (g.standard_normal((T, E)) * scale).astype(np.float32)
+    bias = (g.standard_normal(E) * 0.1).astype(np.float32) if with_bias else None
+    check(logits, bias, k, rsf, renorm)
