@@ -1,22 +1,39 @@
-"""Benchmark of the latent-MoE layer forward on GB300.
+"""Benchmark of the latent-MoE layer forward on one GB300.
 
-Prints ONE JSON line (rank 0).  The headline workload is the prefill layer:
-T=4096 tokens, hidden 7168, latent 2048, 896 experts, top-16, expert
-intermediate 512, shared intermediate 4096, router logits skewed by a Zipf(1.1)
-per-expert offset; the T=8 decode layer of the same model is measured in the
-same run and reported under "decode".  A step is one latent_moe_forward call
-(routing, down-projection, permutation, grouped expert GEMMs with SituGLU,
-combine + RMSNorm, shared expert, up-projection with the shared add).
+Prints ONE JSON line.  The headline workload is the prefill layer: T=4096
+tokens, hidden 7168, latent 2048, 896 experts, top-16, expert intermediate 512,
+shared intermediate 4096, router logits skewed by a Zipf(1.1) per-expert
+offset; the T=8 decode layer of the same model is measured in the same run and
+reported under "decode".  A step is one latent_moe_forward call (routing,
+down-projection, permutation, grouped expert GEMMs with SituGLU, combine +
+RMSNorm, shared expert, up-projection with the shared add).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --case linear|layer|decode|route|route8|situ [--reps N]
 
 Inputs are seeded synthetic tensors (workloads/), resident in HBM before the
 timed region; L2 is flushed between timed steps (a 512 MiB write, then a
-256 MiB read, so that no dirty line is written back inside the timed step).  --impl
-reference times the CPU oracle (oracle/) on a bounded sample of tokens of the
-same workload on the host cores.  With N > 1 (torchrun) every rank runs an
-independent replica (no collective on the data path) and rank 0 reports the
-whole-job rate over the slowest rank.
+256 MiB read, so that no dirty line is written back inside the timed step).
+--impl reference times the CPU oracle (oracle/) on a bounded sample of tokens
+of the same workload on the host cores.
+
+The layer runs on one GPU: its prefill GEMMs pair CTAs in clusters that share
+operand tiles, so the library is only ever driven from a single-GPU process.
+--gpus must be 1 for this arm (the reference arm, which uses no GPU, accepts
+any N: only the process with RANK 0 runs and prints).
+
+--case runs one small, self-contained launch set of a kernel for profiler
+captures and prints "<case>: ok":
+  linear   dense tcgen05 GEMM, out[8192, 8192] = x[8192, 7168] w^T (368 MB of
+           operands, larger than L2; 0.96 TFLOP);
+  layer    one prefill layer forward (T=4096, Zipf routing) of a 128-expert
+           variant of the model (hidden 7168, latent 2048, top-16, d 512,
+           shared 4096): every kernel of the path at full token count with
+           ~2 GB on the device;
+  decode   one decode forward (T=8) of the same 128-expert variant;
+  route    routing of [16384, 896] fp32 logits, top-16;
+  route8   routing of [8, 896] fp32 logits, top-16 (decode);
+  situ     dense SituGLU of bf16 [16384, 8192].
 """
 from __future__ import annotations
 
@@ -34,7 +51,17 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-import workloads as W  # noqa: E402
+
+class _LazyWorkloads:
+    """The seeded input generators, imported on first use (worker processes of
+    the oracle baselines import this module and need only NumPy)."""
+
+    def __getattr__(self, name):
+        import workloads
+        return getattr(workloads, name)
+
+
+W = _LazyWorkloads()
 
 METRIC = "latent-MoE layer tokens/s at T=8 and T=4096; % of HBM / bf16 TC roofline"
 UNIT = "tokens/s"
@@ -136,11 +163,11 @@ class Clocks:
 # --------------------------------------------------------------------------
 # our arm
 # --------------------------------------------------------------------------
-def run_ours(args, rank, world):
+def run_ours(args):
     import torch
     import latent_mixture_experts_sigmoid_gb300 as lm
 
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     lm.load_library()
     pk = peaks()
@@ -167,11 +194,6 @@ def run_ours(args, rank, world):
         # write-backs of those dirty lines happen here, outside the timed region
         flush.zero_()
         flush_rd.sum()
-
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
 
     def measure(d, zipf, steps, warmup):
         T = d.T
@@ -204,7 +226,6 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
         n_used = int((counts.cpu().numpy() > 0).sum())
         # device-timed region: K steps, one event pair around each forward
-        barrier()
         torch.cuda.synchronize()
         e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         per_step = []
@@ -217,7 +238,6 @@ def run_ours(args, rank, world):
             stream.synchronize()
             per_step.append(e_a.elapsed_time(e_b))
         torch.cuda.synchronize()
-        barrier()
         ms = float(sum(per_step))
         # per-stage breakdown: the library records an event after every stage
         # (the events serialise the stages, so this pass is not the headline).
@@ -390,29 +410,17 @@ def run_ours(args, rank, world):
     pre = measure(W.PREFILL, True, args.steps, args.warmup)
     dec = measure(W.DECODE, False, args.steps, args.warmup)
     kern = kernel_lines(max(3, args.steps))
+    if not args.no_cpu_baseline:
+        for name, cb in kernel_cpu_baselines().items():
+            kern[name]["cpu_baseline"] = cb
     clk = clocks.stop()
     wall = time.time() - t_wall0
 
-    # max over ranks
-    def allmax(v):
-        if world == 1:
-            return v
-        import torch.distributed as dist
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    pre_ms = allmax(pre["ms"])
-    dec_ms = allmax(dec["ms"])
-    pre_e2e = allmax(pre["e2e_ms"])
-    dec_e2e = allmax(dec["e2e_ms"])
-    if dec["pre"] is not None:
-        dec["pre"]["ms"] = allmax(dec["pre"]["ms"])
-    if rank != 0:
-        return
+    pre_ms, dec_ms = pre["ms"], dec["ms"]
+    pre_e2e, dec_e2e = pre["e2e_ms"], dec["e2e_ms"]
     K = args.steps
     dP, dDc = W.PREFILL, W.DECODE
-    value = world * dP.T * K / (pre_ms / 1e3)
+    value = dP.T * K / (pre_ms / 1e3)
 
     # roofline of the dominant kernel (the tcgen05 GEMM, all its launches of a step)
     names = lm.STAGE_NAMES
@@ -421,14 +429,26 @@ def run_ours(args, rank, world):
     gemm_stages = ["down", "gemm1", "gemm2", "shared1", "shared2", "up"]
     gemm_ms = sum(st[s] for s in gemm_stages)
     ach_tf = fl["total"] / (gemm_ms / 1e3) / 1e12
+    # the step is about a millisecond at full clock, so the burst peak applies
     roof = {"kernel": "gemm_tc_kernel (all GEMM launches of one prefill forward)",
-            "bound": "tensor", "achieved": round(ach_tf, 1), "peak": pk["bf16_sus"],
-            "unit": "TFLOP/s", "frac": round(ach_tf / pk["bf16_sus"], 4),
-            "peak_source": f"{pk['source']} bf16 sustained",
+            "bound": "tensor", "achieved": round(ach_tf, 1), "peak": pk["bf16"],
+            "unit": "TFLOP/s", "frac": round(ach_tf / pk["bf16"], 4),
+            "peak_source": f"{pk['source']} bf16 burst",
             "traffic": GEMM_SET_DRAM_BYTES,
             "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the six GEMM "
                               "launches of one prefill forward (algorithmic: 2042.8 MB)",
             "flops_per_launch_set": fl["total"], "ms_per_launch_set": round(gemm_ms, 4)}
+    # the grouped expert GEMMs alone (GEMM1 with SituGLU in its epilogue, GEMM2)
+    ex_ms = st["gemm1"] + st["gemm2"]
+    ex_fl = fl["gemm1"] + fl["gemm2"]
+    ex_tf = ex_fl / (ex_ms / 1e3) / 1e12
+    roof["expert_gemms"] = {
+        "achieved": round(ex_tf, 1), "peak": pk["bf16"], "unit": "TFLOP/s",
+        "frac": round(ex_tf / pk["bf16"], 4), "us": round(ex_ms * 1e3, 1),
+        "gemm1_frac": round(fl["gemm1"] / (st["gemm1"] / 1e3) / 1e12 / pk["bf16"], 4),
+        "gemm2_frac": round(fl["gemm2"] / (st["gemm2"] / 1e3) / 1e12 / pk["bf16"], 4),
+        "flops": ex_fl, "what": "grouped GEMM1 (+ SituGLU epilogue) and GEMM2 of the prefill, "
+                               "useful flops (routed rows only) over per-stage CUDA-event time"}
     per_stage_pre = {n: round(v, 4) for n, v in st.items()}
     per_stage_dec = {n: round(v, 4) for n, v in zip(names, dec["per_stage"])}
     # decode roofline: weight streaming of the whole layer
@@ -436,13 +456,13 @@ def run_ours(args, rank, world):
     dec_bytes = sum(by.values())
     dec_us = dec_ms / K * 1e3
     dec_gbs = dec_bytes / (dec_us / 1e6) / 1e9
-    decode = {"workload": "decode T=8", "tokens_per_s": round(world * dDc.T * K / (dec_ms / 1e3), 1),
+    decode = {"workload": "decode T=8", "tokens_per_s": round(dDc.T * K / (dec_ms / 1e3), 1),
               "us_per_step": round(dec_us, 2), "experts_used": dec["n_used"],
               "algorithmic_bytes": dec_bytes,
               "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": pk["hbm"],
                            "unit": "GB/s", "frac": round(dec_gbs / pk["hbm"], 4)},
               "per_stage_ms": per_stage_dec,
-              "e2e_tokens_per_s": round(world * dDc.T * K / (dec_e2e / 1e3), 1),
+              "e2e_tokens_per_s": round(dDc.T * K / (dec_e2e / 1e3), 1),
               "gpu_launches_per_step": lm.latent_moe_launch_count(dDc)}
     if dec["pre"] is not None:
         decode["pre_routed"] = {
@@ -467,7 +487,7 @@ def run_ours(args, rank, world):
     # the library's launches inside the headline's timed region (K prefill forwards)
     launches = lm.latent_moe_launch_count(dP)
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": 1,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(pre_ms / K, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) bf16 weights)",
@@ -478,13 +498,13 @@ def run_ours(args, rank, world):
                    "l2": "flushed between timed steps (512 MiB write, then 256 MiB read, untimed)",
                    "timing": ("eager latent_moe_forward calls" if args.no_graph else
                               "CUDA-graph replay of one latent_moe_forward per step"),
-                   "parallelism": f"replicas x{world}"},
-        "e2e": {"value": round(world * dP.T * K / (pre_e2e / 1e3), 1), "unit": UNIT,
+                   "parallelism": "single GPU"},
+        "e2e": {"value": round(dP.T * K / (pre_e2e / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": pre["h2d"], "d2h_bytes_per_step": pre["d2h"],
                 "method": ("latent_moe_forward per step on host-resident inputs; H2D of step "
                            "n+1 and D2H of step n-1 overlap step n on separate streams "
                            "(timed from the first copy in to the last copy out)"),
-                "serial_value": round(world * dP.T * K / (pre["e2e_serial_ms"] / 1e3), 1)},
+                "serial_value": round(dP.T * K / (pre["e2e_serial_ms"] / 1e3), 1)},
         "gpu_launches": launches * K,
         "roofline": roof,
         "per_stage_ms": per_stage_pre,
@@ -547,9 +567,90 @@ def cpu_baseline(d, budget_s=20.0, sample=16):
                       f"(float64 NumPy oracle, weights pre-generated), {n} call(s)"}
 
 
-def run_reference(args, rank, world):
-    """The CPU oracle as the reference arm: each step is a bounded token sample."""
-    if rank != 0:
+# --------------------------------------------------------------------------
+# the oracle beside the kernel lines: one core, and every host core at once
+# --------------------------------------------------------------------------
+_BARRIER = None
+
+
+def _pool_init(barrier):
+    global _BARRIER
+    _BARRIER = barrier
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+
+
+def _oracle_kernel_job(job):
+    """Run one oracle call on pre-generated inputs; returns (units, seconds).
+
+    In a pool, every worker waits at a barrier before its timed call so that
+    all cores run at once."""
+    from oracle import lmoe_oracle as O
+    kind, inp, units = job
+    if _BARRIER is not None:
+        _BARRIER.wait(timeout=300)
+    t0 = time.perf_counter()
+    if kind == "route":
+        lg, b = inp
+        O.route(lg, b, W_ROUTE_K, W_ROUTE_RSF)
+    elif kind == "situ":
+        x, lb = inp
+        O.situ_and_mul(x, 4.0, lb)
+    else:
+        x, cnt, init = inp
+        O.masked_situ_and_mul(x, cnt, init, 4.0, 8.0)
+    return units, time.perf_counter() - t0
+
+
+# the routing workload's constants, for workers that do not import workloads
+W_ROUTE_K, W_ROUTE_RSF = 16, 2.5
+
+
+def kernel_cpu_baselines(cores=None):
+    """Oracle throughput on a sample of each kernel line's workload (the same
+    seeded rows the GPU line processes), on one core and on every core.
+    Returns {line: cpu_baseline dict}, in the unit of the GPU line."""
+    import multiprocessing as mp
+    assert W.ROUTE_K == W_ROUTE_K and W.ROUTE_RSF == W_ROUTE_RSF
+    cores = cores or os.cpu_count() or 1
+    Er = W.ROUTE_E
+    route_rows, situ_rows = 2048, 1024
+    jobs = {}
+    # routing: tokens of the [16384, 896] workload, one sample per worker
+    jobs["route"] = [("route", (W.logits_rows(Er, range(i * route_rows, (i + 1) * route_rows), 0,
+                                              tie_every=64), W.score_bias(Er, 0)), route_rows)
+                     for i in range(cores)]
+    for lb in (8.0, 0.0):
+        x = W.situ_input(situ_rows, 8192, 0)
+        jobs[f"situ_dense_lb{int(lb)}"] = [("situ", (x, lb), situ_rows * 4096)] * cores
+    xm, cnt = W.masked_situ_input(128, 512, 4096, 0)
+    xm, cnt = xm[:4].copy(), cnt[:4].copy()                  # 4 of the 128 experts
+    init = W.sentinel_like((4, 512, 2048))
+    jobs["situ_masked"] = [("masked", (xm, cnt, init), int(cnt.sum()) * 2048)] * cores
+    unit_of = {"route": ("tokens/s", 1.0), "situ_dense_lb8": ("GB/s", 6e-9),
+               "situ_dense_lb0": ("GB/s", 6e-9), "situ_masked": ("GB/s", 6e-9)}
+    res = {}
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(cores)
+    with ctx.Pool(cores, initializer=_pool_init, initargs=(barrier,)) as pool:
+        for name, js in jobs.items():
+            u1, t1 = _oracle_kernel_job(js[0])                # one core, this process
+            out = pool.map(_oracle_kernel_job, js, chunksize=1)
+            u_all = sum(u for u, _ in out)
+            t_all = max(t for _, t in out)
+            unit, scale = unit_of[name]
+            res[name] = {"value": round(u_all / t_all * scale, 3), "unit": unit, "cores": cores,
+                         "kind": "oracle", "one_core": round(u1 / t1 * scale, 3),
+                         "sample": (f"{js[0][2]} units per core ("
+                                    + ("tokens of the [16384, 896] logits" if name == "route" else
+                                       "output elements of seeded rows of the same workload")
+                                    + "), float64 NumPy oracle, all cores started together")}
+    return res
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is a bounded token sample.
+    Under a multi-process launcher only the process with RANK 0 runs."""
+    if int(os.environ.get("RANK", "0")) != 0:
         return
     from oracle import lmoe_oracle as O
     d = W.PREFILL
@@ -566,7 +667,7 @@ def run_reference(args, rank, world):
     cores = _cores()
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "latent-MoE layer prefill T=4096, Zipf(1.1)-skewed routing",
@@ -579,6 +680,75 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------
+# --case: small launch sets for profiler captures
+# --------------------------------------------------------------------------
+def run_case(name, reps):
+    import dataclasses
+    import torch
+    import latent_mixture_experts_sigmoid_gb300 as lm
+
+    dev = torch.device("cuda:0")
+    lm.load_library()
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def layer(d, zipf):
+        w = {"w13": torch.empty((d.num_experts, 2 * d.inter, d.latent), dtype=torch.bfloat16,
+                                device=dev),
+             "w2": torch.empty((d.num_experts, d.latent, d.inter), dtype=torch.bfloat16, device=dev)}
+        for nm in ("w13", "w2"):
+            for e0, e1, bits in W.expert_chunks(d, nm, 0):
+                w[nm][e0:e1].copy_(bf16(bits))
+        w.update(w_down=bf16(W.w_down(d)), w_up=bf16(W.w_up(d)), ws13=bf16(W.ws13(d)),
+                 ws2=bf16(W.ws2(d)), norm_w=bf16(W.norm_weight(d)),
+                 bias=torch.from_numpy(W.score_bias(d.num_experts)).to(dev))
+        x = bf16(W.hidden_states(d, 0))
+        lg = torch.from_numpy(W.router_logits(d.T, d.num_experts, 0, zipf=zipf)).to(dev)
+        out = torch.empty((d.T, d.hidden), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(lm.latent_moe_workspace_bytes(d), dtype=torch.uint8, device=dev)
+        for _ in range(reps + 1):
+            lm.latent_moe_forward(d, w, x, lg, out, ws)
+
+    def route(T):
+        lg = torch.from_numpy(W.router_logits(T, 896, 0, tie_every=64)).to(dev)
+        b = torch.from_numpy(W.score_bias(896, 0)).to(dev)
+        ids = torch.empty((T, 16), dtype=torch.int32, device=dev)
+        wt = torch.empty((T, 16), dtype=torch.float32, device=dev)
+        for _ in range(reps + 1):
+            lm.moe_route(lg, b, 16, 2.5, ids, wt)
+
+    if name == "linear":
+        g = torch.Generator(device=dev).manual_seed(0)
+        x = torch.randn((8192, 7168), generator=g, device=dev).to(torch.bfloat16)
+        w = (torch.randn((8192, 7168), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        out = torch.empty((8192, 8192), dtype=torch.bfloat16, device=dev)
+        for _ in range(reps + 1):
+            lm.lmoe_linear(x, w, out)
+    elif name == "layer":
+        layer(dataclasses.replace(W.PREFILL, num_experts=128), True)
+    elif name == "decode":
+        layer(dataclasses.replace(W.DECODE, num_experts=128), False)
+    elif name == "route":
+        route(16384)
+    elif name == "route8":
+        route(8)
+    elif name == "situ":
+        x = bf16(W.situ_input(16384, 8192, 0))
+        out = torch.empty((16384, 4096), dtype=torch.bfloat16, device=dev)
+        for _ in range(reps + 1):
+            lm.situ_and_mul(x, out, 4.0, 8.0)
+    torch.cuda.synchronize()
+    err = lm.lmoe_device_error()
+    if err:
+        raise SystemExit(f"device error word {err}")
+    print(f"{name}: ok")
+
+
+CASES = ("linear", "layer", "decode", "route", "route8", "situ")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -589,22 +759,20 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager calls instead of CUDA-graph replays (for profiler runs)")
+    ap.add_argument("--case", choices=CASES,
+                    help="run one small launch set of a kernel (for profiler captures) and exit")
+    ap.add_argument("--reps", type=int, default=2, help="launches of --case after one warm-up")
     args = ap.parse_args()
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        backend = "gloo" if args.impl == "reference" else "nccl"
-        dist.init_process_group(backend)
-    try:
-        if args.impl == "reference":
-            run_reference(args, rank, world)
-        else:
-            run_ours(args, rank, world)
-    finally:
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
+    if args.case:
+        run_case(args.case, args.reps)
+        return
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    if args.gpus != 1:
+        sys.stderr.write("bench.py: the layer runs on one GPU; --gpus must be 1\n")
+        raise SystemExit(2)
+    run_ours(args)
 
 
 if __name__ == "__main__":

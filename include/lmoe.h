@@ -14,6 +14,14 @@
  *     stay valid until the work enqueued on `stream` has finished.  Tensors are
  *     dense and row-major (last index fastest).  Every pointer must be 16-byte
  *     aligned.
+ *   - Every tensor pointer must address memory allocated on the CURRENT
+ *     device (cudaGetDevice): each call asks the runtime for the attributes of
+ *     every pointer it is given (cudaPointerGetAttributes) after the argument
+ *     checks and refuses host memory (pinned or pageable), managed memory and
+ *     another device's memory with LMOE_ERR_DEVICE, launching nothing.  The
+ *     GEMMs of the layer read operand tiles through tensor maps that pairs of
+ *     CTAs share on this GPU, so no call may be handed another GPU's memory.
+ *     A pointer the runtime cannot describe is refused the same way.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     The calls are asynchronous: the return code covers argument validation
  *     and launch errors only.  No call synchronises the host with the device
@@ -52,7 +60,9 @@ typedef enum {
   LMOE_ERR_BETA = -4,        /* beta <= 0 or not finite                         */
   LMOE_ERR_WORKSPACE = -5,   /* workspace NULL or smaller than required         */
   LMOE_ERR_CUDA = -6,        /* a CUDA runtime/driver call failed               */
-  LMOE_ERR_ALIGN = -7        /* a pointer is not 16-byte aligned                */
+  LMOE_ERR_ALIGN = -7,       /* a pointer is not 16-byte aligned                */
+  LMOE_ERR_DEVICE = -8       /* a pointer is not device memory of the current   */
+                             /* device (host, managed or another GPU's memory)  */
 } lmoe_status;
 
 typedef uint16_t lmoe_bf16;
@@ -247,13 +257,17 @@ int latent_moe_forward_routed(const lmoe_dims* dims, const lmoe_weights* weights
 /* GPU that loads the library keeps it until the process exits).  Calls whose */
 /* latent_moe_workspace_bytes exceeds 32 MiB return LMOE_ERR_WORKSPACE and    */
 /* launch nothing (the 896-expert, hidden-7168 layer fits up to T = 15).      */
-/* The first call on a device looks up the array's device address           */
-/* (cudaGetSymbolAddress) with that device current; make that first call     */
-/* before any stream capture.  No call allocates.  Every call on a device     */
-/* shares the one array, which keeps the previous call's contents (nothing in */
-/* it has to start at zero: each call writes every scratch value it reads), */
-/* so calls that may overlap on the GPU (different streams, or host threads) */
-/* race; serialise them on one stream.                                        */
+/* Every call looks up the array's address on the current device            */
+/* (cudaGetSymbolAddress; not cached, so it stays valid across a device      */
+/* reset).  With lazy module loading the first lookup on a device loads the  */
+/* library's module there, which reserves the 32 MiB and may synchronise the */
+/* device: make that first call (or any other call of the library) on each    */
+/* device before a latency-critical path and before any stream capture.       */
+/* No call allocates.  Every call on a device shares the one array, which   */
+/* keeps the previous call's contents (nothing in it has to start at zero:   */
+/* each call writes every scratch value it reads), so calls that may overlap */
+/* on the GPU (different streams, or host threads) race; serialise them on   */
+/* one stream.                                                                */
 int latent_moe_forward_noalloc(const lmoe_dims* dims, const lmoe_weights* weights,
                                const lmoe_bf16* hidden, const float* router_logits,
                                lmoe_bf16* out, const lmoe_debug* dbg, void* stream);

@@ -23,6 +23,7 @@ LMOE_ERR_BETA = -4
 LMOE_ERR_WORKSPACE = -5
 LMOE_ERR_CUDA = -6
 LMOE_ERR_ALIGN = -7
+LMOE_ERR_DEVICE = -8
 
 ABI_FUNCTIONS = ("moe_route", "situ_and_mul", "masked_situ_and_mul", "latent_moe_forward",
                  "latent_moe_forward_routed",

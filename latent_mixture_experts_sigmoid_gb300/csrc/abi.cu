@@ -33,6 +33,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <initializer_list>
 #include <mutex>
 
 #include "gemm_tc.cuh"
@@ -304,6 +305,28 @@ bool aux_for_current_device(AuxStream** out) {
   return true;
 }
 
+// Every non-NULL pointer addresses device memory of the current device
+// (cudaMemoryTypeDevice, owned by this device).  A failed query (no device, a
+// pointer the runtime does not know) counts as a refusal; its error is cleared
+// so that it cannot surface from a later cudaGetLastError.
+bool on_current_device(std::initializer_list<const void*> ptrs) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  for (const void* p : ptrs) {
+    if (p == nullptr) continue;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    if (a.type != cudaMemoryTypeDevice || a.device != dev) return false;
+  }
+  return true;
+}
+
 #define LMOE_TRY(x)                                  \
   do {                                               \
     if ((x) != cudaSuccess) return LMOE_ERR_CUDA;    \
@@ -316,7 +339,7 @@ using namespace lmoe;
 
 extern "C" {
 
-int lmoe_abi_version(void) { return 101; }
+int lmoe_abi_version(void) { return 102; }
 
 const char* lmoe_status_string(int status) {
   switch (status) {
@@ -328,6 +351,7 @@ const char* lmoe_status_string(int status) {
     case LMOE_ERR_WORKSPACE: return "workspace is NULL, misaligned or too small";
     case LMOE_ERR_CUDA: return "a CUDA call failed";
     case LMOE_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case LMOE_ERR_DEVICE: return "a pointer is not device memory of the current device";
     default: return "unknown status";
   }
 }
@@ -345,6 +369,7 @@ int moe_route(const float* router_logits, const float* bias, int T, int E, int t
   if (!aligned16(router_logits) || !aligned16(topk_ids) || !aligned16(topk_weights) ||
       (bias && !aligned16(bias)))
     return LMOE_ERR_ALIGN;
+  if (!on_current_device({router_logits, bias, topk_ids, topk_weights})) return LMOE_ERR_DEVICE;
   if (launch_route(router_logits, bias, T, E, topk, renormalize, rsf, topk_ids, topk_weights,
                    (cudaStream_t)stream) != cudaSuccess)
     return LMOE_ERR_CUDA;
@@ -358,6 +383,7 @@ int situ_and_mul(const lmoe_bf16* in, lmoe_bf16* out, int64_t N, int d, float be
   if (N == 0) return LMOE_OK;
   if (!in || !out) return LMOE_ERR_NULL;
   if (!aligned16(in) || !aligned16(out)) return LMOE_ERR_ALIGN;
+  if (!on_current_device({in, out})) return LMOE_ERR_DEVICE;
   if (launch_situ(in, out, N, d, beta, linear_beta, (cudaStream_t)stream) != cudaSuccess)
     return LMOE_ERR_CUDA;
   return LMOE_OK;
@@ -371,6 +397,7 @@ int masked_situ_and_mul(const lmoe_bf16* in, lmoe_bf16* out, const int32_t* expe
   if (E == 0 || T_max == 0) return LMOE_OK;
   if (!in || !out || !expert_num_tokens) return LMOE_ERR_NULL;
   if (!aligned16(in) || !aligned16(out) || !aligned16(expert_num_tokens)) return LMOE_ERR_ALIGN;
+  if (!on_current_device({in, out, expert_num_tokens})) return LMOE_ERR_DEVICE;
   if (launch_masked_situ(in, out, expert_num_tokens, E, T_max, d, beta, linear_beta,
                          (cudaStream_t)stream) != cudaSuccess)
     return LMOE_ERR_CUDA;
@@ -384,6 +411,7 @@ int lmoe_linear(const lmoe_bf16* x, const lmoe_bf16* w, const lmoe_bf16* add, lm
   if (!x || !w || !out) return LMOE_ERR_NULL;
   if (!aligned16(x) || !aligned16(w) || !aligned16(out) || (add && !aligned16(add)))
     return LMOE_ERR_ALIGN;
+  if (!on_current_device({x, w, add, out})) return LMOE_ERR_DEVICE;
   DenseCfg c = dense_cfg(T, N, K, num_sms());
   c.splits = 1;
   if (gemm_dense(w, N, x, T, K, c, out, 0, 0, add, (cudaStream_t)stream) != cudaSuccess)
@@ -417,11 +445,13 @@ size_t latent_moe_workspace_bytes(const lmoe_dims* dims) {
 }
 
 // The layer forward.  Exactly one of router_logits (the layer routes) and
-// pre_ids/pre_w (routing done ahead by the caller) is given.
+// pre_ids/pre_w (routing done ahead by the caller) is given.  own_workspace:
+// the workspace is the library's own static scratch (known device memory of
+// the current device), so its pointer is not queried.
 static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe_bf16* hidden,
                         const float* router_logits, const int32_t* pre_ids, const float* pre_w,
                         lmoe_bf16* out, void* workspace, size_t workspace_bytes,
-                        const lmoe_debug* dbg, void* stream) {
+                        const lmoe_debug* dbg, void* stream, bool own_workspace) {
   const int v = validate_dims(dims);
   if (v != LMOE_OK) return v;
   if (!wt) return LMOE_ERR_NULL;
@@ -448,6 +478,13 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
     for (const void* p : dp)
       if (p && !aligned16(p)) return LMOE_ERR_ALIGN;
   }
+  if (!on_current_device({hidden, router_logits, pre_ids, pre_w, out, wt->w_down, wt->w13, wt->w2,
+                          wt->w_up, wt->ws13, wt->ws2, wt->norm_w, wt->e_score_correction_bias,
+                          own_workspace ? nullptr : workspace}))
+    return LMOE_ERR_DEVICE;
+  if (dbg && !on_current_device({dbg->topk_ids, dbg->topk_weights, dbg->expert_num_tokens,
+                                 dbg->expert_offsets, dbg->row_of}))
+    return LMOE_ERR_DEVICE;
 
   cudaStream_t s = (cudaStream_t)stream;
   const int T = d.T, k = d.topk, E = d.num_experts, H = d.hidden, L = d.latent;
@@ -645,7 +682,7 @@ int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe
                        const float* router_logits, lmoe_bf16* out, void* workspace,
                        size_t workspace_bytes, const lmoe_debug* dbg, void* stream) {
   return forward_impl(dims, wt, hidden, router_logits, nullptr, nullptr, out, workspace,
-                      workspace_bytes, dbg, stream);
+                      workspace_bytes, dbg, stream, false);
 }
 
 int latent_moe_forward_routed(const lmoe_dims* dims, const lmoe_weights* wt,
@@ -653,7 +690,17 @@ int latent_moe_forward_routed(const lmoe_dims* dims, const lmoe_weights* wt,
                               const float* topk_weights, lmoe_bf16* out, void* workspace,
                               size_t workspace_bytes, const lmoe_debug* dbg, void* stream) {
   return forward_impl(dims, wt, hidden, nullptr, topk_ids, topk_weights, out, workspace,
-                      workspace_bytes, dbg, stream);
+                      workspace_bytes, dbg, stream, false);
 }
 
 }  // extern "C"
+
+namespace lmoe {
+int forward_on_library_scratch(const lmoe_dims* dims, const lmoe_weights* wt,
+                               const lmoe_bf16* hidden, const float* router_logits,
+                               lmoe_bf16* out, void* scratch, size_t scratch_bytes,
+                               const lmoe_debug* dbg, void* stream) {
+  return forward_impl(dims, wt, hidden, router_logits, nullptr, nullptr, out, scratch,
+                      scratch_bytes, dbg, stream, true);
+}
+}  // namespace lmoe

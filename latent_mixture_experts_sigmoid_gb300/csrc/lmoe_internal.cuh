@@ -21,6 +21,13 @@ constexpr int kErrExpertId = 7;
 // Device address of the error word of the current device.
 int* device_error_word();
 
+// latent_moe_forward on the library's own static scratch (device memory of
+// the current device, so its pointer is not queried like a caller's).
+int forward_on_library_scratch(const lmoe_dims* dims, const lmoe_weights* wt,
+                               const lmoe_bf16* hidden, const float* router_logits,
+                               lmoe_bf16* out, void* scratch, size_t scratch_bytes,
+                               const lmoe_debug* dbg, void* stream);
+
 // ---------------------------------------------------------------------------
 // bf16 <-> fp32 on raw 16-bit patterns (round to nearest even on the way down)
 // ---------------------------------------------------------------------------

@@ -10,35 +10,31 @@
 //
 // The array is a file-scope __device__ variable of kStaticScratchBytes
 // (32 MiB): every GPU that loads the library holds it until the process exits.
-// Host code cannot use the variable's name as a device address; its address on
-// a device comes from cudaGetSymbolAddress, called once per device (with that
-// device current) by the first call made on that device, and cached.
-#include <mutex>
-
+// Host code cannot use the variable's name as a device address; every call
+// looks the address up on the current device with cudaGetSymbolAddress.  The
+// lookup is not cached, so a call made after a device reset or a new primary
+// context gets the array of the live context, never a stale address.  With
+// CUDA's lazy module loading, the first lookup on a device loads this
+// library's module there: that reserves the 32 MiB and may synchronise the
+// device, so a caller with a strict latency path makes its first call (or any
+// other call of the library) on each device before that path, and before any
+// stream capture.
 #include "lmoe_internal.cuh"
 
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;
-constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-void* g_scratch_addr[kMaxDevices] = {nullptr};
-std::mutex g_scratch_mu;
-
-// Device address of g_static_scratch on the current device (set up once).
+// Device address of g_static_scratch on the current device.
 int scratch_on_current_device(void** addr) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LMOE_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr)
-      return LMOE_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return LMOE_ERR_CUDA;
   }
-  *addr = g_scratch_addr[dev];
+  *addr = p;
   return LMOE_OK;
 }
 
@@ -57,6 +53,6 @@ extern "C" int latent_moe_forward_noalloc(const lmoe_dims* dims, const lmoe_weig
   void* scratch = nullptr;
   const int st = scratch_on_current_device(&scratch);
   if (st != LMOE_OK) return st;
-  return latent_moe_forward(dims, weights, hidden, router_logits, out, scratch,
-                            kStaticScratchBytes, dbg, stream);
+  return lmoe::forward_on_library_scratch(dims, weights, hidden, router_logits, out, scratch,
+                                          kStaticScratchBytes, dbg, stream);
 }

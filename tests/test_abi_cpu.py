@@ -41,10 +41,10 @@ def test_every_declared_function_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for st in range(-7, 1):
+    for st in range(-8, 1):
         assert lib.lmoe_status_string(st)
     assert lib.lmoe_status_string(-99) == b"unknown status"
-    assert lib.lmoe_abi_version() == 101
+    assert lib.lmoe_abi_version() == 102
 
 
 def test_route_validation(lib):
@@ -136,3 +136,46 @@ def test_package_fails_loudly_without_library(tmp_path):
             b.load_library(str(tmp_path / "missing.so"))
     finally:
         b._lib = saved
+
+
+def _host_buffer(nbytes, align=256):
+    """An aligned view into a numpy host allocation (and the array that owns it)."""
+    import numpy as np
+    raw = np.zeros(nbytes + align, dtype=np.uint8)
+    off = (-raw.ctypes.data) % align
+    return raw[off:off + nbytes], raw
+
+
+def test_host_memory_is_refused_before_any_launch(lib):
+    # Every argument valid except where the memory lives: host (pageable)
+    # buffers are not device memory of the current device, so each entry point
+    # refuses them with LMOE_ERR_DEVICE (-8) and launches nothing.
+    import workloads as W
+    import latent_mixture_experts_sigmoid_gb300 as lm
+    d = lm.make_dims(W.TINY)
+    T, H, L, E, k, dI, ds = 8, 256, 128, 64, 4, 128, 128
+    keep = []
+
+    def buf(nbytes):
+        v, raw = _host_buffer(max(nbytes, 16))
+        keep.append(raw)
+        return ctypes.c_void_p(v.ctypes.data)
+
+    x, lg, out = buf(T * H * 2), buf(T * E * 4), buf(T * H * 2)
+    w = lm.LmoeWeights(buf(L * H * 2).value, buf(E * 2 * dI * L * 2).value,
+                       buf(E * L * dI * 2).value, buf(2 * ds * H * 2).value, buf(H * ds * 2).value,
+                       None, buf(H * L * 2).value, None)
+    n = lib.latent_moe_workspace_bytes(ctypes.byref(d))
+    ws = buf(n)
+    assert lib.latent_moe_forward(ctypes.byref(d), ctypes.byref(w), x, lg, out, ws, n, None,
+                                  None) == -8
+    ids, tw = buf(T * k * 4), buf(T * k * 4)
+    assert lib.latent_moe_forward_routed(ctypes.byref(d), ctypes.byref(w), x, ids, tw, out, ws, n,
+                                         None, None) == -8
+    assert lib.latent_moe_forward_noalloc(ctypes.byref(d), ctypes.byref(w), x, lg, out, None,
+                                          None) in (-8, -6)   # -6: no device to hold the scratch
+    assert lib.moe_route(lg, None, T, E, k, 1, 1, 1, 2.5, ids, tw, None) == -8
+    assert lib.situ_and_mul(x, out, 4, 16, 4.0, 8.0, None) == -8
+    cnt = buf(16)
+    assert lib.masked_situ_and_mul(x, out, cnt, 2, 2, 16, 4.0, 8.0, None) == -8
+    assert lib.lmoe_linear(x, buf(128 * 256 * 2), None, out, 8, 128, 256, None) == -8

@@ -1,5 +1,7 @@
-"""bench.py's multi-process path on CPU: two ranks over gloo (torchrun), the
-reference arm (the oracle) runs on rank 0 only and prints the one JSON line."""
+"""bench.py's command line on the CPU: the layer arm runs on one GPU only and
+refuses any other --gpus before touching a device; the reference arm (the
+oracle, no GPU) prints one JSON line from the process with RANK 0 and nothing
+from the others, also when a multi-process launcher starts it."""
 import json
 import os
 import socket
@@ -17,8 +19,17 @@ def _free_port() -> int:
         return s.getsockname()[1]
 
 
+def test_layer_arm_refuses_more_than_one_gpu():
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "bench.py", "--gpus", "2", "--steps", "1"], cwd=ROOT,
+                       env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 2
+    assert "--gpus must be 1" in r.stderr
+    assert not [l for l in r.stdout.splitlines() if l.startswith("{")]
+
+
 @pytest.mark.timeout(600)
-def test_reference_arm_two_ranks_gloo():
+def test_reference_arm_prints_once_under_a_launcher():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
            "bench.py", "--gpus", "2", "--impl", "reference", "--steps", "1", "--warmup", "0"]

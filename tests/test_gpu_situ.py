@@ -34,10 +34,18 @@ def test_situ_dense_small(N, d, lb):
     assert_situ_close(got, ref)
 
 
+def _pool_map(fn, items):
+    """fn over items on the host's cores (NumPy releases the GIL in its loops)."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max(1, min(32, os.cpu_count() or 1))) as ex:
+        return list(ex.map(fn, items))
+
+
 @pytest.mark.parametrize("lb", [8.0, 0.0])
-def test_situ_dense_full_size_sampled(lb):
-    # the [16384, 2*4096] workload; every output is checked on the GPU against
-    # finite/bounded properties, and 96 sampled rows against the oracle
+def test_situ_dense_full_size(lb):
+    # the [16384, 2*4096] workload: every one of the 67M outputs against the
+    # oracle, in blocks of 512 rows
     from tests.gpu_util import host_bits, assert_situ_close
     N, d = 16384, 4096
     x = W.situ_input(N, 2 * d, seed=0)
@@ -46,11 +54,14 @@ def test_situ_dense_full_size_sampled(lb):
     assert torch.isfinite(o).all()
     if lb > 0:
         assert (o.abs() <= 4.0 * 8.0).all()   # bf16 rounding can reach the bound
-    rows = np.random.default_rng(1).choice(N, 96, replace=False)
-    rows = np.concatenate([[0, N - 1], rows])
-    got = O.bf16_to_f64(host_bits(out[torch.from_numpy(rows).cuda()]))
-    ref = O.bf16_to_f64(O.situ_and_mul(x[rows], 4.0, lb))
-    assert_situ_close(got, ref)
+    got_all = host_bits(out)
+
+    def block(r0):
+        got = O.bf16_to_f64(got_all[r0:r0 + 512])
+        ref = O.bf16_to_f64(O.situ_and_mul(x[r0:r0 + 512], 4.0, lb))
+        assert_situ_close(got, ref)
+
+    _pool_map(block, range(0, N, 512))
 
 
 def _masked(x, counts, beta, lb):
@@ -62,21 +73,21 @@ def _masked(x, counts, beta, lb):
     return out
 
 
-def _check_masked(x, counts, out, lb, sample_rows=None):
+def _check_masked(x, counts, out, lb):
+    """Every padded output row bit-unchanged, every valid row against the oracle."""
     from tests.gpu_util import host_bits, assert_situ_close
     E, T_max, _ = x.shape
-    bits = out.view(torch.int16)
-    for e in range(E):
+    got_all = host_bits(out)
+
+    def expert(e):
         n = min(max(int(counts[e]), 0), T_max)
-        pad = bits[e, n:]
-        assert (pad == np.int16(np.uint16(W.SENTINEL).view(np.int16))).all(), f"expert {e} padding touched"
+        assert (got_all[e, n:] == W.SENTINEL).all(), f"expert {e} padding touched"
         if n:
-            rows = range(n) if sample_rows is None else sorted(set(
-                [0, n - 1] + list(np.random.default_rng(e).choice(n, min(n, sample_rows), replace=False))))
-            rows = list(rows)
-            got = O.bf16_to_f64(host_bits(out[e, rows]))
-            ref = O.bf16_to_f64(O.situ_and_mul(x[e, rows], 4.0, lb))
+            got = O.bf16_to_f64(got_all[e, :n])
+            ref = O.bf16_to_f64(O.situ_and_mul(x[e, :n], 4.0, lb))
             assert_situ_close(got, ref)
+
+    _pool_map(expert, range(E))
 
 
 @pytest.mark.parametrize("lb", [8.0, 0.0])
@@ -91,7 +102,7 @@ def test_masked_full_size():
     # [E=128, T_max=512, 2*2048] with counts uniform in [0, 512]
     x, counts = W.masked_situ_input(128, 512, 2 * 2048, seed=0)
     out = _masked(x, counts, 4.0, 8.0)
-    _check_masked(x, counts, out, 8.0, sample_rows=3)
+    _check_masked(x, counts, out, 8.0)
 
 
 def test_situ_rejects_missing_beta():

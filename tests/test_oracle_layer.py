@@ -149,3 +149,73 @@ def test_lazy_expert_weights_match_stacked():
     wts, x, lg = tiny(8)
     lazy = dict(wts, w13=lambda e: W.w13_expert(D, e, 8), w2=lambda e: W.w2_expert(D, e, 8))
     assert np.array_equal(O.latent_moe_forward(D, wts, x, lg), O.latent_moe_forward(D, lazy, x, lg))
+
+
+# --- RMSNorm gamma and epsilon (vLLM latent_moe_runner page,
+# _shard_up_proj_tail: transform.norm of the reduced latent; vLLM PR #50088,
+# commit 7: the routed sum is complete before the norm) ----------------------
+
+def check_rms_norm_gamma_scales_each_feature_exactly():
+    # gamma = 2^a per feature multiplies column f by exactly 2^a_f (a power of
+    # two changes no rounding), whatever x and eps are
+    g = np.random.default_rng(21)
+    x = g.standard_normal((5, 64)) * 3
+    a = g.integers(-4, 5, 64)
+    for eps in (0.0, 1e-6, 0.5):
+        base = O.rms_norm(x, np.ones(64), eps)
+        scaled = O.rms_norm(x, 2.0 ** a, eps)
+        assert np.array_equal(scaled, base * 2.0 ** a)
+
+
+def test_rms_norm_gamma_scales_each_feature_exactly():
+    check_rms_norm_gamma_scales_each_feature_exactly()
+
+
+def check_rms_norm_constant_row_closed_form():
+    # a row of one value c has mean(x^2) = c^2, so the norm is c / sqrt(c^2 + eps):
+    # with eps of the order of c^2 this separates eps inside the root from
+    # eps added to the root (c / (|c| + eps))
+    for c, eps in ((0.5, 0.25), (-2.0, 4.0), (3.0, 1e-6), (1e-3, 1e-6)):
+        got = O.rms_norm(np.full((1, 32), c), np.ones(32), eps)
+        assert np.allclose(got, c / np.sqrt(c * c + eps), rtol=1e-14, atol=0)
+    # eps = 0: every row has unit RMS, sign kept
+    got = O.rms_norm(np.full((1, 8), -7.0), np.ones(8), 0.0)
+    assert np.array_equal(got, np.full((1, 8), -1.0))
+
+
+def test_rms_norm_constant_row_closed_form():
+    check_rms_norm_constant_row_closed_form()
+
+
+def check_rms_norm_gamma_multiplies():
+    # the gamma != 1 output divided by the gamma = 1 output is gamma itself
+    # (not 1/gamma, not 1): one row with every entry nonzero
+    g = np.random.default_rng(22)
+    x = g.standard_normal((3, 48)) + 4.0
+    gamma = 1.0 + g.random(48)
+    ratio = O.rms_norm(x, gamma, 1e-6) / O.rms_norm(x, np.ones(48), 1e-6)
+    assert np.allclose(ratio, np.broadcast_to(gamma, ratio.shape), rtol=1e-14, atol=0)
+
+
+def test_rms_norm_gamma_multiplies():
+    check_rms_norm_gamma_multiplies()
+
+
+def check_layer_gamma_power_of_two_scales_the_norm_output():
+    # the layer applies gamma to the normalised routed sum: with W_up = I, no
+    # shared expert and gamma = 2^a per feature the output is the gamma = 1
+    # output times 2^a exactly (bf16 rounding commutes with powers of two)
+    d = dataclasses.replace(D, hidden=D.latent, T=8)
+    wts, _, lg = tiny(6)
+    wts = dict(wts, ws13=None, ws2=None, w_up=O.f64_to_bf16_bits(np.eye(d.latent)),
+               w_down=O.f64_to_bf16_bits(np.eye(d.latent)))
+    x = W.hidden_states(d, 6)
+    a = np.random.default_rng(23).integers(-3, 4, d.latent)
+    one = O.bf16_to_f64(O.latent_moe_forward(d, dict(wts, norm_w=None), x, lg))
+    two = O.bf16_to_f64(O.latent_moe_forward(
+        d, dict(wts, norm_w=O.f64_to_bf16_bits(2.0 ** a)), x, lg))
+    assert np.array_equal(two, one * 2.0 ** a)
+
+
+def test_layer_gamma_power_of_two_scales_the_norm_output():
+    check_layer_gamma_power_of_two_scales_the_norm_output()

@@ -48,6 +48,21 @@ def _rms_norm_over_tokens(x, gamma, eps):
     return x / np.sqrt(np.mean(x * x, axis=0, keepdims=True) + eps) * gamma
 
 
+def _rms_norm_gamma_dropped(x, gamma, eps):
+    x = np.asarray(x, np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+
+
+def _rms_norm_gamma_divided(x, gamma, eps):
+    x = np.asarray(x, np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) / gamma
+
+
+def _rms_norm_eps_outside_root(x, gamma, eps):
+    x = np.asarray(x, np.float64)
+    return x / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + eps) * gamma
+
+
 def _permute_descending(ids, E):
     counts, offsets, row_of, tok_of_row = _permute(ids[::-1].copy(), E)
     return counts, offsets, row_of[::-1].copy(), (ids.shape[0] - 1 - tok_of_row).astype(np.int32)
@@ -61,6 +76,11 @@ MUTATIONS = [
     ("route", _route_not_renormalised, L.check_identical_experts_reduce_to_dense_mlp),
     ("route", _route_weights_reversed, L.check_power_of_two_scaled_experts),
     ("rms_norm", _rms_norm_over_tokens, L.check_token_independence),
+    ("rms_norm", _rms_norm_gamma_dropped, L.check_rms_norm_gamma_scales_each_feature_exactly),
+    ("rms_norm", _rms_norm_gamma_dropped, L.check_layer_gamma_power_of_two_scales_the_norm_output),
+    ("rms_norm", _rms_norm_gamma_divided, L.check_rms_norm_gamma_multiplies),
+    ("rms_norm", _rms_norm_gamma_divided, L.check_layer_gamma_power_of_two_scales_the_norm_output),
+    ("rms_norm", _rms_norm_eps_outside_root, L.check_rms_norm_constant_row_closed_form),
     ("permute", _permute_descending, lambda: R.check_permute(
         np.stack([np.random.default_rng(t).permutation(16)[:3] for t in range(20)]).astype(np.int32), 16)),
 ]
