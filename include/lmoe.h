@@ -219,10 +219,18 @@ int latent_moe_launch_count(const lmoe_dims* dims, int has_shared_expert);
 /* hidden [T, H] bf16, router_logits [T, E] fp32, out [T, H] bf16; workspace  */
 /* at least latent_moe_workspace_bytes(dims) bytes, 256-byte aligned, not     */
 /* shared with a concurrent call.  dbg may be NULL.  The shared expert runs  */
-/* on a library-owned second stream of the device, forked from `stream` and  */
-/* joined back to it by events (also inside a stream capture), so all of the */
-/* call's work is ordered after earlier work on `stream` and before later.    */
-/* With dbg->stage_events every stage runs on `stream`, one after another.    */
+/* on a library-owned second stream kept for this (device, `stream`) pair,    */
+/* forked from `stream` and joined back to it by events (also inside a       */
+/* stream capture), so all of the call's work is ordered after earlier work  */
+/* on `stream` and before later.  Calls on different streams share no        */
+/* second stream: host threads may call concurrently, each on its own stream */
+/* and workspace, and one of them may be capturing (capture in thread-local  */
+/* or relaxed mode: during a global-mode capture the runtime may refuse      */
+/* calls it deems unsafe in every other thread).  The second                 */
+/* stream of a caller stream is created by its first call made outside a     */
+/* capture (up to 64 caller streams per device); a call without one runs     */
+/* every stage on `stream` (same results).  With dbg->stage_events every      */
+/* stage runs on `stream`, one after another.                                 */
 int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* weights,
                        const lmoe_bf16* hidden, const float* router_logits,
                        lmoe_bf16* out, void* workspace, size_t workspace_bytes,

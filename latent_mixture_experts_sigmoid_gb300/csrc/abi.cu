@@ -34,7 +34,9 @@
 
 #include <atomic>
 #include <initializer_list>
+#include <memory>
 #include <mutex>
+#include <vector>
 
 #include "gemm_tc.cuh"
 #include "lmoe_internal.cuh"
@@ -272,37 +274,65 @@ int plan_launches(const Plan& p, bool shared) {
   return n;
 }
 
-// The second stream of the forward: the shared expert runs there,
-// forked from and joined back to the caller's stream by two events (so the
-// fork is also recorded by a stream capture).  One per device, created by the
-// first call on it; the mutex keeps the fork/join event pair of one
-// call from interleaving with another host thread's.
+// The second stream of the forward: the shared expert runs there (and at
+// large T the routing and the permutation), forked from and joined back to the
+// caller's stream by events, so that a stream capture records the fork too.
+// There is one per (device, caller stream): calls on different caller streams
+// never share a second stream, so neither one's work is ordered behind the
+// other's, and a capture on one caller stream pulls in only its own second
+// stream.  An entry is created by the first call on that caller stream made
+// outside a stream capture and kept for the life of the process (a stream
+// handle that is destroyed and reused maps to the same entry, which stays
+// valid: the library owns it).  A call that finds no entry while its stream
+// is capturing, or whose device already has kMaxAuxPerDevice entries, runs
+// every stage on the caller's stream instead (same kernels, same results).
+// The entry's mutex keeps the event pair of one call from interleaving with
+// another host thread's call on the same caller stream.
 struct AuxStream {
+  int dev = -1;
+  cudaStream_t caller = nullptr;
   cudaStream_t stream = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr, routed = nullptr;
+  std::mutex mu;
 };
-AuxStream g_aux[64];
-std::mutex g_aux_mu;
+constexpr int kMaxAuxPerDevice = 64;
+std::mutex g_aux_map_mu;
+std::vector<std::unique_ptr<AuxStream>> g_aux_map;
 
-bool aux_for_current_device(AuxStream** out) {
+// The second stream of `caller` on the current device, created on first use;
+// nullptr when the forward must run on the caller's stream alone.
+AuxStream* aux_for(cudaStream_t caller) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  AuxStream& a = g_aux[dev];
-  if (a.stream == nullptr) {
-    cudaStream_t st = nullptr;
-    cudaEvent_t f = nullptr, j = nullptr, r = nullptr;
-    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return false;
-    if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&r, cudaEventDisableTiming) != cudaSuccess)
-      return false;
-    a.stream = st;
-    a.fork = f;
-    a.join = j;
-    a.routed = r;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
   }
-  *out = &a;
-  return true;
+  std::lock_guard<std::mutex> lock(g_aux_map_mu);
+  int on_dev = 0;
+  for (auto& a : g_aux_map) {
+    if (a->dev != dev) continue;
+    if (a->caller == caller) return a.get();
+    ++on_dev;
+  }
+  if (on_dev >= kMaxAuxPerDevice) return nullptr;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(caller, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return nullptr;
+  auto a = std::make_unique<AuxStream>();
+  a->dev = dev;
+  a->caller = caller;
+  if (cudaStreamCreateWithFlags(&a->stream, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&a->fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&a->join, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&a->routed, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;   // (a partially created entry is not kept; its handles leak)
+  }
+  g_aux_map.push_back(std::move(a));
+  return g_aux_map.back().get();
 }
 
 // Every non-NULL pointer addresses device memory of the current device
@@ -508,12 +538,11 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
   // the shared expert gets the second stream, where it fills the gaps the
   // routed path's latency-bound stages leave (not when per-stage timing was
   // asked for, which needs the stages one after another)
-  const bool concurrent = shared && ev == nullptr;
-  AuxStream* aux = nullptr;
-  std::unique_lock<std::mutex> aux_lock(g_aux_mu, std::defer_lock);
+  AuxStream* aux = (shared && ev == nullptr) ? aux_for(s) : nullptr;
+  const bool concurrent = aux != nullptr;
+  std::unique_lock<std::mutex> aux_lock;
   if (concurrent) {
-    aux_lock.lock();
-    if (!aux_for_current_device(&aux)) return LMOE_ERR_CUDA;
+    aux_lock = std::unique_lock<std::mutex>(aux->mu);
     if (cudaEventRecord(aux->fork, s) != cudaSuccess) return LMOE_ERR_CUDA;
   }
   // 9-11. shared expert on the original hidden states (enqueued by a lambda:
