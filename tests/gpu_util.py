@@ -278,6 +278,9 @@ def explain_layer_outliers(got, ref, tokens, mid, ws_view, x_bits, wts, d, case,
         nw_g, nw_o = float(n_g @ wup[f]), float(mid["N"][i] @ wup[f])
         sh_g = float(O.round_bf16(as_g @ ws2[f]))
         sh_o = float(mid["Sh"][i, f])
+        # above 128 tokens the GPU stores its bf16 Sh (below, it stays in the
+        # split-K partials of the last reduction)
+        sh_stored = float(O.bf16_to_f64(ws_view["Sh"][t, f])) if d.T > 128 else None
         recon = float(O.round_bf16(nw_g + sh_g))
         u_out = float(bf16_ulp(np.array(ref[i, f])))
         u_sh = float(bf16_ulp(np.array(max(abs(sh_o), abs(sh_g)))))
@@ -285,6 +288,7 @@ def explain_layer_outliers(got, ref, tokens, mid, ws_view, x_bits, wts, d, case,
             token=t, feature=int(f), ref=float(ref[i, f]), got=float(got[i, f]),
             err_over_rms=float(err[i, f] / rms), out_steps=float((got[i, f] - ref[i, f]) / u_out),
             recon_from_gpu_inputs=recon, sh_oracle=sh_o, sh_from_gpu_As=sh_g,
+            sh_gpu_stored=sh_stored,
             sh_steps=(sh_g - sh_o) / u_sh, nw_diff_in_out_steps=(nw_g - nw_o) / u_out,
             N_row_elements_differing=int((n_g != mid["N"][i]).sum()),
             As_row_elements_differing=int((as_g != as_o).sum())))
