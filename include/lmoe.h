@@ -204,9 +204,10 @@ size_t latent_moe_workspace_bytes(const lmoe_dims* dims);
 /*   6 A bf16 [T*k,L]          7 G bf16 [T*k,2d]          8 act bf16 [T*k,d]   */
 /*   9 Y bf16 [T*k,L]         10 N bf16 [T,L]            11 Gs bf16 [T,2ds]    */
 /*  12 As bf16 [T,ds]         13 Sh bf16 [T,H]                                 */
-/* Z and Sh hold data only when the call did not split K (T > 128).  At      */
-/* T > 128, G holds data only if inter % 128 != 0 and Gs only if            */
-/* shared_inter % 128 != 0 (otherwise SituGLU runs in the GEMM's epilogue).   */
+/* Z and Sh hold data only when the call did not split K (T > 128).  G holds */
+/* data only if inter % 128 != 0 (otherwise SituGLU runs in GEMM1's          */
+/* epilogue); at T > 128, Gs only if shared_inter % 128 != 0 (otherwise it   */
+/* runs in the shared GEMM1's epilogue).                                      */
 /* Returns LMOE_OK or a validation error.                                     */
 enum { LMOE_WS_COUNT = 14 };
 int latent_moe_workspace_offsets(const lmoe_dims* dims, size_t* offsets);

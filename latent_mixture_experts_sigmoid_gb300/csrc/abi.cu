@@ -61,6 +61,12 @@ namespace {
 
 constexpr int kDecodeMaxT = 128;
 constexpr int kMaxSplits = 32;
+// Prefill grouped GEMMs: a CTA's unit with at most this many valid token rows
+// runs in the GEMM's swap form (weight halves on M, tokens on N).
+#ifndef LMOE_SWAP_MAX
+#define LMOE_SWAP_MAX 64
+#endif
+constexpr int kSwapMax = LMOE_SWAP_MAX;
 
 bool finite_pos(float x) { return isfinite(x) && x > 0.0f; }
 
@@ -225,6 +231,7 @@ cudaError_t gemm_grouped(const uint16_t* W, int E, int M_feat, const uint16_t* X
   g.out = out;
   g.ldo = fuse_situ ? M_feat / 2 : M_feat;
   g.fuse_situ = fuse_situ;
+  g.swap_max = tok_on_m ? kSwapMax : 0;
   g.beta = beta;
   g.linear_beta = linear_beta;
   const int feat_tile = fuse_situ ? 256 : (tok_on_m ? bn : 128);
@@ -236,7 +243,7 @@ cudaError_t gemm_grouped(const uint16_t* W, int E, int M_feat, const uint16_t* X
 struct Plan {
   int T;
   bool decode;
-  bool fuse_g1;      // GEMM1 with SituGLU in its epilogue (tokens on M, 2*inter % 256 == 0)
+  bool fuse_g1;      // GEMM1 with SituGLU in its epilogue (inter % 128 == 0)
   bool fuse_s1;      // shared GEMM1 likewise (tokens on M, no split-K, shared_inter % 128 == 0)
   int tile;          // token tile of the grouped GEMMs
   int g1_bn, g2_bn;  // MMA N of the grouped GEMMs
@@ -249,8 +256,10 @@ Plan make_plan(const lmoe_dims& d, int nsm) {
   p.decode = d.T <= kDecodeMaxT;
   p.tile = p.decode ? round_up(d.T, 16) : 128;
   p.g1_bn = p.decode ? p.tile : ((2 * d.inter) % 256 == 0 ? 256 : 128);
-  p.fuse_g1 = !p.decode && d.inter % 128 == 0;
-  if (p.fuse_g1) p.g1_bn = 256;
+  // tokens on M: a 256-row B operand of 128 gate + 128 up rows; weights on M
+  // (decode): the two halves as two MMAs of N = tile tokens
+  p.fuse_g1 = d.inter % 128 == 0;
+  if (p.fuse_g1 && !p.decode) p.g1_bn = 256;
   p.g2_bn = p.decode ? p.tile : (d.latent % 256 == 0 ? 256 : 128);
   p.down = dense_cfg(d.T, d.latent, d.hidden, nsm);
   p.s1 = dense_cfg(d.T, 2 * d.shared_inter, d.hidden, nsm);
@@ -651,8 +660,8 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
   // 5-7. experts
   if (pl.fuse_g1) {
     // act = bf16(SituGLU(bf16(A W13_e^T))) straight from GEMM1's epilogue
-    LMOE_TRY(gemm_grouped(wt->w13, E, 2 * dI, ws.A, rows, L, 1, 256, ws, tile, ws.act, s, 1,
-                          d.beta, d.linear_beta));
+    LMOE_TRY(gemm_grouped(wt->w13, E, 2 * dI, ws.A, rows, L, !decode, pl.g1_bn, ws, tile, ws.act,
+                          s, 1, d.beta, d.linear_beta));
     if (!mark(LMOE_STAGE_GEMM1 + 1)) return LMOE_ERR_CUDA;
   } else {
     LMOE_TRY(gemm_grouped(wt->w13, E, 2 * dI, ws.A, rows, L, !decode, pl.g1_bn, ws, tile, ws.G,

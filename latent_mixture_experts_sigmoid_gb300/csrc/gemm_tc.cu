@@ -57,8 +57,17 @@ __device__ int g_device_error = 0;
 
 namespace {
 
-constexpr int BK = 64;                 // K elements per stage (128 bytes of bf16)
-static_assert(BK == 64, "the MMA issue loop unrolls four K=16 steps per stage");
+// K elements per ring stage: 64 (128-byte rows, 128-byte swizzle) or 32
+// (64-byte rows, 64-byte swizzle: the same bytes in flight split into twice as
+// many, half as large stages, so that less of the ring is held by the MMA
+// currently reading it)
+#ifndef LMOE_BK
+#define LMOE_BK 64
+#endif
+constexpr int BK = LMOE_BK;
+static_assert(BK == 64 || BK == 32, "stages are 64 or 32 K elements wide");
+constexpr int kK16 = BK / 16;          // MMAs (K = 16 each) per stage and accumulator
+constexpr int kMaxStages = 12 * 64 / BK;
 constexpr int BM = 128;                // MMA M
 constexpr int kThreads = 192;          // 6 warps
 constexpr long long kWaitCycles = 1ll << 32;   // ~2 s at 2 GHz
@@ -155,15 +164,17 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), version 1.
+// Shared-memory matrix descriptor: K-major operand, rows of BK * 2 bytes
+// swizzled over that width (128-byte swizzle for 128-byte rows, 64-byte
+// swizzle for 64-byte rows), 8-row groups 8 * BK * 2 bytes apart (stride
+// byte offset), version 1.
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;                 // leading byte offset (unused with this swizzle)
-  d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
+  d |= (uint64_t)1 << 16;                 // leading byte offset (unused with swizzling)
+  d |= (uint64_t)((8 * BK * 2) >> 4) << 32;   // stride byte offset
   d |= (uint64_t)1 << 46;                 // descriptor version
-  d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+  d |= (uint64_t)(BK == 64 ? 2 : 4) << 61;    // 128-byte / 64-byte swizzle
   return d;
 }
 
@@ -334,6 +345,18 @@ __host__ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const 
   return x;
 }
 
+// Token columns of a unit computed in the swap form (0: the regular form).
+// Every unit when the launch is swap_all; otherwise, in grouped GEMMs with
+// tokens on M and 256-row weight tiles, a CTA's unit with at most
+// p.swap_max valid token rows: its 128-row token tile is mostly padding, so
+// the two 128-row halves of the weight tile already in shared memory go on
+// the MMA's M side and the first round_up(nvalid, 16) token rows on N.
+__device__ __forceinline__ int swap_cols(const GemmParams& p, int nvalid, bool swap_all) {
+  if (swap_all) return p.bn;
+  if (nvalid > p.swap_max) return 0;
+  return (nvalid + 15) & ~15;
+}
+
 // kPairs: the CTA-pair form (launched in clusters of two; p.mcast is set)
 template <bool kPairs>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -345,7 +368,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int S = p.stages;
   const int bn = p.bn;
   const uint32_t a_bytes = BM * BK * 2;
-  const uint32_t stage_bytes = a_bytes + (uint32_t)bn * BK * 2;
+  // every unit in the swap form with two weight halves (weights on M, tokens
+  // on N: the decode GEMM1 with SituGLU in its epilogue)
+  const bool swap_all = !p.tok_on_m && p.fuse_situ;
+  // weight rows per stage on the M side: one 128-row box, or the two halves
+  const uint32_t w_bytes = (swap_all ? 2u : 1u) * a_bytes;
+  const uint32_t stage_bytes =
+      (p.tok_on_m ? a_bytes : w_bytes) + (uint32_t)bn * BK * 2;
+  // TMEM columns between the two accumulators (a swap_all unit keeps its gate
+  // and up accumulators side by side)
+  const uint32_t acc_stride = swap_all ? 2u * (uint32_t)bn : (uint32_t)bn;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * stage_bytes);
   // bars: full[S], empty[S], tfull[2], tempty[2], done
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
@@ -445,7 +477,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const CUtensorMap* mapW = p.tok_on_m ? &tmB : &tmA;
   const CUtensorMap* mapX = p.tok_on_m ? &tmA : &tmB;
   const uint32_t offW = p.tok_on_m ? a_bytes : 0u;
-  const uint32_t offX = p.tok_on_m ? 0u : a_bytes;
+  const uint32_t offX = p.tok_on_m ? 0u : w_bytes;
   // the weight tile: one box, or (fused SituGLU) 128 gate rows and the 128 up
   // rows of the same features, stacked into one 256-row operand
   auto load_w = [&](uint32_t dst, uint32_t bar, int kb, int row) {
@@ -536,11 +568,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       pdl_wait();
       const int U = total_units<kPairs>(p, tabs, tok_tile, nfeat);
       const uint32_t idesc = idesc_bf16(BM, bn);
-      // descriptors of stage 0; stage s adds s*stage_bytes, each K=16 step adds
-      // 32 bytes (+2 in the 16-byte address field, which never carries out)
-      const uint64_t da0 = sdesc(smem_u32(smem));
-      const uint64_t db0 = sdesc(smem_u32(smem) + a_bytes);
+      // descriptors of stage 0 (A side = the M operand, B side = the N
+      // operand); stage s adds s*stage_bytes, each K=16 step adds 32 bytes (+2
+      // in the 16-byte address field, which never carries out)
+      const uint64_t dx0 = sdesc(smem_u32(smem) + offX);
+      const uint64_t dw0 = sdesc(smem_u32(smem) + offW);
+      const uint64_t da0 = p.tok_on_m ? dx0 : dw0;
+      const uint64_t db0 = p.tok_on_m ? dw0 : dx0;
       const uint64_t dstep = stage_bytes >> 4;
+      constexpr uint64_t kHalf = (BM * BK * 2) >> 4;   // second 128-row weight box
       uint32_t uit = 0, s = 0, ph = 0;
       uint64_t da = da0, db = db0;
       bool ok = true;
@@ -552,15 +588,31 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * bn);
+        const uint32_t d_tmem = tmem_base + (uint32_t)acc * acc_stride;
+        // the swap form: the two 128-row weight halves of the stage on M, the
+        // unit's first bs token rows on N (each half into its own accumulator)
+        const int bs = swap_cols(p, x.nvalid, swap_all);
+        const uint32_t idesc_s = idesc_bf16(BM, bs > 0 ? bs : 16);
         uint32_t accumulate = 0u;
         for (int kb = x.kb0; kb < x.kb1; ++kb) {
           if (!wait_phase(full_bar((int)s), ph, abort_flag, kErrMmaFull)) { ok = false; break; }
           tc_fence_after();
-          mma_bf16(d_tmem, da, db, idesc, accumulate);
-          mma_bf16(d_tmem, da + 2, db + 2, idesc, 1u);
-          mma_bf16(d_tmem, da + 4, db + 4, idesc, 1u);
-          mma_bf16(d_tmem, da + 6, db + 6, idesc, 1u);
+          if (bs > 0) {
+            const uint64_t dX = p.tok_on_m ? da : db;
+            const uint64_t dW = p.tok_on_m ? db : da;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t dh = d_tmem + (uint32_t)(h * bs);
+              const uint64_t wh = dW + (uint64_t)h * kHalf;
+#pragma unroll
+              for (int j = 0; j < kK16; ++j)
+                mma_bf16(dh, wh + 2 * j, dX + 2 * j, idesc_s, j ? 1u : accumulate);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < kK16; ++j)
+              mma_bf16(d_tmem, da + 2 * j, db + 2 * j, idesc, j ? 1u : accumulate);
+          }
           accumulate = 1u;
           if (kPairs) mma_commit_mc(empty_bar((int)s), (uint16_t)3u);
           else mma_commit(empty_bar((int)s));
@@ -586,8 +638,44 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int acc = (int)(uit & 1u);
       if (!wait_bounded(tfull_bar(acc), (uit >> 1) & 1u, abort_flag, kErrEpilogue)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * bn);
-      if (p.tok_on_m && !p.out_fp32) {
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * acc_stride;
+      const int bs = swap_cols(p, x.nvalid, swap_all);
+      if (bs > 0) {
+        // swap form: row r of each weight half, columns = the unit's tokens.
+        // Fused SituGLU: half 0 holds the gate rows and half 1 the up rows of
+        // output features fcol0 + r; otherwise the halves are output features
+        // fcol0 + r and fcol0 + 128 + r.  Both rounded to bf16 first, as the
+        // stored GEMM output would be.
+        const int fcol0 = x.feat_tile * (p.fuse_situ ? BM : 2 * BM);
+        uint16_t* o = reinterpret_cast<uint16_t*>(p.out);
+        for (int c0 = 0; c0 < bs; c0 += 16) {
+          uint32_t g[16], v[16];
+          tmem_ld16(tbase + (uint32_t)c0, g);
+          tmem_ld16(tbase + (uint32_t)(bs + c0), v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; j += 2) {
+            const int t = c0 + j;
+            const uint32_t gb = pack_bf16x2(__uint_as_float(g[j]), __uint_as_float(g[j + 1]));
+            const uint32_t ub = pack_bf16x2(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+            const long long row = (long long)(x.tok_row0 + t);
+            if (p.fuse_situ) {
+              const uint32_t a = situ2(gb, ub, p.sp);
+              if (t < x.nvalid) o[row * p.ldo + fcol0 + r] = (uint16_t)a;
+              if (t + 1 < x.nvalid) o[(row + 1) * p.ldo + fcol0 + r] = (uint16_t)(a >> 16);
+            } else {
+              if (t < x.nvalid) {
+                o[row * p.ldo + fcol0 + r] = (uint16_t)gb;
+                o[row * p.ldo + fcol0 + BM + r] = (uint16_t)ub;
+              }
+              if (t + 1 < x.nvalid) {
+                o[(row + 1) * p.ldo + fcol0 + r] = (uint16_t)(gb >> 16);
+                o[(row + 1) * p.ldo + fcol0 + BM + r] = (uint16_t)(ub >> 16);
+              }
+            }
+          }
+        }
+      } else if (p.tok_on_m && !p.out_fp32) {
         // row r = token, columns = features.  Per 64-column chunk each thread
         // rounds its row to bf16 (after SituGLU when fused, after adding the
         // bf16 addend in fp32 when there is one) into its warp's staging
@@ -765,16 +853,22 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, int K, int box_r
   cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   BK == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-int stages_for(int bn) {
-  const int stage = BM * BK * 2 + bn * BK * 2;
+// Bytes of one ring stage: the M-side operand (one 128-row box; two for the
+// swap form with weight halves) and bn rows of the N-side operand, 64 K wide.
+int stage_bytes_for(int bn, int tok_on_m, int swap_all) {
+  return (tok_on_m ? 1 : (swap_all ? 2 : 1)) * BM * BK * 2 + bn * BK * 2;
+}
+
+int stages_for(int stage) {
   const int budget = 200 * 1024;
   int s = budget / stage;
-  return s > 12 ? 12 : (s < 2 ? 2 : s);
+  return s > kMaxStages ? kMaxStages : (s < 2 ? 2 : s);
 }
 
 // Clusters of two gemm_tc_kernel CTAs that fit on the device at once with
@@ -808,8 +902,7 @@ int max_pairs_resident(size_t smem) {
 
 // ring of stages, barriers, TMEM holder/abort flag, group tables, and (tokens
 // on M only) the epilogue staging buffers; at most 227 KB
-size_t smem_for(int bn, int stages, int groups, int tok_on_m) {
-  const size_t stage = (size_t)BM * BK * 2 + (size_t)bn * BK * 2;
+size_t smem_for(int stage, int stages, int groups, int tok_on_m) {
   return 1024 + stages * stage + (2 * stages + 5) * 8 + 16 +
          (groups ? (size_t)group_table_ints(groups) * 4 : 0) + 16 +
          (tok_on_m ? 4 * 32 * 32 * 4 : 0);
@@ -834,8 +927,14 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
   p.split_stride = g.split_stride;
   p.out_fp32 = g.out_fp32;
   p.add = g.add;
-  p.stages = stages_for(g.bn);
   p.fuse_situ = g.fuse_situ;
+  const int swap_all = !g.tok_on_m && g.fuse_situ;
+  const int stage = stage_bytes_for(g.bn, g.tok_on_m, swap_all);
+  p.stages = stages_for(stage);
+  // the swap form of sparse units needs the 256-row weight tile in two
+  // 128-row halves and a grouped walk with tokens on M
+  p.swap_max = (g.tok_on_m && g.grp_count && g.bn == 256 && g.splits == 1) ? g.swap_max : 0;
+  if (p.swap_max > 64) p.swap_max = 64;
   // CTA pairs with a multicast operand: tokens on M, 256-row weight tiles, and
   // an even count of weight tiles (or, dense, of token tiles)
   {
@@ -846,7 +945,8 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
   }
   p.sp = make_situ_params(g.beta > 0.0f ? g.beta : 1.0f, g.linear_beta);
   uint32_t cols = 32;
-  while (cols < (uint32_t)(2 * g.bn)) cols <<= 1;
+  while (cols < (uint32_t)((swap_all ? 4 : 2) * g.bn)) cols <<= 1;
+  if (cols > 512) return cudaErrorInvalidValue;
   p.tmem_cols = cols;
 
   CUtensorMap mw, mx;
@@ -855,7 +955,7 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
   if (!make_map(&mw, g.W, (long long)g.G * g.M_feat, g.K, w_box)) return cudaErrorInvalidValue;
   if (!make_map(&mx, g.X, g.x_rows, g.K, x_box)) return cudaErrorInvalidValue;
 
-  const size_t smem = smem_for(g.bn, p.stages, g.grp_count ? g.G : 0, g.tok_on_m);
+  const size_t smem = smem_for(stage, p.stages, g.grp_count ? g.G : 0, g.tok_on_m);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(p.mcast ? gemm_tc_kernel<true> : gemm_tc_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

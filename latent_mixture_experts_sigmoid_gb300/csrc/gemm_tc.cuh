@@ -27,8 +27,12 @@ struct GemmParams {
   const uint16_t* add;     // bf16 [rows, ldo] added before rounding, or NULL
   int stages;
   uint32_t tmem_cols;
-  int fuse_situ;           // tokens on M only: W tile = 128 gate rows + the matching 128 up
-                           // rows; the epilogue writes bf16(SituGLU(bf16(G))) [rows, M_feat/2]
+  int fuse_situ;           // W tile = 128 gate rows + the matching 128 up rows; the epilogue
+                           // writes bf16(SituGLU(bf16(G))) [rows, M_feat/2].  Tokens on M:
+                           // one 256-row B operand; weights on M: the two halves as two
+                           // M = 128 MMAs into two accumulators (the swap form)
+  int swap_max;            // grouped, tokens on M, 256-row weight tiles: a CTA's unit with at
+                           // most this many valid token rows (<= 64) runs in the swap form
   int mcast;               // 1: launched in clusters of two CTAs (the gemm_tc_kernel<true>
                            // form) that share an operand tile by TMA multicast; dense or
                            // grouped, tokens on M, 256-row weight tiles, no split-K
@@ -52,7 +56,9 @@ struct GemmDesc {
   long long split_stride;
   const uint16_t* add;
   int max_units;           // > 0: known upper bound on work units (caps the grid)
-  int fuse_situ;           // see GemmParams; requires tok_on_m, bn == 256, splits == 1
+  int fuse_situ;           // see GemmParams; tokens on M: bn == 256; weights on M: bn <= 128;
+                           // splits == 1
+  int swap_max;            // see GemmParams (0: never)
   float beta, linear_beta;
 };
 

@@ -47,8 +47,9 @@ def run_and_check(d, wdev, wor, zipf, toks):
     Gref = np.stack([O.linear_bf16(f(v["A"][r:r + 1]), wor["w13"](e))[0]
                      for r, e in zip(rr, ids.ravel())])
     act = f(v["act"][rr])
-    if T > 128 and dI % 128 == 0:
-        # prefill: SituGLU runs in GEMM1's epilogue, G is never stored
+    if dI % 128 == 0:
+        # SituGLU runs in GEMM1's epilogue (tokens on M at prefill, weight
+        # halves on M at decode), G is never stored
         res.append(assert_gemm_situ_close(act, Gref, d.beta, d.linear_beta, "gemm1+situ"))
     else:
         G = f(v["G"][rr])
