@@ -35,6 +35,8 @@ the design notes):
   R-8 the shared expert is a SituGLU MLP on the original hidden states, with
       the same beta / linear_beta, unscaled;
   R-10 no linear biases;
+  R-19 router GEMM: fp32 logits = X W_router^T from a bf16 [E, H] weight,
+       rounded once to float32;
   R-11 expert_num_tokens outside [0, T_max] is clamped.
 
 Parity status: every function below is pinned by ``tests/test_oracle_*.py``
@@ -275,6 +277,22 @@ def rms_norm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
     return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * gamma
 
 
+def router_gemm(hidden_bits: np.ndarray, w_router_bits: np.ndarray) -> np.ndarray:
+    """Router logits, float32 [T, E] = fp32(X W_router^T) for bf16 hidden states
+    X [T, H] and a bf16 router weight W_router [E, H] (PyTorch Linear layout, no
+    bias).
+
+    [TRTLLM-20541] Commit 2: the router GEMM runs on the hidden states ahead of
+    the routing kernel (its own stream, or fused with the latent down
+    projection in the "fused router+down projection" configuration);
+    [vLLM-50088] commit 4: DeepSeekV3 routing takes FP32 logits.  The product is
+    formed in float64 and rounded once to float32.
+    """
+    X = bf16_to_f64(hidden_bits)
+    Wr = bf16_to_f64(w_router_bits)
+    return (X @ Wr.T).astype(np.float32)
+
+
 def _expert(W: dict, name: str, e: int) -> np.ndarray:
     v = W[name]
     return v(int(e)) if callable(v) else v[int(e)]
@@ -339,3 +357,17 @@ def latent_moe_forward(dims, W: dict, hidden_bits: np.ndarray, logits: np.ndarra
     if not intermediates:
         return out_bits
     return out_bits, dict(ids=ids, weights=w, Z=Z, Y=Y, C=C, N=N, Sh=Sh)
+
+
+def latent_moe_forward_router(dims, W: dict, hidden_bits: np.ndarray, w_router_bits: np.ndarray,
+                              intermediates: bool = False):
+    """The layer forward with the router GEMM in front of it: the logits are
+    router_gemm(hidden, w_router) and everything else is latent_moe_forward
+    ([TRTLLM-20541] Commit 2: router GEMM -> routing -> routed MoE, with the
+    latent down projection on the same hidden states)."""
+    logits = router_gemm(hidden_bits, w_router_bits)
+    res = latent_moe_forward(dims, W, hidden_bits, logits, intermediates)
+    if not intermediates:
+        return res
+    out, mid = res
+    return out, dict(mid, logits=logits)

@@ -7,10 +7,12 @@ from oracle import lmoe_oracle as O
 import tests.test_oracle_numerics as N
 import tests.test_oracle_route as R
 import tests.test_oracle_layer as L
+import tests.test_oracle_router as RG
 
 _route = O.route
 _situ = O.situ
 _permute = O.permute
+_router_gemm = O.router_gemm
 
 
 def _situ_no_sigmoid(g, u, beta, lb):
@@ -63,6 +65,18 @@ def _rms_norm_eps_outside_root(x, gamma, eps):
     return x / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + eps) * gamma
 
 
+def _router_gemm_bf16_logits(x_bits, w_bits):
+    return O.round_bf16(_router_gemm(x_bits, w_bits)).astype(np.float32)
+
+
+def _router_gemm_rows_reversed(x_bits, w_bits):
+    return _router_gemm(x_bits, w_bits[::-1].copy())
+
+
+def _router_gemm_features_reversed(x_bits, w_bits):
+    return _router_gemm(x_bits[:, ::-1].copy(), w_bits)
+
+
 def _permute_descending(ids, E):
     counts, offsets, row_of, tok_of_row = _permute(ids[::-1].copy(), E)
     return counts, offsets, row_of[::-1].copy(), (ids.shape[0] - 1 - tok_of_row).astype(np.int32)
@@ -81,6 +95,9 @@ MUTATIONS = [
     ("rms_norm", _rms_norm_gamma_divided, L.check_rms_norm_gamma_multiplies),
     ("rms_norm", _rms_norm_gamma_divided, L.check_layer_gamma_power_of_two_scales_the_norm_output),
     ("rms_norm", _rms_norm_eps_outside_root, L.check_rms_norm_constant_row_closed_form),
+    ("router_gemm", _router_gemm_bf16_logits, RG.check_two_hot_router_rows_sum_in_fp32),
+    ("router_gemm", _router_gemm_rows_reversed, RG.check_one_hot_router_rows_pick_features),
+    ("router_gemm", _router_gemm_features_reversed, RG.check_one_hot_router_rows_pick_features),
     ("permute", _permute_descending, lambda: R.check_permute(
         np.stack([np.random.default_rng(t).permutation(16)[:3] for t in range(20)]).astype(np.int32), 16)),
 ]

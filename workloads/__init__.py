@@ -14,7 +14,8 @@ drawing the rest):
 * floats are drawn as float32 ``standard_normal`` and scaled; bf16 tensors are
   the round-to-nearest-even bf16 of those float32 draws (torch's conversion),
   carried as raw ``uint16`` bits;
-* weights are N(0, 0.02^2), hidden states N(0, 1), router logits N(0, 1), the
+* weights are N(0, 0.02^2) (the router weight N(0, 1/hidden), so that its
+  logits are about N(0, 1)), hidden states N(0, 1), router logits N(0, 1), the
   selection bias N(0, 0.1^2) in float32, RMSNorm gamma = 1 (or 1 + N(0, 0.02^2)
   when ``gamma_noise`` is set);
 * the routing-alone workload makes every 64th token (t % 64 == 0) a row of
@@ -45,6 +46,7 @@ import torch
 S_LOGITS, S_BIAS, S_ZIPF, S_W_DOWN, S_W13, S_W2 = 1, 2, 3, 4, 5, 6
 S_WS13, S_WS2, S_NORM, S_W_UP, S_HIDDEN = 7, 8, 9, 10, 11
 S_SITU, S_SITU_MASK, S_SITU_SIGN, S_COUNTS = 12, 13, 14, 15
+S_W_ROUTER = 16
 
 ROW_BLOCK = 64          # rows per independent stream in dense matrices
 SENTINEL = 0xDEAD       # bf16 bit pattern for padded rows
@@ -162,6 +164,13 @@ def w13_all(d: LayerDims, seed: int = 0) -> np.ndarray:
 def w2_all(d: LayerDims, seed: int = 0) -> np.ndarray:
     """All experts' down weights, bf16 bits [E, latent, inter]."""
     return _stack_experts(d, w2_expert, seed)
+
+
+def w_router(d: LayerDims, seed: int = 0) -> np.ndarray:
+    """Router weight, bf16 bits [num_experts, hidden], N(0, 1/hidden): with N(0,1)
+    hidden states the router logits are about N(0,1), like the logits of the
+    routing workloads."""
+    return _normal_rows(seed, S_W_ROUTER, d.num_experts, d.hidden, float(d.hidden) ** -0.5)
 
 
 def norm_weight(d: LayerDims, seed: int = 0, gamma_noise: bool = False) -> np.ndarray:
