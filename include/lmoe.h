@@ -204,12 +204,14 @@ size_t latent_moe_workspace_bytes(const lmoe_dims* dims);
 /*   6 A bf16 [T*k,L]          7 G bf16 [T*k,2d]          8 act bf16 [T*k,d]   */
 /*   9 Y bf16 [T*k,L]         10 N bf16 [T,L]            11 Gs bf16 [T,2ds]    */
 /*  12 As bf16 [T,ds]         13 Sh bf16 [T,H]                                 */
+/*  14 logits fp32 [T, Ep] with Ep = E rounded up to a multiple of 128 (the   */
+/*     router logits of latent_moe_forward_router, columns E..Ep-1 unused)    */
 /* Z and Sh hold data only when the call did not split K (T > 128).  G holds */
 /* data only if inter % 128 != 0 (otherwise SituGLU runs in GEMM1's          */
 /* epilogue); at T > 128, Gs only if shared_inter % 128 != 0 (otherwise it   */
 /* runs in the shared GEMM1's epilogue).                                      */
 /* Returns LMOE_OK or a validation error.                                     */
-enum { LMOE_WS_COUNT = 14 };
+enum { LMOE_WS_COUNT = 15 };
 int latent_moe_workspace_offsets(const lmoe_dims* dims, size_t* offsets);
 
 /* Number of kernel launches latent_moe_forward makes for these dims (0 on   */
@@ -254,6 +256,43 @@ int latent_moe_forward_routed(const lmoe_dims* dims, const lmoe_weights* weights
                               const lmoe_bf16* hidden, const int32_t* topk_ids,
                               const float* topk_weights, lmoe_bf16* out, void* workspace,
                               size_t workspace_bytes, const lmoe_debug* dbg, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Router GEMM ([TRTLLM-20541] Commit 2: the router GEMM produces the logits */
+/* the routing kernel reads; "fused router+down projection" is the           */
+/* configuration that computes it in one pass with the latent down           */
+/* projection; [vLLM-50088] commit 4: DeepSeekV3 routing takes FP32 logits): */
+/*                                                                            */
+/*   logits[t, e] = sum_h hidden[t, h] * w_router[e, h]   (fp32 accumulation, */
+/*                                                         stored fp32)       */
+/*                                                                            */
+/* hidden [T, H] bf16, w_router [E, H] bf16 (PyTorch Linear layout, no bias), */
+/* logits [T, E] fp32 output.  Requires 1 <= E <= 1024, H % 64 == 0, T >= 0. */
+/* The workspace (at least lmoe_router_logits_workspace_bytes(T, E, H)       */
+/* bytes, 256-byte aligned) holds split-K partials at T <= 128 and padded    */
+/* rows when E % 128 != 0.                                                    */
+/* ------------------------------------------------------------------------ */
+size_t lmoe_router_logits_workspace_bytes(int T, int E, int H);
+int lmoe_router_logits(const lmoe_bf16* hidden, const lmoe_bf16* w_router, float* logits, int T,
+                       int E, int H, void* workspace, size_t workspace_bytes, void* stream);
+
+/* The layer forward with its router GEMM: latent_moe_forward on the logits  */
+/* hidden W_router^T (fp32, as lmoe_router_logits computes them) instead of   */
+/* logits passed in.  w_router [num_experts, hidden] bf16.  At T <= 128 the  */
+/* router rows are stacked after the down-projection's rows in one split-K   */
+/* GEMM launch over the hidden states (the fused router + down projection;   */
+/* a small kernel sums the logit partials for the routing); above, the       */
+/* router GEMM is its own launch ahead of the routing (on the second stream, */
+/* beside the down-projection).  Same workspace, limits and errors as         */
+/* latent_moe_forward; the logits are left in the workspace (entry 14).      */
+int latent_moe_forward_router(const lmoe_dims* dims, const lmoe_weights* weights,
+                              const lmoe_bf16* w_router, const lmoe_bf16* hidden, lmoe_bf16* out,
+                              void* workspace, size_t workspace_bytes, const lmoe_debug* dbg,
+                              void* stream);
+
+/* Kernel launches of latent_moe_forward_router for these dims (0 on invalid */
+/* dims), as latent_moe_launch_count counts them.                             */
+int latent_moe_launch_count_router(const lmoe_dims* dims, int has_shared_expert);
 
 /* The layer forward without a caller workspace.  The pages have no          */
 /* counterpart to this entry point; it exists for callers that cannot         */

@@ -29,7 +29,9 @@ ABI_FUNCTIONS = ("moe_route", "situ_and_mul", "masked_situ_and_mul", "latent_moe
                  "latent_moe_forward_routed",
                  "latent_moe_forward_noalloc", "latent_moe_workspace_bytes", "latent_moe_workspace_offsets",
                  "latent_moe_launch_count", "lmoe_linear", "lmoe_status_string",
-                 "lmoe_device_error", "lmoe_abi_version", "lmoe_gemm_unit_walk")
+                 "lmoe_device_error", "lmoe_abi_version", "lmoe_gemm_unit_walk",
+                 "lmoe_router_logits", "lmoe_router_logits_workspace_bytes",
+                 "latent_moe_forward_router", "latent_moe_launch_count_router")
 
 
 class LmoeError(RuntimeError):
@@ -112,6 +114,16 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.lmoe_abi_version.restype = i32
     lib.lmoe_gemm_unit_walk.argtypes = [i32, vp, i32, i32, vp, i32]
     lib.lmoe_gemm_unit_walk.restype = i32
+    lib.lmoe_router_logits_workspace_bytes.argtypes = [i32, i32, i32]
+    lib.lmoe_router_logits_workspace_bytes.restype = ctypes.c_size_t
+    lib.lmoe_router_logits.argtypes = [vp, vp, vp, i32, i32, i32, vp, ctypes.c_size_t, vp]
+    lib.lmoe_router_logits.restype = i32
+    lib.latent_moe_forward_router.argtypes = [ctypes.POINTER(LmoeDims), ctypes.POINTER(LmoeWeights),
+                                              vp, vp, vp, vp, ctypes.c_size_t,
+                                              ctypes.POINTER(LmoeDebug), vp]
+    lib.latent_moe_forward_router.restype = i32
+    lib.latent_moe_launch_count_router.argtypes = [ctypes.POINTER(LmoeDims), i32]
+    lib.latent_moe_launch_count_router.restype = i32
     _lib = lib
     return lib
 
@@ -340,7 +352,7 @@ def latent_moe_forward_noalloc(dims, weights, hidden, router_logits, out, stream
 
 
 WS_NAMES = ("topk_ids", "topk_weights", "counts", "offsets", "row_of", "Z", "A", "G", "act",
-            "Y", "N", "Gs", "As", "Sh")
+            "Y", "N", "Gs", "As", "Sh", "logits")
 
 
 def latent_moe_workspace_offsets(dims) -> dict:
@@ -379,3 +391,44 @@ def gemm_unit_walk(counts, nfeat: int, paired: bool):
     _check(min(0, lib.lmoe_gemm_unit_walk(len(c), c.ctypes.data, nfeat, int(paired),
                                           out.ctypes.data, n)), "lmoe_gemm_unit_walk")
     return out
+
+
+def lmoe_router_logits_workspace_bytes(T: int, E: int, H: int) -> int:
+    return int(load_library().lmoe_router_logits_workspace_bytes(int(T), int(E), int(H)))
+
+
+def lmoe_router_logits(hidden, w_router, logits, workspace, stream=None,
+                       T: int | None = None, E: int | None = None, H: int | None = None):
+    """Router GEMM: logits [T, E] fp32 = hidden [T, H] @ w_router [E, H]^T."""
+    if T is None:
+        T, H = hidden.shape
+        E = w_router.shape[0]
+    T, E, H = int(T), int(E), int(H)
+    wsp, wsn = _workspace(workspace, None)
+    st = load_library().lmoe_router_logits(_dev(hidden, "hidden", _BF16, T * H),
+                                           _dev(w_router, "w_router", _BF16, E * H),
+                                           _dev(logits, "logits", torch.float32, T * E),
+                                           T, E, H, wsp, wsn, _stream(stream))
+    _check(st, "lmoe_router_logits")
+
+
+def latent_moe_forward_router(dims, weights, w_router, hidden, out, workspace,
+                              workspace_bytes: int | None = None, debug: dict | None = None,
+                              stream=None):
+    """The layer forward with its router GEMM (logits = hidden @ w_router^T)."""
+    dd = dims if isinstance(dims, LmoeDims) else make_dims(dims)
+    ww = weights if isinstance(weights, LmoeWeights) else make_weights(weights, dd)
+    T, H, E = int(dd.T), int(dd.hidden), int(dd.num_experts)
+    wsp, wsn = _workspace(workspace, workspace_bytes)
+    dbg, keep = _debug_struct(debug, dd)
+    st = load_library().latent_moe_forward_router(
+        ctypes.byref(dd), ctypes.byref(ww), _dev(w_router, "w_router", _BF16, E * H),
+        _dev(hidden, "hidden", _BF16, T * H), _dev(out, "out", _BF16, T * H), wsp, wsn,
+        ctypes.byref(dbg) if dbg is not None else None, _stream(stream))
+    _check(st, "latent_moe_forward_router")
+
+
+def latent_moe_launch_count_router(dims, has_shared_expert: bool = True) -> int:
+    dd = dims if isinstance(dims, LmoeDims) else make_dims(dims)
+    return int(load_library().latent_moe_launch_count_router(ctypes.byref(dd),
+                                                              1 if has_shared_expert else 0))

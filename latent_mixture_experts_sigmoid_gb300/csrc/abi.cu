@@ -122,8 +122,12 @@ struct Ws {
   int32_t* counts; int32_t* offsets; int32_t* tile_prefix; int32_t* row_of; int32_t* tok_of_row;
   void* perm_scratch;
   uint16_t *Z, *A, *G, *act, *Y, *N, *Gs, *As, *Sh;
+  float *logits;   // router logits [T, round_up(E, 128)] of the router-GEMM forward
   float *Pa, *Pb;
 };
+
+// Router logits rows are padded to whole 128-row weight tiles of the router GEMM.
+size_t padded_experts(int E) { return (size_t)round_up(E, 128); }
 
 size_t carve(const lmoe_dims& d, char* base, Ws* ws) {
   Carver c;
@@ -148,8 +152,12 @@ size_t carve(const lmoe_dims& d, char* base, Ws* ws) {
   w.Gs = c.take<uint16_t>(T * 2 * ds);
   w.As = c.take<uint16_t>(T * ds);
   w.Sh = c.take<uint16_t>(T * H);
+  const size_t Ep = padded_experts(d.num_experts);
+  w.logits = c.take<float>(T * Ep);
   if (d.T <= kDecodeMaxT) {
-    const size_t ma = L > H ? L : H;
+    // split-K partials: the down-projection (with the router rows after the
+    // latent ones in the router-GEMM forward) and the up-projection
+    const size_t ma = (L + Ep > H) ? L + Ep : H;
     const size_t mb = (2 * ds > H) ? 2 * ds : H;
     w.Pa = c.take<float>((size_t)kMaxSplits * T * ma);
     w.Pb = c.take<float>((size_t)kMaxSplits * T * mb);
@@ -185,9 +193,14 @@ int validate_dims(const lmoe_dims* d) {
 cudaError_t gemm_dense(const uint16_t* W, int M_feat, const uint16_t* X, int T, int K,
                        const DenseCfg& c, void* out, int out_fp32, long long split_stride,
                        const uint16_t* add, cudaStream_t s, int fuse_situ = 0, float beta = 1.0f,
-                       float linear_beta = 0.0f) {
+                       float linear_beta = 0.0f, long long w_rows = 0,
+                       const uint16_t* W2 = nullptr, long long w2_rows = 0, int w2_row0 = 0) {
   GemmDesc g{};
   g.W = W;
+  g.w_rows = w_rows;
+  g.W2 = W2;
+  g.w2_rows = w2_rows;
+  g.w2_row0 = w2_row0;
   g.X = X;
   g.x_rows = T;
   g.K = K;
@@ -243,17 +256,23 @@ cudaError_t gemm_grouped(const uint16_t* W, int E, int M_feat, const uint16_t* X
 struct Plan {
   int T;
   bool decode;
+  bool router;       // the forward computes its router logits (router GEMM)
+  int Ep;            // experts padded to whole 128-row router tiles
   bool fuse_g1;      // GEMM1 with SituGLU in its epilogue (inter % 128 == 0)
   bool fuse_s1;      // shared GEMM1 likewise (tokens on M, no split-K, shared_inter % 128 == 0)
   int tile;          // token tile of the grouped GEMMs
   int g1_bn, g2_bn;  // MMA N of the grouped GEMMs
   DenseCfg down, s1, s2, up;
+  DenseCfg rtr;      // the router GEMM: at decode stacked after the down-projection's rows
+                     // (one launch), otherwise its own launch
 };
 
-Plan make_plan(const lmoe_dims& d, int nsm) {
+Plan make_plan(const lmoe_dims& d, int nsm, bool router = false) {
   Plan p;
   p.T = d.T;
   p.decode = d.T <= kDecodeMaxT;
+  p.router = router;
+  p.Ep = (int)padded_experts(d.num_experts);
   p.tile = p.decode ? round_up(d.T, 16) : 128;
   p.g1_bn = p.decode ? p.tile : ((2 * d.inter) % 256 == 0 ? 256 : 128);
   // tokens on M: a 256-row B operand of 128 gate + 128 up rows; weights on M
@@ -261,7 +280,8 @@ Plan make_plan(const lmoe_dims& d, int nsm) {
   p.fuse_g1 = d.inter % 128 == 0;
   if (p.fuse_g1 && !p.decode) p.g1_bn = 256;
   p.g2_bn = p.decode ? p.tile : (d.latent % 256 == 0 ? 256 : 128);
-  p.down = dense_cfg(d.T, d.latent, d.hidden, nsm);
+  p.down = dense_cfg(d.T, router && p.decode ? d.latent + p.Ep : d.latent, d.hidden, nsm);
+  p.rtr = dense_cfg(d.T, p.Ep, d.hidden, nsm);
   p.s1 = dense_cfg(d.T, 2 * d.shared_inter, d.hidden, nsm);
   p.fuse_s1 = p.s1.tok_on_m && p.s1.splits == 1 && p.s1.bn == 256 && d.shared_inter % 128 == 0;
   p.s2 = dense_cfg(d.T, d.hidden, d.shared_inter, nsm);
@@ -280,6 +300,9 @@ int plan_launches(const Plan& p, bool shared) {
   n += 1;                               // up-projection GEMM
   const bool sh_part = shared && p.s2.splits > 1;
   if (p.up.splits > 1 || sh_part) n += 1;   // fixed-order reduction
+  // router GEMM: at decode it shares the down-projection's launch and a
+  // kernel sums its split-K partials; otherwise it is a launch of its own
+  if (p.router) n += 1;
   return n;
 }
 
@@ -409,7 +432,7 @@ int moe_route(const float* router_logits, const float* bias, int T, int E, int t
       (bias && !aligned16(bias)))
     return LMOE_ERR_ALIGN;
   if (!on_current_device({router_logits, bias, topk_ids, topk_weights})) return LMOE_ERR_DEVICE;
-  if (launch_route(router_logits, bias, T, E, topk, renormalize, rsf, topk_ids, topk_weights,
+  if (launch_route(router_logits, E, bias, T, E, topk, renormalize, rsf, topk_ids, topk_weights,
                    (cudaStream_t)stream) != cudaSuccess)
     return LMOE_ERR_CUDA;
   return LMOE_OK;
@@ -466,7 +489,7 @@ int latent_moe_workspace_offsets(const lmoe_dims* dims, size_t* offsets) {
   char* const base = reinterpret_cast<char*>(256);   // never dereferenced
   carve(*dims, base, &w);
   const void* p[LMOE_WS_COUNT] = {w.ids, w.w, w.counts, w.offsets, w.row_of, w.Z, w.A,
-                                  w.G, w.act, w.Y, w.N, w.Gs, w.As, w.Sh};
+                                  w.G, w.act, w.Y, w.N, w.Gs, w.As, w.Sh, w.logits};
   for (int i = 0; i < LMOE_WS_COUNT; ++i)
     offsets[i] = (size_t)(reinterpret_cast<const char*>(p[i]) - base);
   return LMOE_OK;
@@ -489,14 +512,18 @@ size_t latent_moe_workspace_bytes(const lmoe_dims* dims) {
 // the current device), so its pointer is not queried.
 static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe_bf16* hidden,
                         const float* router_logits, const int32_t* pre_ids, const float* pre_w,
-                        lmoe_bf16* out, void* workspace, size_t workspace_bytes,
-                        const lmoe_debug* dbg, void* stream, bool own_workspace) {
+                        const lmoe_bf16* w_router, lmoe_bf16* out, void* workspace,
+                        size_t workspace_bytes, const lmoe_debug* dbg, void* stream,
+                        bool own_workspace) {
   const int v = validate_dims(dims);
   if (v != LMOE_OK) return v;
   if (!wt) return LMOE_ERR_NULL;
   const lmoe_dims d = *dims;
   if (d.T == 0) return LMOE_OK;
-  const bool pre_routed = router_logits == nullptr;
+  // exactly one routing source: the caller's logits, the router GEMM on
+  // w_router, or ids and weights routed ahead
+  const bool router = w_router != nullptr;
+  const bool pre_routed = !router && router_logits == nullptr;
   if (!hidden || (pre_routed && (!pre_ids || !pre_w)) || !out || !wt->w_down || !wt->w13 ||
       !wt->w2 || !wt->w_up)
     return LMOE_ERR_NULL;
@@ -504,7 +531,8 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
   if (shared != (wt->ws2 != nullptr)) return LMOE_ERR_NULL;
   if (shared && d.shared_inter <= 0) return LMOE_ERR_DIM;
   const void* ptrs[] = {hidden, router_logits, pre_ids, pre_w, out, wt->w_down, wt->w13, wt->w2,
-                        wt->w_up, wt->ws13, wt->ws2, wt->norm_w, wt->e_score_correction_bias};
+                        wt->w_up, wt->ws13, wt->ws2, wt->norm_w, wt->e_score_correction_bias,
+                        w_router};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return LMOE_ERR_ALIGN;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return LMOE_ERR_WORKSPACE;
@@ -519,7 +547,7 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
   }
   if (!on_current_device({hidden, router_logits, pre_ids, pre_w, out, wt->w_down, wt->w13, wt->w2,
                           wt->w_up, wt->ws13, wt->ws2, wt->norm_w, wt->e_score_correction_bias,
-                          own_workspace ? nullptr : workspace}))
+                          w_router, own_workspace ? nullptr : workspace}))
     return LMOE_ERR_DEVICE;
   if (dbg && !on_current_device({dbg->topk_ids, dbg->topk_weights, dbg->expert_num_tokens,
                                  dbg->expert_offsets, dbg->row_of}))
@@ -535,7 +563,8 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
   if (pre_routed && !id_err) return LMOE_ERR_CUDA;
   const int dI = d.inter, ds = d.shared_inter;
   const long long rows = (long long)T * k;
-  const Plan pl = make_plan(d, num_sms());
+  const Plan pl = make_plan(d, num_sms(), router);
+  const int Ep = pl.Ep;
   const bool decode = pl.decode;
   const int tile = pl.tile;
   const uint16_t* X = hidden;
@@ -598,9 +627,19 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
   // stream, beside the down-projection (which leaves SMs idle in its last
   // wave), and the caller's stream waits for them before the scatter (at
   // decode sizes this measured slower: they stay on the caller's stream)
+  // the logits the routing reads: the caller's [T, E], or the router GEMM's
+  // [T, Ep] in the workspace
+  const float* lg = router ? ws.logits : router_logits;
+  const long long lg_ld = router ? Ep : E;
   auto route_and_permute = [&](cudaStream_t rs, bool marks) -> int {
+    if (router && !decode) {
+      // router GEMM of its own (fp32 logits straight from the epilogue)
+      DenseCfg cr = pl.rtr;
+      LMOE_TRY(gemm_dense(w_router, Ep, X, T, H, cr, ws.logits, 1, 0, nullptr, rs, 0, 1.0f, 0.0f,
+                          E));
+    }
     if (!pre_routed)
-      LMOE_TRY(launch_route(router_logits, wt->e_score_correction_bias, T, E, k, d.renormalize,
+      LMOE_TRY(launch_route(lg, lg_ld, wt->e_score_correction_bias, T, E, k, d.renormalize,
                             d.routed_scaling_factor, ws.ids, ws.w, rs));
     if (marks && !mark(LMOE_STAGE_ROUTE + 1)) return LMOE_ERR_CUDA;
     return LMOE_OK;
@@ -625,16 +664,32 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
     if (st != LMOE_OK) return st;
     if (cudaEventRecord(aux->join, aux->stream) != cudaSuccess) return LMOE_ERR_CUDA;
   }
-  if (!side_route) {
+  // 2. latent down-projection.  Router GEMM at decode sizes: the router rows
+  // follow the latent rows in one split-K launch over the hidden states
+  // (fp32 partials [splits][T][L + Ep]), a kernel sums the logit columns and
+  // the routing reads them; the per-stage events then show the router GEMM,
+  // the sum and the routing as the routing stage and the down-projection as
+  // an empty stage.
+  const bool stacked = router && decode;
+  const DenseCfg cdown = pl.down;
+  const bool down_split = cdown.splits > 1 || stacked;
+  const int ldz = stacked ? L + Ep : L;
+  const long long down_stride = (long long)T * ldz;
+  if (!side_route && !stacked) {
     st = route_and_permute(s, true);
     if (st != LMOE_OK) return st;
   }
-  // 2. latent down-projection
-  const DenseCfg cdown = pl.down;
-  const bool down_split = cdown.splits > 1;
-  const long long down_stride = (long long)T * L;
-  LMOE_TRY(gemm_dense(wt->w_down, L, X, T, H, cdown, down_split ? (void*)ws.Pa : (void*)ws.Z,
-                      down_split, down_stride, nullptr, s));
+  if (stacked) {
+    LMOE_TRY(gemm_dense(wt->w_down, L + Ep, X, T, H, cdown, ws.Pa, 1, down_stride, nullptr, s, 0,
+                        1.0f, 0.0f, 0, w_router, E, L));
+    LMOE_TRY(launch_sum_splits_cols(ws.Pa, cdown.splits, down_stride, T, ldz, L, E, Ep, ws.logits,
+                                    s));
+    st = route_and_permute(s, true);
+    if (st != LMOE_OK) return st;
+  } else {
+    LMOE_TRY(gemm_dense(wt->w_down, L, X, T, H, cdown, down_split ? (void*)ws.Pa : (void*)ws.Z,
+                        down_split, down_stride, nullptr, s));
+  }
   if (!mark(LMOE_STAGE_DOWN + 1)) return LMOE_ERR_CUDA;
   // small T: permutation and scatter in one launch (every block rebuilds the
   // small counting sort); large T: the scatter after the separate permutation
@@ -646,7 +701,7 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
                                           ws.tile_prefix, ws.row_of, ws.tok_of_row,
                                           down_split ? nullptr : ws.Z,
                                           down_split ? ws.Pa : nullptr, cdown.splits, down_stride,
-                                          L, ws.A, id_err, s));
+                                          ldz, L, ws.A, id_err, s));
   } else {
     st = permute(s);
     if (st != LMOE_OK) return st;
@@ -655,7 +710,7 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
   // 4. routed input into the expert-major rows
   if (!fused_scatter)
     LMOE_TRY(launch_scatter_rows(down_split ? nullptr : ws.Z, down_split ? ws.Pa : nullptr,
-                                 cdown.splits, down_stride, T, L, k, ws.row_of, ws.A, s));
+                                 cdown.splits, down_stride, ldz, T, L, k, ws.row_of, ws.A, s));
   if (!mark(LMOE_STAGE_SCATTER + 1)) return LMOE_ERR_CUDA;
   // 5-7. experts
   if (pl.fuse_g1) {
@@ -719,15 +774,68 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
 int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* wt, const lmoe_bf16* hidden,
                        const float* router_logits, lmoe_bf16* out, void* workspace,
                        size_t workspace_bytes, const lmoe_debug* dbg, void* stream) {
-  return forward_impl(dims, wt, hidden, router_logits, nullptr, nullptr, out, workspace,
+  return forward_impl(dims, wt, hidden, router_logits, nullptr, nullptr, nullptr, out, workspace,
                       workspace_bytes, dbg, stream, false);
+}
+
+int latent_moe_forward_router(const lmoe_dims* dims, const lmoe_weights* wt,
+                              const lmoe_bf16* w_router, const lmoe_bf16* hidden, lmoe_bf16* out,
+                              void* workspace, size_t workspace_bytes, const lmoe_debug* dbg,
+                              void* stream) {
+  if (dims && dims->T != 0 && !w_router) return LMOE_ERR_NULL;
+  return forward_impl(dims, wt, hidden, nullptr, nullptr, nullptr, w_router, out, workspace,
+                      workspace_bytes, dbg, stream, false);
+}
+
+int latent_moe_launch_count_router(const lmoe_dims* dims, int has_shared_expert) {
+  if (validate_dims(dims) != LMOE_OK) return 0;
+  if (dims->T == 0) return 0;
+  return plan_launches(make_plan(*dims, num_sms(), true), has_shared_expert != 0);
+}
+
+size_t lmoe_router_logits_workspace_bytes(int T, int E, int H) {
+  if (T < 0 || E < 1 || E > 1024 || H <= 0 || H % 64) return 0;
+  const size_t Ep = padded_experts(E);
+  size_t n = 0;
+  if (T <= kDecodeMaxT) n = (size_t)kMaxSplits * T * Ep * 4;   // split-K partials
+  else if ((size_t)E != Ep) n = (size_t)T * Ep * 4;          // padded rows
+  return ((n + 255) & ~size_t(255)) + 256;
+}
+
+int lmoe_router_logits(const lmoe_bf16* hidden, const lmoe_bf16* w_router, float* logits, int T,
+                       int E, int H, void* workspace, size_t workspace_bytes, void* stream) {
+  const size_t need = lmoe_router_logits_workspace_bytes(T, E, H);
+  if (need == 0) return LMOE_ERR_DIM;
+  if (T == 0) return LMOE_OK;
+  if (!hidden || !w_router || !logits) return LMOE_ERR_NULL;
+  if (!aligned16(hidden) || !aligned16(w_router) || !aligned16(logits)) return LMOE_ERR_ALIGN;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return LMOE_ERR_WORKSPACE;
+  if (!on_current_device({hidden, w_router, logits, workspace})) return LMOE_ERR_DEVICE;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int Ep = (int)padded_experts(E);
+  const DenseCfg c = dense_cfg(T, Ep, H, num_sms());
+  float* P = static_cast<float*>(workspace);
+  if (!c.tok_on_m) {
+    // weights on M, split K: fp32 partials, then their fixed-order sum
+    const long long stride = (long long)T * Ep;
+    LMOE_TRY(gemm_dense(w_router, Ep, hidden, T, H, c, P, 1, stride, nullptr, s, 0, 1.0f, 0.0f,
+                        E));
+    LMOE_TRY(launch_sum_splits_cols(P, c.splits, stride, T, Ep, 0, E, E, logits, s));
+  } else if (E == Ep) {
+    LMOE_TRY(gemm_dense(w_router, Ep, hidden, T, H, c, logits, 1, 0, nullptr, s));
+  } else {
+    LMOE_TRY(gemm_dense(w_router, Ep, hidden, T, H, c, P, 1, 0, nullptr, s, 0, 1.0f, 0.0f, E));
+    LMOE_TRY(launch_sum_splits_cols(P, 1, 0, T, Ep, 0, E, E, logits, s));
+  }
+  return LMOE_OK;
 }
 
 int latent_moe_forward_routed(const lmoe_dims* dims, const lmoe_weights* wt,
                               const lmoe_bf16* hidden, const int32_t* topk_ids,
                               const float* topk_weights, lmoe_bf16* out, void* workspace,
                               size_t workspace_bytes, const lmoe_debug* dbg, void* stream) {
-  return forward_impl(dims, wt, hidden, nullptr, topk_ids, topk_weights, out, workspace,
+  return forward_impl(dims, wt, hidden, nullptr, topk_ids, topk_weights, nullptr, out, workspace,
                       workspace_bytes, dbg, stream, false);
 }
 
@@ -738,7 +846,7 @@ int forward_on_library_scratch(const lmoe_dims* dims, const lmoe_weights* wt,
                                const lmoe_bf16* hidden, const float* router_logits,
                                lmoe_bf16* out, void* scratch, size_t scratch_bytes,
                                const lmoe_debug* dbg, void* stream) {
-  return forward_impl(dims, wt, hidden, router_logits, nullptr, nullptr, out, scratch,
+  return forward_impl(dims, wt, hidden, router_logits, nullptr, nullptr, nullptr, out, scratch,
                       scratch_bytes, dbg, stream, true);
 }
 }  // namespace lmoe

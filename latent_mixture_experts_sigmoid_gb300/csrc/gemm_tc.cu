@@ -361,7 +361,7 @@ __device__ __forceinline__ int swap_cols(const GemmParams& p, int nvalid, bool s
 template <bool kPairs>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const GemmParams p) {
+               const __grid_constant__ CUtensorMap tmW2, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -479,11 +479,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t offW = p.tok_on_m ? a_bytes : 0u;
   const uint32_t offX = p.tok_on_m ? 0u : w_bytes;
   // the weight tile: one box, or (fused SituGLU) 128 gate rows and the 128 up
-  // rows of the same features, stacked into one 256-row operand
+  // rows of the same features, stacked into one 256-row operand.  With a
+  // second weight matrix (p.w2_row0 > 0: weights on M, one box per unit)
+  // rows from w2_row0 on come from it.
   auto load_w = [&](uint32_t dst, uint32_t bar, int kb, int row) {
     if (p.fuse_situ) {
       tma_load_2d(mapW, dst, bar, kb * BK, row);
       tma_load_2d(mapW, dst + BM * BK * 2, bar, kb * BK, row + p.M_feat / 2);
+    } else if (p.w2_row0 > 0 && row >= p.w2_row0) {
+      tma_load_2d(&tmW2, dst, bar, kb * BK, row - p.w2_row0);
     } else {
       tma_load_2d(mapW, dst, bar, kb * BK, row);
     }
@@ -944,16 +948,30 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
               (nfeat % 2 == 0 || (!g.grp_count && ntok % 2 == 0));
   }
   p.sp = make_situ_params(g.beta > 0.0f ? g.beta : 1.0f, g.linear_beta);
+  // a second weight matrix stacked after the first: weights on M, one
+  // 128-row box per unit, and the first one's rows a whole number of units
+  p.w2_row0 = g.W2 ? g.w2_row0 : 0;
+  if (g.W2 && (g.tok_on_m || g.fuse_situ || g.w2_row0 <= 0 || g.w2_row0 % BM))
+    return cudaErrorInvalidValue;
   uint32_t cols = 32;
   while (cols < (uint32_t)((swap_all ? 4 : 2) * g.bn)) cols <<= 1;
   if (cols > 512) return cudaErrorInvalidValue;
   p.tmem_cols = cols;
 
-  CUtensorMap mw, mx;
+  CUtensorMap mw, mx, mw2;
   const int w_box = (g.fuse_situ || p.mcast) ? BM : (g.tok_on_m ? g.bn : BM);
   const int x_box = g.tok_on_m ? BM : g.bn;
-  if (!make_map(&mw, g.W, (long long)g.G * g.M_feat, g.K, w_box)) return cudaErrorInvalidValue;
+  // the weight map covers the rows that exist (fewer than G * M_feat when the
+  // last feature tile is partial: its missing rows read as zeros)
+  const long long w_rows = g.W2 ? (long long)g.w2_row0
+                                : (g.w_rows > 0 ? g.w_rows : (long long)g.G * g.M_feat);
+  if (!make_map(&mw, g.W, w_rows, g.K, w_box)) return cudaErrorInvalidValue;
   if (!make_map(&mx, g.X, g.x_rows, g.K, x_box)) return cudaErrorInvalidValue;
+  if (g.W2) {
+    if (!make_map(&mw2, g.W2, g.w2_rows, g.K, BM)) return cudaErrorInvalidValue;
+  } else {
+    mw2 = mw;
+  }
 
   const size_t smem = smem_for(stage, p.stages, g.grp_count ? g.G : 0, g.tok_on_m);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
@@ -967,14 +985,15 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
     int np = pairs;
     if (g.max_units > 0 && g.max_units < np) np = g.max_units;
     return launch_k_cluster(gemm_tc_kernel<true>, dim3(2 * np), dim3(kThreads), smem, stream, 2, mx,
-                            mw, p);
+                            mw, mw2, p);
   }
   int grid = num_sms();
   if (g.max_units > 0 && g.max_units < grid) grid = g.max_units;
   if (grid < 1) grid = 1;
   if (g.tok_on_m)
-    return launch_k(gemm_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, stream, mx, mw, p);
-  return launch_k(gemm_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, stream, mw, mx, p);
+    return launch_k(gemm_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, stream, mx, mw, mw2,
+                    p);
+  return launch_k(gemm_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, stream, mw, mx, mw2, p);
 }
 
 int* device_error_word() {

@@ -36,12 +36,15 @@ struct GemmParams {
   int mcast;               // 1: launched in clusters of two CTAs (the gemm_tc_kernel<true>
                            // form) that share an operand tile by TMA multicast; dense or
                            // grouped, tokens on M, 256-row weight tiles, no split-K
+  int w2_row0;             // > 0: weight rows from w2_row0 on are rows (row - w2_row0) of the
+                           // second weight map (weights on M only)
   SituParams sp;
 };
 
 // One GEMM launch:  out[tok, f] = sum_c X[tok, c] W[g*M_feat + f, c] (+ add).
 struct GemmDesc {
-  const uint16_t* W;       // [G*M_feat, K] bf16
+  const uint16_t* W;       // [G*M_feat, K] bf16 (or [w_rows, K])
+  long long w_rows;        // > 0: W has only this many rows; the rest of the tiles read zeros
   const uint16_t* X;       // [x_rows, K] bf16
   long long x_rows;
   int K, M_feat, G;
@@ -59,6 +62,9 @@ struct GemmDesc {
   int fuse_situ;           // see GemmParams; tokens on M: bn == 256; weights on M: bn <= 128;
                            // splits == 1
   int swap_max;            // see GemmParams (0: never)
+  const uint16_t* W2;      // optional second weight matrix [w2_rows, K] bf16, stacked after
+  long long w2_rows;       // the first w2_row0 rows of W (weights on M, w2_row0 % 128 == 0;
+  int w2_row0;             // rows of the stack beyond w2_row0 + w2_rows read as zeros)
   float beta, linear_beta;
 };
 

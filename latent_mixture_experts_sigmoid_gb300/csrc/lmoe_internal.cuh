@@ -198,7 +198,8 @@ inline int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 int num_sms();  // of the current device (cached per device)
 
 // Launchers (return cudaError_t of the launch); arguments already validated.
-cudaError_t launch_route(const float* logits, const float* bias, int T, int E, int k,
+// logits [T, E] fp32 with rows ld >= E elements apart
+cudaError_t launch_route(const float* logits, long long ld, const float* bias, int T, int E, int k,
                          int renorm, float rsf, int32_t* ids, float* w, cudaStream_t s);
 cudaError_t launch_situ(const uint16_t* in, uint16_t* out, long long N, int d, float beta,
                         float lbeta, cudaStream_t s);

@@ -222,8 +222,8 @@ perm_scatter_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, 
                           int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                           int32_t* __restrict__ tile_prefix, int32_t* __restrict__ row_of,
                           int32_t* __restrict__ tok_of_row, const uint16_t* __restrict__ Zb,
-                          const float* __restrict__ Zp, int S, long long split_stride, int L,
-                          uint16_t* __restrict__ A, int* err) {
+                          const float* __restrict__ Zp, int S, long long split_stride, int ldz,
+                          int L, uint16_t* __restrict__ A, int* err) {
   pdl_trigger();
   pdl_wait();
   __shared__ uint32_t bm[1024 * kWords];
@@ -282,7 +282,7 @@ perm_scatter_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, 
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       for (int sp = 0; sp < S; ++sp) {
         const float4* p = reinterpret_cast<const float4*>(Zp + sp * split_stride +
-                                                          (long long)t * L + v * 8);
+                                                          (long long)t * ldz + v * 8);
         const float4 a = __ldg(p), b = __ldg(p + 1);
         acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
         acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
@@ -301,8 +301,8 @@ perm_scatter_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, 
 // row or the bf16 rounding of the fixed-order sum of S fp32 split partials.
 __global__ void __launch_bounds__(256)
 scatter_rows_kernel(const uint16_t* __restrict__ Zb, const float* __restrict__ Zp, int S,
-                    long long split_stride, int L, int k, const int32_t* __restrict__ row_of,
-                    uint16_t* __restrict__ A) {
+                    long long split_stride, int ldz, int L, int k,
+                    const int32_t* __restrict__ row_of, uint16_t* __restrict__ A) {
   pdl_trigger();
   pdl_wait();
   const int t = blockIdx.x;
@@ -313,7 +313,7 @@ scatter_rows_kernel(const uint16_t* __restrict__ Zb, const float* __restrict__ Z
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       for (int s = 0; s < S; ++s) {
         const float4* p = reinterpret_cast<const float4*>(Zp + s * split_stride +
-                                                          (long long)t * L + v * 8);
+                                                          (long long)t * ldz + v * 8);
         const float4 a = __ldg(p), c = __ldg(p + 1);
         acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
         acc[4] += c.x; acc[5] += c.y; acc[6] += c.z; acc[7] += c.w;
@@ -524,19 +524,51 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int tile, vo
 cudaError_t launch_permute_scatter_small(const int32_t* ids, int T, int k, int E, int tile,
                                          int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
                                          int32_t* row_of, int32_t* tok_of_row, const uint16_t* Zb,
-                                         const float* Zp, int S, long long split_stride, int L,
-                                         uint16_t* A, int* err, cudaStream_t s) {
+                                         const float* Zp, int S, long long split_stride,
+                                         int ldz, int L, uint16_t* A, int* err, cudaStream_t s) {
   if (T > kBlkTok || E > 1024 || k > 32) return cudaErrorInvalidValue;
   return launch_k(perm_scatter_small_kernel, dim3(T), dim3(1024), 0, s, ids, T, k, E, tile, counts,
-                  offsets, tile_prefix, row_of, tok_of_row, Zb, Zp, S, split_stride, L, A, err);
+                  offsets, tile_prefix, row_of, tok_of_row, Zb, Zp, S, split_stride, ldz, L, A,
+                  err);
 }
 
 cudaError_t launch_scatter_rows(const uint16_t* Zb, const float* Zp, int S, long long split_stride,
-                                int T, int L, int k, const int32_t* row_of, uint16_t* A,
+                                int ldz, int T, int L, int k, const int32_t* row_of, uint16_t* A,
                                 cudaStream_t s) {
   const int threads = L / 8 < 256 ? ((L / 8 + 31) / 32) * 32 : 256;
-  return launch_k(scatter_rows_kernel, dim3(T), dim3(threads), 0, s, Zb, Zp, S, split_stride, L, k,
-                  row_of, A);
+  return launch_k(scatter_rows_kernel, dim3(T), dim3(threads), 0, s, Zb, Zp, S, split_stride, ldz,
+                  L, k, row_of, A);
+}
+
+// ---- columns of split-K partials summed into an fp32 matrix ------------------
+// out[t, c] = sum_s P[s * sstride + t * ldp + col0 + c] (s ascending) for
+// c < n, written with row stride ldo.  The router logits of the GEMM that
+// shares its launch with the down-projection (their columns follow the
+// latent ones in each partial row).
+__global__ void __launch_bounds__(256)
+sum_splits_cols_kernel(const float* __restrict__ P, int S, long long sstride, int T, long long ldp,
+                       int col0, int n, long long ldo, float* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const long long total = (long long)T * n;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long t = i / n;
+    const int c = (int)(i - t * n);
+    const float* p = P + t * ldp + col0 + c;
+    float acc = 0.0f;
+    for (int sp = 0; sp < S; ++sp) acc += __ldg(p + sp * sstride);
+    out[t * ldo + c] = acc;
+  }
+}
+
+cudaError_t launch_sum_splits_cols(const float* P, int S, long long sstride, int T, long long ldp,
+                                   int col0, int n, long long ldo, float* out, cudaStream_t s) {
+  const long long total = (long long)T * n;
+  const long long blocks = (total + 255) / 256;
+  const int grid = (int)(blocks < 4096 ? blocks : 4096);
+  return launch_k(sum_splits_cols_kernel, dim3(grid > 0 ? grid : 1), dim3(256), 0, s, P, S,
+                  sstride, T, ldp, col0, n, ldo, out);
 }
 
 cudaError_t launch_combine_norm(const uint16_t* Y, const float* w, const int32_t* row_of, int T,

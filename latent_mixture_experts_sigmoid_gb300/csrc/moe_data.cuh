@@ -22,14 +22,20 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int tile, vo
 cudaError_t launch_permute_scatter_small(const int32_t* ids, int T, int k, int E, int tile,
                                          int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
                                          int32_t* row_of, int32_t* tok_of_row, const uint16_t* Zb,
-                                         const float* Zp, int S, long long split_stride, int L,
-                                         uint16_t* A, int* err, cudaStream_t s);
+                                         const float* Zp, int S, long long split_stride,
+                                         int ldz, int L, uint16_t* A, int* err, cudaStream_t s);
 
-// A[row_of[t,j]] = Z[t] for j < k; Z from bf16 rows Zb or from the sum of S
-// fp32 partials Zp (split_stride elements apart).  L % 8 == 0.
+// A[row_of[t,j]] = Z[t] for j < k; Z from bf16 rows Zb ([T, L]) or from the sum
+// of S fp32 partials Zp (split_stride elements apart, rows ldz >= L elements
+// apart, Z in the first L columns).  L % 8 == 0, ldz % 4 == 0.
 cudaError_t launch_scatter_rows(const uint16_t* Zb, const float* Zp, int S, long long split_stride,
-                                int T, int L, int k, const int32_t* row_of, uint16_t* A,
+                                int ldz, int T, int L, int k, const int32_t* row_of, uint16_t* A,
                                 cudaStream_t s);
+
+// out[t, c] = sum_s P[s*sstride + t*ldp + col0 + c] (s ascending), c < n, rows
+// ldo apart.
+cudaError_t launch_sum_splits_cols(const float* P, int S, long long sstride, int T, long long ldp,
+                                   int col0, int n, long long ldo, float* out, cudaStream_t s);
 
 // N[t] = bf16(RMSNorm(sum_j w[t,j] Y[row_of[t,j]]) * gamma).  L % 8 == 0, L <= 8192.
 cudaError_t launch_combine_norm(const uint16_t* Y, const float* w, const int32_t* row_of, int T,

@@ -327,9 +327,9 @@ __device__ __forceinline__ unsigned long long lane_best_exact_chunk(const float*
 // Start the copy of token tt's row into `dst` (nothing for tt >= T), then close the group.
 template <int C, bool VEC>
 __device__ __forceinline__ void stage_row(float* dst, const float* __restrict__ logits,
-                                          long long tt, int T, int E, int lane) {
+                                          long long tt, int T, int E, long long ld, int lane) {
   if (tt < T) {
-    const float* rr = logits + tt * (long long)E;
+    const float* rr = logits + tt * ld;
 #pragma unroll
     for (int c = 0; c < C; ++c) {
       const int e0 = 128 * c + 4 * lane;
@@ -356,8 +356,8 @@ constexpr size_t warp_kernel_smem() {
 
 template <int C, bool VEC, int NSLOT>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, kRouteMinBlocks)
-route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
-                  int k, int renorm, float rsf, int32_t* __restrict__ ids,
+route_warp_kernel(const float* __restrict__ logits, long long ld, const float* __restrict__ bias,
+                  int T, int E, int k, int renorm, float rsf, int32_t* __restrict__ ids,
                   float* __restrict__ weights) {
   constexpr int EW = 128 * C;
   extern __shared__ __align__(16) float srow_all[];   // [warp][slot][EW]
@@ -384,10 +384,11 @@ route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bi
   const f32x2 half2 = f2_splat(0.5f), two2 = f2_splat(2.0f);
   const uint32_t dirs = sort32_directions(lane);
 #pragma unroll
-  for (int p = 0; p < NSLOT - 1; ++p) stage_row<C, VEC>(ring + p * EW, logits, t0 + p * step, T, E, lane);
+  for (int p = 0; p < NSLOT - 1; ++p)
+    stage_row<C, VEC>(ring + p * EW, logits, t0 + p * step, T, E, ld, lane);
   int slot = 0, fill = NSLOT - 1;
   for (long long t = t0; t < T; t += step) {
-    stage_row<C, VEC>(ring + fill * EW, logits, t + (NSLOT - 1) * step, T, E, lane);
+    stage_row<C, VEC>(ring + fill * EW, logits, t + (NSLOT - 1) * step, T, E, ld, lane);
     cp_async_wait<NSLOT - 1>();
     __syncwarp();
     const float* row = ring + slot * EW;
@@ -473,8 +474,8 @@ route_warp_kernel(const float* __restrict__ logits, const float* __restrict__ bi
 // found in parallel: every thread counts the lane maxima above its own.
 template <int EPL, int W>
 __global__ void __launch_bounds__(W * 32)
-route_block_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E,
-                   int k, int renorm, float rsf, int32_t* __restrict__ ids,
+route_block_kernel(const float* __restrict__ logits, long long ld, const float* __restrict__ bias,
+                   int T, int E, int k, int renorm, float rsf, int32_t* __restrict__ ids,
                    float* __restrict__ weights) {
   __shared__ __align__(16) uint32_t smax[W * 32];
   __shared__ int scnt[W];
@@ -500,7 +501,7 @@ route_block_kernel(const float* __restrict__ logits, const float* __restrict__ b
   // this lane's logits of the block's next token are loaded one token ahead
   float xn[EPL];
   auto load_row = [&](long long tt) {
-    const float* rr = logits + tt * (long long)E;
+    const float* rr = logits + tt * ld;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int e = base + lane + stride * i;
@@ -509,7 +510,7 @@ route_block_kernel(const float* __restrict__ logits, const float* __restrict__ b
   };
   load_row(blockIdx.x);
   for (long long t = blockIdx.x; t < T; t += gridDim.x) {
-    const float* row = logits + t * (long long)E;
+    const float* row = logits + t * ld;
     float xv[EPL];
 #pragma unroll
     for (int i = 0; i < EPL; ++i) xv[i] = xn[i];
@@ -590,8 +591,8 @@ route_block_kernel(const float* __restrict__ logits, const float* __restrict__ b
 }
 
 template <int C, bool VEC>
-cudaError_t launch_warp_tier(const float* logits, const float* bias, int T, int E, int k,
-                             int renorm, float rsf, int32_t* ids, float* w, cudaStream_t s) {
+cudaError_t launch_warp_tier(const float* logits, long long ld, const float* bias, int T, int E,
+                             int k, int renorm, float rsf, int32_t* ids, float* w, cudaStream_t s) {
   constexpr size_t smem = warp_kernel_smem<C, kRouteSlots>();
   // resident blocks per SM, per device (the shared-memory attribute is set on
   // each device once, before its first launch)
@@ -615,20 +616,23 @@ cudaError_t launch_warp_tier(const float* logits, const float* bias, int T, int 
   const long long cap = (long long)num_sms() * per_sm;
   const int blocks = (int)(need < cap ? need : cap);
   return launch_k(route_warp_kernel<C, VEC, kRouteSlots>, dim3(blocks), dim3(kWarpsPerBlock * 32),
-                  smem, s, logits, bias, T, E, k, renorm, rsf, ids, w);
+                  smem, s, logits, ld, bias, T, E, k, renorm, rsf, ids, w);
 }
 
 template <int C>
-cudaError_t launch_warp_chunks(const float* logits, const float* bias, int T, int E, int k,
-                               int renorm, float rsf, int32_t* ids, float* w, cudaStream_t s) {
+cudaError_t launch_warp_chunks(const float* logits, long long ld, const float* bias, int T, int E,
+                               int k, int renorm, float rsf, int32_t* ids, float* w,
+                               cudaStream_t s) {
   // 16-byte row loads need every row to start on a 16-byte boundary
-  if (E % 4 == 0) return launch_warp_tier<C, true>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  return launch_warp_tier<C, false>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E % 4 == 0 && ld % 4 == 0)
+    return launch_warp_tier<C, true>(logits, ld, bias, T, E, k, renorm, rsf, ids, w, s);
+  return launch_warp_tier<C, false>(logits, ld, bias, T, E, k, renorm, rsf, ids, w, s);
 }
 
 template <int EPL, int W>
-cudaError_t launch_block_tier(const float* logits, const float* bias, int T, int E, int k,
-                              int renorm, float rsf, int32_t* ids, float* w, cudaStream_t s) {
+cudaError_t launch_block_tier(const float* logits, long long ld, const float* bias, int T, int E,
+                              int k, int renorm, float rsf, int32_t* ids, float* w,
+                              cudaStream_t s) {
   // persistent: as many blocks as fit on the GPU at once loop over the tokens
   // (bias loaded once per block, next token's logits prefetched)
   static std::atomic<int> per_sm_of[64];
@@ -645,8 +649,8 @@ cudaError_t launch_block_tier(const float* logits, const float* bias, int T, int
   }
   const long long cap = (long long)num_sms() * per_sm;
   const int grid = (int)(T < cap ? T : cap);
-  return launch_k(route_block_kernel<EPL, W>, dim3(grid), dim3(W * 32), 0, s, logits, bias, T, E,
-                  k, renorm, rsf, ids, w);
+  return launch_k(route_block_kernel<EPL, W>, dim3(grid), dim3(W * 32), 0, s, logits, ld, bias, T,
+                  E, k, renorm, rsf, ids, w);
 }
 
 }  // namespace
@@ -655,20 +659,20 @@ cudaError_t launch_block_tier(const float* logits, const float* bias, int T, int
 // otherwise a warp per token, C = ceil(E / 128) chunks of four experts per lane.
 constexpr int kBlockMaxT = 512;
 
-cudaError_t launch_route(const float* logits, const float* bias, int T, int E, int k, int renorm,
-                         float rsf, int32_t* ids, float* w, cudaStream_t s) {
+cudaError_t launch_route(const float* logits, long long ld, const float* bias, int T, int E, int k,
+                         int renorm, float rsf, int32_t* ids, float* w, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   if (E > 128 && T <= kBlockMaxT) {
-    if (E <= 256) return launch_block_tier<2, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-    if (E <= 512) return launch_block_tier<4, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-    if (E <= 896) return launch_block_tier<7, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-    return launch_block_tier<8, 4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+    if (E <= 256) return launch_block_tier<2, 4>(logits, ld, bias, T, E, k, renorm, rsf, ids, w, s);
+    if (E <= 512) return launch_block_tier<4, 4>(logits, ld, bias, T, E, k, renorm, rsf, ids, w, s);
+    if (E <= 896) return launch_block_tier<7, 4>(logits, ld, bias, T, E, k, renorm, rsf, ids, w, s);
+    return launch_block_tier<8, 4>(logits, ld, bias, T, E, k, renorm, rsf, ids, w, s);
   }
-  if (E <= 128) return launch_warp_chunks<1>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  if (E <= 256) return launch_warp_chunks<2>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  if (E <= 512) return launch_warp_chunks<4>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  if (E <= 896) return launch_warp_chunks<7>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
-  return launch_warp_chunks<8>(logits, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 128) return launch_warp_chunks<1>(logits, ld, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 256) return launch_warp_chunks<2>(logits, ld, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 512) return launch_warp_chunks<4>(logits, ld, bias, T, E, k, renorm, rsf, ids, w, s);
+  if (E <= 896) return launch_warp_chunks<7>(logits, ld, bias, T, E, k, renorm, rsf, ids, w, s);
+  return launch_warp_chunks<8>(logits, ld, bias, T, E, k, renorm, rsf, ids, w, s);
 }
 
 }  // namespace lmoe

@@ -179,3 +179,30 @@ def test_host_memory_is_refused_before_any_launch(lib):
     cnt = buf(16)
     assert lib.masked_situ_and_mul(x, out, cnt, 2, 2, 16, 4.0, 8.0, None) == -8
     assert lib.lmoe_linear(x, buf(128 * 256 * 2), None, out, 8, 128, 256, None) == -8
+
+
+def test_router_validation(lib):
+    p = ctypes.c_void_p(256)
+    assert lib.lmoe_router_logits_workspace_bytes(8, 64, 256) > 0
+    assert lib.lmoe_router_logits_workspace_bytes(8, 0, 256) == 0          # E < 1
+    assert lib.lmoe_router_logits_workspace_bytes(8, 2000, 256) == 0       # E > 1024
+    assert lib.lmoe_router_logits_workspace_bytes(8, 64, 100) == 0         # H % 64
+    n = lib.lmoe_router_logits_workspace_bytes(8, 64, 256)
+    assert lib.lmoe_router_logits(p, p, p, 8, 64, 100, p, n, None) == -2
+    assert lib.lmoe_router_logits(None, p, p, 8, 64, 256, p, n, None) == -1
+    assert lib.lmoe_router_logits(p, p, ctypes.c_void_p(260), 8, 64, 256, p, n, None) == -7
+    assert lib.lmoe_router_logits(p, p, p, 8, 64, 256, p, n - 256, None) == -5
+    assert lib.lmoe_router_logits(None, None, None, 0, 64, 256, None, 0, None) == 0
+    import workloads as W
+    import latent_mixture_experts_sigmoid_gb300 as lm
+    d = lm.make_dims(W.TINY)
+    w = lm.LmoeWeights(256, 256, 256, None, None, None, 256, None)
+    nb = lib.latent_moe_workspace_bytes(ctypes.byref(d))
+    fr = lib.latent_moe_forward_router
+    assert fr(ctypes.byref(d), ctypes.byref(w), None, p, p, p, nb, None, None) == -1
+    assert fr(ctypes.byref(d), ctypes.byref(w), ctypes.c_void_p(264), p, p, p, nb, None,
+              None) == -7
+    assert fr(ctypes.byref(d), ctypes.byref(w), p, p, p, ctypes.c_void_p(272), nb, None,
+              None) == -5
+    assert lib.latent_moe_launch_count_router(ctypes.byref(d), 1) == \
+        lib.latent_moe_launch_count(ctypes.byref(d), 1) + 1

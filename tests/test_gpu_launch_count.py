@@ -56,3 +56,12 @@ def test_launch_count_matches_captured_kernels(cuda_ok, T, shared):
     with torch.cuda.graph(g, stream=s):
         lm.latent_moe_forward(d, wdev, x, lg, out, ws, stream=s)
     assert _kernel_nodes(g) == lm.latent_moe_launch_count(d, shared)
+    # the forward with its router GEMM
+    wr = dev_bf16(W.w_router(d, 1))
+    with torch.cuda.stream(s):
+        lm.latent_moe_forward_router(d, wdev, wr, x, out, ws, stream=s)
+    s.synchronize()
+    g2 = torch.cuda.CUDAGraph(keep_graph=True)
+    with torch.cuda.graph(g2, stream=s):
+        lm.latent_moe_forward_router(d, wdev, wr, x, out, ws, stream=s)
+    assert _kernel_nodes(g2) == lm.latent_moe_launch_count_router(d, shared)
