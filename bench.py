@@ -342,6 +342,61 @@ def run_ours(args):
                     e2e_ms=e2e_ms, e2e_serial_ms=e2e_serial_ms, h2d=T * d.hidden * 2 + T * d.num_experts * 4,
                     d2h=T * d.hidden * 2, pre=pre)
 
+    def measure_router(d, zipf, steps, warmup):
+        """The layer with its router GEMM: latent_moe_forward_router (at T <= 128
+        the router rows share the down-projection's launch) against the router
+        GEMM as its own op (lmoe_router_logits) followed by latent_moe_forward,
+        each one CUDA-graph replay per step, L2 flushed between steps."""
+        T, E, H = d.T, d.num_experts, d.hidden
+        x = dev_bf16(W.hidden_states(d, 0))
+        wr = dev_bf16(W.w_router(d, 0))
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(lm.latent_moe_workspace_bytes(d), dtype=torch.uint8, device=dev)
+        lg = torch.empty((T, E), dtype=torch.float32, device=dev)
+        rws = torch.empty(lm.lmoe_router_logits_workspace_bytes(T, E, H), dtype=torch.uint8,
+                          device=dev)
+
+        def fused():
+            lm.latent_moe_forward_router(d, w, wr, x, out, ws, stream=stream)
+
+        def separate():
+            lm.lmoe_router_logits(x, wr, lg, rws, stream=stream)
+            lm.latent_moe_forward(d, w, x, lg, out, ws, stream=stream)
+
+        res = {}
+        for name, fn in (("fused", fused), ("separate", separate)):
+            with torch.cuda.stream(stream):
+                for _ in range(warmup):
+                    fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            for _ in range(warmup):
+                with torch.cuda.stream(stream):
+                    g.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            tot = 0.0
+            for _ in range(steps):
+                with torch.cuda.stream(stream):
+                    flush_l2()
+                    a.record(stream)
+                    g.replay()
+                    b.record(stream)
+                stream.synchronize()
+                tot += a.elapsed_time(b)
+            res[name] = tot / steps * 1e3
+        return {"us_per_step_fused": round(res["fused"], 2),
+                "us_per_step_separate_router_op": round(res["separate"], 2),
+                "tokens_per_s_fused": round(T / (res["fused"] / 1e6), 1),
+                "launches_fused": lm.latent_moe_launch_count_router(d),
+                "what": ("latent_moe_forward_router" + (" (router rows stacked after the "
+                         "down-projection's in one split-K GEMM)" if T <= 128 else
+                         " (router GEMM its own launch on the second stream)") +
+                         " against lmoe_router_logits + latent_moe_forward; router weight "
+                         "bf16 [E, H] N(0, 1/H)")}
+
     def time_launches(fns, reps):
         """Average device time per launch of `reps` back-to-back launches.
 
@@ -409,6 +464,8 @@ def run_ours(args):
     t_wall0 = time.time()
     pre = measure(W.PREFILL, True, args.steps, args.warmup)
     dec = measure(W.DECODE, False, args.steps, args.warmup)
+    rtr_dec = measure_router(W.DECODE, False, args.steps, args.warmup)
+    rtr_pre = measure_router(W.PREFILL, True, args.steps, args.warmup)
     kern = kernel_lines(max(3, args.steps))
     if not args.no_cpu_baseline:
         for name, cb in kernel_cpu_baselines().items():
@@ -464,6 +521,7 @@ def run_ours(args):
               "per_stage_ms": per_stage_dec,
               "e2e_tokens_per_s": round(dDc.T * K / (dec_e2e / 1e3), 1),
               "gpu_launches_per_step": lm.latent_moe_launch_count(dDc)}
+    decode["router_gemm"] = rtr_dec
     if dec["pre"] is not None:
         decode["pre_routed"] = {
             "us_per_step": round(dec["pre"]["ms"] / K * 1e3, 2),
@@ -511,6 +569,7 @@ def run_ours(args):
         "layer_gflop": round(fl["total"] / 1e9, 1),
         "layer_tflops": round(fl["total"] / (pre_ms / K / 1e3) / 1e12, 1),
         "decode": decode,
+        "prefill_router_gemm": rtr_pre,
         "kernels": kern,
         "clocks": clk,
         "wall_s": round(wall, 1),

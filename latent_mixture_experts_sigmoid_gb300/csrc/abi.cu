@@ -61,12 +61,6 @@ namespace {
 
 constexpr int kDecodeMaxT = 128;
 constexpr int kMaxSplits = 32;
-// Prefill grouped GEMMs: a CTA's unit with at most this many valid token rows
-// runs in the GEMM's swap form (weight halves on M, tokens on N).
-#ifndef LMOE_SWAP_MAX
-#define LMOE_SWAP_MAX 64
-#endif
-constexpr int kSwapMax = LMOE_SWAP_MAX;
 
 bool finite_pos(float x) { return isfinite(x) && x > 0.0f; }
 
@@ -244,7 +238,6 @@ cudaError_t gemm_grouped(const uint16_t* W, int E, int M_feat, const uint16_t* X
   g.out = out;
   g.ldo = fuse_situ ? M_feat / 2 : M_feat;
   g.fuse_situ = fuse_situ;
-  g.swap_max = tok_on_m ? kSwapMax : 0;
   g.beta = beta;
   g.linear_beta = linear_beta;
   const int feat_tile = fuse_situ ? 256 : (tok_on_m ? bn : 128);

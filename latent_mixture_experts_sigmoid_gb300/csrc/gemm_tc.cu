@@ -345,39 +345,36 @@ __host__ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const 
   return x;
 }
 
-// Token columns of a unit computed in the swap form (0: the regular form).
-// Every unit when the launch is swap_all; otherwise, in grouped GEMMs with
-// tokens on M and 256-row weight tiles, a CTA's unit with at most
-// p.swap_max valid token rows: its 128-row token tile is mostly padding, so
-// the two 128-row halves of the weight tile already in shared memory go on
-// the MMA's M side and the first round_up(nvalid, 16) token rows on N.
-__device__ __forceinline__ int swap_cols(const GemmParams& p, int nvalid, bool swap_all) {
-  if (swap_all) return p.bn;
-  if (nvalid > p.swap_max) return 0;
-  return (nvalid + 15) & ~15;
-}
+// Forms of the kernel beyond the CTA pairs (one instance each: compiled into
+// the regular form, even unused, their code measurably slowed it):
+//   kFormSwap   weights on M, tokens on N, no pairs; every unit's weight tile
+//               is two 128-row halves, the gate and up rows of the same 128
+//               features, each multiplied into its own accumulator, so that
+//               the epilogue applies SituGLU (p.fuse_situ is set);
+//   kFormStack  weights on M; weight rows from p.w2_row0 on come from a second
+//               matrix (its own tensor map), stacked after the first.
+enum : int { kFormRegular = 0, kFormSwap = 1, kFormStack = 2 };
 
-// kPairs: the CTA-pair form (launched in clusters of two; p.mcast is set)
-template <bool kPairs>
+// kPairs: the CTA-pair form (launched in clusters of two; p.mcast is set).
+template <bool kPairs, int kForm>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmW2, const GemmParams p) {
+  constexpr bool kSwap = kForm == kFormSwap;
+  constexpr bool kStack = kForm == kFormStack;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int S = p.stages;
   const int bn = p.bn;
   const uint32_t a_bytes = BM * BK * 2;
-  // every unit in the swap form with two weight halves (weights on M, tokens
-  // on N: the decode GEMM1 with SituGLU in its epilogue)
-  const bool swap_all = !p.tok_on_m && p.fuse_situ;
   // weight rows per stage on the M side: one 128-row box, or the two halves
-  const uint32_t w_bytes = (swap_all ? 2u : 1u) * a_bytes;
+  const uint32_t w_bytes = (kSwap ? 2u : 1u) * a_bytes;
   const uint32_t stage_bytes =
       (p.tok_on_m ? a_bytes : w_bytes) + (uint32_t)bn * BK * 2;
-  // TMEM columns between the two accumulators (a swap_all unit keeps its gate
-  // and up accumulators side by side)
-  const uint32_t acc_stride = swap_all ? 2u * (uint32_t)bn : (uint32_t)bn;
+  // TMEM columns between the two accumulators (a swap-form unit keeps its
+  // gate and up accumulators side by side)
+  const uint32_t acc_stride = kSwap ? 2u * (uint32_t)bn : (uint32_t)bn;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * stage_bytes);
   // bars: full[S], empty[S], tfull[2], tempty[2], done
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
@@ -479,14 +476,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t offW = p.tok_on_m ? a_bytes : 0u;
   const uint32_t offX = p.tok_on_m ? 0u : w_bytes;
   // the weight tile: one box, or (fused SituGLU) 128 gate rows and the 128 up
-  // rows of the same features, stacked into one 256-row operand.  With a
-  // second weight matrix (p.w2_row0 > 0: weights on M, one box per unit)
-  // rows from w2_row0 on come from it.
+  // rows of the same features, stacked into one 256-row operand.  In the
+  // stacked form rows from p.w2_row0 on come from the second weight matrix.
   auto load_w = [&](uint32_t dst, uint32_t bar, int kb, int row) {
     if (p.fuse_situ) {
       tma_load_2d(mapW, dst, bar, kb * BK, row);
       tma_load_2d(mapW, dst + BM * BK * 2, bar, kb * BK, row + p.M_feat / 2);
-    } else if (p.w2_row0 > 0 && row >= p.w2_row0) {
+    } else if (kStack && row >= p.w2_row0) {
       tma_load_2d(&tmW2, dst, bar, kb * BK, row - p.w2_row0);
     } else {
       tma_load_2d(mapW, dst, bar, kb * BK, row);
@@ -580,7 +576,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint64_t da0 = p.tok_on_m ? dx0 : dw0;
       const uint64_t db0 = p.tok_on_m ? dw0 : dx0;
       const uint64_t dstep = stage_bytes >> 4;
-      constexpr uint64_t kHalf = (BM * BK * 2) >> 4;   // second 128-row weight box
       uint32_t uit = 0, s = 0, ph = 0;
       uint64_t da = da0, db = db0;
       bool ok = true;
@@ -593,25 +588,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)acc * acc_stride;
-        // the swap form: the two 128-row weight halves of the stage on M, the
-        // unit's first bs token rows on N (each half into its own accumulator)
-        const int bs = swap_cols(p, x.nvalid, swap_all);
-        const uint32_t idesc_s = idesc_bf16(BM, bs > 0 ? bs : 16);
         uint32_t accumulate = 0u;
         for (int kb = x.kb0; kb < x.kb1; ++kb) {
           if (!wait_phase(full_bar((int)s), ph, abort_flag, kErrMmaFull)) { ok = false; break; }
           tc_fence_after();
-          if (bs > 0) {
-            const uint64_t dX = p.tok_on_m ? da : db;
-            const uint64_t dW = p.tok_on_m ? db : da;
+          if constexpr (kSwap) {
+            // the stage's two 128-row weight halves on M (A side), the unit's
+            // tokens on N, each half into its own accumulator
+            constexpr uint64_t kHalf = (BM * BK * 2) >> 4;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t dh = d_tmem + (uint32_t)(h * bs);
-              const uint64_t wh = dW + (uint64_t)h * kHalf;
+            for (int h = 0; h < 2; ++h)
 #pragma unroll
               for (int j = 0; j < kK16; ++j)
-                mma_bf16(dh, wh + 2 * j, dX + 2 * j, idesc_s, j ? 1u : accumulate);
-            }
+                mma_bf16(d_tmem + (uint32_t)(h * bn), da + (uint64_t)h * kHalf + 2 * j, db + 2 * j,
+                         idesc, j ? 1u : accumulate);
           } else {
 #pragma unroll
             for (int j = 0; j < kK16; ++j)
@@ -643,40 +633,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (!wait_bounded(tfull_bar(acc), (uit >> 1) & 1u, abort_flag, kErrEpilogue)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * acc_stride;
-      const int bs = swap_cols(p, x.nvalid, swap_all);
-      if (bs > 0) {
-        // swap form: row r of each weight half, columns = the unit's tokens.
-        // Fused SituGLU: half 0 holds the gate rows and half 1 the up rows of
-        // output features fcol0 + r; otherwise the halves are output features
-        // fcol0 + r and fcol0 + 128 + r.  Both rounded to bf16 first, as the
-        // stored GEMM output would be.
-        const int fcol0 = x.feat_tile * (p.fuse_situ ? BM : 2 * BM);
+      if constexpr (kSwap) {
+        // row r of the gate half and of the up half (output feature fcol0 + r),
+        // columns = the unit's tokens; both rounded to bf16 first, as the
+        // stored GEMM output would be, then SituGLU
+        const int fcol0 = x.feat_tile * BM;
         uint16_t* o = reinterpret_cast<uint16_t*>(p.out);
-        for (int c0 = 0; c0 < bs; c0 += 16) {
+        for (int c0 = 0; c0 < bn; c0 += 16) {
           uint32_t g[16], v[16];
           tmem_ld16(tbase + (uint32_t)c0, g);
-          tmem_ld16(tbase + (uint32_t)(bs + c0), v);
+          tmem_ld16(tbase + (uint32_t)(bn + c0), v);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 16; j += 2) {
             const int t = c0 + j;
             const uint32_t gb = pack_bf16x2(__uint_as_float(g[j]), __uint_as_float(g[j + 1]));
             const uint32_t ub = pack_bf16x2(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+            const uint32_t a = situ2(gb, ub, p.sp);
             const long long row = (long long)(x.tok_row0 + t);
-            if (p.fuse_situ) {
-              const uint32_t a = situ2(gb, ub, p.sp);
-              if (t < x.nvalid) o[row * p.ldo + fcol0 + r] = (uint16_t)a;
-              if (t + 1 < x.nvalid) o[(row + 1) * p.ldo + fcol0 + r] = (uint16_t)(a >> 16);
-            } else {
-              if (t < x.nvalid) {
-                o[row * p.ldo + fcol0 + r] = (uint16_t)gb;
-                o[row * p.ldo + fcol0 + BM + r] = (uint16_t)ub;
-              }
-              if (t + 1 < x.nvalid) {
-                o[(row + 1) * p.ldo + fcol0 + r] = (uint16_t)(gb >> 16);
-                o[(row + 1) * p.ldo + fcol0 + BM + r] = (uint16_t)(ub >> 16);
-              }
-            }
+            if (t < x.nvalid) o[row * p.ldo + fcol0 + r] = (uint16_t)a;
+            if (t + 1 < x.nvalid) o[(row + 1) * p.ldo + fcol0 + r] = (uint16_t)(a >> 16);
           }
         }
       } else if (p.tok_on_m && !p.out_fp32) {
@@ -865,8 +841,8 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, int K, int box_r
 
 // Bytes of one ring stage: the M-side operand (one 128-row box; two for the
 // swap form with weight halves) and bn rows of the N-side operand, 64 K wide.
-int stage_bytes_for(int bn, int tok_on_m, int swap_all) {
-  return (tok_on_m ? 1 : (swap_all ? 2 : 1)) * BM * BK * 2 + bn * BK * 2;
+int stage_bytes_for(int bn, int tok_on_m, int swap) {
+  return (tok_on_m ? 1 : (swap ? 2 : 1)) * BM * BK * 2 + bn * BK * 2;
 }
 
 int stages_for(int stage) {
@@ -899,7 +875,9 @@ int max_pairs_resident(size_t smem) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int pairs = 0;
-  if (cudaOccupancyMaxActiveClusters(&pairs, gemm_tc_kernel<true>, &cfg) != cudaSuccess) pairs = 0;
+  if (cudaOccupancyMaxActiveClusters(&pairs, gemm_tc_kernel<true, kFormRegular>, &cfg) !=
+      cudaSuccess)
+    pairs = 0;
   if (n < 16) cache[n++] = Entry{dev, smem, pairs};
   return pairs;
 }
@@ -932,13 +910,13 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
   p.out_fp32 = g.out_fp32;
   p.add = g.add;
   p.fuse_situ = g.fuse_situ;
-  const int swap_all = !g.tok_on_m && g.fuse_situ;
-  const int stage = stage_bytes_for(g.bn, g.tok_on_m, swap_all);
+  // weights on M with SituGLU fused: the swap-form instance (gate and up
+  // halves as two MMAs per stage); it writes bf16 and does not split K
+  const int swap = !g.tok_on_m && g.fuse_situ;
+  if (swap && (g.splits != 1 || g.out_fp32 || g.add || g.bn > 128 || g.W2))
+    return cudaErrorInvalidValue;
+  const int stage = stage_bytes_for(g.bn, g.tok_on_m, swap);
   p.stages = stages_for(stage);
-  // the swap form of sparse units needs the 256-row weight tile in two
-  // 128-row halves and a grouped walk with tokens on M
-  p.swap_max = (g.tok_on_m && g.grp_count && g.bn == 256 && g.splits == 1) ? g.swap_max : 0;
-  if (p.swap_max > 64) p.swap_max = 64;
   // CTA pairs with a multicast operand: tokens on M, 256-row weight tiles, and
   // an even count of weight tiles (or, dense, of token tiles)
   {
@@ -954,7 +932,7 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
   if (g.W2 && (g.tok_on_m || g.fuse_situ || g.w2_row0 <= 0 || g.w2_row0 % BM))
     return cudaErrorInvalidValue;
   uint32_t cols = 32;
-  while (cols < (uint32_t)((swap_all ? 4 : 2) * g.bn)) cols <<= 1;
+  while (cols < (uint32_t)((swap ? 4 : 2) * g.bn)) cols <<= 1;
   if (cols > 512) return cudaErrorInvalidValue;
   p.tmem_cols = cols;
 
@@ -975,8 +953,11 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
 
   const size_t smem = smem_for(stage, p.stages, g.grp_count ? g.G : 0, g.tok_on_m);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(p.mcast ? gemm_tc_kernel<true> : gemm_tc_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto* kern = p.mcast ? gemm_tc_kernel<true, kFormRegular>
+                       : swap ? gemm_tc_kernel<false, kFormSwap>
+                              : g.W2 ? gemm_tc_kernel<false, kFormStack>
+                                     : gemm_tc_kernel<false, kFormRegular>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (p.mcast) {
     // as many CTA pairs as can be resident at once (pairs share a GPC)
@@ -984,16 +965,14 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
     if (pairs < 1) return cudaErrorInvalidConfiguration;
     int np = pairs;
     if (g.max_units > 0 && g.max_units < np) np = g.max_units;
-    return launch_k_cluster(gemm_tc_kernel<true>, dim3(2 * np), dim3(kThreads), smem, stream, 2, mx,
-                            mw, mw2, p);
+    return launch_k_cluster(gemm_tc_kernel<true, kFormRegular>, dim3(2 * np), dim3(kThreads), smem,
+                            stream, 2, mx, mw, mw2, p);
   }
   int grid = num_sms();
   if (g.max_units > 0 && g.max_units < grid) grid = g.max_units;
   if (grid < 1) grid = 1;
-  if (g.tok_on_m)
-    return launch_k(gemm_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, stream, mx, mw, mw2,
-                    p);
-  return launch_k(gemm_tc_kernel<false>, dim3(grid), dim3(kThreads), smem, stream, mw, mx, mw2, p);
+  if (g.tok_on_m) return launch_k(kern, dim3(grid), dim3(kThreads), smem, stream, mx, mw, mw2, p);
+  return launch_k(kern, dim3(grid), dim3(kThreads), smem, stream, mw, mx, mw2, p);
 }
 
 int* device_error_word() {

@@ -30,9 +30,8 @@ struct GemmParams {
   int fuse_situ;           // W tile = 128 gate rows + the matching 128 up rows; the epilogue
                            // writes bf16(SituGLU(bf16(G))) [rows, M_feat/2].  Tokens on M:
                            // one 256-row B operand; weights on M: the two halves as two
-                           // M = 128 MMAs into two accumulators (the swap form)
-  int swap_max;            // grouped, tokens on M, 256-row weight tiles: a CTA's unit with at
-                           // most this many valid token rows (<= 64) runs in the swap form
+                           // M = 128 MMAs into two accumulators (the kernel's swap-form
+                           // instance)
   int mcast;               // 1: launched in clusters of two CTAs (the gemm_tc_kernel<true>
                            // form) that share an operand tile by TMA multicast; dense or
                            // grouped, tokens on M, 256-row weight tiles, no split-K
@@ -61,7 +60,6 @@ struct GemmDesc {
   int max_units;           // > 0: known upper bound on work units (caps the grid)
   int fuse_situ;           // see GemmParams; tokens on M: bn == 256; weights on M: bn <= 128;
                            // splits == 1
-  int swap_max;            // see GemmParams (0: never)
   const uint16_t* W2;      // optional second weight matrix [w2_rows, K] bf16, stacked after
   long long w2_rows;       // the first w2_row0 rows of W (weights on M, w2_row0 % 128 == 0;
   int w2_row0;             // rows of the stack beyond w2_row0 + w2_rows read as zeros)
