@@ -230,8 +230,8 @@ int latent_moe_launch_count(const lmoe_dims* dims, int has_shared_expert);
 /* and workspace, and one of them may be capturing (capture in thread-local  */
 /* or relaxed mode: during a global-mode capture the runtime may refuse      */
 /* calls it deems unsafe in every other thread).  The second                 */
-/* stream of a caller stream is created by its first call made outside a     */
-/* capture (up to 64 caller streams per device); a call without one runs     */
+/* stream of a caller stream is created by its first call (also inside a     */
+/* capture; up to 64 caller streams per device); a call without one runs     */
 /* every stage on `stream` (same results).  With dbg->stage_events every      */
 /* stage runs on `stream`, one after another.                                 */
 int latent_moe_forward(const lmoe_dims* dims, const lmoe_weights* weights,

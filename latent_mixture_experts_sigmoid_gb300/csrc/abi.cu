@@ -306,11 +306,11 @@ int plan_launches(const Plan& p, bool shared) {
 // never share a second stream, so neither one's work is ordered behind the
 // other's, and a capture on one caller stream pulls in only its own second
 // stream.  An entry is created by the first call on that caller stream made
-// outside a stream capture and kept for the life of the process (a stream
+// (also inside a stream capture) and kept for the life of the process (a stream
 // handle that is destroyed and reused maps to the same entry, which stays
-// valid: the library owns it).  A call that finds no entry while its stream
-// is capturing, or whose device already has kMaxAuxPerDevice entries, runs
-// every stage on the caller's stream instead (same kernels, same results).
+// valid: the library owns it).  A call whose device already has
+// kMaxAuxPerDevice entries, or that cannot create one, runs every stage on
+// the caller's stream instead (same kernels, same results).
 // The entry's mutex keeps the event pair of one call from interleaving with
 // another host thread's call on the same caller stream.
 struct AuxStream {
@@ -340,12 +340,9 @@ AuxStream* aux_for(cudaStream_t caller) {
     ++on_dev;
   }
   if (on_dev >= kMaxAuxPerDevice) return nullptr;
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(caller, &cs) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  if (cs != cudaStreamCaptureStatusNone) return nullptr;
+  // (creating a stream and events is allowed while `caller` is capturing: they
+  // are not stream work, and the fork event pulls the new stream into the
+  // capture)
   auto a = std::make_unique<AuxStream>();
   a->dev = dev;
   a->caller = caller;
