@@ -375,12 +375,16 @@ def run_ours(args):
                 for _ in range(warmup):
                     fn()
             torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                fn()
+            if args.no_graph:
+                replay = fn
+            else:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    fn()
+                replay = g.replay
             for _ in range(warmup):
                 with torch.cuda.stream(stream):
-                    g.replay()
+                    replay()
             torch.cuda.synchronize()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             tot = 0.0
@@ -388,7 +392,7 @@ def run_ours(args):
                 with torch.cuda.stream(stream):
                     flush_l2()
                     a.record(stream)
-                    g.replay()
+                    replay()
                     b.record(stream)
                 stream.synchronize()
                 tot += a.elapsed_time(b)
