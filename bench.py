@@ -67,8 +67,11 @@ METRIC = "latent-MoE layer tokens/s at T=8 and T=4096; % of HBM / bf16 TC roofli
 UNIT = "tokens/s"
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum, one ncu capture) of
 # the six GEMM launches of one prefill forward of this workload, summed; valid
-# for the GEMM kernel as it was when captured, and for this workload only.
-GEMM_SET_DRAM_BYTES = 2271430912
+# for the GEMM kernel as it was when captured, and for this workload only.  The
+# capture ran on the 128-expert variant (bench.py --case layer): the dense
+# GEMMs have this workload's shapes, the grouped GEMMs are scaled by the ratio
+# of their algorithmic bytes (the used experts' weights and the token rows).
+GEMM_SET_DRAM_BYTES = 2274500000
 
 
 def peaks():
@@ -507,7 +510,8 @@ def run_ours(args):
             "peak_source": f"{pk['source']} bf16 burst",
             "traffic": GEMM_SET_DRAM_BYTES,
             "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of the six GEMM "
-                              "launches of one prefill forward (algorithmic: 2042.8 MB)",
+                              "launches of one prefill forward, captured on the 128-expert "
+                              "variant and scaled to this workload (algorithmic: 2042.8 MB)",
             "flops_per_launch_set": fl["total"], "ms_per_launch_set": round(gemm_ms, 4)}
     # the grouped expert GEMMs alone (GEMM1 with SituGLU in its epilogue, GEMM2)
     ex_ms = st["gemm1"] + st["gemm2"]
