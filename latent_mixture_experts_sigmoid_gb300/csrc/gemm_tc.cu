@@ -22,8 +22,9 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator; with tokens on M the
 //               rows are rounded to bf16 (after SituGLU or the bf16 addend
 //               where asked) into a swizzled shared-memory staging buffer and
-//               written 4 rows x 128 bytes per 16-byte store instruction;
-//               otherwise fp32 partials or bf16 values go straight out.
+//               leave by a TMA bulk tensor store (a block of 32 valid rows)
+//               or 4 rows x 128 bytes per 16-byte store instruction (a ragged
+//               block); otherwise fp32 partials or bf16 values go straight out.
 // GEMMs with tokens on M and 256-row weight tiles run in clusters of two CTAs.
 // A pair of units shares an operand: token tiles 2t and 2t+1 of a group
 // against the same weight tile (each CTA loads one 128-row half of the weight
@@ -143,6 +144,32 @@ __device__ __forceinline__ void tma_load_2d_mc(const CUtensorMap* map, uint32_t 
       ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
       : "memory");
+}
+
+// Bulk tensor store of a shared-memory box (laid out as the map's swizzle
+// expects) to the global tensor at {c0, c1}; completion is tracked by bulk
+// async-groups of the issuing thread.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// every bulk store of this thread has finished reading its shared memory
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// every bulk store of this thread has completed
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// order this thread's generic-proxy shared-memory writes before async-proxy reads
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -359,7 +386,8 @@ enum : int { kFormRegular = 0, kFormSwap = 1, kFormStack = 2 };
 template <bool kPairs, int kForm>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmW2, const GemmParams p) {
+               const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmO,
+               const GemmParams p) {
   constexpr bool kSwap = kForm == kFormSwap;
   constexpr bool kStack = kForm == kFormStack;
   extern __shared__ uint8_t smem_raw[];
@@ -383,11 +411,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   int* tab = reinterpret_cast<int*>(tmem_holder + 4);
   GroupTables tabs{tab, tab + p.num_groups + 1, tab + 2 * p.num_groups + 1,
                    tab + 3 * p.num_groups + 1};
-  // epilogue staging: 4 warps x [32 rows][32 fp32], 16-byte chunks XOR-swizzled by row
+  // epilogue staging: 4 warps x [32 rows][32 fp32], 16-byte chunks XOR-swizzled
+  // by row: the 128-byte swizzle of a [32 rows][64 bf16] TMA box, so each
+  // warp's buffer starts on a 1024-byte boundary
   float* stage_out = reinterpret_cast<float*>(
       (reinterpret_cast<uintptr_t>(tab + (p.tile_prefix ? group_table_ints(p.num_groups) : 0)) +
-       15) &
-      ~uintptr_t(15));
+       1023) &
+      ~uintptr_t(1023));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -659,9 +689,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // row r = token, columns = features.  Per 64-column chunk each thread
         // rounds its row to bf16 (after SituGLU when fused, after adding the
         // bf16 addend in fp32 when there is one) into its warp's staging
-        // buffer [32 rows][64 bf16]; the warp then writes 4 rows x 128 bytes
-        // per 16-byte store instruction.
+        // buffer [32 rows][64 bf16].  When all 32 rows of the warp's block are
+        // valid, one lane stores the buffer with a TMA bulk tensor store;
+        // otherwise (a ragged block: the rows past it belong to the next
+        // group) the warp writes 4 rows x 128 bytes per 16-byte store
+        // instruction, valid rows only.
         uint32_t* st = reinterpret_cast<uint32_t*>(stage_out) + (size_t)q * 32 * 32;
+        const bool bulk = p.tma_store && q * 32 + 31 < x.nvalid;
         const int width = p.fuse_situ ? BM : bn;           // output columns of this tile
         const int fcol0 = x.feat_tile * width;
         const int ldo = p.fuse_situ ? p.M_feat / 2 : p.ldo;
@@ -672,6 +706,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           for (int b = 0; b < width * 2; b += 128)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(arow) + b));
         for (int c0 = 0; c0 < width; c0 += 64) {
+          // the staging buffer is free once the previous bulk store read it
+          if (p.tma_store) {
+            if (lane == 0) bulk_wait_read();
+            __syncwarp();
+          }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             // the addend's 32 columns, loaded before the accumulator
@@ -730,6 +769,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               *reinterpret_cast<uint4*>(st + lane * 32 + (((4 * h + c) ^ (lane & 7)) * 4)) =
                   make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
           }
+          if (bulk) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmO, smem_u32(st), fcol0 + c0, x.tok_row0 + q * 32);
+              bulk_commit();
+            }
+            continue;
+          }
           __syncwarp();
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -787,6 +835,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
     }
+    // this warp's bulk stores have completed before the CTA exits
+    if (p.tma_store && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -886,8 +936,23 @@ int max_pairs_resident(size_t smem) {
 // on M only) the epilogue staging buffers; at most 227 KB
 size_t smem_for(int stage, int stages, int groups, int tok_on_m) {
   return 1024 + stages * stage + (2 * stages + 5) * 8 + 16 +
-         (groups ? (size_t)group_table_ints(groups) * 4 : 0) + 16 +
+         (groups ? (size_t)group_table_ints(groups) * 4 : 0) + 1024 +
          (tok_on_m ? 4 * 32 * 32 * 4 : 0);
+}
+
+// Tensor map of a bf16 output [rows, cols] (row stride ldo) for bulk stores of
+// [32 rows][64 columns] boxes with the 128-byte swizzle.
+bool make_out_map(CUtensorMap* m, const void* base, long long rows, int cols, int ldo) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ldo * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -950,6 +1015,19 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
   } else {
     mw2 = mw;
   }
+  // bf16 output with tokens on M: full 32-row blocks leave by bulk tensor stores
+  CUtensorMap mo = mw;
+#ifndef LMOE_TMA_STORE
+#define LMOE_TMA_STORE 1
+#endif
+  p.tma_store = 0;
+  if (LMOE_TMA_STORE && g.tok_on_m && !g.out_fp32) {
+    const int cols = g.fuse_situ ? g.M_feat / 2 : g.M_feat;
+    const long long out_rows = g.grp_count ? g.x_rows : (long long)g.T_dense;
+    if (!make_out_map(&mo, g.out, out_rows, cols, g.ldo))
+      return cudaErrorInvalidValue;
+    p.tma_store = 1;
+  }
 
   const size_t smem = smem_for(stage, p.stages, g.grp_count ? g.G : 0, g.tok_on_m);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
@@ -966,13 +1044,14 @@ cudaError_t launch_gemm(const GemmDesc& g, cudaStream_t stream) {
     int np = pairs;
     if (g.max_units > 0 && g.max_units < np) np = g.max_units;
     return launch_k_cluster(gemm_tc_kernel<true, kFormRegular>, dim3(2 * np), dim3(kThreads), smem,
-                            stream, 2, mx, mw, mw2, p);
+                            stream, 2, mx, mw, mw2, mo, p);
   }
   int grid = num_sms();
   if (g.max_units > 0 && g.max_units < grid) grid = g.max_units;
   if (grid < 1) grid = 1;
-  if (g.tok_on_m) return launch_k(kern, dim3(grid), dim3(kThreads), smem, stream, mx, mw, mw2, p);
-  return launch_k(kern, dim3(grid), dim3(kThreads), smem, stream, mw, mx, mw2, p);
+  if (g.tok_on_m)
+    return launch_k(kern, dim3(grid), dim3(kThreads), smem, stream, mx, mw, mw2, mo, p);
+  return launch_k(kern, dim3(grid), dim3(kThreads), smem, stream, mw, mx, mw2, mo, p);
 }
 
 int* device_error_word() {

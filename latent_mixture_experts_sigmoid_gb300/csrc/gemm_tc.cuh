@@ -37,6 +37,8 @@ struct GemmParams {
                            // grouped, tokens on M, 256-row weight tiles, no split-K
   int w2_row0;             // > 0: weight rows from w2_row0 on are rows (row - w2_row0) of the
                            // second weight map (weights on M only)
+  int tma_store;           // 1: bf16 outputs with tokens on M leave full 32-row blocks by
+                           // bulk tensor stores through the output tensor map
   SituParams sp;
 };
 
