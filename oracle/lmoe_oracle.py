@@ -37,6 +37,8 @@ the design notes):
   R-10 no linear biases;
   R-19 router GEMM: fp32 logits = X W_router^T from a bf16 [E, H] weight,
        rounded once to float32;
+  R-20 MXFP4 experts: E2M1 codes two per byte (element 2i in the low nibble),
+       one scale exponent (bias 127) per 32 elements along K;
   R-11 expert_num_tokens outside [0, T_max] is clamped.
 
 Parity status: every function below is pinned by ``tests/test_oracle_*.py``
@@ -293,6 +295,65 @@ def router_gemm(hidden_bits: np.ndarray, w_router_bits: np.ndarray) -> np.ndarra
     return (X @ Wr.T).astype(np.float32)
 
 
+# ---------------------------------------------------------------------------
+# Block-scaled (MXFP4) expert weights
+# ---------------------------------------------------------------------------
+# [vLLM-50088] commits 4-5 and [TRTLLM-20541] run the routed experts of this
+# layer with MXFP4 weights (the TRTLLM-Gen MXE4M3 x MXE2M1 path), with SituGLU
+# acting on the dequantized gate/up.  An MXFP4 value is a 4-bit float with one
+# sign bit, two exponent bits (bias 1) and one mantissa bit (E2M1), times a
+# power of two shared by each block of 32 consecutive elements (an unsigned
+# 8-bit exponent, bias 127).  Storage read here (R-20): two codes per byte,
+# element 2i in the low nibble; scales [rows, K/32].
+
+
+def e2m1_value(code: np.ndarray) -> np.ndarray:
+    """float64 value of 4-bit E2M1 codes (bit 3 sign, bits 2-1 exponent, bit 0
+    mantissa): exponent field 0 is subnormal (mantissa * 1/2), otherwise
+    2^(e-1) * (1 + mantissa/2)."""
+    code = np.asarray(code).astype(np.int64)
+    sign = np.where(code & 8, -1.0, 1.0)
+    e = (code >> 1) & 3
+    m = code & 1
+    mag = np.where(e == 0, m * 0.5, np.ldexp(1.0 + m * 0.5, (e - 1).astype(np.int64)))
+    return sign * mag
+
+
+def e8m0_value(s: np.ndarray) -> np.ndarray:
+    """float64 value of unsigned 8-bit E8M0 scale exponents: 2^(s - 127), and
+    NaN for 255 (the format's one non-number)."""
+    s = np.asarray(s).astype(np.int64)
+    return np.where(s == 255, np.nan, np.ldexp(1.0, s - 127))
+
+
+def unpack_e2m1(packed: np.ndarray) -> np.ndarray:
+    """uint8 [rows, K/2] -> 4-bit codes [rows, K]: element 2i is the low nibble
+    of byte i, element 2i+1 its high nibble."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    codes = np.empty(packed.shape[:-1] + (2 * packed.shape[-1],), dtype=np.uint8)
+    codes[..., 0::2] = packed & np.uint8(15)
+    codes[..., 1::2] = packed >> np.uint8(4)
+    return codes
+
+
+def dequant_mxfp4(packed: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """float64 [rows, K] from packed codes [rows, K/2] (uint8) and per-32
+    scale exponents [rows, K/32] (uint8): E2M1 value * 2^(scale - 127), exactly."""
+    codes = unpack_e2m1(packed)
+    scale = e8m0_value(scales)
+    return e2m1_value(codes) * np.repeat(scale, 32, axis=-1)
+
+
+def mxfp4_as_bf16_bits(packed: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """The dequantized weights as bf16 bits (exact when every scale exponent
+    is in 2..252, where each E2M1 value times the power of two is a bf16 value)."""
+    w = dequant_mxfp4(packed, scales)
+    bits = f64_to_bf16_bits(w)
+    fin = np.isfinite(w)
+    assert np.array_equal(bf16_to_f64(bits)[fin], w[fin]), "MXFP4 value not exact in bf16"
+    return bits
+
+
 def _expert(W: dict, name: str, e: int) -> np.ndarray:
     v = W[name]
     return v(int(e)) if callable(v) else v[int(e)]
@@ -371,3 +432,18 @@ def latent_moe_forward_router(dims, W: dict, hidden_bits: np.ndarray, w_router_b
         return res
     out, mid = res
     return out, dict(mid, logits=logits)
+
+
+def latent_moe_forward_mxfp4(dims, W: dict, Q: dict, hidden_bits: np.ndarray,
+                             logits: np.ndarray, intermediates: bool = False):
+    """The layer forward with MXFP4 routed experts: Q holds w13_q, w13_s,
+    w2_q, w2_s (stacked [E, ...] arrays, or callables e -> (codes, scales)),
+    W the other weights.  The experts' GEMMs use the dequantized weights
+    exactly; everything else is latent_moe_forward."""
+    def expert(name):
+        q, sc = Q[name + "_q"], Q[name + "_s"]
+        if callable(q):
+            return lambda e: mxfp4_as_bf16_bits(*q(e))
+        return lambda e: mxfp4_as_bf16_bits(q[int(e)], sc[int(e)])
+    return latent_moe_forward(dims, dict(W, w13=expert("w13"), w2=expert("w2")), hidden_bits,
+                              logits, intermediates)

@@ -3,16 +3,20 @@ caught by one of the pins.  This shows the pins bite."""
 import numpy as np
 import pytest
 
+import workloads as W
 from oracle import lmoe_oracle as O
 import tests.test_oracle_numerics as N
 import tests.test_oracle_route as R
 import tests.test_oracle_layer as L
 import tests.test_oracle_router as RG
+import tests.test_oracle_mxfp4 as MX
 
 _route = O.route
 _situ = O.situ
 _permute = O.permute
 _router_gemm = O.router_gemm
+_e2m1_value = O.e2m1_value
+_dequant_mxfp4 = O.dequant_mxfp4
 
 
 def _situ_no_sigmoid(g, u, beta, lb):
@@ -77,6 +81,38 @@ def _router_gemm_features_reversed(x_bits, w_bits):
     return _router_gemm(x_bits[:, ::-1].copy(), w_bits)
 
 
+def _e2m1_no_subnormal(code):
+    # exponent field 0 read like the others: 2^(e-1) * (1 + m/2)
+    code = np.asarray(code).astype(np.int64)
+    e, m = (code >> 1) & 3, code & 1
+    return np.where(code & 8, -1.0, 1.0) * np.ldexp(1.0 + m * 0.5, e - 1)
+
+
+def _dequant_nibbles_swapped(packed, scales):
+    p = np.asarray(packed, dtype=np.uint8)
+    return _dequant_mxfp4(((p & 15) << 4 | (p >> 4)).astype(np.uint8), scales)
+
+
+def _dequant_scale_bias_128(packed, scales):
+    return _dequant_mxfp4(packed, scales) * 0.5
+
+
+def _dequant_blocks_of_16(packed, scales):
+    codes = O.unpack_e2m1(packed)
+    sc = np.repeat(np.ldexp(1.0, np.asarray(scales, np.int64) - 127), 16, axis=-1)
+    sc = np.concatenate([sc, sc], axis=-1)[..., :codes.shape[-1]]
+    return O.e2m1_value(codes) * sc
+
+
+def _dequant_up_from_gate_rows(packed, scales):
+    # a w13 read with its gate rows standing in for the up rows too
+    w = _dequant_mxfp4(packed, scales)
+    if w.shape[0] != 2 * W.TINY.inter:
+        return w
+    h = w.shape[0] // 2
+    return np.concatenate([w[:h], w[:h]])
+
+
 def _permute_descending(ids, E):
     counts, offsets, row_of, tok_of_row = _permute(ids[::-1].copy(), E)
     return counts, offsets, row_of[::-1].copy(), (ids.shape[0] - 1 - tok_of_row).astype(np.int32)
@@ -98,6 +134,11 @@ MUTATIONS = [
     ("router_gemm", _router_gemm_bf16_logits, RG.check_two_hot_router_rows_sum_in_fp32),
     ("router_gemm", _router_gemm_rows_reversed, RG.check_one_hot_router_rows_pick_features),
     ("router_gemm", _router_gemm_features_reversed, RG.check_one_hot_router_rows_pick_features),
+    ("e2m1_value", _e2m1_no_subnormal, MX.test_e2m1_positive_value_set),
+    ("dequant_mxfp4", _dequant_nibbles_swapped, MX.check_nibble_order),
+    ("dequant_mxfp4", _dequant_scale_bias_128, MX.check_scale_blocks),
+    ("dequant_mxfp4", _dequant_blocks_of_16, MX.check_scale_blocks),
+    ("dequant_mxfp4", _dequant_up_from_gate_rows, MX.check_gate_and_up_halves),
     ("permute", _permute_descending, lambda: R.check_permute(
         np.stack([np.random.default_rng(t).permutation(16)[:3] for t in range(20)]).astype(np.int32), 16)),
 ]

@@ -47,6 +47,7 @@ S_LOGITS, S_BIAS, S_ZIPF, S_W_DOWN, S_W13, S_W2 = 1, 2, 3, 4, 5, 6
 S_WS13, S_WS2, S_NORM, S_W_UP, S_HIDDEN = 7, 8, 9, 10, 11
 S_SITU, S_SITU_MASK, S_SITU_SIGN, S_COUNTS = 12, 13, 14, 15
 S_W_ROUTER = 16
+S_FP4_W13, S_FP4_W2 = 17, 18
 
 ROW_BLOCK = 64          # rows per independent stream in dense matrices
 SENTINEL = 0xDEAD       # bf16 bit pattern for padded rows
@@ -304,3 +305,45 @@ def expert_chunks(d: LayerDims, name: str, seed: int = 0, chunk: int = 64):
         with ThreadPoolExecutor(_threads()) as ex:
             parts = list(ex.map(lambda e: fn(d, e, seed), range(e0, e1)))
         yield e0, e1, np.stack(parts)
+
+
+# --- block-scaled (MXFP4) expert weights ---------------------------------------
+# Each expert matrix [rows, K] is stored as 4-bit codes, two per byte (element
+# 2i in the low nibble of byte i, element 2i+1 in the high nibble), and one
+# 8-bit power-of-two scale exponent per 32 consecutive elements of a row.  The
+# generator draws the codes and the exponents directly (no quantisation of
+# float weights): codes uniform over the 16 patterns, exponents uniform in
+# [118, 120], so that the weights have magnitudes like the bf16 N(0, 0.02^2)
+# weights (the largest code value, 6, times 2^-8 is 0.023).
+MXFP4_BLOCK = 32
+MXFP4_SCALE_LO, MXFP4_SCALE_HI = 118, 120
+
+
+def mxfp4_matrix(seed: int, stream: int, index: int, rows: int, K: int):
+    """(packed codes uint8 [rows, K/2], scale exponents uint8 [rows, K/32])."""
+    g = _rng(seed, stream, index)
+    codes = g.integers(0, 16, size=(rows, K), dtype=np.uint8)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << np.uint8(4))).astype(np.uint8)
+    scales = g.integers(MXFP4_SCALE_LO, MXFP4_SCALE_HI + 1, size=(rows, K // MXFP4_BLOCK),
+                        dtype=np.uint8)
+    return packed, scales
+
+
+def mxfp4_w13_expert(d: LayerDims, e: int, seed: int = 0):
+    """Expert e gate|up weight in MXFP4: [2*inter, latent/2] codes, [2*inter, latent/32] scales."""
+    return mxfp4_matrix(seed, S_FP4_W13, e, 2 * d.inter, d.latent)
+
+
+def mxfp4_w2_expert(d: LayerDims, e: int, seed: int = 0):
+    """Expert e down weight in MXFP4: [latent, inter/2] codes, [latent, inter/32] scales."""
+    return mxfp4_matrix(seed, S_FP4_W2, e, d.latent, d.inter)
+
+
+def mxfp4_experts(d: LayerDims, seed: int = 0) -> dict:
+    """Every expert's MXFP4 weights stacked: w13_q [E, 2d, L/2], w13_s [E, 2d, L/32],
+    w2_q [E, L, d/2], w2_s [E, L, d/32]."""
+    with ThreadPoolExecutor(_threads()) as ex:
+        a = list(ex.map(lambda e: mxfp4_w13_expert(d, e, seed), range(d.num_experts)))
+        b = list(ex.map(lambda e: mxfp4_w2_expert(d, e, seed), range(d.num_experts)))
+    return dict(w13_q=np.stack([x[0] for x in a]), w13_s=np.stack([x[1] for x in a]),
+                w2_q=np.stack([x[0] for x in b]), w2_s=np.stack([x[1] for x in b]))
