@@ -112,6 +112,16 @@ def gemm_bytes(d, n_used):
         up=2 * (H * L + T * L + 2 * T * H))
 
 
+def mxfp4_expert_bytes(d, n_used):
+    """Bytes the two MXFP4 expert stages must move at least once: the used
+    experts' 4-bit codes and their scales (4.25 bits a weight), the input rows
+    and the bf16 outputs."""
+    L, dI, R = d.latent, d.inter, d.T * d.topk
+    wb = 0.5 + 1.0 / 32
+    return dict(gemm1=int(n_used * 2 * dI * L * wb + 2 * (R * L + R * dI)),
+                gemm2=int(n_used * L * dI * wb + 2 * (R * dI + R * L)))
+
+
 # --------------------------------------------------------------------------
 # clocks sampled during the timed region
 # --------------------------------------------------------------------------
@@ -414,6 +424,87 @@ def run_ours(args):
                          " against lmoe_router_logits + latent_moe_forward; router weight "
                          "bf16 [E, H] N(0, 1/H)")}
 
+    def measure_mxfp4(d, zipf, steps, warmup, q):
+        """latent_moe_forward_mxfp4 (routed experts in MXFP4, the rest bf16),
+        one CUDA-graph replay per step, L2 flushed between steps; per-stage
+        times from the library's stage events in a separate pass."""
+        T = d.T
+        x = dev_bf16(W.hidden_states(d, 0))
+        lgd = torch.from_numpy(W.router_logits(T, d.num_experts, 0, zipf=zipf)).to(dev)
+        out = torch.empty((T, d.hidden), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(lm.latent_moe_workspace_bytes_mxfp4(d), dtype=torch.uint8, device=dev)
+        counts = torch.empty(d.num_experts, dtype=torch.int32, device=dev)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(lm.NUM_STAGES + 1)]
+        dbg = {"expert_num_tokens": counts, "stage_events": evs}
+        wq = dict(w, w13=None, w2=None)
+
+        def fwd():
+            lm.latent_moe_forward_mxfp4(d, wq, q, x, lgd, out, ws, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                lm.latent_moe_forward_mxfp4(d, wq, q, x, lgd, out, ws, debug=dbg, stream=stream)
+        torch.cuda.synchronize()
+        n_used = int((counts.cpu().numpy() > 0).sum())
+        if args.no_graph:
+            replay = fwd
+        else:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fwd()
+            replay = g.replay
+        for _ in range(warmup):
+            with torch.cuda.stream(stream):
+                replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot = 0.0
+        for _ in range(steps):
+            with torch.cuda.stream(stream):
+                flush_l2()
+                a.record(stream)
+                replay()
+                b.record(stream)
+            stream.synchronize()
+            tot += a.elapsed_time(b)
+        per_stage = np.zeros(lm.NUM_STAGES)
+        for _ in range(steps):
+            with torch.cuda.stream(stream):
+                flush_l2()
+                torch.cuda._sleep(2_000_000)
+                lm.latent_moe_forward_mxfp4(d, wq, q, x, lgd, out, ws, debug=dbg, stream=stream)
+            stream.synchronize()
+            per_stage += np.array([evs[i].elapsed_time(evs[i + 1]) for i in range(lm.NUM_STAGES)])
+        st = dict(zip(lm.STAGE_NAMES, per_stage / steps))
+        us = tot / steps * 1e3
+        eb = mxfp4_expert_bytes(d, n_used)
+        ex_us = (st["gemm1"] + st["situ"] + st["gemm2"]) * 1e3
+        res = {"us_per_step": round(us, 2), "tokens_per_s": round(T / (us / 1e6), 1),
+               "experts_used": n_used, "launches": lm.latent_moe_launch_count_mxfp4(d),
+               "per_stage_ms": {n: round(v, 4) for n, v in st.items()}}
+        if T <= 128:
+            gb = (eb["gemm1"] + eb["gemm2"]) / (ex_us / 1e6) / 1e9
+            by = gemm_bytes(d, n_used)
+            layer_bytes = sum(v for k2, v in by.items() if k2 not in ("gemm1", "gemm2")) + \
+                eb["gemm1"] + eb["gemm2"]
+            res["expert_kernels"] = {
+                "kernel": "fp4_gemv_kernel (GEMM1 + SituGLU, GEMM2 on the 4-bit weights)",
+                "bound": "hbm", "us": round(ex_us, 2), "algorithmic_bytes": eb,
+                "achieved": round(gb, 1), "peak": pk["hbm"], "unit": "GB/s",
+                "frac": round(gb / pk["hbm"], 4),
+                "timing": "per-stage CUDA events (stages serialised)"}
+            lgb = layer_bytes / (us / 1e6) / 1e9
+            res["roofline"] = {"bound": "hbm", "algorithmic_bytes": int(layer_bytes),
+                               "achieved": round(lgb, 1), "peak": pk["hbm"], "unit": "GB/s",
+                               "frac": round(lgb / pk["hbm"], 4)}
+        res["what"] = ("latent_moe_forward_mxfp4: routed experts as MXFP4 (E2M1 codes, one E8M0 "
+                       "scale per 32; codes uniform, scale exponents 118..120), every other "
+                       "weight bf16 as in the bf16 lines" +
+                       (": the expert stages read the 4-bit weights directly" if T <= 128 else
+                        ": every expert dequantized to bf16 in the workspace each call, then "
+                        "the tensor-core GEMMs"))
+        return res
+
     def time_launches(fns, reps):
         """Average device time per launch of `reps` back-to-back launches.
 
@@ -483,6 +574,15 @@ def run_ours(args):
     dec = measure(W.DECODE, False, args.steps, args.warmup)
     rtr_dec = measure_router(W.DECODE, False, args.steps, args.warmup)
     rtr_pre = measure_router(W.PREFILL, True, args.steps, args.warmup)
+    # the same model with MXFP4 routed experts (bf16 experts released first)
+    del w["w13"], w["w2"]
+    torch.cuda.empty_cache()
+    qh = W.mxfp4_experts(dD, 0)
+    q4 = {k2: torch.from_numpy(v).to(dev) for k2, v in qh.items()}
+    del qh
+    fp4_dec = measure_mxfp4(W.DECODE, False, args.steps, args.warmup, q4)
+    fp4_pre = measure_mxfp4(W.PREFILL, True, args.steps, args.warmup, q4)
+    del q4
     kern = kernel_lines(max(3, args.steps))
     if not args.no_cpu_baseline:
         for name, cb in kernel_cpu_baselines().items():
@@ -540,6 +640,7 @@ def run_ours(args):
               "e2e_tokens_per_s": round(dDc.T * K / (dec_e2e / 1e3), 1),
               "gpu_launches_per_step": lm.latent_moe_launch_count(dDc)}
     decode["router_gemm"] = rtr_dec
+    decode["mxfp4"] = fp4_dec
     if dec["pre"] is not None:
         decode["pre_routed"] = {
             "us_per_step": round(dec["pre"]["ms"] / K * 1e3, 2),
@@ -588,6 +689,7 @@ def run_ours(args):
         "layer_tflops": round(fl["total"] / (pre_ms / K / 1e3) / 1e12, 1),
         "decode": decode,
         "prefill_router_gemm": rtr_pre,
+        "prefill_mxfp4": fp4_pre,
         "kernels": kern,
         "clocks": clk,
         "wall_s": round(wall, 1),
@@ -807,6 +909,18 @@ def run_case(name, reps):
         layer(dataclasses.replace(W.PREFILL, num_experts=128), True)
     elif name == "decode":
         layer(dataclasses.replace(W.DECODE, num_experts=128), False)
+    elif name == "decode_mxfp4":
+        d = dataclasses.replace(W.DECODE, num_experts=128)
+        w = {"w_down": bf16(W.w_down(d)), "w_up": bf16(W.w_up(d)), "ws13": bf16(W.ws13(d)),
+             "ws2": bf16(W.ws2(d)), "norm_w": bf16(W.norm_weight(d)),
+             "bias": torch.from_numpy(W.score_bias(d.num_experts)).to(dev)}
+        q = {k2: torch.from_numpy(v).to(dev) for k2, v in W.mxfp4_experts(d, 0).items()}
+        x = bf16(W.hidden_states(d, 0))
+        lg = torch.from_numpy(W.router_logits(d.T, d.num_experts, 0)).to(dev)
+        out = torch.empty((d.T, d.hidden), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(lm.latent_moe_workspace_bytes_mxfp4(d), dtype=torch.uint8, device=dev)
+        for _ in range(reps + 1):
+            lm.latent_moe_forward_mxfp4(d, w, q, x, lg, out, ws)
     elif name == "route":
         route(16384)
     elif name == "route8":
@@ -823,7 +937,7 @@ def run_case(name, reps):
     print(f"{name}: ok")
 
 
-CASES = ("linear", "layer", "decode", "route", "route8", "situ")
+CASES = ("linear", "layer", "decode", "decode_mxfp4", "route", "route8", "situ")
 
 
 def main():

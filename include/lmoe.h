@@ -294,6 +294,60 @@ int latent_moe_forward_router(const lmoe_dims* dims, const lmoe_weights* weights
 /* dims), as latent_moe_launch_count counts them.                             */
 int latent_moe_launch_count_router(const lmoe_dims* dims, int has_shared_expert);
 
+/* ------------------------------------------------------------------------ */
+/* Block-scaled (MXFP4) routed experts ([vLLM-50088] commits 4-5: the        */
+/* TRTLLM-Gen MXFP4 MoE backend runs this layer's routed experts, SituGLU    */
+/* acting on the dequantized gate/up; [TRTLLM-20541]: Kimi K3 decode with    */
+/* the MXFP4 MoE).  Each expert matrix [rows, K] is stored as               */
+/*   codes  uint8 [rows, K/2]:  two 4-bit E2M1 values per byte, element 2i  */
+/*          in the low nibble of byte i, element 2i+1 in the high nibble     */
+/*          (E2M1: bit 3 sign, bits 2-1 exponent with bias 1, bit 0         */
+/*          mantissa; exponent 0 is subnormal: 0 or 0.5)                    */
+/*   scales uint8 [rows, K/32]: one power of two per 32 consecutive elements */
+/*          of a row, 2^(s - 127) (E8M0; 255 is NaN)                        */
+/* and weight[r, c] = E2M1(code[r, c]) * 2^(scale[r, c/32] - 127).  The      */
+/* activations stay bf16 (W4A16): the expert GEMMs compute with the exact   */
+/* dequantized weights.  Scale exponents 2..252 keep every weight a bf16     */
+/* value; outside that range the prefill path rounds the weight to bf16.     */
+/* ------------------------------------------------------------------------ */
+typedef struct lmoe_mxfp4_experts {
+  const uint8_t* w13_codes;   /* [E, 2d, L/2] (rows as lmoe_weights.w13)     */
+  const uint8_t* w13_scales;  /* [E, 2d, L/32]                               */
+  const uint8_t* w2_codes;    /* [E, L, d/2]                                 */
+  const uint8_t* w2_scales;   /* [E, L, d/32]                                */
+} lmoe_mxfp4_experts;
+
+/* out [rows, K] bf16 = the dequantized weights (rounded to bf16, exact for */
+/* scale exponents 2..252).  K % 32 == 0, rows >= 0; codes and out 16-byte  */
+/* aligned device pointers of the current device.                           */
+int lmoe_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, lmoe_bf16* out,
+                       int64_t rows, int K, void* stream);
+
+/* Workspace bytes of latent_moe_forward_mxfp4 (0 on invalid dims): the      */
+/* workspace of latent_moe_forward, plus at T > 128 room for every expert's */
+/* weights dequantized to bf16 (E * 3 * inter * latent * 2 bytes).          */
+size_t latent_moe_workspace_bytes_mxfp4(const lmoe_dims* dims);
+
+/* The layer forward with MXFP4 routed experts: latent_moe_forward with      */
+/* weights->w13 and weights->w2 unused (may be NULL) and the experts' GEMMs  */
+/* on `experts` instead.  At T <= 128 (decode) the two expert stages read    */
+/* the 4-bit weights directly (one kernel per stage over the active experts, */
+/* GEMM1's gate/up and SituGLU in one kernel); above, the weights are        */
+/* dequantized into the workspace each call and the bf16 tensor-core path    */
+/* runs on them (a caller that runs prefill repeatedly on the same weights   */
+/* can dequantize once with lmoe_dequant_mxfp4 and call latent_moe_forward). */
+/* Limits: those of latent_moe_forward and inter <= 8192.  The four expert   */
+/* pointers are required (LMOE_ERR_NULL), the codes 16-byte aligned          */
+/* (LMOE_ERR_ALIGN), device memory of the current device (LMOE_ERR_DEVICE).  */
+/* The workspace layout (latent_moe_workspace_offsets) is the same.          */
+int latent_moe_forward_mxfp4(const lmoe_dims* dims, const lmoe_weights* weights,
+                             const lmoe_mxfp4_experts* experts, const lmoe_bf16* hidden,
+                             const float* router_logits, lmoe_bf16* out, void* workspace,
+                             size_t workspace_bytes, const lmoe_debug* dbg, void* stream);
+
+/* Kernel launches of latent_moe_forward_mxfp4 (0 on invalid dims).         */
+int latent_moe_launch_count_mxfp4(const lmoe_dims* dims, int has_shared_expert);
+
 /* The layer forward without a caller workspace.  The pages have no          */
 /* counterpart to this entry point; it exists for callers that cannot         */
 /* allocate device memory: a plugin that an inference runtime calls with only */

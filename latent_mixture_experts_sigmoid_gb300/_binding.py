@@ -31,7 +31,9 @@ ABI_FUNCTIONS = ("moe_route", "situ_and_mul", "masked_situ_and_mul", "latent_moe
                  "latent_moe_launch_count", "lmoe_linear", "lmoe_status_string",
                  "lmoe_device_error", "lmoe_abi_version", "lmoe_gemm_unit_walk",
                  "lmoe_router_logits", "lmoe_router_logits_workspace_bytes",
-                 "latent_moe_forward_router", "latent_moe_launch_count_router")
+                 "latent_moe_forward_router", "latent_moe_launch_count_router",
+                 "lmoe_dequant_mxfp4", "latent_moe_workspace_bytes_mxfp4",
+                 "latent_moe_forward_mxfp4", "latent_moe_launch_count_mxfp4")
 
 
 class LmoeError(RuntimeError):
@@ -53,6 +55,11 @@ class LmoeWeights(ctypes.Structure):
     _fields_ = [("w_down", ctypes.c_void_p), ("w13", ctypes.c_void_p), ("w2", ctypes.c_void_p),
                 ("ws13", ctypes.c_void_p), ("ws2", ctypes.c_void_p), ("norm_w", ctypes.c_void_p),
                 ("w_up", ctypes.c_void_p), ("e_score_correction_bias", ctypes.c_void_p)]
+
+
+class LmoeMxfp4Experts(ctypes.Structure):
+    _fields_ = [("w13_codes", ctypes.c_void_p), ("w13_scales", ctypes.c_void_p),
+                ("w2_codes", ctypes.c_void_p), ("w2_scales", ctypes.c_void_p)]
 
 
 class LmoeDebug(ctypes.Structure):
@@ -124,6 +131,16 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.latent_moe_forward_router.restype = i32
     lib.latent_moe_launch_count_router.argtypes = [ctypes.POINTER(LmoeDims), i32]
     lib.latent_moe_launch_count_router.restype = i32
+    lib.lmoe_dequant_mxfp4.argtypes = [vp, vp, vp, i64, i32, vp]
+    lib.lmoe_dequant_mxfp4.restype = i32
+    lib.latent_moe_workspace_bytes_mxfp4.argtypes = [ctypes.POINTER(LmoeDims)]
+    lib.latent_moe_workspace_bytes_mxfp4.restype = ctypes.c_size_t
+    lib.latent_moe_forward_mxfp4.argtypes = [ctypes.POINTER(LmoeDims), ctypes.POINTER(LmoeWeights),
+                                             ctypes.POINTER(LmoeMxfp4Experts), vp, vp, vp, vp,
+                                             ctypes.c_size_t, ctypes.POINTER(LmoeDebug), vp]
+    lib.latent_moe_forward_mxfp4.restype = i32
+    lib.latent_moe_launch_count_mxfp4.argtypes = [ctypes.POINTER(LmoeDims), i32]
+    lib.latent_moe_launch_count_mxfp4.restype = i32
     _lib = lib
     return lib
 
@@ -432,3 +449,64 @@ def latent_moe_launch_count_router(dims, has_shared_expert: bool = True) -> int:
     dd = dims if isinstance(dims, LmoeDims) else make_dims(dims)
     return int(load_library().latent_moe_launch_count_router(ctypes.byref(dd),
                                                               1 if has_shared_expert else 0))
+
+
+# --- block-scaled (MXFP4) routed experts -------------------------------------------
+
+
+def lmoe_dequant_mxfp4(codes, scales, out, stream=None, rows: int | None = None,
+                       K: int | None = None):
+    """out [rows, K] bf16 = E2M1(codes) * 2^(scales - 127); codes uint8
+    [rows, K/2] (element 2i in the low nibble), scales uint8 [rows, K/32]."""
+    if rows is None:
+        K = out.shape[-1]
+        rows = out.numel() // K
+    rows, K = int(rows), int(K)
+    st = load_library().lmoe_dequant_mxfp4(_dev(codes, "codes", torch.uint8, rows * K // 2),
+                                           _dev(scales, "scales", torch.uint8, rows * K // 32),
+                                           _dev(out, "out", _BF16, rows * K), rows, K,
+                                           _stream(stream))
+    _check(st, "lmoe_dequant_mxfp4")
+
+
+def make_mxfp4_experts(q: dict, dims=None) -> LmoeMxfp4Experts:
+    """LmoeMxfp4Experts from a dict with w13_q, w13_s, w2_q, w2_s (uint8
+    tensors; with `dims` each is checked against its documented size)."""
+    names = ("w13_q", "w13_s", "w2_q", "w2_s")
+    if dims is None:
+        return LmoeMxfp4Experts(*[_ptr(q.get(n)) for n in names])
+    E, L, dI = int(dims.num_experts), int(dims.latent), int(dims.inter)
+    need = (E * 2 * dI * L // 2, E * 2 * dI * L // 32, E * L * dI // 2, E * L * dI // 32)
+    return LmoeMxfp4Experts(*[_dev(q.get(n), n, torch.uint8, c) for n, c in zip(names, need)])
+
+
+def latent_moe_workspace_bytes_mxfp4(dims) -> int:
+    dd = dims if isinstance(dims, LmoeDims) else make_dims(dims)
+    return int(load_library().latent_moe_workspace_bytes_mxfp4(ctypes.byref(dd)))
+
+
+def latent_moe_forward_mxfp4(dims, weights, experts, hidden, router_logits, out, workspace,
+                             workspace_bytes: int | None = None, debug: dict | None = None,
+                             stream=None):
+    """The layer forward with MXFP4 routed experts (weights' w13 / w2 unused)."""
+    dd = dims if isinstance(dims, LmoeDims) else make_dims(dims)
+    if isinstance(weights, LmoeWeights):
+        ww = weights
+    else:
+        ww = make_weights(dict(weights, w13=None, w2=None), dd)
+    qq = experts if isinstance(experts, LmoeMxfp4Experts) else make_mxfp4_experts(experts, dd)
+    T, H, E = int(dd.T), int(dd.hidden), int(dd.num_experts)
+    wsp, wsn = _workspace(workspace, workspace_bytes)
+    dbg, keep = _debug_struct(debug, dd)
+    st = load_library().latent_moe_forward_mxfp4(
+        ctypes.byref(dd), ctypes.byref(ww), ctypes.byref(qq), _dev(hidden, "hidden", _BF16, T * H),
+        _dev(router_logits, "router_logits", torch.float32, T * E),
+        _dev(out, "out", _BF16, T * H), wsp, wsn,
+        ctypes.byref(dbg) if dbg is not None else None, _stream(stream))
+    _check(st, "latent_moe_forward_mxfp4")
+
+
+def latent_moe_launch_count_mxfp4(dims, has_shared_expert: bool = True) -> int:
+    dd = dims if isinstance(dims, LmoeDims) else make_dims(dims)
+    return int(load_library().latent_moe_launch_count_mxfp4(ctypes.byref(dd),
+                                                             1 if has_shared_expert else 0))

@@ -41,6 +41,7 @@
 #include "gemm_tc.cuh"
 #include "lmoe_internal.cuh"
 #include "moe_data.cuh"
+#include "mxfp4.cuh"
 
 namespace lmoe {
 
@@ -118,12 +119,14 @@ struct Ws {
   uint16_t *Z, *A, *G, *act, *Y, *N, *Gs, *As, *Sh;
   float *logits;   // router logits [T, round_up(E, 128)] of the router-GEMM forward
   float *Pa, *Pb;
+  int32_t* active;          // active experts in expert order (decode permutation)
+  uint16_t *Wd13, *Wd2;     // MXFP4 experts dequantized to bf16 (MXFP4 forward, T > 128)
 };
 
 // Router logits rows are padded to whole 128-row weight tiles of the router GEMM.
 size_t padded_experts(int E) { return (size_t)round_up(E, 128); }
 
-size_t carve(const lmoe_dims& d, char* base, Ws* ws) {
+size_t carve(const lmoe_dims& d, char* base, Ws* ws, bool mxfp4 = false) {
   Carver c;
   c.base = base;
   const size_t T = d.T, k = d.topk, E = d.num_experts, L = d.latent, H = d.hidden;
@@ -157,6 +160,13 @@ size_t carve(const lmoe_dims& d, char* base, Ws* ws) {
     w.Pb = c.take<float>((size_t)kMaxSplits * T * mb);
   } else {
     w.Pa = w.Pb = nullptr;
+  }
+  w.active = c.take<int32_t>(E);
+  if (mxfp4 && d.T > kDecodeMaxT) {
+    w.Wd13 = c.take<uint16_t>(E * 2 * dI * L);
+    w.Wd2 = c.take<uint16_t>(E * L * dI);
+  } else {
+    w.Wd13 = w.Wd2 = nullptr;
   }
   if (ws) *ws = w;
   return (c.off + 255) & ~size_t(255);
@@ -282,10 +292,13 @@ Plan make_plan(const lmoe_dims& d, int nsm, bool router = false) {
   return p;
 }
 
-int plan_launches(const Plan& p, bool shared) {
+int plan_launches(const Plan& p, bool shared, bool mxfp4 = false) {
   // one permutation kernel for T <= 256; at decode sizes it also does the scatter
   const int perm = p.T <= 256 ? 1 : 3;
-  const int experts = p.fuse_g1 ? 2 : 3;  // GEMM1 (+ SituGLU unless fused), GEMM2
+  // GEMM1 (+ SituGLU unless fused), GEMM2; MXFP4 experts: at decode one kernel
+  // per stage on the 4-bit weights, above two dequantization kernels first
+  int experts = p.fuse_g1 ? 2 : 3;
+  if (mxfp4) experts = p.decode ? 2 : experts + 2;
   // route, down, permute, scatter (fused into the permutation at decode sizes),
   // experts, combine
   int n = 1 + 1 + perm + (p.decode ? 0 : 1) + experts + 1;
@@ -391,7 +404,7 @@ using namespace lmoe;
 
 extern "C" {
 
-int lmoe_abi_version(void) { return 102; }
+int lmoe_abi_version(void) { return 103; }
 
 const char* lmoe_status_string(int status) {
   switch (status) {
@@ -504,7 +517,7 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
                         const float* router_logits, const int32_t* pre_ids, const float* pre_w,
                         const lmoe_bf16* w_router, lmoe_bf16* out, void* workspace,
                         size_t workspace_bytes, const lmoe_debug* dbg, void* stream,
-                        bool own_workspace) {
+                        bool own_workspace, const lmoe_mxfp4_experts* fq = nullptr) {
   const int v = validate_dims(dims);
   if (v != LMOE_OK) return v;
   if (!wt) return LMOE_ERR_NULL;
@@ -514,20 +527,27 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
   // w_router, or ids and weights routed ahead
   const bool router = w_router != nullptr;
   const bool pre_routed = !router && router_logits == nullptr;
-  if (!hidden || (pre_routed && (!pre_ids || !pre_w)) || !out || !wt->w_down || !wt->w13 ||
-      !wt->w2 || !wt->w_up)
+  if (!hidden || (pre_routed && (!pre_ids || !pre_w)) || !out || !wt->w_down || !wt->w_up)
     return LMOE_ERR_NULL;
+  // routed experts: bf16 (w13, w2) or MXFP4 (fq)
+  if (fq) {
+    if (!fq->w13_codes || !fq->w13_scales || !fq->w2_codes || !fq->w2_scales) return LMOE_ERR_NULL;
+    if (d.inter > 8192) return LMOE_ERR_DIM;
+    if (!aligned16(fq->w13_codes) || !aligned16(fq->w2_codes)) return LMOE_ERR_ALIGN;
+  } else if (!wt->w13 || !wt->w2) {
+    return LMOE_ERR_NULL;
+  }
   const bool shared = wt->ws13 != nullptr;
   if (shared != (wt->ws2 != nullptr)) return LMOE_ERR_NULL;
   if (shared && d.shared_inter <= 0) return LMOE_ERR_DIM;
-  const void* ptrs[] = {hidden, router_logits, pre_ids, pre_w, out, wt->w_down, wt->w13, wt->w2,
-                        wt->w_up, wt->ws13, wt->ws2, wt->norm_w, wt->e_score_correction_bias,
-                        w_router};
+  const void* ptrs[] = {hidden, router_logits, pre_ids, pre_w, out, wt->w_down,
+                        fq ? nullptr : wt->w13, fq ? nullptr : wt->w2, wt->w_up, wt->ws13,
+                        wt->ws2, wt->norm_w, wt->e_score_correction_bias, w_router};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return LMOE_ERR_ALIGN;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return LMOE_ERR_WORKSPACE;
   Ws ws;
-  const size_t need = carve(d, static_cast<char*>(workspace), &ws);
+  const size_t need = carve(d, static_cast<char*>(workspace), &ws, fq != nullptr);
   if (workspace_bytes < need) return LMOE_ERR_WORKSPACE;
   if (dbg) {
     const void* dp[] = {dbg->topk_ids, dbg->topk_weights, dbg->expert_num_tokens,
@@ -535,9 +555,12 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
     for (const void* p : dp)
       if (p && !aligned16(p)) return LMOE_ERR_ALIGN;
   }
-  if (!on_current_device({hidden, router_logits, pre_ids, pre_w, out, wt->w_down, wt->w13, wt->w2,
-                          wt->w_up, wt->ws13, wt->ws2, wt->norm_w, wt->e_score_correction_bias,
-                          w_router, own_workspace ? nullptr : workspace}))
+  if (!on_current_device({hidden, router_logits, pre_ids, pre_w, out, wt->w_down,
+                          fq ? nullptr : wt->w13, fq ? nullptr : wt->w2, wt->w_up, wt->ws13,
+                          wt->ws2, wt->norm_w, wt->e_score_correction_bias, w_router,
+                          own_workspace ? nullptr : workspace}))
+    return LMOE_ERR_DEVICE;
+  if (fq && !on_current_device({fq->w13_codes, fq->w13_scales, fq->w2_codes, fq->w2_scales}))
     return LMOE_ERR_DEVICE;
   if (dbg && !on_current_device({dbg->topk_ids, dbg->topk_weights, dbg->expert_num_tokens,
                                  dbg->expert_offsets, dbg->row_of}))
@@ -691,7 +714,7 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
                                           ws.tile_prefix, ws.row_of, ws.tok_of_row,
                                           down_split ? nullptr : ws.Z,
                                           down_split ? ws.Pa : nullptr, cdown.splits, down_stride,
-                                          ldz, L, ws.A, id_err, s));
+                                          ldz, L, ws.A, ws.active, id_err, s));
   } else {
     st = permute(s);
     if (st != LMOE_OK) return st;
@@ -703,20 +726,44 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
                                  cdown.splits, down_stride, ldz, T, L, k, ws.row_of, ws.A, s));
   if (!mark(LMOE_STAGE_SCATTER + 1)) return LMOE_ERR_CUDA;
   // 5-7. experts
-  if (pl.fuse_g1) {
-    // act = bf16(SituGLU(bf16(A W13_e^T))) straight from GEMM1's epilogue
-    LMOE_TRY(gemm_grouped(wt->w13, E, 2 * dI, ws.A, rows, L, !decode, pl.g1_bn, ws, tile, ws.act,
-                          s, 1, d.beta, d.linear_beta));
-    if (!mark(LMOE_STAGE_GEMM1 + 1)) return LMOE_ERR_CUDA;
+  const uint16_t* W13 = wt->w13;
+  const uint16_t* W2 = wt->w2;
+  if (fq && decode) {
+    // MXFP4 at decode sizes: GEMM1 + SituGLU and GEMM2 straight from the 4-bit
+    // weights, one block per (active expert, column strip)
+    const int slots = (long long)E < rows ? E : (int)rows;
+    LMOE_TRY(launch_fp4_expert_gemv(fq->w13_codes, fq->w13_scales, ws.A, ws.act, ws.counts,
+                                    ws.offsets, ws.active, ws.tile_prefix + E, slots, L, dI, 1,
+                                    d.beta, d.linear_beta, s));
+    if (!mark(LMOE_STAGE_GEMM1 + 1) || !mark(LMOE_STAGE_SITU + 1)) return LMOE_ERR_CUDA;
+    LMOE_TRY(launch_fp4_expert_gemv(fq->w2_codes, fq->w2_scales, ws.act, ws.Y, ws.counts,
+                                    ws.offsets, ws.active, ws.tile_prefix + E, slots, dI, L, 0,
+                                    d.beta, d.linear_beta, s));
+    if (!mark(LMOE_STAGE_GEMM2 + 1)) return LMOE_ERR_CUDA;
   } else {
-    LMOE_TRY(gemm_grouped(wt->w13, E, 2 * dI, ws.A, rows, L, !decode, pl.g1_bn, ws, tile, ws.G,
-                          s));
-    if (!mark(LMOE_STAGE_GEMM1 + 1)) return LMOE_ERR_CUDA;
-    LMOE_TRY(launch_situ(ws.G, ws.act, rows, dI, d.beta, d.linear_beta, s));
+    if (fq) {
+      // MXFP4 above decode sizes: every expert's weights dequantized to bf16 in
+      // the workspace, then the tensor-core path
+      LMOE_TRY(launch_dequant_mxfp4(fq->w13_codes, fq->w13_scales, ws.Wd13,
+                                    (long long)E * 2 * dI, L, s));
+      LMOE_TRY(launch_dequant_mxfp4(fq->w2_codes, fq->w2_scales, ws.Wd2, (long long)E * L, dI, s));
+      W13 = ws.Wd13;
+      W2 = ws.Wd2;
+    }
+    if (pl.fuse_g1) {
+      // act = bf16(SituGLU(bf16(A W13_e^T))) straight from GEMM1's epilogue
+      LMOE_TRY(gemm_grouped(W13, E, 2 * dI, ws.A, rows, L, !decode, pl.g1_bn, ws, tile, ws.act, s,
+                            1, d.beta, d.linear_beta));
+      if (!mark(LMOE_STAGE_GEMM1 + 1)) return LMOE_ERR_CUDA;
+    } else {
+      LMOE_TRY(gemm_grouped(W13, E, 2 * dI, ws.A, rows, L, !decode, pl.g1_bn, ws, tile, ws.G, s));
+      if (!mark(LMOE_STAGE_GEMM1 + 1)) return LMOE_ERR_CUDA;
+      LMOE_TRY(launch_situ(ws.G, ws.act, rows, dI, d.beta, d.linear_beta, s));
+    }
+    if (!mark(LMOE_STAGE_SITU + 1)) return LMOE_ERR_CUDA;
+    LMOE_TRY(gemm_grouped(W2, E, L, ws.act, rows, dI, !decode, pl.g2_bn, ws, tile, ws.Y, s));
+    if (!mark(LMOE_STAGE_GEMM2 + 1)) return LMOE_ERR_CUDA;
   }
-  if (!mark(LMOE_STAGE_SITU + 1)) return LMOE_ERR_CUDA;
-  LMOE_TRY(gemm_grouped(wt->w2, E, L, ws.act, rows, dI, !decode, pl.g2_bn, ws, tile, ws.Y, s));
-  if (!mark(LMOE_STAGE_GEMM2 + 1)) return LMOE_ERR_CUDA;
   // 8. combine + RMSNorm
   LMOE_TRY(launch_combine_norm(ws.Y, topw, ws.row_of, T, k, L, wt->norm_w, d.rms_eps, ws.N, s));
   if (!mark(LMOE_STAGE_COMBINE + 1)) return LMOE_ERR_CUDA;
@@ -827,6 +874,39 @@ int latent_moe_forward_routed(const lmoe_dims* dims, const lmoe_weights* wt,
                               size_t workspace_bytes, const lmoe_debug* dbg, void* stream) {
   return forward_impl(dims, wt, hidden, nullptr, topk_ids, topk_weights, nullptr, out, workspace,
                       workspace_bytes, dbg, stream, false);
+}
+
+int lmoe_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, lmoe_bf16* out, int64_t rows,
+                       int K, void* stream) {
+  if (rows < 0 || K <= 0 || K % 32) return LMOE_ERR_DIM;
+  if (rows == 0) return LMOE_OK;
+  if (!codes || !scales || !out) return LMOE_ERR_NULL;
+  if (!aligned16(codes) || !aligned16(out)) return LMOE_ERR_ALIGN;
+  if (!on_current_device({codes, scales, out})) return LMOE_ERR_DEVICE;
+  if (launch_dequant_mxfp4(codes, scales, out, rows, K, (cudaStream_t)stream) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  return LMOE_OK;
+}
+
+size_t latent_moe_workspace_bytes_mxfp4(const lmoe_dims* dims) {
+  if (validate_dims(dims) != LMOE_OK || dims->inter > 8192) return 0;
+  return carve(*dims, nullptr, nullptr, true);
+}
+
+int latent_moe_forward_mxfp4(const lmoe_dims* dims, const lmoe_weights* wt,
+                             const lmoe_mxfp4_experts* experts, const lmoe_bf16* hidden,
+                             const float* router_logits, lmoe_bf16* out, void* workspace,
+                             size_t workspace_bytes, const lmoe_debug* dbg, void* stream) {
+  if (dims && dims->T != 0 && (!experts || !router_logits)) return LMOE_ERR_NULL;
+  lmoe_mxfp4_experts none{};
+  return forward_impl(dims, wt, hidden, router_logits, nullptr, nullptr, nullptr, out, workspace,
+                      workspace_bytes, dbg, stream, false, experts ? experts : &none);
+}
+
+int latent_moe_launch_count_mxfp4(const lmoe_dims* dims, int has_shared_expert) {
+  if (validate_dims(dims) != LMOE_OK || dims->inter > 8192) return 0;
+  if (dims->T == 0) return 0;
+  return plan_launches(make_plan(*dims, num_sms()), has_shared_expert != 0, true);
 }
 
 }  // extern "C"

@@ -223,7 +223,7 @@ perm_scatter_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, 
                           int32_t* __restrict__ tile_prefix, int32_t* __restrict__ row_of,
                           int32_t* __restrict__ tok_of_row, const uint16_t* __restrict__ Zb,
                           const float* __restrict__ Zp, int S, long long split_stride, int ldz,
-                          int L, uint16_t* __restrict__ A, int* err) {
+                          int L, uint16_t* __restrict__ A, int32_t* __restrict__ active, int* err) {
   pdl_trigger();
   pdl_wait();
   __shared__ uint32_t bm[1024 * kWords];
@@ -255,6 +255,9 @@ perm_scatter_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, 
       counts[e] = c;
       offsets[e] = off;
       tile_prefix[e] = toff;
+      // with tile >= every count an active expert owns exactly one tile, so
+      // its tile offset is its rank among the active experts
+      if (active && c > 0) active[toff] = e;
     }
     if (e == 0) {
       offsets[E] = all;
@@ -525,11 +528,12 @@ cudaError_t launch_permute_scatter_small(const int32_t* ids, int T, int k, int E
                                          int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
                                          int32_t* row_of, int32_t* tok_of_row, const uint16_t* Zb,
                                          const float* Zp, int S, long long split_stride,
-                                         int ldz, int L, uint16_t* A, int* err, cudaStream_t s) {
-  if (T > kBlkTok || E > 1024 || k > 32) return cudaErrorInvalidValue;
+                                         int ldz, int L, uint16_t* A, int32_t* active, int* err,
+                                         cudaStream_t s) {
+  if (T > kBlkTok || E > 1024 || k > 32 || (active && tile < T)) return cudaErrorInvalidValue;
   return launch_k(perm_scatter_small_kernel, dim3(T), dim3(1024), 0, s, ids, T, k, E, tile, counts,
                   offsets, tile_prefix, row_of, tok_of_row, Zb, Zp, S, split_stride, ldz, L, A,
-                  err);
+                  active, err);
 }
 
 cudaError_t launch_scatter_rows(const uint16_t* Zb, const float* Zp, int S, long long split_stride,

@@ -18,12 +18,15 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int tile, vo
                            int32_t* row_of, int32_t* tok_of_row, int* err, cudaStream_t s);
 
 // launch_permute followed by launch_scatter_rows in one launch of T blocks,
-// for T <= 256, E <= 1024, k <= 32 (the small-T path).
+// for T <= 256, E <= 1024, k <= 32 (the small-T path).  active (optional,
+// needs tile >= T): active[i] = the i-th expert with a nonzero count, for
+// i < tile_prefix[E].
 cudaError_t launch_permute_scatter_small(const int32_t* ids, int T, int k, int E, int tile,
                                          int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
                                          int32_t* row_of, int32_t* tok_of_row, const uint16_t* Zb,
                                          const float* Zp, int S, long long split_stride,
-                                         int ldz, int L, uint16_t* A, int* err, cudaStream_t s);
+                                         int ldz, int L, uint16_t* A, int32_t* active, int* err,
+                                         cudaStream_t s);
 
 // A[row_of[t,j]] = Z[t] for j < k; Z from bf16 rows Zb ([T, L]) or from the sum
 // of S fp32 partials Zp (split_stride elements apart, rows ldz >= L elements

@@ -44,7 +44,7 @@ def test_status_strings(lib):
     for st in range(-8, 1):
         assert lib.lmoe_status_string(st)
     assert lib.lmoe_status_string(-99) == b"unknown status"
-    assert lib.lmoe_abi_version() == 102
+    assert lib.lmoe_abi_version() == 103
 
 
 def test_route_validation(lib):
@@ -206,3 +206,49 @@ def test_router_validation(lib):
               None) == -5
     assert lib.latent_moe_launch_count_router(ctypes.byref(d), 1) == \
         lib.latent_moe_launch_count(ctypes.byref(d), 1) + 1
+
+
+def test_mxfp4_validation(lib):
+    # host-side checks of the MXFP4 entry points, all before any device access
+    import dataclasses
+    import workloads as W
+    import latent_mixture_experts_sigmoid_gb300 as lm
+    p = ctypes.c_void_p(256)
+    assert lib.lmoe_dequant_mxfp4(p, p, p, 4, 48, None) == -2             # K % 32
+    assert lib.lmoe_dequant_mxfp4(p, p, p, -1, 64, None) == -2            # rows < 0
+    assert lib.lmoe_dequant_mxfp4(None, p, p, 4, 64, None) == -1
+    assert lib.lmoe_dequant_mxfp4(p, p, ctypes.c_void_p(264), 4, 64, None) == -7
+    assert lib.lmoe_dequant_mxfp4(None, None, None, 0, 64, None) == 0     # empty
+    d = lm.make_dims(W.TINY)
+    nb = lib.latent_moe_workspace_bytes_mxfp4(ctypes.byref(d))
+    assert nb >= lib.latent_moe_workspace_bytes(ctypes.byref(d))
+    # above 128 tokens the workspace also holds every expert dequantized
+    dp = lm.make_dims(dataclasses.replace(W.TINY, T=300))
+    E, L, dI = W.TINY.num_experts, W.TINY.latent, W.TINY.inter
+    assert (lib.latent_moe_workspace_bytes_mxfp4(ctypes.byref(dp)) -
+            lib.latent_moe_workspace_bytes(ctypes.byref(dp))) >= E * 3 * dI * L * 2
+    big = lm.make_dims(dataclasses.replace(W.TINY, inter=8256))
+    assert lib.latent_moe_workspace_bytes_mxfp4(ctypes.byref(big)) == 0   # inter > 8192
+    w = lm.LmoeWeights(256, None, None, None, None, None, 256, None)     # w13 / w2 unused
+    q = lm.LmoeMxfp4Experts(256, 256, 256, 256)
+    fwd = lib.latent_moe_forward_mxfp4
+    assert fwd(ctypes.byref(d), ctypes.byref(w), None, p, p, p, p, nb, None, None) == -1
+    qn = lm.LmoeMxfp4Experts(256, None, 256, 256)
+    assert fwd(ctypes.byref(d), ctypes.byref(w), ctypes.byref(qn), p, p, p, p, nb, None,
+               None) == -1
+    qa = lm.LmoeMxfp4Experts(264, 256, 256, 256)                          # codes misaligned
+    assert fwd(ctypes.byref(d), ctypes.byref(w), ctypes.byref(qa), p, p, p, p, nb, None,
+               None) == -7
+    assert fwd(ctypes.byref(big), ctypes.byref(w), ctypes.byref(q), p, p, p, p, nb, None,
+               None) == -2
+    assert fwd(ctypes.byref(d), ctypes.byref(w), ctypes.byref(q), p, p, p, ctypes.c_void_p(272),
+               nb, None, None) == -5
+    # without a device the pointers cannot be device memory
+    assert fwd(ctypes.byref(d), ctypes.byref(w), ctypes.byref(q), p, p, p, p, nb, None,
+               None) == -8
+    # launches: decode replaces GEMM1 + SituGLU and GEMM2 by one kernel each;
+    # above 128 tokens two dequantization kernels come first
+    n_bf16 = lib.latent_moe_launch_count(ctypes.byref(d), 1)
+    assert lib.latent_moe_launch_count_mxfp4(ctypes.byref(d), 1) == n_bf16
+    assert lib.latent_moe_launch_count_mxfp4(ctypes.byref(dp), 1) == \
+        lib.latent_moe_launch_count(ctypes.byref(dp), 1) + 2

@@ -65,3 +65,31 @@ def test_launch_count_matches_captured_kernels(cuda_ok, T, shared):
     with torch.cuda.graph(g2, stream=s):
         lm.latent_moe_forward_router(d, wdev, wr, x, out, ws, stream=s)
     assert _kernel_nodes(g2) == lm.latent_moe_launch_count_router(d, shared)
+
+
+@pytest.mark.parametrize("T", [8, 300])
+def test_mxfp4_launch_count_matches_captured_kernels(cuda_ok, T):
+    if not hasattr(torch.cuda.CUDAGraph, "raw_cuda_graph"):
+        pytest.skip("this PyTorch does not expose the captured graph")
+    import numpy as np
+    from tests.gpu_util import DEV, weights_to_device, dev_bf16, dev_f32
+    lm.load_library()
+    d = dataclasses.replace(W.TINY, T=T)
+    wdev = weights_to_device(dict(W.layer_weights(d, 1), w13=None, w2=None))
+    qdev = {k: torch.from_numpy(np.ascontiguousarray(v)).to(DEV)
+            for k, v in W.mxfp4_experts(d, 1).items()}
+    x = dev_bf16(W.hidden_states(d, 1))
+    lg = dev_f32(W.router_logits(d.T, d.num_experts, 1))
+    out = torch.empty((T, d.hidden), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(lm.latent_moe_workspace_bytes_mxfp4(d), dtype=torch.uint8, device=DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        lm.latent_moe_forward_mxfp4(d, wdev, qdev, x, lg, out, ws, stream=s)
+    s.synchronize()
+    try:
+        g = torch.cuda.CUDAGraph(keep_graph=True)
+    except TypeError:
+        pytest.skip("this PyTorch cannot keep the captured graph")
+    with torch.cuda.graph(g, stream=s):
+        lm.latent_moe_forward_mxfp4(d, wdev, qdev, x, lg, out, ws, stream=s)
+    assert _kernel_nodes(g) == lm.latent_moe_launch_count_mxfp4(d)
