@@ -9,7 +9,7 @@ down-projection, permutation, grouped expert GEMMs with SituGLU, combine +
 RMSNorm, shared expert, up-projection with the shared add).
 
   python bench.py [--steps K] [--warmup W] [--impl ours|reference]
-  python bench.py --case linear|layer|decode|route|route8|situ [--reps N]
+  python bench.py --case linear|layer|decode|decode_mxfp4|route|route8|situ [--reps N]
 
 Inputs are seeded synthetic tensors (workloads/), resident in HBM before the
 timed region; L2 is flushed between timed steps (a 512 MiB write, then a

@@ -336,9 +336,13 @@ size_t latent_moe_workspace_bytes_mxfp4(const lmoe_dims* dims);
 /* dequantized into the workspace each call and the bf16 tensor-core path    */
 /* runs on them (a caller that runs prefill repeatedly on the same weights   */
 /* can dequantize once with lmoe_dequant_mxfp4 and call latent_moe_forward). */
-/* Limits: those of latent_moe_forward and inter <= 8192.  The four expert   */
-/* pointers are required (LMOE_ERR_NULL), the codes 16-byte aligned          */
-/* (LMOE_ERR_ALIGN), device memory of the current device (LMOE_ERR_DEVICE).  */
+/* Limits: those of latent_moe_forward and latent <= 4096, inter <= 4096.    */
+/* The four expert pointers are required (LMOE_ERR_NULL), codes and scales   */
+/* 16-byte aligned (LMOE_ERR_ALIGN), device memory of the current device     */
+/* (LMOE_ERR_DEVICE).  At T <= 128 the expert inputs enter the 4-bit kernels */
+/* as f16 scaled per token by a power of two (exact for every element within */
+/* 2^30 of the token's largest; smaller ones round to the f16 subnormal grid)*/
+/* and the products are summed in fp32 on the tensor cores.                  */
 /* The workspace layout (latent_moe_workspace_offsets) is the same.          */
 int latent_moe_forward_mxfp4(const lmoe_dims* dims, const lmoe_weights* weights,
                              const lmoe_mxfp4_experts* experts, const lmoe_bf16* hidden,

@@ -532,8 +532,10 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
   // routed experts: bf16 (w13, w2) or MXFP4 (fq)
   if (fq) {
     if (!fq->w13_codes || !fq->w13_scales || !fq->w2_codes || !fq->w2_scales) return LMOE_ERR_NULL;
-    if (d.inter > 8192) return LMOE_ERR_DIM;
-    if (!aligned16(fq->w13_codes) || !aligned16(fq->w2_codes)) return LMOE_ERR_ALIGN;
+    if (d.inter > 4096 || d.latent > 4096) return LMOE_ERR_DIM;
+    if (!aligned16(fq->w13_codes) || !aligned16(fq->w2_codes) || !aligned16(fq->w13_scales) ||
+        !aligned16(fq->w2_scales))
+      return LMOE_ERR_ALIGN;
   } else if (!wt->w13 || !wt->w2) {
     return LMOE_ERR_NULL;
   }
@@ -732,13 +734,15 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
     // MXFP4 at decode sizes: GEMM1 + SituGLU and GEMM2 straight from the 4-bit
     // weights, one block per (active expert, column strip)
     const int slots = (long long)E < rows ? E : (int)rows;
+    int* dev_err = device_error_word();
+    if (!dev_err) return LMOE_ERR_CUDA;
     LMOE_TRY(launch_fp4_expert_gemv(fq->w13_codes, fq->w13_scales, ws.A, ws.act, ws.counts,
-                                    ws.offsets, ws.active, ws.tile_prefix + E, slots, L, dI, 1,
-                                    d.beta, d.linear_beta, s));
+                                    ws.offsets, ws.active, ws.tile_prefix + E, slots, E, L, dI, 1,
+                                    d.beta, d.linear_beta, dev_err, s));
     if (!mark(LMOE_STAGE_GEMM1 + 1) || !mark(LMOE_STAGE_SITU + 1)) return LMOE_ERR_CUDA;
     LMOE_TRY(launch_fp4_expert_gemv(fq->w2_codes, fq->w2_scales, ws.act, ws.Y, ws.counts,
-                                    ws.offsets, ws.active, ws.tile_prefix + E, slots, dI, L, 0,
-                                    d.beta, d.linear_beta, s));
+                                    ws.offsets, ws.active, ws.tile_prefix + E, slots, E, dI, L, 0,
+                                    d.beta, d.linear_beta, dev_err, s));
     if (!mark(LMOE_STAGE_GEMM2 + 1)) return LMOE_ERR_CUDA;
   } else {
     if (fq) {
@@ -889,7 +893,7 @@ int lmoe_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, lmoe_bf16* o
 }
 
 size_t latent_moe_workspace_bytes_mxfp4(const lmoe_dims* dims) {
-  if (validate_dims(dims) != LMOE_OK || dims->inter > 8192) return 0;
+  if (validate_dims(dims) != LMOE_OK || dims->inter > 4096 || dims->latent > 4096) return 0;
   return carve(*dims, nullptr, nullptr, true);
 }
 
@@ -904,7 +908,7 @@ int latent_moe_forward_mxfp4(const lmoe_dims* dims, const lmoe_weights* wt,
 }
 
 int latent_moe_launch_count_mxfp4(const lmoe_dims* dims, int has_shared_expert) {
-  if (validate_dims(dims) != LMOE_OK || dims->inter > 8192) return 0;
+  if (validate_dims(dims) != LMOE_OK || dims->inter > 4096 || dims->latent > 4096) return 0;
   if (dims->T == 0) return 0;
   return plan_launches(make_plan(*dims, num_sms()), has_shared_expert != 0, true);
 }

@@ -21,6 +21,9 @@ constexpr int kErrExpertId = 7;
 // Device address of the error word of the current device.
 int* device_error_word();
 
+// The driver's cuTensorMapEncodeTiled (looked up once), or nullptr.
+void* tensor_map_encoder();
+
 // latent_moe_forward on the library's own static scratch (device memory of
 // the current device, so its pointer is not queried like a caller's).
 int forward_on_library_scratch(const lmoe_dims* dims, const lmoe_weights* wt,

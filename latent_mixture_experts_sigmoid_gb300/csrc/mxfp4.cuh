@@ -11,18 +11,20 @@ namespace lmoe {
 cudaError_t launch_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, uint16_t* out,
                                  long long rows, int K, cudaStream_t s);
 
-// Decode expert stage on MXFP4 weights, one block per (active expert, column
-// strip): out[row, c] for the rows offsets[e] .. offsets[e] + counts[e] - 1
-// of each active expert e (active[0 .. *n_active - 1], slots >= *n_active),
-// from the bf16 input rows x [rows, K].
+// Decode expert stage on MXFP4 weights (a persistent kernel, one block per
+// SM): out[row, c] for the rows offsets[e] .. offsets[e] + counts[e] - 1 of
+// each active expert e (active[0 .. *n_active - 1], slots >= *n_active), from
+// the bf16 input rows x [rows, K].
 //   situ != 0: codes [E, 2 * ncols, K/2]; out = bf16(SituGLU(bf16(x Wg^T),
 //              bf16(x Wu^T))) with Wg rows 0..ncols-1, Wu rows ncols..;
 //   situ == 0: codes [E, ncols, K/2]; out = bf16(x W^T).
-// K % 32 == 0, K <= 8192.
+// E experts; K % 64 == 0, K <= 4096, ncols % 16 == 0, codes and scales
+// 16-byte aligned.  A bounded wait that runs out records 8 in the device error
+// word `err`.
 cudaError_t launch_fp4_expert_gemv(const uint8_t* codes, const uint8_t* scales, const uint16_t* x,
                                    uint16_t* out, const int32_t* counts, const int32_t* offsets,
                                    const int32_t* active, const int32_t* n_active, int slots,
-                                   int K, int ncols, int situ, float beta, float lbeta,
-                                   cudaStream_t s);
+                                   int E, int K, int ncols, int situ, float beta, float lbeta,
+                                   int* err, cudaStream_t s);
 
 }  // namespace lmoe

@@ -227,8 +227,10 @@ def test_mxfp4_validation(lib):
     E, L, dI = W.TINY.num_experts, W.TINY.latent, W.TINY.inter
     assert (lib.latent_moe_workspace_bytes_mxfp4(ctypes.byref(dp)) -
             lib.latent_moe_workspace_bytes(ctypes.byref(dp))) >= E * 3 * dI * L * 2
-    big = lm.make_dims(dataclasses.replace(W.TINY, inter=8256))
-    assert lib.latent_moe_workspace_bytes_mxfp4(ctypes.byref(big)) == 0   # inter > 8192
+    big = lm.make_dims(dataclasses.replace(W.TINY, inter=4160))
+    assert lib.latent_moe_workspace_bytes_mxfp4(ctypes.byref(big)) == 0   # inter > 4096
+    wide = lm.make_dims(dataclasses.replace(W.TINY, latent=4224))
+    assert lib.latent_moe_workspace_bytes_mxfp4(ctypes.byref(wide)) == 0  # latent > 4096
     w = lm.LmoeWeights(256, None, None, None, None, None, 256, None)     # w13 / w2 unused
     q = lm.LmoeMxfp4Experts(256, 256, 256, 256)
     fwd = lib.latent_moe_forward_mxfp4
@@ -238,6 +240,9 @@ def test_mxfp4_validation(lib):
                None) == -1
     qa = lm.LmoeMxfp4Experts(264, 256, 256, 256)                          # codes misaligned
     assert fwd(ctypes.byref(d), ctypes.byref(w), ctypes.byref(qa), p, p, p, p, nb, None,
+               None) == -7
+    qs = lm.LmoeMxfp4Experts(256, 260, 256, 256)                          # scales misaligned
+    assert fwd(ctypes.byref(d), ctypes.byref(w), ctypes.byref(qs), p, p, p, p, nb, None,
                None) == -7
     assert fwd(ctypes.byref(big), ctypes.byref(w), ctypes.byref(q), p, p, p, p, nb, None,
                None) == -2

@@ -157,23 +157,72 @@ def test_mxfp4_tiny_layer_token_counts(T):
 def test_mxfp4_layer_shapes(variant):
     d = W.TINY
     if variant == "ragged":
-        # latent 384 (12 scale blocks: 16-lane rows with 4 idle lanes), inter
-        # 192 (6 blocks: 8-lane rows), 40 experts
+        # latent 384 (192-byte code rows: 64-byte swizzle), inter 192 (96-byte
+        # rows: 32-byte swizzle, 6 scale blocks), 40 experts
         d = dataclasses.replace(d, T=5, hidden=384, latent=384, inter=192, shared_inter=320,
                                 num_experts=40, topk=6)
     elif variant == "crowded":
-        # 128 tokens over 16 experts: ~32 rows an expert, 16 passes of the
-        # staged input over the same register-held codes
+        # 128 tokens over 16 experts: ~32 rows an expert, several passes of up
+        # to 8 tokens over the same strip
         d = dataclasses.replace(d, T=128, num_experts=16, topk=4)
     elif variant == "wide_k1":
-        # GEMM1 over latent 8192: 256 scale blocks a row, 8 a lane
-        d = dataclasses.replace(d, T=4, latent=8192, inter=256, num_experts=4, topk=2)
+        # GEMM1 over latent 4096 (the largest the MXFP4 forward takes): one
+        # token a stage, two stages
+        d = dataclasses.replace(d, T=4, latent=4096, inter=256, num_experts=4, topk=2)
     elif variant == "wide_k2":
-        # GEMM2 over inter 8192 (the largest the MXFP4 forward takes)
-        d = dataclasses.replace(d, T=4, latent=128, inter=8192, num_experts=4, topk=2)
+        # GEMM2 over inter 4096
+        d = dataclasses.replace(d, T=4, latent=128, inter=4096, num_experts=4, topk=2)
     elif variant == "max_experts":
         d = dataclasses.replace(d, T=8, num_experts=1024, topk=32)
     tiny_case(d, seed=7)
+
+
+@pytest.mark.parametrize("log2_scale", [-60, 40])
+def test_mxfp4_decode_input_scale_extremes(log2_scale):
+    # the 4-bit decode kernels scale each token's input rows by a power of two
+    # into the f16 range; hidden states scaled by 2^-60 or 2^40 (exact in
+    # bf16) move the expert inputs far outside it, with the stages still
+    # matching the oracle fed the GPU's own inputs
+    from tests.gpu_util import host_bits, assert_layer_close, addend_scale
+    d = dataclasses.replace(W.TINY, T=6)
+    wts, Q, wdev, qdev = _tiny(d, 9)
+    x = O.f64_to_bf16_bits(O.bf16_to_f64(W.hidden_states(d, 9)) * 2.0 ** log2_scale)
+    lg = W.router_logits(d.T, d.num_experts, 9)
+    out, ws = run_mxfp4(d, wdev, qdev, x, lg, keep_ws=True)
+    ref_bits, mid = O.latent_moe_forward_mxfp4(d, wts, Q, x, lg, intermediates=True)
+    ref = O.bf16_to_f64(ref_bits)
+    got = O.bf16_to_f64(host_bits(out))
+    assert np.isfinite(got).all()
+    assert_layer_close(got, ref, TOL, scale=addend_scale(ref, mid, wts["w_up"]))
+    check_expert_stages(d, lambda n, e: (Q[n + "_q"][e], Q[n + "_s"][e]), list(range(d.T)), ws,
+                        lg, wts["bias"])
+
+
+@pytest.mark.parametrize("T", [8, 300])
+def test_mxfp4_zero_scale_blocks(T):
+    # scale exponent 0 (2^-127: the weights of the block are bf16/fp32
+    # subnormals) on a seeded 5% of the blocks: the 4-bit decode kernels take
+    # their exact scale path for such items, the prefill path dequantizes them
+    # exactly; both against the oracle
+    from tests.gpu_util import host_bits, assert_layer_close, addend_scale
+    d = dataclasses.replace(W.TINY, T=T)
+    wts = W.layer_weights(d, 12)
+    Q = W.mxfp4_experts(d, 12)
+    g = np.random.default_rng(12)
+    for name in ("w13_s", "w2_s"):
+        Q[name] = Q[name].copy()
+        Q[name][g.random(Q[name].shape) < 0.05] = 0
+    from tests.gpu_util import weights_to_device
+    wdev = weights_to_device(dict(wts, w13=None, w2=None))
+    x = W.hidden_states(d, 12)
+    lg = W.router_logits(d.T, d.num_experts, 12)
+    out, ws = run_mxfp4(d, wdev, device_mxfp4(Q), x, lg, keep_ws=True)
+    ref_bits, mid = O.latent_moe_forward_mxfp4(d, wts, Q, x, lg, intermediates=True)
+    ref = O.bf16_to_f64(ref_bits)
+    got = O.bf16_to_f64(host_bits(out))
+    assert_layer_close(got, ref, TOL, scale=addend_scale(ref, mid, wts["w_up"]))
+    check_expert_stages(d, lambda n, e: (Q[n + "_q"][e], Q[n + "_s"][e]), list(range(min(T, 24))),
+                        ws, lg, wts["bias"])
 
 
 def test_mxfp4_prefill_is_the_bf16_forward_on_dequantized_weights():
