@@ -488,7 +488,8 @@ def run_ours(args):
             layer_bytes = sum(v for k2, v in by.items() if k2 not in ("gemm1", "gemm2")) + \
                 eb["gemm1"] + eb["gemm2"]
             res["expert_kernels"] = {
-                "kernel": "fp4_gemv_kernel (GEMM1 + SituGLU, GEMM2 on the 4-bit weights)",
+                "kernel": "fp4_expert_kernel (GEMM1 + SituGLU and GEMM2 on the 4-bit weights: TMA "
+                          "strips, codes widened to f16 in registers, mma.sync m16n8k16)",
                 "bound": "hbm", "us": round(ex_us, 2), "algorithmic_bytes": eb,
                 "achieved": round(gb, 1), "peak": pk["hbm"], "unit": "GB/s",
                 "frac": round(gb / pk["hbm"], 4),
@@ -501,8 +502,8 @@ def run_ours(args):
                        "scale per 32; codes uniform, scale exponents 118..120), every other "
                        "weight bf16 as in the bf16 lines" +
                        (": the expert stages read the 4-bit weights directly" if T <= 128 else
-                        ": every expert dequantized to bf16 in the workspace each call, then "
-                        "the tensor-core GEMMs"))
+                        ": the experts with routed tokens dequantized to bf16 in the workspace "
+                        "each call, then the tensor-core GEMMs"))
         return res
 
     def time_launches(fns, reps):

@@ -332,10 +332,11 @@ size_t latent_moe_workspace_bytes_mxfp4(const lmoe_dims* dims);
 /* weights->w13 and weights->w2 unused (may be NULL) and the experts' GEMMs  */
 /* on `experts` instead.  At T <= 128 (decode) the two expert stages read    */
 /* the 4-bit weights directly (one kernel per stage over the active experts, */
-/* GEMM1's gate/up and SituGLU in one kernel); above, the weights are        */
-/* dequantized into the workspace each call and the bf16 tensor-core path    */
-/* runs on them (a caller that runs prefill repeatedly on the same weights   */
-/* can dequantize once with lmoe_dequant_mxfp4 and call latent_moe_forward). */
+/* GEMM1's gate/up and SituGLU in one kernel); above, the weights of the    */
+/* experts that received tokens are dequantized into the workspace each call */
+/* and the bf16 tensor-core path runs on them (a caller that runs prefill    */
+/* repeatedly on the same weights can dequantize once with                   */
+/* lmoe_dequant_mxfp4 and call latent_moe_forward).                          */
 /* Limits: those of latent_moe_forward and latent <= 4096, inter <= 4096.    */
 /* The four expert pointers are required (LMOE_ERR_NULL), codes and scales   */
 /* 16-byte aligned (LMOE_ERR_ALIGN), device memory of the current device     */

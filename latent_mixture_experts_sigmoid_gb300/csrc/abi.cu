@@ -746,11 +746,13 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
     if (!mark(LMOE_STAGE_GEMM2 + 1)) return LMOE_ERR_CUDA;
   } else {
     if (fq) {
-      // MXFP4 above decode sizes: every expert's weights dequantized to bf16 in
-      // the workspace, then the tensor-core path
+      // MXFP4 above decode sizes: the weights of every expert with routed
+      // tokens dequantized to bf16 in the workspace, then the tensor-core path
+      // (the grouped GEMMs read no rows of the others)
       LMOE_TRY(launch_dequant_mxfp4(fq->w13_codes, fq->w13_scales, ws.Wd13,
-                                    (long long)E * 2 * dI, L, s));
-      LMOE_TRY(launch_dequant_mxfp4(fq->w2_codes, fq->w2_scales, ws.Wd2, (long long)E * L, dI, s));
+                                    (long long)E * 2 * dI, L, s, ws.counts, 2 * dI));
+      LMOE_TRY(launch_dequant_mxfp4(fq->w2_codes, fq->w2_scales, ws.Wd2, (long long)E * L, dI, s,
+                                    ws.counts, L));
       W13 = ws.Wd13;
       W2 = ws.Wd2;
     }

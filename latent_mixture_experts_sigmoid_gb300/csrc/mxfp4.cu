@@ -71,16 +71,19 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
 
 // ---- dequantization: out[r, :] = bf16(w[r, :]) --------------------------------
 // One warp per row at a time; a lane converts 8 codes (one 32-bit word) into 8
-// bf16 values (one 16-byte store) per step.
+// bf16 values (one 16-byte store) per step.  With `counts`, the rows of an
+// expert e (rows_per_expert consecutive rows) are skipped when counts[e] is 0.
 __global__ void __launch_bounds__(256)
 dequant_kernel(const uint32_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-               uint4* __restrict__ out, long long rows, int words_per_row, int nblk) {
+               uint4* __restrict__ out, long long rows, int words_per_row, int nblk,
+               const int32_t* __restrict__ counts, int rows_per_expert) {
   pdl_trigger();
   pdl_wait();   // out may still be read by the previous forward's GEMMs
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   const int lane = threadIdx.x & 31;
   for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
        r += warps) {
+    if (counts && counts[r / rows_per_expert] == 0) continue;   // (warp-uniform)
     const uint32_t* cr = codes + r * words_per_row;
     const uint8_t* sr = scales + r * nblk;
     uint4* orow = out + r * words_per_row;
@@ -742,7 +745,8 @@ cudaError_t launch_expert_kernel(GemvArgs& a, int slots, int E, cudaStream_t s) 
 }  // namespace
 
 cudaError_t launch_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, uint16_t* out,
-                                 long long rows, int K, cudaStream_t s) {
+                                 long long rows, int K, cudaStream_t s, const int32_t* counts,
+                                 int rows_per_expert) {
   if (rows <= 0) return cudaSuccess;
   const long long warps = rows < (1ll << 20) ? rows : (1ll << 20);
   long long blocks = (warps + 7) / 8;
@@ -750,7 +754,7 @@ cudaError_t launch_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, ui
   if (blocks > cap) blocks = cap;
   return launch_k(dequant_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
                   reinterpret_cast<const uint32_t*>(codes), scales, reinterpret_cast<uint4*>(out),
-                  rows, K / 8, K / 32);
+                  rows, K / 8, K / 32, counts, rows_per_expert > 0 ? rows_per_expert : 1);
 }
 
 cudaError_t launch_fp4_expert_gemv(const uint8_t* codes, const uint8_t* scales, const uint16_t* x,

@@ -8,8 +8,11 @@ namespace lmoe {
 
 // out [rows, K] bf16 = E2M1(codes) * 2^(scales - 127), rounded to bf16.
 // codes [rows, K/2] (16-byte aligned), scales [rows, K/32]; K % 32 == 0.
+// With counts: the rows_per_expert rows of expert e are left untouched when
+// counts[e] == 0 (experts no token was routed to).
 cudaError_t launch_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, uint16_t* out,
-                                 long long rows, int K, cudaStream_t s);
+                                 long long rows, int K, cudaStream_t s,
+                                 const int32_t* counts = nullptr, int rows_per_expert = 0);
 
 // Decode expert stage on MXFP4 weights (a persistent kernel, one block per
 // SM): out[row, c] for the rows offsets[e] .. offsets[e] + counts[e] - 1 of
