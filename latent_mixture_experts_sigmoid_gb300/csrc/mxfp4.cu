@@ -215,6 +215,9 @@ __device__ __noinline__ bool bar_wait_slow(uint32_t bar, uint32_t parity, volati
   }
   return true;
 }
+// Warps that go on to warp-synchronous instructions (shuffles, mma.sync) take
+// the outcome for the whole warp (__all_sync): a wait that runs out in one lane
+// then never leaves the other lanes at a collective the first one skipped.
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          int* err) {
   return bar_try(bar, parity) || bar_wait_slow(bar, parity, abort_flag, err);
@@ -562,7 +565,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     while (live0 || live1) {
       if (turn ? !live1 : !live0) { turn = !turn; continue; }
       const int s = turn ? cw + kConverterWarps : cw;
-      if (!bar_wait(smem_addr(full + s), turn ? ph1 : ph0, abort_flag, a.err)) break;
+      if (!__all_sync(0xffffffffu, bar_wait(smem_addr(full + s), turn ? ph1 : ph0, abort_flag, a.err)))
+        break;
       StageHdr& h = hdr[s];
       const int e = h.e;
       if (e >= 0) {
@@ -626,7 +630,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   float* part = reinterpret_cast<float*>(ring + (size_t)s * a.stage_bytes + a.part_off);
   const int jb_mid = nblk / 2;
   while (true) {
-    if (!bar_wait(smem_addr(ready + s), ph, abort_flag, a.err)) break;
+    if (!__all_sync(0xffffffffu, bar_wait(smem_addr(ready + s), ph, abort_flag, a.err))) break;
     const StageHdr& h = hdr[s];
     if (h.e < 0) break;
     float acc[kTiles][4];
@@ -640,7 +644,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       if (lane == 0) bar_arrive(smem_addr(half_done + s));
     } else {
       accumulate_blocks<kRows, kTiles>(a, st, h, lane, 0, jb_mid, acc);
-      if (!bar_wait(smem_addr(half_done + s), ph, abort_flag, a.err)) break;
+      if (!__all_sync(0xffffffffu, bar_wait(smem_addr(half_done + s), ph, abort_flag, a.err))) break;
       // the two halves in a fixed order: the first half's blocks, then the second's
 #pragma unroll
       for (int t = 0; t < kTiles; ++t)

@@ -212,8 +212,9 @@ __device__ __forceinline__ unsigned long long lane_best_exact(const float* __res
 // Rows are staged in shared memory by cp.async in a ring of NSLOT rows per
 // warp, so that NSLOT - 1 rows are in flight while one is processed (a warp
 // handles only a few tokens, and one row in flight per warp leaves the copy
-// latency exposed); padding slots hold NaN, which neither a maximum nor a
-// candidate test picks up.  Lane l owns the
+// latency exposed); padding slots hold the logit 0 and the bias -inf, so their
+// cheap key is -inf, below every threshold (the threshold is clamped to a
+// finite value).  Lane l owns the
 // experts e = 128*c + 4*l + j (chunk c < C, j < 4): one 16-byte copy and one
 // 16-byte shared load per chunk when E is a multiple of 4.
 //
@@ -302,6 +303,25 @@ __device__ __forceinline__ void warp_sort64(float& v0, float& v1, int lane) {
   }
 }
 
+// The 16th largest of one value per lane: each half of the warp sorted (the
+// lower ascending, the upper descending, the first four stages of the 32-wide
+// network), the larger of each cross pair kept in the upper half (these are the
+// 16 largest), and their minimum.
+__device__ __forceinline__ float warp_kth16(float v, uint32_t dirs, int lane) {
+  int s = 0;
+#pragma unroll
+  for (int size = 2; size <= 16; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1, ++s) {
+      const float p = __shfl_xor_sync(FULL, v, stride);
+      v = ((dirs >> s) & 1u) ? fminf(v, p) : fmaxf(v, p);
+    }
+  }
+  const float p = __shfl_xor_sync(FULL, v, 16);
+  const uint32_t o = __reduce_max_sync(FULL, (lane & 16) ? ~orderable(fmaxf(v, p)) : 0u);
+  return from_orderable(~o);
+}
+
 __device__ __forceinline__ float candidate_threshold2(float a2) {
   return a2 - (0x1p-8f + 0x1p-20f * fmaxf(fabsf(a2), 1.0f));
 }
@@ -366,14 +386,13 @@ route_warp_kernel(const float* __restrict__ logits, long long ld, const float* _
   __shared__ __align__(16) uint32_t skey[kWarpsPerBlock][32];
   pdl_trigger();
   if (E < EW) {
-    // padding slots (never written by the copies) read as NaN
-    const float4 qnan4 = make_float4(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000),
-                                     __int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+    // padding slots (never written by the copies) hold 0
     for (int i = threadIdx.x; i < kWarpsPerBlock * NSLOT * EW / 4; i += blockDim.x)
-      reinterpret_cast<float4*>(srow_all)[i] = qnan4;
+      reinterpret_cast<float4*>(srow_all)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   }
   // the bias is a model parameter: read while the preceding kernel drains
-  for (int e = threadIdx.x; e < EW; e += blockDim.x) sbias[e] = (bias && e < E) ? __ldg(bias + e) : 0.0f;
+  for (int e = threadIdx.x; e < EW; e += blockDim.x)
+    sbias[e] = e < E ? (bias ? __ldg(bias + e) : 0.0f) : -INFINITY;
   pdl_wait();
   __syncthreads();
   const int lane = threadIdx.x & 31;
@@ -394,8 +413,9 @@ route_warp_kernel(const float* __restrict__ logits, long long ld, const float* _
     const float* row = ring + slot * EW;
     if (++slot == NSLOT) slot = 0;
     if (++fill == NSLOT) fill = 0;
-    // pass A: doubled cheap keys, two group maxima per lane
-    float ka[4 * C];
+    // pass A: doubled cheap keys as pairs (elements 4c, 4c+1 | 4c+2, 4c+3), two
+    // group maxima per lane
+    f32x2 kp[2 * C];
     float g0 = -INFINITY, g1 = -INFINITY;
 #pragma unroll
     for (int c = 0; c < C; ++c) {
@@ -404,35 +424,49 @@ route_warp_kernel(const float* __restrict__ logits, long long ld, const float* _
       const float4 b = *reinterpret_cast<const float4*>(sbias + e0);
       const f32x2 h01 = f2_mul(f2_make(__float_as_uint(x.x), __float_as_uint(x.y)), half2);
       const f32x2 h23 = f2_mul(f2_make(__float_as_uint(x.z), __float_as_uint(x.w)), half2);
-      const f32x2 k01 = f2_fma(f2_make(__float_as_uint(b.x), __float_as_uint(b.y)), two2,
-                               f2_make(__float_as_uint(tanh_fast(f2_lo(h01))),
-                                       __float_as_uint(tanh_fast(f2_hi(h01)))));
-      const f32x2 k23 = f2_fma(f2_make(__float_as_uint(b.z), __float_as_uint(b.w)), two2,
-                               f2_make(__float_as_uint(tanh_fast(f2_lo(h23))),
-                                       __float_as_uint(tanh_fast(f2_hi(h23)))));
-      ka[4 * c] = f2_lo(k01); ka[4 * c + 1] = f2_hi(k01);
-      ka[4 * c + 2] = f2_lo(k23); ka[4 * c + 3] = f2_hi(k23);
-      g0 = fmaxf(g0, fmaxf(ka[4 * c], ka[4 * c + 1]));
-      g1 = fmaxf(g1, fmaxf(ka[4 * c + 2], ka[4 * c + 3]));
+      kp[2 * c] = f2_fma(f2_make(__float_as_uint(b.x), __float_as_uint(b.y)), two2,
+                         f2_make(__float_as_uint(tanh_fast(f2_lo(h01))),
+                                 __float_as_uint(tanh_fast(f2_hi(h01)))));
+      kp[2 * c + 1] = f2_fma(f2_make(__float_as_uint(b.z), __float_as_uint(b.w)), two2,
+                             f2_make(__float_as_uint(tanh_fast(f2_lo(h23))),
+                                     __float_as_uint(tanh_fast(f2_hi(h23)))));
+      g0 = fmaxf(g0, fmaxf(f2_lo(kp[2 * c]), f2_hi(kp[2 * c])));
+      g1 = fmaxf(g1, fmaxf(f2_lo(kp[2 * c + 1]), f2_hi(kp[2 * c + 1])));
     }
-    float thr = candidate_threshold2(__shfl_sync(FULL, warp_sort32(fmaxf(g0, g1), dirs), 32 - k));
-    uint32_t cmask = 0;
+    const float gm = fmaxf(g0, g1);
+    float thr = candidate_threshold2(k == 16 ? warp_kth16(gm, dirs, lane)
+                                             : __shfl_sync(FULL, warp_sort32(gm, dirs), 32 - k));
+    thr = fmaxf(thr, -0x1p127f);   // finite: padding keys (-inf) stay below it
+    // candidate bits: the sign of (key - thr) of every element, shifted in from
+    // the last element down, so that bit i ends up clear for a candidate
+    uint32_t below = 0u;
+    {
+      const f32x2 nthr = f2_splat(-thr);
 #pragma unroll
-    for (int i = 0; i < 4 * C; ++i)
-      if (ka[i] >= thr) cmask |= 1u << i;
+      for (int j = 2 * C - 1; j >= 0; --j) {
+        const f32x2 d = f2_add(kp[j], nthr);
+        below = __funnelshift_l((uint32_t)(d >> 32), below, 1);
+        below = __funnelshift_l((uint32_t)d, below, 1);
+      }
+    }
+    uint32_t cmask = ~below & (4 * C >= 32 ? 0xFFFFFFFFu : (1u << (4 * C)) - 1u);
     int total = (int)__reduce_add_sync(FULL, (uint32_t)__popc(cmask));
     if (total > 32) {
       // refine the bound with the 64 group maxima
       warp_sort64(g0, g1, lane);
       const int kpos = 64 - k;
-      thr = candidate_threshold2(__shfl_sync(FULL, (kpos & 1) ? g1 : g0, kpos >> 1));
+      thr = fmaxf(candidate_threshold2(__shfl_sync(FULL, (kpos & 1) ? g1 : g0, kpos >> 1)),
+                  -0x1p127f);
       cmask = 0;
 #pragma unroll
-      for (int i = 0; i < 4 * C; ++i)
-        if (ka[i] >= thr) cmask |= 1u << i;
+      for (int i = 0; i < 4 * C; ++i) {
+        const float v = (i & 1) ? f2_hi(kp[i >> 1]) : f2_lo(kp[i >> 1]);
+        if (v >= thr) cmask |= 1u << i;
+      }
       total = (int)__reduce_add_sync(FULL, (uint32_t)__popc(cmask));
     }
-    if (total <= 32) {
+    // fewer than k candidates only where keys overflow to -inf: the exact fallback
+    if (total <= 32 && total >= k) {
       const int ccount = __popc(cmask);
       int incl = ccount;
 #pragma unroll

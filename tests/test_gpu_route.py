@@ -69,8 +69,8 @@ def test_route_shapes(E, k):
 @pytest.mark.parametrize("E,k,renorm", [(600, 16, 1), (1001, 16, 1), (896, 8, 0), (130, 32, 1),
                                          (257, 3, 1)])
 def test_route_warp_kernel_shapes(E, k, renorm):
-    # T > 512: the warp-per-token kernel.  E = 600 leaves padded chunks (NaN
-    # slots), E = 1001 and 257 are not multiples of 4 (4-byte row copies),
+    # T > 512: the warp-per-token kernel.  E = 600 leaves padded chunks (slots
+    # with the logit 0 and the bias -inf), E = 1001 and 257 are not multiples of 4 (4-byte row copies),
     # k = 32 fills the candidate window, renorm = 0 keeps the raw scores
     T = 700
     g = np.random.default_rng(E * 7 + k)
@@ -78,6 +78,20 @@ def test_route_warp_kernel_shapes(E, k, renorm):
     logits[::64] = logits[::64, :1]          # every 64th row tied
     bias = (g.standard_normal(E) * 0.1).astype(np.float32)
     check(logits, bias, k, 2.5, renorm=renorm)
+
+
+@pytest.mark.parametrize("T,E,k", [(700, 20, 16), (700, 40, 16), (97, 300, 16), (700, 300, 32)])
+def test_route_extreme_bias(T, E, k):
+    # biases of +-3e38: doubled cheap keys overflow to +-inf (threshold clamped
+    # finite, fewer than k candidates -> the exact selection), tied exact keys
+    # of 3e38 (the lower index first); E = 20 with k = 16 leaves fewer than k
+    # lanes with an expert, so the k-th lane maximum is -inf
+    g = np.random.default_rng(T + E + k)
+    logits = g.standard_normal((T, E)).astype(np.float32)
+    bias = (g.standard_normal(E) * 0.1).astype(np.float32)
+    bias[::7] = -3e38
+    bias[3::11] = 3e38
+    check(logits, bias, k, 2.5)
 
 
 def test_route_sigmoid_bit_exact():
