@@ -70,31 +70,54 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
 }
 
 // ---- dequantization: out[r, :] = bf16(w[r, :]) --------------------------------
-// One warp per row at a time; a lane converts 8 codes (one 32-bit word) into 8
-// bf16 values (one 16-byte store) per step.  With `counts`, the rows of an
-// expert e (rows_per_expert consecutive rows) are skipped when counts[e] is 0.
+// The codes and the output are one flat sequence of words: word q is 8 codes
+// (4 bytes, element 0 in the low nibble) and 8 bf16 outputs (16 bytes), with
+// the scale byte scales[q / 4] (rows are whole 32-element blocks).  A warp
+// takes a unit of up to kDqUnitWords consecutive words of one group (the rows
+// of one expert, or everything); its lanes take words lane, lane + 32, ..., with
+// kDqInFlight of them loaded before any is converted, so that a warp's loads
+// are 128-byte lines and its stores 512-byte runs.  With `counts`, the units
+// of a group g with counts[g] == 0 (an expert no token was routed to) are
+// skipped as a whole.
+constexpr int kDqUnitWords = 1024;
+constexpr int kDqInFlight = 8;
+
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, uint32_t s) {
+  const float sc = e8m0_to_f32(s);
+  float v[8];
+  e2m1x8_to_f32(w, v);
+  return make_uint4(pack_bf16x2(v[0] * sc, v[1] * sc), pack_bf16x2(v[2] * sc, v[3] * sc),
+                    pack_bf16x2(v[4] * sc, v[5] * sc), pack_bf16x2(v[6] * sc, v[7] * sc));
+}
+
 __global__ void __launch_bounds__(256)
 dequant_kernel(const uint32_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-               uint4* __restrict__ out, long long rows, int words_per_row, int nblk,
-               const int32_t* __restrict__ counts, int rows_per_expert) {
+               uint4* __restrict__ out, long long words, long long words_per_group,
+               const int32_t* __restrict__ counts) {
   pdl_trigger();
   pdl_wait();   // out may still be read by the previous forward's GEMMs
-  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  const long long units_per_group = (words_per_group + kDqUnitWords - 1) / kDqUnitWords;
+  const long long units = (words + words_per_group - 1) / words_per_group * units_per_group;
+  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
   const int lane = threadIdx.x & 31;
-  for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
-       r += warps) {
-    if (counts && counts[r / rows_per_expert] == 0) continue;   // (warp-uniform)
-    const uint32_t* cr = codes + r * words_per_row;
-    const uint8_t* sr = scales + r * nblk;
-    uint4* orow = out + r * words_per_row;
-#pragma unroll 4
-    for (int g = lane; g < words_per_row; g += 32) {
-      const float sc = e8m0_to_f32(__ldg(sr + (g >> 2)));
-      float v[8];
-      e2m1x8_to_f32(__ldg(cr + g), v);
-      orow[g] = make_uint4(pack_bf16x2(v[0] * sc, v[1] * sc), pack_bf16x2(v[2] * sc, v[3] * sc),
-                           pack_bf16x2(v[4] * sc, v[5] * sc), pack_bf16x2(v[6] * sc, v[7] * sc));
+  for (long long u = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units;
+       u += nwarps) {
+    const long long g = u / units_per_group;
+    if (counts && counts[g] == 0) continue;   // (warp-uniform)
+    const long long q0 = g * words_per_group + (u - g * units_per_group) * kDqUnitWords;
+    const long long q1 = min(q0 + kDqUnitWords, min((g + 1) * words_per_group, words));
+    long long q = q0 + lane;
+    for (; q + 32 * (kDqInFlight - 1) < q1; q += 32 * kDqInFlight) {
+      uint32_t w[kDqInFlight], sv[kDqInFlight];
+#pragma unroll
+      for (int i = 0; i < kDqInFlight; ++i) {
+        w[i] = __ldg(codes + q + 32 * i);
+        sv[i] = __ldg(scales + ((q + 32 * i) >> 2));
+      }
+#pragma unroll
+      for (int i = 0; i < kDqInFlight; ++i) out[q + 32 * i] = dequant_word(w[i], sv[i]);
     }
+    for (; q < q1; q += 32) out[q] = dequant_word(__ldg(codes + q), __ldg(scales + (q >> 2)));
   }
 }
 
@@ -752,13 +775,18 @@ cudaError_t launch_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, ui
                                  long long rows, int K, cudaStream_t s, const int32_t* counts,
                                  int rows_per_expert) {
   if (rows <= 0) return cudaSuccess;
-  const long long warps = rows < (1ll << 20) ? rows : (1ll << 20);
-  long long blocks = (warps + 7) / 8;
+  const long long words_per_row = K / 8;
+  const long long words = rows * words_per_row;
+  const long long per_group =
+      counts ? (long long)(rows_per_expert > 0 ? rows_per_expert : 1) * words_per_row : words;
+  const long long units =
+      (words + per_group - 1) / per_group * ((per_group + kDqUnitWords - 1) / kDqUnitWords);
+  long long grid = (units + 7) / 8;
   const long long cap = (long long)num_sms() * 8;
-  if (blocks > cap) blocks = cap;
-  return launch_k(dequant_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
+  if (grid > cap) grid = cap;
+  return launch_k(dequant_kernel, dim3((unsigned)grid), dim3(256), 0, s,
                   reinterpret_cast<const uint32_t*>(codes), scales, reinterpret_cast<uint4*>(out),
-                  rows, K / 8, K / 32, counts, rows_per_expert > 0 ? rows_per_expert : 1);
+                  words, per_group, counts);
 }
 
 cudaError_t launch_fp4_expert_gemv(const uint8_t* codes, const uint8_t* scales, const uint16_t* x,

@@ -50,7 +50,8 @@ def _dequant_gpu(packed, scales):
     return host_bits(out)
 
 
-@pytest.mark.parametrize("rows,K", [(1, 32), (37, 96), (1000, 2048), (4096, 512)])
+@pytest.mark.parametrize("rows,K", [(1, 32), (37, 96), (1000, 2048), (4096, 512),
+                                    (3, 32 * 700), (5, 32 * 1031)])
 def test_dequant_bit_exact(rows, K):
     g = np.random.default_rng(rows + K)
     packed = g.integers(0, 256, size=(rows, K // 2), dtype=np.uint8)
