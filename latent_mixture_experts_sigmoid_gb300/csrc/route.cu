@@ -234,7 +234,9 @@ __device__ __forceinline__ unsigned long long lane_best_exact(const float* __res
 // across the warp); in the rare case that leaves more than 32 candidates it is
 // refined to the k-th largest of 64 group maxima (j < 2 and j >= 2 of every
 // lane), and only then does the exact fallback run.
-constexpr int kWarpsPerBlock = 4;
+// Seven warps a block and four blocks an SM: 28 resident warps, the most that
+// the two-row rings (7 KB a warp) and 72 registers a thread allow together.
+constexpr int kWarpsPerBlock = 7;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -367,7 +369,7 @@ __device__ __forceinline__ void stage_row(float* dst, const float* __restrict__ 
 
 // ring depth and the blocks per SM the register budget is sized for
 constexpr int kRouteSlots = 2;
-constexpr int kRouteMinBlocks = 6;
+constexpr int kRouteMinBlocks = 4;   // (three for 8 chunks: their rings take 8 KB a warp)
 
 template <int C, int NSLOT>
 constexpr size_t warp_kernel_smem() {
@@ -375,7 +377,7 @@ constexpr size_t warp_kernel_smem() {
 }
 
 template <int C, bool VEC, int NSLOT>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32, kRouteMinBlocks)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, C >= 8 ? 3 : kRouteMinBlocks)
 route_warp_kernel(const float* __restrict__ logits, long long ld, const float* __restrict__ bias,
                   int T, int E, int k, int renorm, float rsf, int32_t* __restrict__ ids,
                   float* __restrict__ weights) {
