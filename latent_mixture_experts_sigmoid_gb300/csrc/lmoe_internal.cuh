@@ -21,7 +21,7 @@ constexpr int kErrExpertId = 7;
 // Device address of the error word of the current device.
 int* device_error_word();
 
-// The driver's cuTensorMapEncodeTiled (looked up once), or nullptr.
+// The CUDA driver API's cuTensorMapEncodeTiled (looked up once), or nullptr.
 void* tensor_map_encoder();
 
 // latent_moe_forward on the library's own static scratch (device memory of
