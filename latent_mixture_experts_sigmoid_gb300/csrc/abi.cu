@@ -666,7 +666,25 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
   };
   int st = LMOE_OK;
   const bool side_route = concurrent && !decode;
-  if (concurrent) {
+  // At decode sizes with bf16 experts the shared expert forks off after the
+  // routed GEMM1: from the start it held SMs that GEMM1's persistent CTAs then
+  // reached late (its CTAs finished up to 26 us apart); after GEMM1 it runs
+  // beside GEMM2, the combine and the up-projection (182.5-182.8 against
+  // 186.9 us per decode step).  The MXFP4 expert kernels keep the early fork
+  // (138.9 against 145.7 us): their blocks take an SM's shared memory, so
+  // nothing of the shared expert runs beside them and the early stages are
+  // where it fits.
+  const bool late_shared = concurrent && decode && fq == nullptr;
+  auto fork_shared_late = [&]() -> int {
+    if (!late_shared) return LMOE_OK;
+    if (cudaEventRecord(aux->fork, s) != cudaSuccess) return LMOE_ERR_CUDA;
+    if (cudaStreamWaitEvent(aux->stream, aux->fork, 0) != cudaSuccess) return LMOE_ERR_CUDA;
+    const int r = shared_expert(aux->stream, false);
+    if (r != LMOE_OK) return r;
+    if (cudaEventRecord(aux->join, aux->stream) != cudaSuccess) return LMOE_ERR_CUDA;
+    return LMOE_OK;
+  };
+  if (concurrent && !late_shared) {
     if (cudaStreamWaitEvent(aux->stream, aux->fork, 0) != cudaSuccess) return LMOE_ERR_CUDA;
     if (side_route) {
       st = route_and_permute(aux->stream, false);
@@ -767,6 +785,8 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
       LMOE_TRY(launch_situ(ws.G, ws.act, rows, dI, d.beta, d.linear_beta, s));
     }
     if (!mark(LMOE_STAGE_SITU + 1)) return LMOE_ERR_CUDA;
+    st = fork_shared_late();
+    if (st != LMOE_OK) return st;
     LMOE_TRY(gemm_grouped(W2, E, L, ws.act, rows, dI, !decode, pl.g2_bn, ws, tile, ws.Y, s));
     if (!mark(LMOE_STAGE_GEMM2 + 1)) return LMOE_ERR_CUDA;
   }
