@@ -666,15 +666,15 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
   };
   int st = LMOE_OK;
   const bool side_route = concurrent && !decode;
-  // At decode sizes with bf16 experts the shared expert forks off after the
-  // routed GEMM1: from the start it held SMs that GEMM1's persistent CTAs then
-  // reached late (its CTAs finished up to 26 us apart); after GEMM1 it runs
-  // beside GEMM2, the combine and the up-projection (182.5-182.8 against
-  // 186.9 us per decode step).  The MXFP4 expert kernels keep the early fork
-  // (138.9 against 145.7 us): their blocks take an SM's shared memory, so
-  // nothing of the shared expert runs beside them and the early stages are
-  // where it fits.
-  const bool late_shared = concurrent && decode && fq == nullptr;
+  // At decode sizes the shared expert forks off late.  With bf16 experts after
+  // the routed GEMM1: from the start it held SMs that GEMM1's persistent CTAs
+  // then reached late (its CTAs finished up to 26 us apart); after GEMM1 it
+  // runs beside GEMM2, the combine and the up-projection (182.5-182.8 against
+  // 186.9 us per decode step).  With MXFP4 experts after the scatter, ahead of
+  // the expert kernels (151.7 against 154.7 us in graph replays after an L2
+  // flush; after GEMM1 it was slower: their blocks take an SM's shared memory,
+  // so nothing of the shared expert runs beside them).
+  const bool late_shared = concurrent && decode;
   auto fork_shared_late = [&]() -> int {
     if (!late_shared) return LMOE_OK;
     if (cudaEventRecord(aux->fork, s) != cudaSuccess) return LMOE_ERR_CUDA;
@@ -745,6 +745,10 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
     LMOE_TRY(launch_scatter_rows(down_split ? nullptr : ws.Z, down_split ? ws.Pa : nullptr,
                                  cdown.splits, down_stride, ldz, T, L, k, ws.row_of, ws.A, s));
   if (!mark(LMOE_STAGE_SCATTER + 1)) return LMOE_ERR_CUDA;
+  if (fq && decode) {
+    st = fork_shared_late();
+    if (st != LMOE_OK) return st;
+  }
   // 5-7. experts
   const uint16_t* W13 = wt->w13;
   const uint16_t* W2 = wt->w2;
