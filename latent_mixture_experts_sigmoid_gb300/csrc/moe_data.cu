@@ -210,6 +210,34 @@ perm_rows_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
   }
 }
 
+// acc[0..7] += the 8 floats at P + s * stride + off for s = 0 .. S-1, added in
+// ascending s; the loads of four splits are issued before any of their sums,
+// so that a row of split partials costs about S/4 load latencies, not S.
+__device__ __forceinline__ void sum8_splits(const float* __restrict__ P, int S, long long stride,
+                                            long long off, float (&acc)[8]) {
+  int s = 0;
+  for (; s + 4 <= S; s += 4) {
+    float4 a[4], c[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float4* p = reinterpret_cast<const float4*>(P + (s + b) * stride + off);
+      a[b] = __ldg(p);
+      c[b] = __ldg(p + 1);
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      acc[0] += a[b].x; acc[1] += a[b].y; acc[2] += a[b].z; acc[3] += a[b].w;
+      acc[4] += c[b].x; acc[5] += c[b].y; acc[6] += c[b].z; acc[7] += c[b].w;
+    }
+  }
+  for (; s < S; ++s) {
+    const float4* p = reinterpret_cast<const float4*>(P + s * stride + off);
+    const float4 a = __ldg(p), c = __ldg(p + 1);
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += c.x; acc[5] += c.y; acc[6] += c.z; acc[7] += c.w;
+  }
+}
+
 // ---- permutation and scatter in one kernel, for small T (decode) -------------
 // T blocks of 1024 threads (T <= 256, E <= 1024).  Every block rebuilds the
 // whole counting sort of the T*k (token, slot) pairs in shared memory (bitmaps,
@@ -283,13 +311,7 @@ perm_scatter_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, 
     uint4 o;
     if (Zp) {
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int sp = 0; sp < S; ++sp) {
-        const float4* p = reinterpret_cast<const float4*>(Zp + sp * split_stride +
-                                                          (long long)t * ldz + v * 8);
-        const float4 a = __ldg(p), b = __ldg(p + 1);
-        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-      }
+      sum8_splits(Zp, S, split_stride, (long long)t * ldz + v * 8, acc);
       o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
                      pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
     } else {
@@ -314,13 +336,7 @@ scatter_rows_kernel(const uint16_t* __restrict__ Zb, const float* __restrict__ Z
     uint4 o;
     if (Zp) {
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int s = 0; s < S; ++s) {
-        const float4* p = reinterpret_cast<const float4*>(Zp + s * split_stride +
-                                                          (long long)t * ldz + v * 8);
-        const float4 a = __ldg(p), c = __ldg(p + 1);
-        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-        acc[4] += c.x; acc[5] += c.y; acc[6] += c.z; acc[7] += c.w;
-      }
+      sum8_splits(Zp, S, split_stride, (long long)t * ldz + v * 8, acc);
       o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
                      pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
     } else {
@@ -420,20 +436,10 @@ reduce_splits_kernel(const float* __restrict__ P, int S, long long sstride,
   for (long long v = blockIdx.x * (long long)blockDim.x + threadIdx.x; v < n8;
        v += (long long)gridDim.x * blockDim.x) {
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int s = 0; s < S; ++s) {
-      const float4* p = reinterpret_cast<const float4*>(P + s * sstride) + 2 * v;
-      const float4 a = __ldg(p), c = __ldg(p + 1);
-      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-      acc[4] += c.x; acc[5] += c.y; acc[6] += c.z; acc[7] += c.w;
-    }
+    sum8_splits(P, S, sstride, 8 * v, acc);
     if (Q) {
       float qa[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int s = 0; s < S2; ++s) {
-        const float4* p = reinterpret_cast<const float4*>(Q + s * qstride) + 2 * v;
-        const float4 a = __ldg(p), c = __ldg(p + 1);
-        qa[0] += a.x; qa[1] += a.y; qa[2] += a.z; qa[3] += a.w;
-        qa[4] += c.x; qa[5] += c.y; qa[6] += c.z; qa[7] += c.w;
-      }
+      sum8_splits(Q, S2, qstride, 8 * v, qa);
 #pragma unroll
       for (int i = 0; i < 8; i += 2) {
         const uint32_t b2 = pack_bf16x2(qa[i], qa[i + 1]);   // the bf16 shared output
@@ -465,17 +471,8 @@ reduce_situ_kernel(const float* __restrict__ P, int S, long long sstride, int T,
     const long long t = v / (d / 8);
     const int c = (int)(v - t * (d / 8)) * 8;
     float g[8] = {0, 0, 0, 0, 0, 0, 0, 0}, u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int s = 0; s < S; ++s) {
-      const float* base = P + s * sstride + t * (2LL * d) + c;
-      const float4 g0 = __ldg(reinterpret_cast<const float4*>(base));
-      const float4 g1 = __ldg(reinterpret_cast<const float4*>(base) + 1);
-      const float4 u0 = __ldg(reinterpret_cast<const float4*>(base + d));
-      const float4 u1 = __ldg(reinterpret_cast<const float4*>(base + d) + 1);
-      g[0] += g0.x; g[1] += g0.y; g[2] += g0.z; g[3] += g0.w;
-      g[4] += g1.x; g[5] += g1.y; g[6] += g1.z; g[7] += g1.w;
-      u[0] += u0.x; u[1] += u0.y; u[2] += u0.z; u[3] += u0.w;
-      u[4] += u1.x; u[5] += u1.y; u[6] += u1.z; u[7] += u1.w;
-    }
+    sum8_splits(P, S, sstride, t * (2LL * d) + c, g);
+    sum8_splits(P, S, sstride, t * (2LL * d) + c + d, u);
     uint32_t pk[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
