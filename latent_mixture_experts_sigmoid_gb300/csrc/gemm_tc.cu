@@ -395,9 +395,8 @@ __host__ __device__ __forceinline__ Unit decode_unit(const GemmParams& p, const 
 //               features, each multiplied into its own accumulator, so that
 //               the epilogue applies SituGLU (p.fuse_situ is set).  Each half
 //               has an MMA issuer of its own (warp 1: gate, warp 6: up): with
-//               16 tokens on N an MMA is cheap to execute but not to issue,
-//               and one thread issuing both halves' MMAs held every stage
-//               (182.8 against 176.6-178.7 us per decode step, bit-identical);
+//               16 tokens on N an MMA is cheap to execute but not to issue
+//               (about 1 us per decode step, bit-identical);
 //   kFormStack  weights on M; weight rows from p.w2_row0 on come from a second
 //               matrix (its own tensor map), stacked after the first.
 enum : int { kFormRegular = 0, kFormSwap = 1, kFormStack = 2 };
