@@ -304,6 +304,35 @@ def test_graph_replay_and_determinism():
     assert torch.equal(a.view(torch.int16), c.view(torch.int16))
 
 
+@pytest.mark.parametrize("T", [1, 128])
+def test_decode_layer_graph_replays_are_bit_identical(big_weights, T):
+    # the 896-expert layer at decode sizes (GEMM1 + SituGLU with its two MMA
+    # issuers at 16 and 128 token columns, the shared expert forked onto the
+    # second stream after GEMM1): 20 graph replays, each bit-identical to the
+    # eager forward, and no device error
+    from tests.gpu_util import dev_bf16, dev_f32, DEV
+    d = dataclasses.replace(W.DECODE, T=T)
+    wdev, _ = big_weights
+    x = dev_bf16(W.hidden_states(d, 5))
+    lg = dev_f32(W.router_logits(d.T, d.num_experts, 5))
+    ws = torch.empty(lm.latent_moe_workspace_bytes(d), dtype=torch.uint8, device=DEV)
+    ref = torch.empty((d.T, d.hidden), dtype=torch.bfloat16, device=DEV)
+    out = torch.empty_like(ref)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        lm.latent_moe_forward(d, wdev, x, lg, ref, ws, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        lm.latent_moe_forward(d, wdev, x, lg, out, ws, stream=s)
+    for _ in range(20):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert lm.lmoe_device_error() == 0
+
+
 def test_invalid_arguments_are_rejected():
     from tests.gpu_util import DEV
     d = W.TINY
