@@ -25,6 +25,8 @@
 //               leave by a TMA bulk tensor store (a block of 32 valid rows)
 //               or 4 rows x 128 bytes per 16-byte store instruction (a ragged
 //               block); otherwise fp32 partials or bf16 values go straight out.
+//   warp 6      (the weights-on-M GEMM1 + SituGLU instance only) a second MMA
+//               issuer: the up halves, beside warp 1's gate halves.
 // GEMMs with tokens on M and 256-row weight tiles run in clusters of two CTAs.
 // A pair of units shares an operand: token tiles 2t and 2t+1 of a group
 // against the same weight tile (each CTA loads one 128-row half of the weight
@@ -84,7 +86,7 @@ static_assert(BK == 64 || BK == 32, "stages are 64 or 32 K elements wide");
 constexpr int kK16 = BK / 16;          // MMAs (K = 16 each) per stage and accumulator
 constexpr int kMaxStages = 12 * 64 / BK;
 constexpr int BM = 128;                // MMA M
-constexpr int kThreads = 192;          // 6 warps
+constexpr int kThreads = 192;          // 6 warps (7 in the swap form, below)
 // the swap form adds a seventh warp: the second MMA issuer (the up halves)
 constexpr int kThreadsSwap = 224;
 constexpr long long kWaitCycles = 1ll << 32;   // ~2 s at 2 GHz
