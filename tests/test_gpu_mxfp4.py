@@ -148,9 +148,10 @@ def test_mxfp4_tiny_layer():
     tiny_case(W.TINY, literal="MXFP4 tiny layer T=8")
 
 
-@pytest.mark.parametrize("T", [1, 3, 17, 100, 128, 129, 300])
+@pytest.mark.parametrize("T", [1, 3, 17, 100, 128, 129, 200, 256, 257, 300])
 def test_mxfp4_tiny_layer_token_counts(T):
     # decode regime (4-bit kernels) up to 128 tokens, dequantized prefill above
+    # (its permutation in one block up to 256 tokens, in three passes above)
     tiny_case(dataclasses.replace(W.TINY, T=T), seed=T)
 
 
