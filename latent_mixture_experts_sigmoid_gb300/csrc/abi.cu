@@ -61,6 +61,18 @@ int num_sms() {
 namespace {
 
 constexpr int kDecodeMaxT = 128;
+// MXFP4 experts at decode sizes: an expert with more than this many tokens
+// (more than two 8-token passes of the 4-bit kernels, which run in one block
+// per column strip and re-read its codes) is widened to bf16 into a compact
+// workspace copy and runs on the tensor-core GEMMs instead; the others stay on
+// the 4-bit kernels.  The split is made on the device from the permutation's
+// counts.  (Measured on the 896-expert layer: 16 against 32 and 64 tokens,
+// with skewed and with spread-out routing.)
+constexpr int kFp4HeavyTokens = 16;
+// ... when at least this many experts are that heavy (a few heavy experts give
+// the GEMMs too few units to hide their latency: then all stay on the 4-bit
+// kernels)
+constexpr int kFp4MinHeavy = 4;
 constexpr int kMaxSplits = 32;
 
 bool finite_pos(float x) { return isfinite(x) && x > 0.0f; }
@@ -120,8 +132,21 @@ struct Ws {
   float *logits;   // router logits [T, round_up(E, 128)] of the router-GEMM forward
   float *Pa, *Pb;
   int32_t* active;          // active experts in expert order (decode permutation)
-  uint16_t *Wd13, *Wd2;     // MXFP4 experts dequantized to bf16 (MXFP4 forward, T > 128)
+  uint16_t *Wd13, *Wd2;     // MXFP4 experts dequantized to bf16 (MXFP4 forward: every
+                            // expert at T > 128, the heavy slots at decode sizes)
+  // MXFP4 forward at decode sizes with heavy slots: the light experts' list
+  // and count, the heavy slots' group tables
+  int32_t *light, *n_light, *h_expert, *h_count, *h_offset, *h_prefix;
 };
+
+// Heavy-expert slots of the MXFP4 forward at decode sizes: an upper bound on
+// the experts with more than kFp4HeavyTokens of the T*k (token, slot) pairs
+// (0 when no expert can have that many, or GEMM1 cannot fuse SituGLU).
+int fp4_heavy_slots(const lmoe_dims& d) {
+  if (d.T > kDecodeMaxT || d.T <= kFp4HeavyTokens || d.inter % 128) return 0;
+  const long long h = (long long)d.T * d.topk / (kFp4HeavyTokens + 1);
+  return (int)(h < d.num_experts ? h : d.num_experts);
+}
 
 // Router logits rows are padded to whole 128-row weight tiles of the router GEMM.
 size_t padded_experts(int E) { return (size_t)round_up(E, 128); }
@@ -162,9 +187,20 @@ size_t carve(const lmoe_dims& d, char* base, Ws* ws, bool mxfp4 = false) {
     w.Pa = w.Pb = nullptr;
   }
   w.active = c.take<int32_t>(E);
+  w.light = w.n_light = w.h_expert = w.h_count = w.h_offset = w.h_prefix = nullptr;
+  const size_t Hs = mxfp4 ? (size_t)fp4_heavy_slots(d) : 0;
   if (mxfp4 && d.T > kDecodeMaxT) {
     w.Wd13 = c.take<uint16_t>(E * 2 * dI * L);
     w.Wd2 = c.take<uint16_t>(E * L * dI);
+  } else if (Hs > 0) {
+    w.Wd13 = c.take<uint16_t>(Hs * 2 * dI * L);
+    w.Wd2 = c.take<uint16_t>(Hs * L * dI);
+    w.light = c.take<int32_t>(E);
+    w.n_light = c.take<int32_t>(1);
+    w.h_expert = c.take<int32_t>(Hs);
+    w.h_count = c.take<int32_t>(Hs);
+    w.h_offset = c.take<int32_t>(Hs);
+    w.h_prefix = c.take<int32_t>(Hs + 1);
   } else {
     w.Wd13 = w.Wd2 = nullptr;
   }
@@ -265,6 +301,7 @@ struct Plan {
   bool fuse_s1;      // shared GEMM1 likewise (tokens on M, no split-K, shared_inter % 128 == 0)
   int tile;          // token tile of the grouped GEMMs
   int g1_bn, g2_bn;  // MMA N of the grouped GEMMs
+  int fp4_heavy;     // heavy-expert slots of the MXFP4 forward (decode sizes)
   DenseCfg down, s1, s2, up;
   DenseCfg rtr;      // the router GEMM: at decode stacked after the down-projection's rows
                      // (one launch), otherwise its own launch
@@ -277,6 +314,7 @@ Plan make_plan(const lmoe_dims& d, int nsm, bool router = false) {
   p.router = router;
   p.Ep = (int)padded_experts(d.num_experts);
   p.tile = p.decode ? round_up(d.T, 16) : 128;
+  p.fp4_heavy = fp4_heavy_slots(d);
   p.g1_bn = p.decode ? p.tile : ((2 * d.inter) % 256 == 0 ? 256 : 128);
   // tokens on M: a 256-row B operand of 128 gate + 128 up rows; weights on M
   // (decode): the two halves as two MMAs of N = tile tokens
@@ -296,9 +334,12 @@ int plan_launches(const Plan& p, bool shared, bool mxfp4 = false) {
   // one permutation kernel for T <= 256; at decode sizes it also does the scatter
   const int perm = p.T <= 256 ? 1 : 3;
   // GEMM1 (+ SituGLU unless fused), GEMM2; MXFP4 experts: at decode one kernel
-  // per stage on the 4-bit weights, above two dequantization kernels first
+  // per stage on the 4-bit weights, above one dequantization kernel first
   int experts = p.fuse_g1 ? 2 : 3;
-  if (mxfp4) experts = p.decode ? 2 : experts + 2;
+  if (mxfp4) experts = p.decode ? 2 : experts + 1;
+  // heavy experts at decode (split off in the permutation kernel): their
+  // dequantization, GEMM1 + SituGLU, GEMM2
+  if (mxfp4 && p.decode && p.fp4_heavy > 0) experts += 3;
   // route, down, permute, scatter (fused into the permutation at decode sizes),
   // experts, combine
   int n = 1 + 1 + perm + (p.decode ? 0 : 1) + experts + 1;
@@ -730,11 +771,15 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
   if (side_route) {
     if (cudaStreamWaitEvent(s, aux->routed, 0) != cudaSuccess) return LMOE_ERR_CUDA;
   } else if (fused_scatter) {
+    // (MXFP4 with heavy slots: the permutation also splits the experts)
+    HeavySplit hs{kFp4HeavyTokens + 1, kFp4MinHeavy, pl.fp4_heavy, ws.light, ws.n_light,
+                  ws.h_expert, ws.h_count, ws.h_offset, ws.h_prefix};
     LMOE_TRY(launch_permute_scatter_small(ids, T, k, E, tile, ws.counts, ws.offsets,
                                           ws.tile_prefix, ws.row_of, ws.tok_of_row,
                                           down_split ? nullptr : ws.Z,
                                           down_split ? ws.Pa : nullptr, cdown.splits, down_stride,
-                                          ldz, L, ws.A, ws.active, id_err, s));
+                                          ldz, L, ws.A, ws.active, id_err, s,
+                                          fq && pl.fp4_heavy > 0 ? &hs : nullptr));
   } else {
     st = permute(s);
     if (st != LMOE_OK) return st;
@@ -754,27 +799,51 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
   const uint16_t* W2 = wt->w2;
   if (fq && decode) {
     // MXFP4 at decode sizes: GEMM1 + SituGLU and GEMM2 straight from the 4-bit
-    // weights, one block per (active expert, column strip)
+    // weights, one block per (active expert, column strip).  With heavy slots
+    // (T > kFp4HeavyTokens) the permutation has split the active experts by
+    // their counts: the light ones stay on the 4-bit kernels, the heavy ones
+    // are widened to bf16 into the slots and run on the tensor-core GEMMs
+    // (each path writes only its own experts' rows of act and Y)
     const int slots = (long long)E < rows ? E : (int)rows;
+    const int H = pl.fp4_heavy;
     int* dev_err = device_error_word();
     if (!dev_err) return LMOE_ERR_CUDA;
+    const int32_t* list = ws.active;
+    const int32_t* n_list = ws.tile_prefix + E;
+    Ws wh = ws;
+    if (H > 0) {
+      list = ws.light;
+      n_list = ws.n_light;
+      LMOE_TRY(launch_dequant_mxfp4_pair(fq->w13_codes, fq->w13_scales, ws.Wd13,
+                                         (long long)H * 2 * dI, L, fq->w2_codes, fq->w2_scales,
+                                         ws.Wd2, (long long)H * L, dI, s, ws.h_count, 2 * dI, L,
+                                         ws.h_expert));
+      wh.counts = ws.h_count;
+      wh.offsets = ws.h_offset;
+      wh.tile_prefix = ws.h_prefix;
+    }
     LMOE_TRY(launch_fp4_expert_gemv(fq->w13_codes, fq->w13_scales, ws.A, ws.act, ws.counts,
-                                    ws.offsets, ws.active, ws.tile_prefix + E, slots, E, L, dI, 1,
-                                    d.beta, d.linear_beta, dev_err, s));
+                                    ws.offsets, list, n_list, slots, E, L, dI, 1, d.beta,
+                                    d.linear_beta, dev_err, s));
+    if (H > 0)
+      LMOE_TRY(gemm_grouped(ws.Wd13, H, 2 * dI, ws.A, rows, L, false, pl.g1_bn, wh, tile, ws.act,
+                            s, 1, d.beta, d.linear_beta));
     if (!mark(LMOE_STAGE_GEMM1 + 1) || !mark(LMOE_STAGE_SITU + 1)) return LMOE_ERR_CUDA;
     LMOE_TRY(launch_fp4_expert_gemv(fq->w2_codes, fq->w2_scales, ws.act, ws.Y, ws.counts,
-                                    ws.offsets, ws.active, ws.tile_prefix + E, slots, E, dI, L, 0,
-                                    d.beta, d.linear_beta, dev_err, s));
+                                    ws.offsets, list, n_list, slots, E, dI, L, 0, d.beta,
+                                    d.linear_beta, dev_err, s));
+    if (H > 0)
+      LMOE_TRY(gemm_grouped(ws.Wd2, H, L, ws.act, rows, dI, false, pl.g2_bn, wh, tile, ws.Y, s));
     if (!mark(LMOE_STAGE_GEMM2 + 1)) return LMOE_ERR_CUDA;
   } else {
     if (fq) {
       // MXFP4 above decode sizes: the weights of every expert with routed
       // tokens dequantized to bf16 in the workspace, then the tensor-core path
       // (the grouped GEMMs read no rows of the others)
-      LMOE_TRY(launch_dequant_mxfp4(fq->w13_codes, fq->w13_scales, ws.Wd13,
-                                    (long long)E * 2 * dI, L, s, ws.counts, 2 * dI));
-      LMOE_TRY(launch_dequant_mxfp4(fq->w2_codes, fq->w2_scales, ws.Wd2, (long long)E * L, dI, s,
-                                    ws.counts, L));
+      LMOE_TRY(launch_dequant_mxfp4_pair(fq->w13_codes, fq->w13_scales, ws.Wd13,
+                                         (long long)E * 2 * dI, L, fq->w2_codes, fq->w2_scales,
+                                         ws.Wd2, (long long)E * L, dI, s, ws.counts, 2 * dI, L,
+                                         nullptr));
       W13 = ws.Wd13;
       W2 = ws.Wd2;
     }

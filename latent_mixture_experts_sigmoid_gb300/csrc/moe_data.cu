@@ -185,6 +185,41 @@ perm_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int tile
   }
 }
 
+// ---- MXFP4 decode: experts split by token count ------------------------------
+// Called by every thread of one block of 1024 with its expert's count c
+// (thread e = expert e, c = 0 for e >= E).  Experts with at least heavy_min
+// tokens are heavy when there are at least min_heavy of them (else none is);
+// the others with tokens are light.  light[0 .. *n_light - 1] the light
+// experts (expert order); the first #heavy slots of h_expert / h_count /
+// h_offset [H] the heavy ones (expert, count, first row), the other slots
+// count 0; h_prefix [H+1] = min(j, #heavy) (one token tile a heavy expert:
+// the grouped GEMM's tile prefix over the H slots).
+__device__ void split_heavy_block(int c, int off, const HeavySplit& hs, int* sh) {
+  const int e = threadIdx.x;
+  bool heavy = c >= hs.heavy_min;
+  int nh = 0, nl = 0;
+  const int hi = block_exclusive_scan(heavy ? 1 : 0, sh, &nh);
+  if (nh < hs.min_heavy || nh > hs.H) {   // (nh > H cannot happen: H >= T*k / heavy_min)
+    heavy = false;
+    nh = 0;
+  }
+  const bool lite = c > 0 && !heavy;
+  const int li = block_exclusive_scan(lite ? 1 : 0, sh, &nl);
+  if (lite) hs.light[li] = e;
+  if (heavy) {
+    hs.h_expert[hi] = e;
+    hs.h_count[hi] = c;
+    hs.h_offset[hi] = off;
+  }
+  for (int j = nh + e; j < hs.H; j += blockDim.x) {
+    hs.h_expert[j] = 0;
+    hs.h_count[j] = 0;
+    hs.h_offset[j] = 0;
+  }
+  for (int j = e; j <= hs.H; j += blockDim.x) hs.h_prefix[j] = min(j, nh);
+  if (e == 0) hs.n_light[0] = nl;
+}
+
 // ---- permutation, pass 3: row of every (token, slot) -------------------------
 __global__ void __launch_bounds__(kBlkTok)
 perm_rows_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
@@ -251,7 +286,8 @@ perm_scatter_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, 
                           int32_t* __restrict__ tile_prefix, int32_t* __restrict__ row_of,
                           int32_t* __restrict__ tok_of_row, const uint16_t* __restrict__ Zb,
                           const float* __restrict__ Zp, int S, long long split_stride, int ldz,
-                          int L, uint16_t* __restrict__ A, int32_t* __restrict__ active, int* err) {
+                          int L, uint16_t* __restrict__ A, int32_t* __restrict__ active,
+                          const HeavySplit hs, int* err) {
   pdl_trigger();
   pdl_wait();
   __shared__ uint32_t bm[1024 * kWords];
@@ -291,6 +327,7 @@ perm_scatter_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, 
       offsets[E] = all;
       tile_prefix[E] = all_tiles;
     }
+    if (hs.H > 0) split_heavy_block(e < E ? c : 0, off, hs, sh);
   }
   __syncthreads();
   const int t = blockIdx.x;
@@ -526,11 +563,18 @@ cudaError_t launch_permute_scatter_small(const int32_t* ids, int T, int k, int E
                                          int32_t* row_of, int32_t* tok_of_row, const uint16_t* Zb,
                                          const float* Zp, int S, long long split_stride,
                                          int ldz, int L, uint16_t* A, int32_t* active, int* err,
-                                         cudaStream_t s) {
+                                         cudaStream_t s, const HeavySplit* split) {
   if (T > kBlkTok || E > 1024 || k > 32 || (active && tile < T)) return cudaErrorInvalidValue;
+  HeavySplit hs{};
+  if (split) {
+    if (split->H < 1 || split->heavy_min < 1 || !split->light || !split->n_light ||
+        !split->h_expert || !split->h_count || !split->h_offset || !split->h_prefix)
+      return cudaErrorInvalidValue;
+    hs = *split;
+  }
   return launch_k(perm_scatter_small_kernel, dim3(T), dim3(1024), 0, s, ids, T, k, E, tile, counts,
                   offsets, tile_prefix, row_of, tok_of_row, Zb, Zp, S, split_stride, ldz, L, A,
-                  active, err);
+                  active, hs, err);
 }
 
 cudaError_t launch_scatter_rows(const uint16_t* Zb, const float* Zp, int S, long long split_stride,

@@ -17,16 +17,29 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int tile, vo
                            int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
                            int32_t* row_of, int32_t* tok_of_row, int* err, cudaStream_t s);
 
+// The experts of the permutation split by token count (MXFP4 decode):
+// experts with at least heavy_min tokens are heavy when there are at least
+// min_heavy of them (else none is), the others with tokens light.
+// light [E]: light[0 .. *n_light - 1] the light experts in expert order;
+// h_expert / h_count / h_offset [H]: the heavy experts (expert, count, first
+// row) in the first #heavy slots, count 0 in the others; h_prefix [H+1] =
+// min(j, #heavy) (one token tile a heavy expert: the grouped GEMM's tile
+// prefix over the H slots).  H >= T*k / heavy_min.
+struct HeavySplit {
+  int heavy_min, min_heavy, H;
+  int32_t *light, *n_light, *h_expert, *h_count, *h_offset, *h_prefix;
+};
+
 // launch_permute followed by launch_scatter_rows in one launch of T blocks,
 // for T <= 256, E <= 1024, k <= 32 (the small-T path).  active (optional,
 // needs tile >= T): active[i] = the i-th expert with a nonzero count, for
-// i < tile_prefix[E].
+// i < tile_prefix[E].  split (optional): the experts also split by count.
 cudaError_t launch_permute_scatter_small(const int32_t* ids, int T, int k, int E, int tile,
                                          int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
                                          int32_t* row_of, int32_t* tok_of_row, const uint16_t* Zb,
                                          const float* Zp, int S, long long split_stride,
                                          int ldz, int L, uint16_t* A, int32_t* active, int* err,
-                                         cudaStream_t s);
+                                         cudaStream_t s, const HeavySplit* split = nullptr);
 
 // A[row_of[t,j]] = Z[t] for j < k; Z from bf16 rows Zb ([T, L]) or from the sum
 // of S fp32 partials Zp (split_stride elements apart, rows ldz >= L elements

@@ -78,7 +78,10 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
 // kDqInFlight of them loaded before any is converted, so that a warp's loads
 // are 128-byte lines and its stores 512-byte runs.  With `counts`, the units
 // of a group g with counts[g] == 0 (an expert no token was routed to) are
-// skipped as a whole.
+// skipped as a whole.  With `src_group`, output group g is read from the
+// codes and scales of group src_group[g] (a compact copy of some experts).
+// One launch takes up to two such jobs (the units of the first, then the
+// second's).
 constexpr int kDqUnitWords = 1024;
 constexpr int kDqInFlight = 8;
 
@@ -90,34 +93,60 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, uint32_t s) {
                     pack_bf16x2(v[4] * sc, v[5] * sc), pack_bf16x2(v[6] * sc, v[7] * sc));
 }
 
-__global__ void __launch_bounds__(256)
-dequant_kernel(const uint32_t* __restrict__ codes, const uint8_t* __restrict__ scales,
-               uint4* __restrict__ out, long long words, long long words_per_group,
-               const int32_t* __restrict__ counts) {
+struct DqJob {
+  const uint32_t* codes;
+  const uint8_t* scales;
+  uint4* out;
+  long long words, words_per_group;
+  const int32_t* counts;
+  const int32_t* src_group;
+};
+
+__host__ __device__ __forceinline__ long long dq_units(const DqJob& j) {
+  if (j.words <= 0) return 0;
+  return (j.words + j.words_per_group - 1) / j.words_per_group *
+         ((j.words_per_group + kDqUnitWords - 1) / kDqUnitWords);
+}
+
+__global__ void __launch_bounds__(256) dequant_kernel(const DqJob j0, const DqJob j1) {
   pdl_trigger();
   pdl_wait();   // out may still be read by the previous forward's GEMMs
-  const long long units_per_group = (words_per_group + kDqUnitWords - 1) / kDqUnitWords;
-  const long long units = (words + words_per_group - 1) / words_per_group * units_per_group;
+  const long long units0 = dq_units(j0), units = units0 + dq_units(j1);
   const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
   const int lane = threadIdx.x & 31;
-  for (long long u = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units;
-       u += nwarps) {
+  for (long long uu = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); uu < units;
+       uu += nwarps) {
+    const bool second = uu >= units0;   // (warp-uniform)
+    const long long u = second ? uu - units0 : uu;
+    const uint32_t* __restrict__ codes = second ? j1.codes : j0.codes;
+    const uint8_t* __restrict__ scales = second ? j1.scales : j0.scales;
+    uint4* __restrict__ out = second ? j1.out : j0.out;
+    const long long words = second ? j1.words : j0.words;
+    const long long words_per_group = second ? j1.words_per_group : j0.words_per_group;
+    const int32_t* __restrict__ counts = second ? j1.counts : j0.counts;
+    const int32_t* __restrict__ src_group = second ? j1.src_group : j0.src_group;
+    const long long units_per_group = (words_per_group + kDqUnitWords - 1) / kDqUnitWords;
     const long long g = u / units_per_group;
     if (counts && counts[g] == 0) continue;   // (warp-uniform)
+    // source word = output word + shift (a group is whole rows: a multiple of
+    // 4 words, so the scale byte of a word is still its source index / 4)
+    const long long shift = src_group ? ((long long)__ldg(src_group + g) - g) * words_per_group : 0;
     const long long q0 = g * words_per_group + (u - g * units_per_group) * kDqUnitWords;
     const long long q1 = min(q0 + kDqUnitWords, min((g + 1) * words_per_group, words));
+    const uint32_t* cs = codes + shift;
+    const uint8_t* ss = scales + shift / 4;
     long long q = q0 + lane;
     for (; q + 32 * (kDqInFlight - 1) < q1; q += 32 * kDqInFlight) {
       uint32_t w[kDqInFlight], sv[kDqInFlight];
 #pragma unroll
       for (int i = 0; i < kDqInFlight; ++i) {
-        w[i] = __ldg(codes + q + 32 * i);
-        sv[i] = __ldg(scales + ((q + 32 * i) >> 2));
+        w[i] = __ldg(cs + q + 32 * i);
+        sv[i] = __ldg(ss + ((q + 32 * i) >> 2));
       }
 #pragma unroll
       for (int i = 0; i < kDqInFlight; ++i) out[q + 32 * i] = dequant_word(w[i], sv[i]);
     }
-    for (; q < q1; q += 32) out[q] = dequant_word(__ldg(codes + q), __ldg(scales + (q >> 2)));
+    for (; q < q1; q += 32) out[q] = dequant_word(__ldg(cs + q), __ldg(ss + (q >> 2)));
   }
 }
 
@@ -771,22 +800,49 @@ cudaError_t launch_expert_kernel(GemvArgs& a, int slots, int E, cudaStream_t s) 
 
 }  // namespace
 
-cudaError_t launch_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, uint16_t* out,
-                                 long long rows, int K, cudaStream_t s, const int32_t* counts,
-                                 int rows_per_expert) {
-  if (rows <= 0) return cudaSuccess;
+namespace {
+DqJob dq_job(const uint8_t* codes, const uint8_t* scales, uint16_t* out, long long rows, int K,
+             const int32_t* counts, int rows_per_expert, const int32_t* src_group) {
+  DqJob j{};
+  if (rows <= 0) return j;
   const long long words_per_row = K / 8;
-  const long long words = rows * words_per_row;
-  const long long per_group =
-      counts ? (long long)(rows_per_expert > 0 ? rows_per_expert : 1) * words_per_row : words;
-  const long long units =
-      (words + per_group - 1) / per_group * ((per_group + kDqUnitWords - 1) / kDqUnitWords);
+  j.codes = reinterpret_cast<const uint32_t*>(codes);
+  j.scales = scales;
+  j.out = reinterpret_cast<uint4*>(out);
+  j.words = rows * words_per_row;
+  j.words_per_group =
+      counts ? (long long)(rows_per_expert > 0 ? rows_per_expert : 1) * words_per_row : j.words;
+  j.counts = counts;
+  j.src_group = src_group;
+  return j;
+}
+
+cudaError_t launch_dq(const DqJob& j0, const DqJob& j1, cudaStream_t s) {
+  const long long units = dq_units(j0) + dq_units(j1);
+  if (units == 0) return cudaSuccess;
   long long grid = (units + 7) / 8;
   const long long cap = (long long)num_sms() * 8;
   if (grid > cap) grid = cap;
-  return launch_k(dequant_kernel, dim3((unsigned)grid), dim3(256), 0, s,
-                  reinterpret_cast<const uint32_t*>(codes), scales, reinterpret_cast<uint4*>(out),
-                  words, per_group, counts);
+  return launch_k(dequant_kernel, dim3((unsigned)grid), dim3(256), 0, s, j0, j1);
+}
+}  // namespace
+
+cudaError_t launch_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, uint16_t* out,
+                                 long long rows, int K, cudaStream_t s, const int32_t* counts,
+                                 int rows_per_expert, const int32_t* src_group) {
+  return launch_dq(dq_job(codes, scales, out, rows, K, counts, rows_per_expert, src_group),
+                   DqJob{}, s);
+}
+
+cudaError_t launch_dequant_mxfp4_pair(const uint8_t* codes0, const uint8_t* scales0,
+                                      uint16_t* out0, long long rows0, int K0,
+                                      const uint8_t* codes1, const uint8_t* scales1,
+                                      uint16_t* out1, long long rows1, int K1, cudaStream_t s,
+                                      const int32_t* counts, int rows_per_expert0,
+                                      int rows_per_expert1, const int32_t* src_group) {
+  return launch_dq(
+      dq_job(codes0, scales0, out0, rows0, K0, counts, rows_per_expert0, src_group),
+      dq_job(codes1, scales1, out1, rows1, K1, counts, rows_per_expert1, src_group), s);
 }
 
 cudaError_t launch_fp4_expert_gemv(const uint8_t* codes, const uint8_t* scales, const uint16_t* x,

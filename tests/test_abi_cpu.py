@@ -225,6 +225,13 @@ def test_mxfp4_validation(lib):
     # above 128 tokens the workspace also holds every expert dequantized
     dp = lm.make_dims(dataclasses.replace(W.TINY, T=300))
     E, L, dI = W.TINY.num_experts, W.TINY.latent, W.TINY.inter
+    # at 17..128 tokens the T*k/17 heavy-expert slots (bf16 weights + tables)
+    for T in (16, 17, 128):
+        dm = lm.make_dims(dataclasses.replace(W.TINY, T=T))
+        extra = (lib.latent_moe_workspace_bytes_mxfp4(ctypes.byref(dm)) -
+                 lib.latent_moe_workspace_bytes(ctypes.byref(dm)))
+        H = min(E, T * W.TINY.topk // 17) if T > 16 else 0
+        assert H * 3 * dI * L * 2 <= extra <= H * 3 * dI * L * 2 + (E + 4 * H + 2) * 4 + 8 * 256
     assert (lib.latent_moe_workspace_bytes_mxfp4(ctypes.byref(dp)) -
             lib.latent_moe_workspace_bytes(ctypes.byref(dp))) >= E * 3 * dI * L * 2
     big = lm.make_dims(dataclasses.replace(W.TINY, inter=4160))
@@ -252,8 +259,14 @@ def test_mxfp4_validation(lib):
     assert fwd(ctypes.byref(d), ctypes.byref(w), ctypes.byref(q), p, p, p, p, nb, None,
                None) == -8
     # launches: decode replaces GEMM1 + SituGLU and GEMM2 by one kernel each;
-    # above 128 tokens two dequantization kernels come first
+    # above 16 tokens (where an expert can get more than 16) the compact
+    # dequantization of the heavy experts and their two grouped GEMMs follow;
+    # above 128 tokens one dequantization kernel comes first
     n_bf16 = lib.latent_moe_launch_count(ctypes.byref(d), 1)
     assert lib.latent_moe_launch_count_mxfp4(ctypes.byref(d), 1) == n_bf16
+    for T, extra in ((16, 0), (17, 3), (128, 3)):
+        dm = lm.make_dims(dataclasses.replace(W.TINY, T=T))
+        assert lib.latent_moe_launch_count_mxfp4(ctypes.byref(dm), 1) == \
+            lib.latent_moe_launch_count(ctypes.byref(dm), 1) + extra
     assert lib.latent_moe_launch_count_mxfp4(ctypes.byref(dp), 1) == \
-        lib.latent_moe_launch_count(ctypes.byref(dp), 1) + 2
+        lib.latent_moe_launch_count(ctypes.byref(dp), 1) + 1

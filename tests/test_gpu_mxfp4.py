@@ -155,7 +155,8 @@ def test_mxfp4_tiny_layer_token_counts(T):
     tiny_case(dataclasses.replace(W.TINY, T=T), seed=T)
 
 
-@pytest.mark.parametrize("variant", ["ragged", "crowded", "wide_k1", "wide_k2", "max_experts"])
+@pytest.mark.parametrize("variant", ["ragged", "crowded", "all_heavy", "wide_k1", "wide_k2",
+                                     "max_experts"])
 def test_mxfp4_layer_shapes(variant):
     d = W.TINY
     if variant == "ragged":
@@ -165,8 +166,13 @@ def test_mxfp4_layer_shapes(variant):
                                 num_experts=40, topk=6)
     elif variant == "crowded":
         # 128 tokens over 16 experts: ~32 rows an expert, several passes of up
-        # to 8 tokens over the same strip
+        # to 8 tokens over the same strip; the experts with more than 16 run
+        # on the tensor-core GEMMs, the others on the 4-bit kernels
         d = dataclasses.replace(d, T=128, num_experts=16, topk=4)
+    elif variant == "all_heavy":
+        # 64 rows for each of 4 experts: all on the tensor-core GEMMs, the
+        # 4-bit kernels get no expert
+        d = dataclasses.replace(d, T=128, num_experts=4, topk=2)
     elif variant == "wide_k1":
         # GEMM1 over latent 4096 (the largest the MXFP4 forward takes): one
         # token a stage, two stages
@@ -274,13 +280,38 @@ def test_mxfp4_decode_full_size(decode_full):
                         lg, wor["bias"])
 
 
-def test_mxfp4_decode_graph_replay(decode_full):
+def test_mxfp4_decode_skewed_full_size(decode_full):
+    # 64 tokens of the 896-expert layer with Zipf-skewed routing: the experts
+    # most tokens choose get more than 16 rows and run on the tensor-core
+    # GEMMs from a compact bf16 copy, the rest on the 4-bit kernels
+    from tests.gpu_util import host_bits, assert_layer_close, addend_scale, record_literal
+    d, wdev, qdev, wor, Q = decode_full
+    d = dataclasses.replace(d, T=64)
+    x = W.hidden_states(d, 5)
+    lg = W.router_logits(d.T, d.num_experts, 5, zipf=True)
+    ids, _ = O.route(lg, wor["bias"], d.topk, d.routed_scaling_factor, d.renormalize)
+    counts = np.bincount(ids.ravel(), minlength=d.num_experts)
+    assert (counts > 16).sum() >= 4 and ((counts > 0) & (counts <= 16)).sum() >= 4
+    out, ws = run_mxfp4(d, wdev, qdev, x, lg, keep_ws=True)
+    ref_bits, mid = O.latent_moe_forward_mxfp4(d, wor, Q, x, lg, intermediates=True)
+    ref = O.bf16_to_f64(ref_bits)
+    got = O.bf16_to_f64(host_bits(out))
+    assert_layer_close(got, ref, TOL, scale=addend_scale(ref, mid, wor["w_up"]))
+    record_literal(got, ref, "MXFP4 decode layer T=64 Zipf", TOL)
+    check_expert_stages(d, lambda n, e: (Q[n + "_q"][e], Q[n + "_s"][e]),
+                        list(range(12)) + [d.T - 1], ws, lg, wor["bias"])
+
+
+@pytest.mark.parametrize("T,zipf", [(8, False), (64, True)])
+def test_mxfp4_decode_graph_replay(decode_full, T, zipf):
     # the decode forward captured in a CUDA graph reproduces the eager output
-    # bit for bit (no host state decides anything at replay)
+    # bit for bit (no host state decides anything at replay; at T = 64 the
+    # device splits the experts between the two expert paths)
     from tests.gpu_util import DEV, dev_bf16, dev_f32
     d, wdev, qdev, _, _ = decode_full
+    d = dataclasses.replace(d, T=T)
     x = dev_bf16(W.hidden_states(d, 0))
-    lg = dev_f32(W.router_logits(d.T, d.num_experts, 0))
+    lg = dev_f32(W.router_logits(d.T, d.num_experts, 0, zipf=zipf))
     out = torch.empty((d.T, d.hidden), dtype=torch.bfloat16, device=DEV)
     ws = torch.empty(lm.latent_moe_workspace_bytes_mxfp4(d), dtype=torch.uint8, device=DEV)
     s = torch.cuda.Stream()
