@@ -61,11 +61,11 @@ int num_sms() {
 namespace {
 
 constexpr int kDecodeMaxT = 128;
-// MXFP4 experts at decode sizes: an expert with more than this many tokens
-// (more than two 8-token passes of the 4-bit kernels, which run in one block
-// per column strip and re-read its codes) is widened to bf16 into a compact
-// workspace copy and runs on the tensor-core GEMMs instead; the others stay on
-// the 4-bit kernels.  The split is made on the device from the permutation's
+// MXFP4 experts: an expert with more than this many tokens (more than two
+// 8-token passes of the 4-bit kernels, which run in one block per column
+// strip and re-read its codes) is widened to bf16 into a compact workspace
+// copy and runs on the tensor-core GEMMs instead; the others stay on the
+// 4-bit kernels.  The split is made on the device from the permutation's
 // counts.  (Measured on the 896-expert layer: 16 against 32 and 64 tokens,
 // with skewed and with spread-out routing.)
 constexpr int kFp4HeavyTokens = 16;
@@ -139,13 +139,23 @@ struct Ws {
   int32_t *light, *n_light, *h_expert, *h_count, *h_offset, *h_prefix;
 };
 
-// Heavy-expert slots of the MXFP4 forward at decode sizes: an upper bound on
-// the experts with more than kFp4HeavyTokens of the T*k (token, slot) pairs
-// (0 when no expert can have that many, or GEMM1 cannot fuse SituGLU).
+// Heavy-expert slots of the MXFP4 forward: an upper bound on the experts with
+// more than kFp4HeavyTokens of the T*k (token, slot) pairs (0 when no expert
+// can have that many, or GEMM1 cannot fuse SituGLU).
 int fp4_heavy_slots(const lmoe_dims& d) {
-  if (d.T > kDecodeMaxT || d.T <= kFp4HeavyTokens || d.inter % 128) return 0;
+  if (d.T <= kFp4HeavyTokens || d.inter % 128) return 0;
   const long long h = (long long)d.T * d.topk / (kFp4HeavyTokens + 1);
   return (int)(h < d.num_experts ? h : d.num_experts);
+}
+
+// The MXFP4 forward runs the 4-bit expert kernels for its light experts: at
+// decode sizes, and above them wherever the heavy experts can be split off
+// (GEMM1 fuses SituGLU); otherwise (inter % 128 != 0 above decode sizes) it
+// widens every expert with tokens to bf16 and runs the tensor-core GEMMs
+// (measured on the 896-expert layer, the split path is the faster one at
+// every T from 17 to 4096, with and without skewed routing).
+bool fp4_direct(const lmoe_dims& d) {
+  return d.T <= kDecodeMaxT || fp4_heavy_slots(d) > 0;
 }
 
 // Router logits rows are padded to whole 128-row weight tiles of the router GEMM.
@@ -189,7 +199,7 @@ size_t carve(const lmoe_dims& d, char* base, Ws* ws, bool mxfp4 = false) {
   w.active = c.take<int32_t>(E);
   w.light = w.n_light = w.h_expert = w.h_count = w.h_offset = w.h_prefix = nullptr;
   const size_t Hs = mxfp4 ? (size_t)fp4_heavy_slots(d) : 0;
-  if (mxfp4 && d.T > kDecodeMaxT) {
+  if (mxfp4 && !fp4_direct(d)) {
     w.Wd13 = c.take<uint16_t>(E * 2 * dI * L);
     w.Wd2 = c.take<uint16_t>(E * L * dI);
   } else if (Hs > 0) {
@@ -301,7 +311,8 @@ struct Plan {
   bool fuse_s1;      // shared GEMM1 likewise (tokens on M, no split-K, shared_inter % 128 == 0)
   int tile;          // token tile of the grouped GEMMs
   int g1_bn, g2_bn;  // MMA N of the grouped GEMMs
-  int fp4_heavy;     // heavy-expert slots of the MXFP4 forward (decode sizes)
+  bool fp4_direct;   // the MXFP4 forward runs the 4-bit expert kernels
+  int fp4_heavy;     // heavy-expert slots of the MXFP4 forward
   DenseCfg down, s1, s2, up;
   DenseCfg rtr;      // the router GEMM: at decode stacked after the down-projection's rows
                      // (one launch), otherwise its own launch
@@ -314,6 +325,7 @@ Plan make_plan(const lmoe_dims& d, int nsm, bool router = false) {
   p.router = router;
   p.Ep = (int)padded_experts(d.num_experts);
   p.tile = p.decode ? round_up(d.T, 16) : 128;
+  p.fp4_direct = fp4_direct(d);
   p.fp4_heavy = fp4_heavy_slots(d);
   p.g1_bn = p.decode ? p.tile : ((2 * d.inter) % 256 == 0 ? 256 : 128);
   // tokens on M: a 256-row B operand of 128 gate + 128 up rows; weights on M
@@ -333,13 +345,12 @@ Plan make_plan(const lmoe_dims& d, int nsm, bool router = false) {
 int plan_launches(const Plan& p, bool shared, bool mxfp4 = false) {
   // one permutation kernel for T <= 256; at decode sizes it also does the scatter
   const int perm = p.T <= 256 ? 1 : 3;
-  // GEMM1 (+ SituGLU unless fused), GEMM2; MXFP4 experts: at decode one kernel
-  // per stage on the 4-bit weights, above one dequantization kernel first
+  // GEMM1 (+ SituGLU unless fused), GEMM2; MXFP4 experts: one kernel per
+  // stage on the 4-bit weights, with heavy slots also the heavy experts'
+  // dequantization, GEMM1 + SituGLU and GEMM2 (split off in the permutation);
+  // without the 4-bit kernels, one dequantization kernel first
   int experts = p.fuse_g1 ? 2 : 3;
-  if (mxfp4) experts = p.decode ? 2 : experts + 1;
-  // heavy experts at decode (split off in the permutation kernel): their
-  // dequantization, GEMM1 + SituGLU, GEMM2
-  if (mxfp4 && p.decode && p.fp4_heavy > 0) experts += 3;
+  if (mxfp4) experts = p.fp4_direct ? 2 + (p.fp4_heavy > 0 ? 3 : 0) : experts + 1;
   // route, down, permute, scatter (fused into the permutation at decode sizes),
   // experts, combine
   int n = 1 + 1 + perm + (p.decode ? 0 : 1) + experts + 1;
@@ -700,9 +711,15 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
     if (marks && !mark(LMOE_STAGE_ROUTE + 1)) return LMOE_ERR_CUDA;
     return LMOE_OK;
   };
+  // MXFP4 experts with heavy slots: the permutation also splits the experts
+  // by count (heavy ones in token tiles of the grouped GEMMs)
+  const bool fp4_split = fq && pl.fp4_direct && pl.fp4_heavy > 0;
+  const HeavySplit hsplit{kFp4HeavyTokens + 1, kFp4MinHeavy, pl.fp4_heavy, tile, ws.light,
+                          ws.n_light, ws.h_expert, ws.h_count, ws.h_offset, ws.h_prefix};
   auto permute = [&](cudaStream_t rs) -> int {
     LMOE_TRY(launch_permute(ids, T, k, E, tile, ws.perm_scratch, ws.counts, ws.offsets,
-                            ws.tile_prefix, ws.row_of, ws.tok_of_row, id_err, rs));
+                            ws.tile_prefix, ws.row_of, ws.tok_of_row, id_err, rs,
+                            fp4_split ? &hsplit : nullptr));
     return LMOE_OK;
   };
   int st = LMOE_OK;
@@ -771,15 +788,12 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
   if (side_route) {
     if (cudaStreamWaitEvent(s, aux->routed, 0) != cudaSuccess) return LMOE_ERR_CUDA;
   } else if (fused_scatter) {
-    // (MXFP4 with heavy slots: the permutation also splits the experts)
-    HeavySplit hs{kFp4HeavyTokens + 1, kFp4MinHeavy, pl.fp4_heavy, ws.light, ws.n_light,
-                  ws.h_expert, ws.h_count, ws.h_offset, ws.h_prefix};
     LMOE_TRY(launch_permute_scatter_small(ids, T, k, E, tile, ws.counts, ws.offsets,
                                           ws.tile_prefix, ws.row_of, ws.tok_of_row,
                                           down_split ? nullptr : ws.Z,
                                           down_split ? ws.Pa : nullptr, cdown.splits, down_stride,
                                           ldz, L, ws.A, ws.active, id_err, s,
-                                          fq && pl.fp4_heavy > 0 ? &hs : nullptr));
+                                          fp4_split ? &hsplit : nullptr));
   } else {
     st = permute(s);
     if (st != LMOE_OK) return st;
@@ -790,19 +804,19 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
     LMOE_TRY(launch_scatter_rows(down_split ? nullptr : ws.Z, down_split ? ws.Pa : nullptr,
                                  cdown.splits, down_stride, ldz, T, L, k, ws.row_of, ws.A, s));
   if (!mark(LMOE_STAGE_SCATTER + 1)) return LMOE_ERR_CUDA;
-  if (fq && decode) {
+  if (fq && pl.fp4_direct) {
     st = fork_shared_late();
     if (st != LMOE_OK) return st;
   }
   // 5-7. experts
   const uint16_t* W13 = wt->w13;
   const uint16_t* W2 = wt->w2;
-  if (fq && decode) {
-    // MXFP4 at decode sizes: GEMM1 + SituGLU and GEMM2 straight from the 4-bit
-    // weights, one block per (active expert, column strip).  With heavy slots
-    // (T > kFp4HeavyTokens) the permutation has split the active experts by
-    // their counts: the light ones stay on the 4-bit kernels, the heavy ones
-    // are widened to bf16 into the slots and run on the tensor-core GEMMs
+  if (fq && pl.fp4_direct) {
+    // MXFP4: GEMM1 + SituGLU and GEMM2 straight from the 4-bit weights, one
+    // block per (active expert, column strip).  With heavy
+    // slots (T > kFp4HeavyTokens) the permutation has split the active experts
+    // by their counts: the light ones stay on the 4-bit kernels, the heavy
+    // ones are widened to bf16 into the slots and run on the tensor-core GEMMs
     // (each path writes only its own experts' rows of act and Y)
     const int slots = (long long)E < rows ? E : (int)rows;
     const int H = pl.fp4_heavy;
@@ -826,18 +840,19 @@ static int forward_impl(const lmoe_dims* dims, const lmoe_weights* wt, const lmo
                                     ws.offsets, list, n_list, slots, E, L, dI, 1, d.beta,
                                     d.linear_beta, dev_err, s));
     if (H > 0)
-      LMOE_TRY(gemm_grouped(ws.Wd13, H, 2 * dI, ws.A, rows, L, false, pl.g1_bn, wh, tile, ws.act,
-                            s, 1, d.beta, d.linear_beta));
+      LMOE_TRY(gemm_grouped(ws.Wd13, H, 2 * dI, ws.A, rows, L, !decode, pl.g1_bn, wh, tile,
+                            ws.act, s, 1, d.beta, d.linear_beta));
     if (!mark(LMOE_STAGE_GEMM1 + 1) || !mark(LMOE_STAGE_SITU + 1)) return LMOE_ERR_CUDA;
     LMOE_TRY(launch_fp4_expert_gemv(fq->w2_codes, fq->w2_scales, ws.act, ws.Y, ws.counts,
                                     ws.offsets, list, n_list, slots, E, dI, L, 0, d.beta,
                                     d.linear_beta, dev_err, s));
     if (H > 0)
-      LMOE_TRY(gemm_grouped(ws.Wd2, H, L, ws.act, rows, dI, false, pl.g2_bn, wh, tile, ws.Y, s));
+      LMOE_TRY(gemm_grouped(ws.Wd2, H, L, ws.act, rows, dI, !decode, pl.g2_bn, wh, tile, ws.Y, s));
     if (!mark(LMOE_STAGE_GEMM2 + 1)) return LMOE_ERR_CUDA;
   } else {
     if (fq) {
-      // MXFP4 above decode sizes: the weights of every expert with routed
+      // MXFP4 without the 4-bit kernels (inter % 128 != 0 above decode
+      // sizes): the weights of every expert with routed
       // tokens dequantized to bf16 in the workspace, then the tensor-core path
       // (the grouped GEMMs read no rows of the others)
       LMOE_TRY(launch_dequant_mxfp4_pair(fq->w13_codes, fq->w13_scales, ws.Wd13,

@@ -93,12 +93,50 @@ __device__ int block_exclusive_scan(int v, int* sh /* [32] */, int* total) {
   return r;
 }
 
+// ---- MXFP4 experts: split by token count -------------------------------------
+// Called by every thread of one block of 1024 with its expert's count c
+// (thread e = expert e, c = 0 for e >= E).  Experts with at least heavy_min
+// tokens are heavy when there are at least min_heavy of them (else none is);
+// the others with tokens are light.  light[0 .. *n_light - 1] the light
+// experts (expert order); the first #heavy slots of h_expert / h_count /
+// h_offset [H] the heavy ones (expert, count, first row), the other slots
+// count 0; h_prefix [H+1] the grouped GEMM's tile prefix over the H slots
+// (ceil(count / tile) token tiles a heavy expert).
+__device__ void split_heavy_block(int c, int off, const HeavySplit& hs, int* sh) {
+  const int e = threadIdx.x;
+  bool heavy = c >= hs.heavy_min;
+  int nh = 0, nl = 0, tiles = 0;
+  const int hi = block_exclusive_scan(heavy ? 1 : 0, sh, &nh);
+  if (nh < hs.min_heavy || nh > hs.H) {   // (nh > H cannot happen: H >= T*k / heavy_min)
+    heavy = false;
+    nh = 0;
+  }
+  const bool lite = c > 0 && !heavy;
+  const int li = block_exclusive_scan(lite ? 1 : 0, sh, &nl);
+  const int ht = block_exclusive_scan(heavy ? (c + hs.tile - 1) / hs.tile : 0, sh, &tiles);
+  if (lite) hs.light[li] = e;
+  if (heavy) {
+    hs.h_expert[hi] = e;
+    hs.h_count[hi] = c;
+    hs.h_offset[hi] = off;
+    hs.h_prefix[hi] = ht;
+  }
+  for (int j = nh + e; j < hs.H; j += blockDim.x) {
+    hs.h_expert[j] = 0;
+    hs.h_count[j] = 0;
+    hs.h_offset[j] = 0;
+  }
+  for (int j = nh + e; j <= hs.H; j += blockDim.x) hs.h_prefix[j] = tiles;
+  if (e == 0) hs.n_light[0] = nl;
+}
+
 // ---- permutation, pass 2: counts, offsets, tile prefix, block bases ----------
 // One block of 1024 threads; expert e is handled by thread e (E <= 1024).
 __global__ void __launch_bounds__(1024)
 perm_scan_kernel(const int32_t* __restrict__ blk_cnt, int nblk, int E, int tile,
                  int32_t* __restrict__ blk_base, int32_t* __restrict__ counts,
-                 int32_t* __restrict__ offsets, int32_t* __restrict__ tile_prefix) {
+                 int32_t* __restrict__ offsets, int32_t* __restrict__ tile_prefix,
+                 const HeavySplit hs) {
   pdl_trigger();
   pdl_wait();
   __shared__ int sh[33];
@@ -125,6 +163,7 @@ perm_scan_kernel(const int32_t* __restrict__ blk_cnt, int nblk, int E, int tile,
     offsets[E] = all;
     tile_prefix[E] = all_tiles;
   }
+  if (hs.H > 0) split_heavy_block(e < E ? total : 0, off, hs, sh);
 }
 
 // ---- permutation in one block, for T <= 256 (one bitmap block) ---------------
@@ -134,7 +173,7 @@ __global__ void __launch_bounds__(1024)
 perm_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int tile,
                   int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                   int32_t* __restrict__ tile_prefix, int32_t* __restrict__ row_of,
-                  int32_t* __restrict__ tok_of_row, int* err) {
+                  int32_t* __restrict__ tok_of_row, const HeavySplit hs, int* err) {
   pdl_trigger();
   pdl_wait();
   __shared__ uint32_t bm[1024 * kWords];
@@ -169,6 +208,7 @@ perm_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int tile
     offsets[E] = all;
     tile_prefix[E] = all_tiles;
   }
+  if (hs.H > 0) split_heavy_block(e < E ? c : 0, off, hs, sh);
   __syncthreads();
   if (t < T) {
     const int w = t >> 5;
@@ -183,41 +223,6 @@ perm_small_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int tile
       tok_of_row[row] = t;
     }
   }
-}
-
-// ---- MXFP4 decode: experts split by token count ------------------------------
-// Called by every thread of one block of 1024 with its expert's count c
-// (thread e = expert e, c = 0 for e >= E).  Experts with at least heavy_min
-// tokens are heavy when there are at least min_heavy of them (else none is);
-// the others with tokens are light.  light[0 .. *n_light - 1] the light
-// experts (expert order); the first #heavy slots of h_expert / h_count /
-// h_offset [H] the heavy ones (expert, count, first row), the other slots
-// count 0; h_prefix [H+1] = min(j, #heavy) (one token tile a heavy expert:
-// the grouped GEMM's tile prefix over the H slots).
-__device__ void split_heavy_block(int c, int off, const HeavySplit& hs, int* sh) {
-  const int e = threadIdx.x;
-  bool heavy = c >= hs.heavy_min;
-  int nh = 0, nl = 0;
-  const int hi = block_exclusive_scan(heavy ? 1 : 0, sh, &nh);
-  if (nh < hs.min_heavy || nh > hs.H) {   // (nh > H cannot happen: H >= T*k / heavy_min)
-    heavy = false;
-    nh = 0;
-  }
-  const bool lite = c > 0 && !heavy;
-  const int li = block_exclusive_scan(lite ? 1 : 0, sh, &nl);
-  if (lite) hs.light[li] = e;
-  if (heavy) {
-    hs.h_expert[hi] = e;
-    hs.h_count[hi] = c;
-    hs.h_offset[hi] = off;
-  }
-  for (int j = nh + e; j < hs.H; j += blockDim.x) {
-    hs.h_expert[j] = 0;
-    hs.h_count[j] = 0;
-    hs.h_offset[j] = 0;
-  }
-  for (int j = e; j <= hs.H; j += blockDim.x) hs.h_prefix[j] = min(j, nh);
-  if (e == 0) hs.n_light[0] = nl;
 }
 
 // ---- permutation, pass 3: row of every (token, slot) -------------------------
@@ -529,6 +534,11 @@ int grid_for(long long n, int threads) {
 
 }  // namespace
 
+static bool valid_split(const HeavySplit& h) {
+  return h.H >= 1 && h.heavy_min >= 1 && h.tile >= 1 && h.light && h.n_light && h.h_expert &&
+         h.h_count && h.h_offset && h.h_prefix;
+}
+
 size_t permute_scratch_bytes(int T, int E) {
   const long long nblk = (T + kBlkTok - 1) / kBlkTok;
   return (size_t)(nblk * E * kWords * 4 + 2 * nblk * E * 4);
@@ -536,11 +546,17 @@ size_t permute_scratch_bytes(int T, int E) {
 
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int tile, void* scratch,
                            int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
-                           int32_t* row_of, int32_t* tok_of_row, int* err, cudaStream_t s) {
+                           int32_t* row_of, int32_t* tok_of_row, int* err, cudaStream_t s,
+                           const HeavySplit* split) {
   const int nblk = (T + kBlkTok - 1) / kBlkTok;
+  HeavySplit hs{};
+  if (split) {
+    if (!valid_split(*split)) return cudaErrorInvalidValue;
+    hs = *split;
+  }
   if (nblk == 1)
     return launch_k(perm_small_kernel, dim3(1), dim3(1024), 0, s, ids, T, k, E, tile, counts,
-                    offsets, tile_prefix, row_of, tok_of_row, err);
+                    offsets, tile_prefix, row_of, tok_of_row, hs, err);
   uint32_t* bitmaps = reinterpret_cast<uint32_t*>(scratch);
   int32_t* blk_cnt = reinterpret_cast<int32_t*>(bitmaps + (size_t)nblk * E * kWords);
   int32_t* blk_base = blk_cnt + (size_t)nblk * E;
@@ -552,7 +568,7 @@ cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int tile, vo
                err);
   if (e != cudaSuccess) return e;
   e = launch_k(perm_scan_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)blk_cnt, nblk, E,
-               tile, blk_base, counts, offsets, tile_prefix);
+               tile, blk_base, counts, offsets, tile_prefix, hs);
   if (e != cudaSuccess) return e;
   return launch_k(perm_rows_kernel, dim3(nblk), dim3(kBlkTok), 0, s, ids, T, k, E,
                   (const uint32_t*)bitmaps, (const int32_t*)blk_base, row_of, tok_of_row);
@@ -567,9 +583,7 @@ cudaError_t launch_permute_scatter_small(const int32_t* ids, int T, int k, int E
   if (T > kBlkTok || E > 1024 || k > 32 || (active && tile < T)) return cudaErrorInvalidValue;
   HeavySplit hs{};
   if (split) {
-    if (split->H < 1 || split->heavy_min < 1 || !split->light || !split->n_light ||
-        !split->h_expert || !split->h_count || !split->h_offset || !split->h_prefix)
-      return cudaErrorInvalidValue;
+    if (!valid_split(*split)) return cudaErrorInvalidValue;
     hs = *split;
   }
   return launch_k(perm_scatter_small_kernel, dim3(T), dim3(1024), 0, s, ids, T, k, E, tile, counts,

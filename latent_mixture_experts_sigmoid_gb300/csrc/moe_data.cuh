@@ -6,29 +6,31 @@
 
 namespace lmoe {
 
+// The experts of a permutation split by token count (MXFP4 experts): experts
+// with at least heavy_min tokens are heavy when there are at least min_heavy
+// of them (else none is), the others with tokens light.
+// light [E]: light[0 .. *n_light - 1] the light experts in expert order;
+// h_expert / h_count / h_offset [H]: the heavy experts (expert, count, first
+// row) in the first #heavy slots, count 0 in the others; h_prefix [H+1]: the
+// grouped GEMM's tile prefix over the H slots (ceil(count / tile) token tiles
+// a heavy expert).  H >= T*k / heavy_min.
+struct HeavySplit {
+  int heavy_min, min_heavy, H, tile;
+  int32_t *light, *n_light, *h_expert, *h_count, *h_offset, *h_prefix;
+};
+
 // Scratch bytes launch_permute needs for T tokens and E experts.
 size_t permute_scratch_bytes(int T, int E);
 
 // ids [T,k] -> counts [E], offsets [E+1], tile_prefix [E+1] (prefix of
 // ceil(count/tile)), row_of [T,k], tok_of_row [T*k].  E <= 1024.  An id
 // outside [0, E) is read as 0 and, if err is given, recorded there
-// (kErrExpertId) by the first pass.
+// (kErrExpertId) by the first pass.  split (optional): the experts also
+// split by count.
 cudaError_t launch_permute(const int32_t* ids, int T, int k, int E, int tile, void* scratch,
                            int32_t* counts, int32_t* offsets, int32_t* tile_prefix,
-                           int32_t* row_of, int32_t* tok_of_row, int* err, cudaStream_t s);
-
-// The experts of the permutation split by token count (MXFP4 decode):
-// experts with at least heavy_min tokens are heavy when there are at least
-// min_heavy of them (else none is), the others with tokens light.
-// light [E]: light[0 .. *n_light - 1] the light experts in expert order;
-// h_expert / h_count / h_offset [H]: the heavy experts (expert, count, first
-// row) in the first #heavy slots, count 0 in the others; h_prefix [H+1] =
-// min(j, #heavy) (one token tile a heavy expert: the grouped GEMM's tile
-// prefix over the H slots).  H >= T*k / heavy_min.
-struct HeavySplit {
-  int heavy_min, min_heavy, H;
-  int32_t *light, *n_light, *h_expert, *h_count, *h_offset, *h_prefix;
-};
+                           int32_t* row_of, int32_t* tok_of_row, int* err, cudaStream_t s,
+                           const HeavySplit* split = nullptr);
 
 // launch_permute followed by launch_scatter_rows in one launch of T blocks,
 // for T <= 256, E <= 1024, k <= 32 (the small-T path).  active (optional,

@@ -222,11 +222,11 @@ def test_mxfp4_validation(lib):
     d = lm.make_dims(W.TINY)
     nb = lib.latent_moe_workspace_bytes_mxfp4(ctypes.byref(d))
     assert nb >= lib.latent_moe_workspace_bytes(ctypes.byref(d))
-    # above 128 tokens the workspace also holds every expert dequantized
+    # at 300 tokens the T*k/17 slots are every expert
     dp = lm.make_dims(dataclasses.replace(W.TINY, T=300))
     E, L, dI = W.TINY.num_experts, W.TINY.latent, W.TINY.inter
-    # at 17..128 tokens the T*k/17 heavy-expert slots (bf16 weights + tables)
-    for T in (16, 17, 128):
+    # above 16 tokens the T*k/17 heavy-expert slots (bf16 weights + tables)
+    for T in (16, 17, 128, 129, 256):
         dm = lm.make_dims(dataclasses.replace(W.TINY, T=T))
         extra = (lib.latent_moe_workspace_bytes_mxfp4(ctypes.byref(dm)) -
                  lib.latent_moe_workspace_bytes(ctypes.byref(dm)))
@@ -261,12 +261,14 @@ def test_mxfp4_validation(lib):
     # launches: decode replaces GEMM1 + SituGLU and GEMM2 by one kernel each;
     # above 16 tokens (where an expert can get more than 16) the compact
     # dequantization of the heavy experts and their two grouped GEMMs follow;
-    # above 128 tokens one dequantization kernel comes first
+    # with inter % 128 != 0 above 128 tokens one dequantization kernel of
+    # every expert with tokens comes first
     n_bf16 = lib.latent_moe_launch_count(ctypes.byref(d), 1)
     assert lib.latent_moe_launch_count_mxfp4(ctypes.byref(d), 1) == n_bf16
-    for T, extra in ((16, 0), (17, 3), (128, 3)):
+    for T, extra in ((16, 0), (17, 3), (128, 3), (129, 3), (256, 3), (300, 3)):
         dm = lm.make_dims(dataclasses.replace(W.TINY, T=T))
         assert lib.latent_moe_launch_count_mxfp4(ctypes.byref(dm), 1) == \
             lib.latent_moe_launch_count(ctypes.byref(dm), 1) + extra
-    assert lib.latent_moe_launch_count_mxfp4(ctypes.byref(dp), 1) == \
-        lib.latent_moe_launch_count(ctypes.byref(dp), 1) + 1
+    dq = lm.make_dims(dataclasses.replace(W.TINY, T=300, inter=192))
+    assert lib.latent_moe_launch_count_mxfp4(ctypes.byref(dq), 1) == \
+        lib.latent_moe_launch_count(ctypes.byref(dq), 1) + 1

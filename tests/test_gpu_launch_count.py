@@ -67,7 +67,7 @@ def test_launch_count_matches_captured_kernels(cuda_ok, T, shared):
     assert _kernel_nodes(g2) == lm.latent_moe_launch_count_router(d, shared)
 
 
-@pytest.mark.parametrize("T", [8, 64, 300])
+@pytest.mark.parametrize("T", [8, 64, 200, 300])
 def test_mxfp4_launch_count_matches_captured_kernels(cuda_ok, T):
     if not hasattr(torch.cuda.CUDAGraph, "raw_cuda_graph"):
         pytest.skip("this PyTorch does not expose the captured graph")

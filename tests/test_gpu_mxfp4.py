@@ -3,14 +3,15 @@ oracle.
 
 Dequantization: bit-exact (every MXFP4 weight with a scale exponent in 2..252
 is a bf16 value; exponent 0 too for these magnitudes; 255 gives NaN).
-Decode expert kernels (4-bit weights read directly): each stage fed the GPU's
+Expert stages (4-bit weights read directly; experts with more than 16 tokens
+on the tensor-core GEMMs from a compact bf16 copy): each stage fed the GPU's
 own inputs against the oracle's stage on the dequantized weights, to the
 stage bounds the bf16 path meets (tests/gpu_util.assert_stage_close,
 assert_gemm_situ_close).  Layer: within max(2e-2 rms, 2 bf16 steps at the
 largest addend of the final sum) everywhere, the literal 2e-2 rms bound
-asserted on the tiny layers.  Above 128 tokens the MXFP4 forward runs the bf16
-kernels on weights it dequantizes, so its output is bit-identical to
-latent_moe_forward on lmoe_dequant_mxfp4's weights.
+asserted on the tiny layers.  With inter % 128 != 0 above 128 tokens the
+MXFP4 forward runs the bf16 kernels on weights it dequantizes, so its output
+is bit-identical to latent_moe_forward on lmoe_dequant_mxfp4's weights.
 """
 import dataclasses
 
@@ -150,8 +151,9 @@ def test_mxfp4_tiny_layer():
 
 @pytest.mark.parametrize("T", [1, 3, 17, 100, 128, 129, 200, 256, 257, 300])
 def test_mxfp4_tiny_layer_token_counts(T):
-    # decode regime (4-bit kernels) up to 128 tokens, dequantized prefill above
-    # (its permutation in one block up to 256 tokens, in three passes above)
+    # the 4-bit kernels (heavy experts split off to the tensor-core GEMMs
+    # above 16 tokens; the decode-sized dense GEMMs up to 128, the one-block
+    # permutation up to 256, three passes above)
     tiny_case(dataclasses.replace(W.TINY, T=T), seed=T)
 
 
@@ -234,10 +236,11 @@ def test_mxfp4_zero_scale_blocks(T):
 
 
 def test_mxfp4_prefill_is_the_bf16_forward_on_dequantized_weights():
-    # above 128 tokens: the same kernels as latent_moe_forward once the weights
-    # are dequantized, so bit-identical outputs
+    # inter % 128 != 0 above 128 tokens: the same kernels as
+    # latent_moe_forward once the weights are dequantized, so bit-identical
+    # outputs
     from tests.gpu_util import DEV, dev_bf16, dev_f32
-    d = dataclasses.replace(W.TINY, T=300)
+    d = dataclasses.replace(W.TINY, T=300, inter=192)
     wts, Q, wdev, qdev = _tiny(d, 4)
     x = W.hidden_states(d, 4)
     lg = W.router_logits(d.T, d.num_experts, 4)
@@ -300,6 +303,34 @@ def test_mxfp4_decode_skewed_full_size(decode_full):
     record_literal(got, ref, "MXFP4 decode layer T=64 Zipf", TOL)
     check_expert_stages(d, lambda n, e: (Q[n + "_q"][e], Q[n + "_s"][e]),
                         list(range(12)) + [d.T - 1], ws, lg, wor["bias"])
+
+
+def test_mxfp4_prefill_zipf_sampled(decode_full):
+    # the prefill workload (T = 4096, Zipf-skewed routing) with MXFP4 experts:
+    # the experts with more than 16 tokens on the tensor-core GEMMs from their
+    # bf16 copies, the others on the 4-bit kernels; a seeded sample of tokens
+    # plus the first token of every used expert against the oracle, and the
+    # expert stages of the first token of every used expert (both paths)
+    from tests.gpu_util import host_bits, assert_layer_close, addend_scale, record_literal
+    d, wdev, qdev, wor, Q = decode_full
+    d = dataclasses.replace(d, T=4096)
+    x = W.hidden_states(d, 0)
+    lg = W.router_logits(d.T, d.num_experts, 0, zipf=True)
+    ids, _ = O.route(lg, wor["bias"], d.topk, d.routed_scaling_factor, d.renormalize)
+    counts = np.bincount(ids.ravel(), minlength=d.num_experts)
+    assert (counts > 16).sum() >= 4 and ((counts > 0) & (counts <= 16)).sum() >= 4
+    out, ws = run_mxfp4(d, wdev, qdev, x, lg, keep_ws=True)
+    first_of_expert = [int(np.argmax((ids == e).any(axis=1))) for e in np.unique(ids)]
+    toks = np.unique(np.concatenate([[0, d.T - 1], first_of_expert,
+                                     np.random.default_rng(4).choice(d.T, 96, replace=False)]))
+    ref_bits, mid = O.latent_moe_forward_mxfp4(d, wor, Q, x[toks], lg[toks], intermediates=True)
+    ref = O.bf16_to_f64(ref_bits)
+    got = O.bf16_to_f64(host_bits(out))[toks]
+    assert_layer_close(got, ref, TOL, scale=addend_scale(ref, mid, wor["w_up"]))
+    record_literal(got, ref, f"MXFP4 prefill layer T=4096 Zipf ({len(toks)} sampled tokens)", TOL)
+    check_expert_stages(d, lambda n, e: (Q[n + "_q"][e], Q[n + "_s"][e]),
+                        sorted(set(first_of_expert)), ws, lg, wor["bias"])
+    assert torch.isfinite(out.float()).all()
 
 
 @pytest.mark.parametrize("T,zipf", [(8, False), (64, True)])
