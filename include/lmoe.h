@@ -324,24 +324,23 @@ int lmoe_dequant_mxfp4(const uint8_t* codes, const uint8_t* scales, lmoe_bf16* o
                        int64_t rows, int K, void* stream);
 
 /* Workspace bytes of latent_moe_forward_mxfp4 (0 on invalid dims): the      */
-/* workspace of latent_moe_forward, plus at T > 128 room for every expert's */
-/* weights dequantized to bf16 (E * 3 * inter * latent * 2 bytes), and at   */
-/* 16 < T <= 128 (inter % 128 == 0) room for H = min(E, T*topk / 17) such   */
-/* experts (H * 3 * inter * latent * 2 bytes) and their tables.             */
+/* workspace of latent_moe_forward, plus at T > 16 (inter % 128 == 0) room   */
+/* for H = min(E, T*topk / 17) experts' weights dequantized to bf16          */
+/* (H * 3 * inter * latent * 2 bytes) and their tables, or with             */
+/* inter % 128 != 0 at T > 128 room for every expert's (H = E).              */
 size_t latent_moe_workspace_bytes_mxfp4(const lmoe_dims* dims);
 
 /* The layer forward with MXFP4 routed experts: latent_moe_forward with      */
 /* weights->w13 and weights->w2 unused (may be NULL) and the experts' GEMMs  */
-/* on `experts` instead.  At T <= 128 (decode) the two expert stages read    */
-/* the 4-bit weights directly (one kernel per stage over the active experts, */
-/* GEMM1's gate/up and SituGLU in one kernel); an expert that received more  */
-/* than 16 tokens (possible at T > 16) is instead dequantized into the       */
-/* workspace and runs on the bf16 tensor-core path (the device picks these   */
-/* experts from the routing; inter % 128 == 0).  Above 128 tokens the        */
-/* weights of every expert that received tokens are dequantized into the     */
-/* workspace each call and the bf16 tensor-core path runs on them (a caller  */
-/* that runs prefill repeatedly on the same weights can dequantize once with */
-/* lmoe_dequant_mxfp4 and call latent_moe_forward).                          */
+/* on `experts` instead.  The two expert stages read the 4-bit weights      */
+/* directly (one kernel per stage over the active experts, GEMM1's gate/up  */
+/* and SituGLU in one kernel), except that the experts that received more    */
+/* than 16 tokens, when at least 4 did (the device picks them from the       */
+/* routing; inter % 128 == 0), are dequantized into the workspace each call  */
+/* and run on the bf16 tensor-core path.  With inter % 128 != 0 above 128    */
+/* tokens every expert that received tokens takes that path.  (A caller that */
+/* runs large batches repeatedly on the same weights can also dequantize     */
+/* once with lmoe_dequant_mxfp4 and call latent_moe_forward.)                */
 /* Limits: those of latent_moe_forward and latent <= 4096, inter <= 4096.    */
 /* The four expert pointers are required (LMOE_ERR_NULL), codes and scales   */
 /* 16-byte aligned (LMOE_ERR_ALIGN), device memory of the current device     */
